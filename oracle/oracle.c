@@ -1,0 +1,616 @@
+/*
+ * oracle.c -- plain, slow CPU oracle of the W4A16 INT4 Mixture-of-Experts
+ * expert computation.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, __graft_entry__.smoke() and the
+ * CPU-baseline / reference legs of bench.py load this library.  The CUDA path
+ * never calls it and shares no code with it.
+ *
+ * What it follows (page: "vLLM x Novita AI: Chord W4A16 INT4 MoE kernels for
+ * Kimi K2.x", novita.ai):
+ *   - TL;DR: BF16 activations, INT4 weights, group-32 scales.
+ *   - "vLLM integration": the uint4 / group-32 / BF16-scale schema; routing
+ *     consumed as moe_align_block_size buffers (sorted_ids / expert_ids /
+ *     num_tokens_padded), over-allocated.
+ *   - "Kernel optimisation / H200 and Blackwell indexed decode": dequant is
+ *     subtract-then-scale, w = (q - 8) * scale, keeping the unfused BF16
+ *     rounding order.
+ *   - "Kernel optimisation / grouped SM90 kernels" and Fig. 3: indexed layout
+ *     (padding lives in the index as a sentinel), contiguous layout (rows per
+ *     expert padded to 128 with m_indices = -1 on padding), masked layout
+ *     (fixed row budget per expert, masked_m valid counts, flat output).
+ *   - "Measurement": gate_up and down are the two GEMM calls of a layer.
+ * The expert MLP itself (gate/up GEMM, SiLU(gate) * up, down GEMM, top-k
+ * weighted sum per token) is the standard MoE layer the page accelerates.
+ *
+ * Readings where the page is silent (each is one choice, applied everywhere):
+ *   R1 codes: 8 per int32 along K, element c = 8w+i in bits [4i, 4i+4).
+ *   R2 zero point fixed at 8; no per-group zero.
+ *   R3 dequant: W = RNE_bf16( float(q-8) * float(s) ), one rounding (the
+ *      product of a 4-bit integer and an 8-bit significand is exact in fp32).
+ *   R4 scale groups: 32 consecutive input channels, scales [E, N, K/32].
+ *   R5 fused gate/up: rows 0..I-1 are gate, rows I..2I-1 are up.
+ *   R6 FP32 accumulation in ascending input channel; products of two bf16
+ *      values are exact in fp32.
+ *   R7 g and u are not rounded before SiLU; h = RNE_bf16(silu(g) * u),
+ *      silu(v) = v / (1 + exp(-v)) in fp32.
+ *   R8 per-pair down output y kept in fp32.
+ *   R9 router weights applied in the combine, after down, in fp32, summed in
+ *      ascending slot order over the local slots; out = RNE_bf16(sum), 0 when
+ *      the token has no local slot.
+ *   R10 align: experts in ascending local id, pairs p = t*k + j ascending
+ *      inside an expert, each expert padded to a multiple of block_m with the
+ *      sentinel T*k, empty experts get no block, sorted_ids tail = sentinel,
+ *      expert_ids tail = -1.
+ *   R11 pairs routed to a non-local expert (expert_map = -1) are dropped.
+ *
+ * Every function below is pinned by the CPU tests (closed forms, exhaustive
+ * dequant against exact rational rounding, brute-force fp64 evaluation,
+ * routing invariants, cross-layout agreement); none is "parity unpinned".
+ *
+ * Built with -O2 -ffp-contract=off so that every a*b+c stays two roundings
+ * exactly as written.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ------------------------------------------------------------------------- */
+/* test-only planted mistakes: 0 = none.  The tests set one at a time and     */
+/* check that some pin fails; nothing else sets this.                         */
+/* ------------------------------------------------------------------------- */
+enum {
+    MUT_NONE = 0,
+    MUT_NIBBLE_HIGH_FIRST = 1, /* R1 violated: element c in bits [28-4i, 32-4i) */
+    MUT_GATE_UP_SWAPPED = 2,   /* R5 violated */
+    MUT_DEQUANT_FMA = 3,       /* R3 violated: (128+q)*s - bf16(136*s), the folded form */
+    MUT_SCALE_GROUP = 4,       /* R4 violated: the next group's scale */
+    MUT_ZERO_SIGN = 5,         /* (8 - q) instead of (q - 8) */
+    MUT_DROP_WEIGHT = 6,       /* R9 violated: router weight ignored */
+    MUT_DROP_LAST_SLOT = 7,    /* combine stops one slot early */
+    MUT_ALIGN_DESCENDING = 8,  /* R10 violated: pairs descending inside an expert */
+    MUT_SILU_SIGN = 9,         /* silu(v) = v / (1 + exp(v)) */
+    MUT_DOWN_TRANSPOSED = 10,  /* down weight read as [I, H] */
+    MUT_ALIGN_NO_PAD = 11,     /* segments not padded to block_m */
+    MUT_CODE_OFFSET = 12,      /* reads the code of element c+1 */
+};
+static int g_mutation = 0;
+void oracle_set_mutation(int m) { g_mutation = m; }
+int oracle_get_mutation(void) { return g_mutation; }
+
+/* ------------------------------------------------------------------------- */
+/* bf16 <-> fp32                                                             */
+/* ------------------------------------------------------------------------- */
+float oracle_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round-to-nearest-even of an fp32 value to bf16.  NaN stays NaN (quiet). */
+uint16_t oracle_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+static float rbf(float f) { return oracle_bf16_to_f32(oracle_f32_to_bf16(f)); }
+
+/* silu(v) = v / (1 + exp(-v)) in fp32 (R7). */
+float oracle_silu(float v)
+{
+    if (g_mutation == MUT_SILU_SIGN)
+        return v / (1.0f + expf(v));
+    return v / (1.0f + expf(-v));
+}
+
+/* ------------------------------------------------------------------------- */
+/* threads: a plain parallel-for over independent items                     */
+/* ------------------------------------------------------------------------- */
+static int g_threads = 0;
+void oracle_set_threads(int n) { g_threads = n; }
+int oracle_num_threads(void)
+{
+    if (g_threads > 0)
+        return g_threads;
+    const char* env = getenv("ORACLE_THREADS");
+    if (env && atoi(env) > 0)
+        return atoi(env);
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+typedef void (*range_fn)(void* ctx, int64_t begin, int64_t end);
+typedef struct {
+    range_fn fn;
+    void* ctx;
+    int64_t begin, end;
+} range_job;
+
+static void* range_trampoline(void* p)
+{
+    range_job* j = (range_job*)p;
+    j->fn(j->ctx, j->begin, j->end);
+    return NULL;
+}
+
+static void parallel_for(int64_t n, range_fn fn, void* ctx)
+{
+    int nt = oracle_num_threads();
+    if (nt > 256)
+        nt = 256;
+    if (n <= 0)
+        return;
+    if (nt <= 1 || n == 1) {
+        fn(ctx, 0, n);
+        return;
+    }
+    if (nt > n)
+        nt = (int)n;
+    pthread_t th[256];
+    range_job jobs[256];
+    int started[256];
+    for (int i = 0; i < nt; ++i) {
+        jobs[i].fn = fn;
+        jobs[i].ctx = ctx;
+        jobs[i].begin = n * i / nt;
+        jobs[i].end = n * (i + 1) / nt;
+        started[i] = pthread_create(&th[i], NULL, range_trampoline, &jobs[i]) == 0;
+        if (!started[i])
+            fn(ctx, jobs[i].begin, jobs[i].end);
+    }
+    for (int i = 0; i < nt; ++i)
+        if (started[i])
+            pthread_join(th[i], NULL);
+}
+
+/* ------------------------------------------------------------------------- */
+/* weights: unpack (R1) and dequantise (R2, R3, R4)                          */
+/* ------------------------------------------------------------------------- */
+
+/* 4-bit code of element (n, c) of a [N, K] weight stored as [N, K/8] words. */
+int oracle_code(const int32_t* wq, int64_t K, int64_t n, int64_t c)
+{
+    if (g_mutation == MUT_CODE_OFFSET)
+        c = (c + 1) % K;
+    uint32_t w = (uint32_t)wq[n * (K / 8) + c / 8];
+    int i = (int)(c % 8);
+    if (g_mutation == MUT_NIBBLE_HIGH_FIRST)
+        i = 7 - i;
+    return (int)((w >> (4 * i)) & 0xFu);
+}
+
+/* The scale of element (n, c): scales stored [N, K/32]. */
+static float scale_of(const uint16_t* ws, int64_t K, int64_t n, int64_t c)
+{
+    int64_t g = c / 32;
+    if (g_mutation == MUT_SCALE_GROUP)
+        g = (g + 1) % (K / 32);
+    return oracle_bf16_to_f32(ws[n * (K / 32) + g]);
+}
+
+/* W[n, c] = RNE_bf16( float(q - 8) * float(s) ): one rounding. */
+float oracle_dequant_one(const int32_t* wq, const uint16_t* ws, int64_t K, int64_t n, int64_t c)
+{
+    int q = oracle_code(wq, K, n, c);
+    float s = scale_of(ws, K, n, c);
+    if (g_mutation == MUT_DEQUANT_FMA) /* magic-number form folded into one multiply-add */
+        return rbf((float)(128 + q) * s - rbf(136.0f * s));
+    float d = (g_mutation == MUT_ZERO_SIGN) ? (float)(8 - q) : (float)(q - 8);
+    return rbf(d * s);
+}
+
+typedef struct {
+    const int32_t* wq;
+    const uint16_t* ws;
+    int64_t K;
+    float* out;
+} dequant_ctx;
+
+static void dequant_rows(void* p, int64_t b, int64_t e)
+{
+    dequant_ctx* c = (dequant_ctx*)p;
+    for (int64_t n = b; n < e; ++n)
+        for (int64_t k = 0; k < c->K; ++k)
+            c->out[n * c->K + k] = oracle_dequant_one(c->wq, c->ws, c->K, n, k);
+}
+
+/* Dequantise a whole [N, K] weight to fp32 values (each one a bf16 value). */
+void oracle_dequant(const int32_t* wq, const uint16_t* ws, int64_t N, int64_t K, float* out)
+{
+    dequant_ctx c = {wq, ws, K, out};
+    parallel_for(N, dequant_rows, &c);
+}
+
+/* ------------------------------------------------------------------------- */
+/* align (R10, R11)                                                          */
+/* ------------------------------------------------------------------------- */
+int64_t oracle_align_capacity(int64_t T, int64_t k, int64_t E_local, int64_t block_m)
+{
+    if (block_m <= 0)
+        return -1;
+    int64_t worst = T * k + E_local * (block_m - 1);
+    return (worst + block_m - 1) / block_m * block_m;
+}
+
+/* local expert of a global id, -1 when not local or out of range */
+static int64_t local_of(int32_t gid, int64_t E_global, const int32_t* expert_map, int64_t E_local)
+{
+    if (gid < 0 || gid >= E_global)
+        return -1;
+    int64_t l = expert_map ? expert_map[gid] : gid;
+    if (l < 0 || l >= E_local)
+        return -1;
+    return l;
+}
+
+/*
+ * Group the local (token, slot) pairs by expert.  Returns 0, or -1 when the
+ * capacity is too small.  Outputs:
+ *   sorted_ids[capacity]        pair ids, sentinel T*k on padding and tail
+ *   expert_ids[capacity/block_m] expert of each block, -1 on the tail
+ *   num_tokens_padded[0]         sum over experts of ceil(c_e/block_m)*block_m
+ */
+int oracle_moe_align(const int32_t* topk_ids, int64_t T, int64_t k, int64_t E_global,
+                     const int32_t* expert_map, int64_t E_local, int64_t block_m,
+                     int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_tokens_padded,
+                     int64_t capacity)
+{
+    const int64_t P = T * k;
+    const int32_t sentinel = (int32_t)P;
+    if (block_m <= 0 || capacity % block_m != 0)
+        return -1;
+    for (int64_t i = 0; i < capacity; ++i)
+        sorted_ids[i] = sentinel;
+    for (int64_t b = 0; b < capacity / block_m; ++b)
+        expert_ids[b] = -1;
+    int64_t pos = 0;
+    for (int64_t e = 0; e < E_local; ++e) {
+        int64_t count = 0;
+        for (int64_t p = 0; p < P; ++p)
+            if (local_of(topk_ids[p], E_global, expert_map, E_local) == e)
+                ++count;
+        if (count == 0)
+            continue;
+        int64_t padded = (g_mutation == MUT_ALIGN_NO_PAD)
+                             ? count
+                             : (count + block_m - 1) / block_m * block_m;
+        if (pos + padded > capacity)
+            return -1;
+        int64_t r = pos;
+        if (g_mutation == MUT_ALIGN_DESCENDING) {
+            for (int64_t p = P - 1; p >= 0; --p)
+                if (local_of(topk_ids[p], E_global, expert_map, E_local) == e)
+                    sorted_ids[r++] = (int32_t)p;
+        } else {
+            for (int64_t p = 0; p < P; ++p)
+                if (local_of(topk_ids[p], E_global, expert_map, E_local) == e)
+                    sorted_ids[r++] = (int32_t)p;
+        }
+        for (int64_t b = pos / block_m; b < (pos + padded + block_m - 1) / block_m; ++b)
+            expert_ids[b] = (int32_t)e;
+        pos += padded;
+    }
+    num_tokens_padded[0] = (int32_t)pos;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* the expert MLP of a set of rows that share one expert                     */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    const float* W13;   /* [2I, H] dequantised */
+    const float* W2;    /* [H, I]  dequantised */
+    int64_t H, I;
+    int64_t nrows;
+    const uint16_t* const* xrows; /* nrows pointers to bf16 rows of length H */
+    float* g;            /* [nrows, I] */
+    float* u;            /* [nrows, I] */
+    uint16_t* h;         /* [nrows, I] bf16 */
+    float* y;            /* [nrows, H] */
+} mlp_ctx;
+
+/* g[r, n] = sum_c x[r, c] * W13[n, c];  u[r, n] = sum_c x[r, c] * W13[I + n, c] */
+static void mlp_gate_up(void* p, int64_t b, int64_t e)
+{
+    mlp_ctx* m = (mlp_ctx*)p;
+    const int64_t H = m->H, I = m->I;
+    int64_t gate_row0 = 0, up_row0 = I;
+    if (g_mutation == MUT_GATE_UP_SWAPPED) {
+        gate_row0 = I;
+        up_row0 = 0;
+    }
+    for (int64_t n = b; n < e; ++n) {
+        const float* wg = m->W13 + (gate_row0 + n) * H;
+        const float* wu = m->W13 + (up_row0 + n) * H;
+        for (int64_t r = 0; r < m->nrows; ++r) {
+            const uint16_t* x = m->xrows[r];
+            float ag = 0.0f, au = 0.0f;
+            for (int64_t c = 0; c < H; ++c) {
+                float xv = oracle_bf16_to_f32(x[c]);
+                ag += xv * wg[c];
+                au += xv * wu[c];
+            }
+            m->g[r * I + n] = ag;
+            m->u[r * I + n] = au;
+            m->h[r * I + n] = oracle_f32_to_bf16(oracle_silu(ag) * au);
+        }
+    }
+}
+
+/* y[r, n] = sum_i h[r, i] * W2[n, i] */
+static void mlp_down(void* p, int64_t b, int64_t e)
+{
+    mlp_ctx* m = (mlp_ctx*)p;
+    const int64_t H = m->H, I = m->I;
+    for (int64_t n = b; n < e; ++n) {
+        for (int64_t r = 0; r < m->nrows; ++r) {
+            const uint16_t* h = m->h + r * I;
+            float acc = 0.0f;
+            for (int64_t i = 0; i < I; ++i) {
+                float w = (g_mutation == MUT_DOWN_TRANSPOSED) ? m->W2[i * H + n] : m->W2[n * I + i];
+                acc += oracle_bf16_to_f32(h[i]) * w;
+            }
+            m->y[r * H + n] = acc;
+        }
+    }
+}
+
+/* Dequantise expert e and run its MLP on nrows activation rows. */
+static int expert_mlp(const int32_t* w13_q, const uint16_t* w13_s, const int32_t* w2_q,
+                      const uint16_t* w2_s, int64_t e, int64_t H, int64_t I, int64_t nrows,
+                      const uint16_t* const* xrows, float* g, float* u, uint16_t* h, float* y)
+{
+    float* W13 = (float*)malloc(sizeof(float) * (size_t)(2 * I * H));
+    float* W2 = (float*)malloc(sizeof(float) * (size_t)(H * I));
+    if (!W13 || !W2) {
+        free(W13);
+        free(W2);
+        return -1;
+    }
+    oracle_dequant(w13_q + e * (2 * I) * (H / 8), w13_s + e * (2 * I) * (H / 32), 2 * I, H, W13);
+    oracle_dequant(w2_q + e * H * (I / 8), w2_s + e * H * (I / 32), H, I, W2);
+    mlp_ctx m = {W13, W2, H, I, nrows, xrows, g, u, h, y};
+    parallel_for(I, mlp_gate_up, &m);
+    parallel_for(H, mlp_down, &m);
+    free(W13);
+    free(W2);
+    return 0;
+}
+
+/* One expert's MLP on explicit rows; exposed for tests. x: [nrows, H] bf16. */
+int oracle_expert_mlp(const int32_t* w13_q, const uint16_t* w13_s, const int32_t* w2_q,
+                      const uint16_t* w2_s, int64_t e, int64_t H, int64_t I, int64_t nrows,
+                      const uint16_t* x, float* g, float* u, uint16_t* h, float* y)
+{
+    const uint16_t** rows = (const uint16_t**)malloc(sizeof(void*) * (size_t)(nrows > 0 ? nrows : 1));
+    if (!rows)
+        return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        rows[r] = x + r * H;
+    int rc = expert_mlp(w13_q, w13_s, w2_q, w2_s, e, H, I, nrows, rows, g, u, h, y);
+    free(rows);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* combine (R9)                                                              */
+/* ------------------------------------------------------------------------- */
+/* out[t, n] = RNE_bf16( sum over local slots j ascending of w[t, j] * y[t*k + j, n] ) */
+static void combine(const float* y_pairs, const uint8_t* is_local, const float* topk_weights,
+                    int64_t T, int64_t k, int64_t H, uint16_t* out)
+{
+    int64_t kk = (g_mutation == MUT_DROP_LAST_SLOT) ? k - 1 : k;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t n = 0; n < H; ++n) {
+            float acc = 0.0f;
+            for (int64_t j = 0; j < kk; ++j) {
+                int64_t p = t * k + j;
+                if (!is_local[p])
+                    continue;
+                float w = (g_mutation == MUT_DROP_WEIGHT) ? 1.0f : topk_weights[p];
+                acc += w * y_pairs[p * H + n];
+            }
+            out[t * H + n] = oracle_f32_to_bf16(acc);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* indexed layer                                                             */
+/* ------------------------------------------------------------------------- */
+/*
+ * The whole layer on the indexed (moe_align_block_size) layout.  For each
+ * padded row r < num_tokens_padded whose pair p = sorted_ids[r] is not the
+ * sentinel, the token t = p / k goes through the MLP of expert
+ * expert_ids[r / block_m]; then the combine.  Optional outputs:
+ *   h_rows [capacity, I] bf16 (rows of sentinel entries set to 0),
+ *   y_pairs [T*k, H] fp32 (pairs that are not local set to 0).
+ * Returns 0, or -1 on an inconsistent index / allocation failure.
+ */
+int oracle_moe_indexed(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E_local,
+                       int64_t k, const int32_t* w13_q, const uint16_t* w13_s,
+                       const int32_t* w2_q, const uint16_t* w2_s, const float* topk_weights,
+                       const int32_t* sorted_ids, const int32_t* expert_ids,
+                       const int32_t* num_tokens_padded, int64_t capacity, int64_t block_m,
+                       uint16_t* out, uint16_t* h_rows, float* y_pairs_out)
+{
+    const int64_t P = T * k;
+    const int64_t ntp = num_tokens_padded[0];
+    if (ntp < 0 || ntp > capacity || block_m <= 0)
+        return -1;
+    float* y_pairs = (float*)calloc((size_t)(P > 0 ? P : 1) * (size_t)H, sizeof(float));
+    uint8_t* is_local = (uint8_t*)calloc((size_t)(P > 0 ? P : 1), 1);
+    int64_t* rows_of = (int64_t*)malloc(sizeof(int64_t) * (size_t)(ntp > 0 ? ntp : 1));
+    const uint16_t** xrows = (const uint16_t**)malloc(sizeof(void*) * (size_t)(ntp > 0 ? ntp : 1));
+    int rc = 0;
+    if (!y_pairs || !is_local || !rows_of || !xrows) {
+        rc = -1;
+        goto done;
+    }
+    if (h_rows)
+        memset(h_rows, 0, sizeof(uint16_t) * (size_t)(capacity * I));
+    for (int64_t e = 0; e < E_local && rc == 0; ++e) {
+        int64_t n = 0;
+        for (int64_t r = 0; r < ntp; ++r) {
+            int32_t p = sorted_ids[r];
+            if (p < 0 || p >= P)
+                continue;
+            if (expert_ids[r / block_m] != e)
+                continue;
+            rows_of[n] = r;
+            xrows[n] = x + (p / k) * H;
+            ++n;
+        }
+        if (n == 0)
+            continue;
+        float* g = (float*)malloc(sizeof(float) * (size_t)(n * I));
+        float* u = (float*)malloc(sizeof(float) * (size_t)(n * I));
+        uint16_t* h = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n * I));
+        float* y = (float*)malloc(sizeof(float) * (size_t)(n * H));
+        if (!g || !u || !h || !y ||
+            expert_mlp(w13_q, w13_s, w2_q, w2_s, e, H, I, n, xrows, g, u, h, y) != 0) {
+            rc = -1;
+        } else {
+            for (int64_t i = 0; i < n; ++i) {
+                int64_t r = rows_of[i];
+                int64_t p = sorted_ids[r];
+                is_local[p] = 1;
+                memcpy(y_pairs + p * H, y + i * H, sizeof(float) * (size_t)H);
+                if (h_rows)
+                    memcpy(h_rows + r * I, h + i * I, sizeof(uint16_t) * (size_t)I);
+            }
+        }
+        free(g);
+        free(u);
+        free(h);
+        free(y);
+    }
+    if (rc == 0) {
+        combine(y_pairs, is_local, topk_weights, T, k, H, out);
+        if (y_pairs_out)
+            memcpy(y_pairs_out, y_pairs, sizeof(float) * (size_t)(P * H));
+    }
+done:
+    free(y_pairs);
+    free(is_local);
+    free(rows_of);
+    free(xrows);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* grouped layer: contiguous (mode 0) and masked (mode 1)                    */
+/* ------------------------------------------------------------------------- */
+/*
+ * mode 0 (contiguous): a is [M, H]; row r belongs to expert m_indices[r], or
+ *   is padding when m_indices[r] < 0.
+ * mode 1 (masked): a is [E, max_m, H] (M = E*max_m); row e*max_m + i belongs
+ *   to expert e when i < masked_m[e], else it is ignored.
+ * out_rows [M, H] bf16: RNE_bf16(y) of each valid row, 0 on other rows.
+ * Optional token combine: with row_to_pair [M] (pair id t*k+j or -1) and
+ *   topk_weights [T, k], out_tokens [T, H] gets the same combine as the
+ *   indexed layer over the pairs that have a valid row.
+ * Optional h_rows [M, I] bf16 and y_rows [M, H] fp32 (0 on invalid rows).
+ */
+int oracle_moe_grouped(int mode, const uint16_t* a, int64_t M, int64_t H, int64_t I,
+                       int64_t E_local, const int32_t* m_indices, const int32_t* masked_m,
+                       int64_t max_m, const int32_t* w13_q, const uint16_t* w13_s,
+                       const int32_t* w2_q, const uint16_t* w2_s, const int32_t* row_to_pair,
+                       const float* topk_weights, int64_t T, int64_t k, uint16_t* out_rows,
+                       uint16_t* out_tokens, uint16_t* h_rows, float* y_rows)
+{
+    if (mode != 0 && mode != 1)
+        return -1;
+    if (mode == 1 && M != E_local * max_m)
+        return -1;
+    int64_t* rows_of = (int64_t*)malloc(sizeof(int64_t) * (size_t)(M > 0 ? M : 1));
+    const uint16_t** xrows = (const uint16_t**)malloc(sizeof(void*) * (size_t)(M > 0 ? M : 1));
+    float* yall = (float*)calloc((size_t)(M > 0 ? M : 1) * (size_t)H, sizeof(float));
+    int rc = 0;
+    if (!rows_of || !xrows || !yall) {
+        rc = -1;
+        goto done;
+    }
+    for (int64_t r = 0; r < M; ++r)
+        for (int64_t c = 0; c < H; ++c)
+            out_rows[r * H + c] = 0;
+    if (h_rows)
+        memset(h_rows, 0, sizeof(uint16_t) * (size_t)(M * I));
+    for (int64_t e = 0; e < E_local && rc == 0; ++e) {
+        int64_t n = 0;
+        for (int64_t r = 0; r < M; ++r) {
+            int valid;
+            if (mode == 0)
+                valid = m_indices[r] == e;
+            else
+                valid = (r / max_m == e) && (r % max_m) < masked_m[e];
+            if (!valid)
+                continue;
+            rows_of[n] = r;
+            xrows[n] = a + r * H;
+            ++n;
+        }
+        if (n == 0)
+            continue;
+        float* g = (float*)malloc(sizeof(float) * (size_t)(n * I));
+        float* u = (float*)malloc(sizeof(float) * (size_t)(n * I));
+        uint16_t* h = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n * I));
+        float* y = (float*)malloc(sizeof(float) * (size_t)(n * H));
+        if (!g || !u || !h || !y ||
+            expert_mlp(w13_q, w13_s, w2_q, w2_s, e, H, I, n, xrows, g, u, h, y) != 0) {
+            rc = -1;
+        } else {
+            for (int64_t i = 0; i < n; ++i) {
+                int64_t r = rows_of[i];
+                for (int64_t c = 0; c < H; ++c)
+                    out_rows[r * H + c] = oracle_f32_to_bf16(y[i * H + c]);
+                memcpy(yall + r * H, y + i * H, sizeof(float) * (size_t)H);
+                if (h_rows)
+                    memcpy(h_rows + r * I, h + i * I, sizeof(uint16_t) * (size_t)I);
+            }
+        }
+        free(g);
+        free(u);
+        free(h);
+        free(y);
+    }
+    if (rc == 0 && y_rows)
+        memcpy(y_rows, yall, sizeof(float) * (size_t)(M * H));
+    if (rc == 0 && out_tokens && row_to_pair && topk_weights) {
+        const int64_t P = T * k;
+        float* y_pairs = (float*)calloc((size_t)(P > 0 ? P : 1) * (size_t)H, sizeof(float));
+        uint8_t* is_local = (uint8_t*)calloc((size_t)(P > 0 ? P : 1), 1);
+        if (!y_pairs || !is_local) {
+            rc = -1;
+        } else {
+            for (int64_t r = 0; r < M; ++r) {
+                int valid = (mode == 0) ? (m_indices[r] >= 0)
+                                        : ((r % max_m) < masked_m[r / max_m]);
+                int64_t p = row_to_pair[r];
+                if (!valid || p < 0 || p >= P)
+                    continue;
+                is_local[p] = 1;
+                memcpy(y_pairs + p * H, yall + r * H, sizeof(float) * (size_t)H);
+            }
+            combine(y_pairs, is_local, topk_weights, T, k, H, out_tokens);
+        }
+        free(y_pairs);
+        free(is_local);
+    }
+done:
+    free(rows_of);
+    free(xrows);
+    free(yall);
+    return rc;
+}

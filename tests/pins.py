@@ -1,0 +1,514 @@
+"""Pins of the CPU oracle: checks against what the Chord W4A16 MoE page and
+plain mathematics fix, written independently of oracle.c.
+
+Each pin returns (ok: bool, detail: str) so that the same checks serve both the
+plain pin tests and the planted-mistake tests (a pin must fail when one mistake
+is planted in the oracle).
+
+Independent pieces used here (none calls oracle.c):
+  * rne_bf16: round-to-nearest-even to bf16 of float64 values through
+    frexp / rint (not the bit trick oracle.c uses);
+  * decode_codes: nibble extraction with numpy shifts;
+  * brute_force_token: a per-token fp64 evaluation of the expert MLP and the
+    combine, one token at a time.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from w4a16_int4_mixture_gb300 import synth
+
+BF16_MAX = float.fromhex("0x1.fep127")
+
+
+def rne_bf16(v) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value, ties to even.  Handles
+    normal, subnormal, overflow (to inf), inf and NaN."""
+    v = np.asarray(v, dtype=np.float64)
+    out = np.empty_like(v)
+    fin = np.isfinite(v)
+    out[~fin] = v[~fin]
+    x = v[fin]
+    m, e = np.frexp(x)                      # x = m * 2**e, 0.5 <= |m| < 1
+    # bf16 keeps 8 significant bits for normals; below 2**-126 the spacing is 2**-133
+    e_eff = np.maximum(e, -125)
+    q = np.rint(np.ldexp(x, 8 - e_eff))     # rint rounds half to even
+    r = np.ldexp(q, e_eff - 8)
+    # values at or beyond max + half an ulp round to infinity
+    limit = BF16_MAX + float.fromhex("0x1p119")
+    r = np.where(np.abs(x) >= limit, np.copysign(np.inf, x), r)
+    out[fin] = r
+    return out
+
+
+def f64_to_bf16_bits(v) -> np.ndarray:
+    """Bits of float64 values that are already bf16 values (exact narrowing)."""
+    v = np.asarray(v, dtype=np.float64)
+    b = (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    return b
+
+
+def bf16_bits_to_f64(b) -> np.ndarray:
+    return oracle.bf16_to_f32(np.asarray(b, dtype=np.uint16)).astype(np.float64)
+
+
+def decode_codes(wq: np.ndarray) -> np.ndarray:
+    """[..., K/8] int32 words -> [..., K] codes, element 8w+i from bits [4i, 4i+4)."""
+    w = np.asarray(wq).view(np.uint32)
+    sh = (np.arange(8, dtype=np.uint32) * 4)
+    c = (w[..., None] >> sh) & np.uint32(0xF)
+    return c.reshape(w.shape[:-1] + (w.shape[-1] * 8,)).astype(np.int64)
+
+
+def dequant_f64(wq: np.ndarray, ws: np.ndarray) -> np.ndarray:
+    """Reference dequant of one [N, K] weight, float64 holding bf16 values."""
+    q = decode_codes(wq)
+    K = q.shape[-1]
+    s = bf16_bits_to_f64(ws)
+    s_full = np.repeat(s, 32, axis=-1)[..., :K]
+    return rne_bf16((q - 8).astype(np.float64) * s_full)
+
+
+def silu64(v):
+    v = np.asarray(v, dtype=np.float64)
+    return v / (1.0 + np.exp(-v))
+
+
+def rounding_ratio(got, ref) -> float:
+    """max |got - ref| / (ulp_bf16(ref)/2 + 1e-4 * rms(ref)): got is ref rounded
+    to bf16 up to fp32 accumulation error when this is <= 1."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    ulp_r = np.ldexp(1.0, np.frexp(np.maximum(np.abs(ref), 1e-30))[1] - 8)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return float(np.max(np.abs(got - ref) / (0.5 * ulp_r + 1e-4 * rms + 1e-30)))
+
+
+def tolerance_violation(out, ref) -> float:
+    """max over elements of |out-ref| / (1e-2*|ref| + 1e-3*rms(ref)); <= 1 passes."""
+    out = np.asarray(out, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    bound = 1e-2 * np.abs(ref) + 1e-3 * rms
+    err = np.abs(out - ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, err / bound, np.where(err > 0, np.inf, 0.0))
+    return float(np.max(ratio))
+
+
+# --------------------------------------------------------------------------
+# brute force: one token at a time, fp64, straight from the definition
+# --------------------------------------------------------------------------
+def brute_force_token(inp: synth.MoEInputs, t: int, local_of_slot):
+    """fp64 output row of token t: sum over local slots j of
+    w[t,j] * W2_e (bf16(silu(W13_e[:I] x) * (W13_e[I:] x))).  Also returns the
+    per-slot pre-rounding (g, u) for finer checks."""
+    s = inp.shape
+    x = bf16_bits_to_f64(inp.x[t])
+    acc = np.zeros(s.H, dtype=np.float64)
+    parts = []
+    for j in range(s.k):
+        e = local_of_slot[t, j]
+        if e < 0:
+            continue
+        W13 = dequant_f64(inp.w13_q[e], inp.w13_s[e])
+        W2 = dequant_f64(inp.w2_q[e], inp.w2_s[e])
+        g = W13[:s.I] @ x
+        u = W13[s.I:] @ x
+        h = rne_bf16(silu64(g) * u)
+        y = W2 @ h
+        acc += float(inp.topk_weights[t, j]) * y
+        parts.append((j, e, g, u, h, y))
+    return acc, parts
+
+
+# --------------------------------------------------------------------------
+# pins
+# --------------------------------------------------------------------------
+def pin_dequant_exhaustive():
+    """All 16 codes x all 65536 bf16 scale bit patterns vs exact RNE."""
+    N, K = 65536, 32
+    codes = np.tile(np.arange(32) % 16, (N, 1))
+    wq = synth.pack_codes(codes)
+    ws = np.arange(N, dtype=np.uint32).astype(np.uint16).reshape(N, 1)
+    got = oracle.dequant(wq, ws, N, K)
+    s = bf16_bits_to_f64(ws)                          # [N, 1]
+    with np.errstate(invalid="ignore"):
+        exact = (codes - 8).astype(np.float64) * s     # exact in float64
+    want = rne_bf16(exact)
+    g = got.astype(np.float64)
+    both_nan = np.isnan(g) & np.isnan(want)
+    same = both_nan | (f64_to_bf16_bits(np.where(np.isnan(g), 0, g)) ==
+                       f64_to_bf16_bits(np.where(np.isnan(want), 0, want)))
+    same &= (np.isnan(g) == np.isnan(want))
+    bad = np.size(same) - int(np.count_nonzero(same))
+    return bad == 0, f"{bad} mismatching dequant values"
+
+
+def pin_dequant_zero_code():
+    """Code 8 dequantises to exactly 0 for every finite scale."""
+    N, K = 1024, 32
+    wq = synth.pack_codes(np.full((N, K), 8))
+    rng = np.random.default_rng(5)
+    ws = (rng.integers(0, 0x7F80, size=(N, 1)) | (rng.integers(0, 2, size=(N, 1)) << 15)
+          ).astype(np.uint16)
+    got = oracle.dequant(wq, ws, N, K)
+    return bool(np.all(got == 0.0)), "code 8 must give 0"
+
+
+def pin_one_hot_structure(seed=11):
+    """x = unit vector at channel c0: gate/up outputs equal one dequantised weight
+    column, so nibble order, scale group axis, zero point and gate/up order are
+    all visible.  Explicit codes -> packed with the storage convention."""
+    rng = np.random.default_rng(seed)
+    E, H, I = 2, 64, 32
+    c13 = rng.integers(0, 16, size=(E, 2 * I, H))
+    c2 = rng.integers(0, 16, size=(E, H, I))
+    s13 = synth.scales(rng, E, 2 * I, H, sigma=0.5)
+    s2 = synth.scales(rng, E, H, I, sigma=0.5)
+    w13 = synth.pack_codes(c13)
+    w2 = synth.pack_codes(c2)
+    ok = True
+    detail = ""
+    for e in range(E):
+        for c0 in (0, 5, 31, 32, 45, 63):
+            x = np.zeros((1, H), np.uint16)
+            x[0, c0] = 0x3F80  # 1.0
+            g, u, h, y = oracle.expert_mlp(w13, s13, w2, s2, e, x)
+            sg = bf16_bits_to_f64(s13[e, :, c0 // 32])
+            col = rne_bf16((c13[e, :, c0] - 8) * sg)
+            if not (np.array_equal(g[0].astype(np.float64), col[:I]) and
+                    np.array_equal(u[0].astype(np.float64), col[I:])):
+                ok = False
+                detail = f"gate/up column mismatch e={e} c0={c0}"
+    return ok, detail
+
+
+def pin_down_one_hot(seed=12):
+    """Down GEMM on a unit intermediate vector equals one column of W2.
+    Built through the MLP with gate = +1 weights on one channel: choose codes so
+    h is a known one-hot bf16 vector."""
+    E, H, I = 1, 64, 32
+    rng = np.random.default_rng(seed)
+    # gate rows: code 9 (w=+s) on channel 0 only, else 8 (w=0); up rows likewise
+    c13 = np.full((E, 2 * I, H), 8)
+    i0 = 7
+    c13[0, i0, 0] = 9        # gate_i0 = x0
+    c13[0, I + i0, 0] = 9    # up_i0 = x0
+    s13 = synth.const_scales(E, 2 * I, H, 0x3F80)
+    c2 = rng.integers(0, 16, size=(E, H, I))
+    s2 = synth.scales(rng, E, H, I, sigma=0.5)
+    w13 = synth.pack_codes(c13)
+    w2 = synth.pack_codes(c2)
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = 0x4000  # 2.0
+    g, u, h, y = oracle.expert_mlp(w13, s13, w2, s2, 0, x)
+    hv = rne_bf16(silu64(2.0) * 2.0)
+    h_want = np.zeros(I)
+    h_want[i0] = hv
+    if not np.array_equal(bf16_bits_to_f64(h[0]), h_want):
+        return False, "h is not the expected one-hot vector"
+    col = rne_bf16((c2[0, :, i0] - 8) * bf16_bits_to_f64(s2[0, :, i0 // 32])) * hv
+    ok = np.array_equal(y[0].astype(np.float64), col)
+    return ok, "down output is not the expected W2 column"
+
+
+def _closed_form_inputs(code13_gate, code13_up, code2, T=6, k=3, E=4, H=64, I=32, seed=3):
+    """Unit scales, small-integer activations, exact dyadic router weights."""
+    rng = np.random.default_rng(seed)
+    shape = synth.MoEShape("closed", T=T, k=k, E_global=E, E_local=E, H=H, I=I, block_m=4,
+                           seed=seed)
+    c13 = np.empty((E, 2 * I, H), np.int64)
+    c13[:, :I] = code13_gate
+    c13[:, I:] = code13_up
+    c2 = np.full((E, H, I), code2)
+    xi = rng.integers(-2, 3, size=(T, H)).astype(np.float32)
+    x = (xi.view(np.uint32) >> 16).astype(np.uint16)   # small integers are bf16-exact
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    w = np.tile(np.array([0.5, 0.25, 0.25][:k], np.float32), (T, 1))
+    inp = synth.MoEInputs(shape, x, synth.pack_codes(c13), synth.const_scales(E, 2 * I, H, 0x3F80),
+                          synth.pack_codes(c2), synth.const_scales(E, H, I, 0x3F80), ids, w, None)
+    return inp, xi
+
+
+def pin_closed_form_equal_codes(c=11):
+    """All codes c, unit scales: g = u = (c-8) * sum(x) =: G for every channel,
+    h = bf16(silu(G) * G), y = (c-8) * I * h, out = y (weights sum to 1)."""
+    inp, xi = _closed_form_inputs(c, c, c)
+    s = inp.shape
+    _, out = oracle.run_workload(inp)
+    got = bf16_bits_to_f64(out)
+    G = (c - 8) * xi.sum(axis=1).astype(np.float64)           # exact
+    h = rne_bf16(silu64(G) * G)
+    # silu in fp32 may round differently from fp64 by an ulp before the bf16
+    # rounding; take the fp32 value the oracle's silu gives when they disagree
+    h32 = np.array([oracle.bf16_to_f32(np.array([oracle.f32_to_bf16(
+        np.float32(oracle.silu(float(v))) * np.float32(v))]))[0] for v in G], np.float64)
+    y = (c - 8) * s.I * h32
+    want = rne_bf16(y)[:, None] * np.ones((1, s.H))
+    ok = np.array_equal(got, want) and np.max(np.abs(h - h32) / np.maximum(np.abs(h), 1e-30)) < 1e-2
+    return ok, "closed form (equal codes) mismatch"
+
+
+def pin_closed_form_gate_up_order():
+    """Gate codes 9 (w=+1), up codes 10 (w=+2), down codes 9: with S = sum(x),
+    g = S, u = 2S, h = bf16(silu(S) * 2S), y = I * h."""
+    inp, xi = _closed_form_inputs(9, 10, 9)
+    s = inp.shape
+    _, out = oracle.run_workload(inp)
+    got = bf16_bits_to_f64(out)
+    S = xi.sum(axis=1).astype(np.float64)
+    h = np.array([oracle.bf16_to_f32(np.array([oracle.f32_to_bf16(
+        np.float32(oracle.silu(float(v))) * np.float32(2 * v))]))[0] for v in S], np.float64)
+    h64 = rne_bf16(silu64(S) * 2 * S)
+    y = s.I * h
+    want = rne_bf16(y)[:, None] * np.ones((1, s.H))
+    ok = np.array_equal(got, want) and np.allclose(h, h64, rtol=1e-2)
+    return ok, "closed form (gate/up order) mismatch"
+
+
+def pin_zero_weights():
+    """All codes 8: every weight is 0, so the output is exactly 0."""
+    inp, _ = _closed_form_inputs(8, 8, 8)
+    _, out = oracle.run_workload(inp)
+    return bool(np.all(bf16_bits_to_f64(out) == 0.0)), "nonzero output with zero weights"
+
+
+def small_random_inputs(seed=0, T=12, k=3, Eg=6, El=5, H=64, I=32, bm=4, emap=True):
+    rng = np.random.default_rng(seed)
+    shape = synth.MoEShape("small", T=T, k=k, E_global=Eg, E_local=El, H=H, I=I, block_m=bm,
+                           seed=seed)
+    inp = synth.make_inputs(shape, seed=seed)
+    # a non-identity expert map: local experts are a shuffled subset
+    if emap:
+        m = np.full(Eg, -1, np.int32)
+        chosen = rng.permutation(Eg)[:El]
+        m[chosen] = np.arange(El, dtype=np.int32)
+        inp.expert_map = m
+    # scales large enough that bf16 rounding of h matters
+    inp.w13_s = synth.scales(rng, El, 2 * I, H, sigma=0.1)
+    inp.w2_s = synth.scales(rng, El, H, I, sigma=0.1)
+    return inp
+
+
+def pin_brute_force(seed=0, **kw):
+    """Oracle layer vs per-token fp64 brute force.  Pre-rounding g, u agree to
+    fp32 accumulation error; h to one bf16 ulp; the output within a tolerance
+    ten times tighter than the GPU bound."""
+    inp = small_random_inputs(seed, **kw)
+    s = inp.shape
+    lid = synth.local_ids(inp)
+    (sorted_ids, expert_ids, ntp), (out, h_rows, y_pairs) = oracle.run_workload(
+        inp, want_h=True, want_y=True)
+    got = bf16_bits_to_f64(out)
+    ok = True
+    worst = 0.0
+    for t in range(s.T):
+        ref, parts = brute_force_token(inp, t, lid)
+        for (j, e, g, u, h, y) in parts:
+            p = t * s.k + j
+            r = int(np.nonzero(sorted_ids[:ntp] == p)[0][0])
+            h_or = bf16_bits_to_f64(h_rows[r])
+            # h within one bf16 ulp (the fp32 accumulation can flip a rounding)
+            ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(h), 1e-30))[1] - 8)
+            if np.any(np.abs(h_or - h) > ulp * 1.0001):
+                ok = False
+            # y from the oracle's own h, fp64
+            W2 = dequant_f64(inp.w2_q[e], inp.w2_s[e])
+            y64 = W2 @ h_or
+            bound = 1e-5 * (np.abs(W2) @ np.abs(h_or)) + 1e-30
+            if np.any(np.abs(y_pairs[p] - y64) > bound):
+                ok = False
+        # the oracle output is the bf16 rounding of the exact value, up to fp32
+        # accumulation error
+        worst = max(worst, rounding_ratio(got[t], ref))
+    ok = ok and worst <= 1.0
+    return ok, f"brute force worst ratio {worst:.3g}"
+
+
+def pin_topk1_identity(seed=21):
+    """k = 1 with weight 1: the layer output is bf16 of that expert's MLP output."""
+    inp = small_random_inputs(seed, k=1, emap=False, El=6, Eg=6)
+    inp.topk_weights[:] = 1.0
+    s = inp.shape
+    _, out = oracle.run_workload(inp)
+    got = bf16_bits_to_f64(out)
+    ok = True
+    for t in range(s.T):
+        e = int(inp.topk_ids[t, 0])
+        W13 = dequant_f64(inp.w13_q[e], inp.w13_s[e])
+        W2 = dequant_f64(inp.w2_q[e], inp.w2_s[e])
+        x = bf16_bits_to_f64(inp.x[t])
+        h = rne_bf16(silu64(W13[:s.I] @ x) * (W13[s.I:] @ x))
+        y = W2 @ h
+        if rounding_ratio(got[t], y) > 1.0:
+            ok = False
+    return ok, "top-1 identity"
+
+
+def pin_token_permutation(seed=31):
+    """Permuting tokens permutes output rows bit-exactly."""
+    inp = small_random_inputs(seed)
+    s = inp.shape
+    _, out = oracle.run_workload(inp)
+    perm = np.random.default_rng(seed + 1).permutation(s.T)
+    inp2 = synth.MoEInputs(s, inp.x[perm], inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s,
+                           inp.topk_ids[perm], inp.topk_weights[perm], inp.expert_map)
+    _, out2 = oracle.run_workload(inp2)
+    return bool(np.array_equal(out[perm], out2)), "token permutation changed outputs"
+
+
+def pin_cross_layout(seed=41):
+    """Indexed, grouped-contiguous and grouped-masked layers agree bit-exactly on
+    the same draw (per-row outputs and token outputs)."""
+    inp = small_random_inputs(seed)
+    s = inp.shape
+    _, (out, h_rows, y_pairs) = oracle.run_workload(inp, want_h=True, want_y=True)
+    a2, m_idx, r2p = synth.grouped_contiguous_layout(inp, align=8)
+    rows_c, tok_c = oracle.moe_grouped("contiguous", a2, inp.w13_q, inp.w13_s, inp.w2_q,
+                                       inp.w2_s, m_indices=m_idx, row_to_pair=r2p,
+                                       topk_weights=inp.topk_weights, T=s.T, k=s.k)
+    a3, mm, r2p3 = synth.grouped_masked_layout(inp)
+    rows_m, tok_m = oracle.moe_grouped("masked", a3, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s,
+                                       masked_m=mm, row_to_pair=r2p3,
+                                       topk_weights=inp.topk_weights, T=s.T, k=s.k)
+    ok = np.array_equal(tok_c, out) and np.array_equal(tok_m, out)
+    valid = r2p >= 0
+    ok &= np.array_equal(rows_c[valid], f64_to_bf16_bits(rne_bf16(y_pairs[r2p[valid]])))
+    v3 = r2p3 >= 0
+    ok &= np.array_equal(rows_m[v3], f64_to_bf16_bits(rne_bf16(y_pairs[r2p3[v3]])))
+    return bool(ok), "layouts disagree"
+
+
+def check_align(topk_ids, E_global, expert_map, E_local, bm, sorted_ids, expert_ids, ntp):
+    """Routing invariants of the aligned layout.  Returns a list of failures."""
+    T, k = topk_ids.shape
+    P = T * k
+    sent = P
+    fails = []
+    flat = topk_ids.reshape(-1)
+    lid = np.full(P, -1)
+    for p in range(P):
+        g = int(flat[p])
+        if 0 <= g < E_global:
+            l = g if expert_map is None else int(expert_map[g])
+            if 0 <= l < E_local:
+                lid[p] = l
+    counts = np.bincount(lid[lid >= 0], minlength=E_local)
+    want_ntp = int(sum(-(-c // bm) * bm for c in counts))
+    if ntp != want_ntp:
+        fails.append(f"ntp {ntp} != {want_ntp}")
+    cap = sorted_ids.size
+    if ntp > cap or ntp % bm:
+        fails.append("ntp beyond capacity or not a block multiple")
+        return fails
+    body = sorted_ids[:ntp]
+    real = body[body != sent]
+    if not np.array_equal(np.sort(real), np.nonzero(lid >= 0)[0]):
+        fails.append("local pairs are not each present exactly once")
+    if np.any(sorted_ids[ntp:] != sent):
+        fails.append("tail is not the sentinel")
+    if np.any((body < 0) | (body > sent)):
+        fails.append("out-of-range pair id")
+    nb = ntp // bm
+    if np.any(expert_ids[nb:] != -1):
+        fails.append("expert_ids tail is not -1")
+    eb = expert_ids[:nb]
+    if nb and (np.any(np.diff(eb) < 0) or eb.min() < 0 or eb.max() >= E_local):
+        fails.append("expert_ids not ascending / in range")
+    pos = 0
+    for e in range(E_local):
+        c = counts[e]
+        if c == 0:
+            if np.any(eb == e):
+                fails.append(f"empty expert {e} has a block")
+            continue
+        seg = -(-c // bm) * bm
+        blk = eb[pos // bm:(pos + seg) // bm]
+        if blk.size != seg // bm or np.any(blk != e):
+            fails.append(f"expert {e} blocks wrong")
+        part = sorted_ids[pos:pos + seg]
+        want = np.nonzero(lid == e)[0]
+        if not np.array_equal(part[:c], want):
+            fails.append(f"expert {e} pairs not ascending")
+        if np.any(part[c:] != sent):
+            fails.append(f"expert {e} padding not sentinel")
+        pos += seg
+    return fails
+
+
+def pin_align_invariants(seed=0, n=40):
+    rng = np.random.default_rng(seed)
+    for it in range(n):
+        T = int(rng.integers(0, 40))
+        k = int(rng.integers(1, 5))
+        Eg = int(rng.integers(k, 20))
+        El = int(rng.integers(1, Eg + 1))
+        bm = int(rng.choice([1, 2, 4, 8, 16]))
+        ids = np.stack([rng.permutation(Eg)[:k] for _ in range(T)]).astype(np.int32) \
+            if T else np.zeros((0, k), np.int32)
+        emap = None
+        if rng.random() < 0.6:
+            emap = np.full(Eg, -1, np.int32)
+            emap[rng.permutation(Eg)[:El]] = np.arange(El, dtype=np.int32)
+        else:
+            El = Eg
+        si, ei, ntp = oracle.moe_align(ids, Eg, emap, El, bm)
+        f = check_align(ids, Eg, emap, El, bm, si, ei, ntp)
+        if f:
+            return False, f"draw {it}: {f[:3]}"
+        # token permutation: pair sets per expert follow the relabelling
+        if T > 1:
+            perm = rng.permutation(T)
+            si2, ei2, ntp2 = oracle.moe_align(ids[perm], Eg, emap, El, bm)
+            if ntp2 != ntp or not np.array_equal(ei2, ei):
+                return False, "token permutation changed the block structure"
+            body = si[:ntp]
+            body2 = si2[:ntp]
+            real2 = body2[body2 != T * k]
+            # new token i is old token perm[i]
+            relabel = perm[real2 // k] * k + real2 % k
+            if not np.array_equal(np.sort(relabel), np.sort(body[body != T * k])):
+                return False, "token permutation changed the pair set"
+    return True, ""
+
+
+def pin_silu():
+    """silu(0) = 0; fp32 silu within 4 fp32 ulps of the fp64 definition over
+    a wide range; silu(v) -> v for large v and -> 0 for very negative v."""
+    if oracle.silu(0.0) != 0.0:
+        return False, "silu(0) != 0"
+    vs = np.concatenate([np.linspace(-30, 30, 2001), [-1e-3, 1e-3, 0.5, -0.5, 80.0, -80.0]])
+    worst = 0.0
+    for v in vs:
+        v32 = float(np.float32(v))
+        got = oracle.silu(v32)
+        want = float(silu64(v32))
+        ulp = np.spacing(np.float32(abs(want))) if want != 0 else np.float32(1e-45)
+        worst = max(worst, abs(got - want) / float(ulp))
+    if abs(oracle.silu(50.0) - 50.0) > 1e-5 or abs(oracle.silu(-50.0)) > 1e-18:
+        return False, "silu tails"
+    return worst <= 4.0, f"silu worst {worst:.2f} ulp"
+
+
+ALL_PINS = {
+    "silu": pin_silu,
+    "dequant_exhaustive": pin_dequant_exhaustive,
+    "dequant_zero_code": pin_dequant_zero_code,
+    "one_hot_structure": pin_one_hot_structure,
+    "down_one_hot": pin_down_one_hot,
+    "closed_form_equal_codes": pin_closed_form_equal_codes,
+    "closed_form_gate_up_order": pin_closed_form_gate_up_order,
+    "zero_weights": pin_zero_weights,
+    "brute_force": pin_brute_force,
+    "topk1_identity": pin_topk1_identity,
+    "token_permutation": pin_token_permutation,
+    "cross_layout": pin_cross_layout,
+    "align_invariants": pin_align_invariants,
+}
