@@ -1,0 +1,255 @@
+/*
+ * chord.h -- C ABI of the GB300 (sm_103a) W4A16 INT4 Mixture-of-Experts library.
+ *
+ * The operation (page: "vLLM x Novita AI: Chord W4A16 INT4 MoE kernels for
+ * Kimi K2.x", novita.ai; sections TL;DR, "Two kernel families", "vLLM
+ * integration", "Kernel optimisation", Fig. 3):
+ *   BF16 activations x unsigned INT4 weight codes with one BF16 scale per 32
+ *   input channels, dequantised as w = (q - 8) * scale (subtract, then scale,
+ *   one bf16 rounding).  Per routed (token, slot) pair of a local expert e:
+ *     g = W13_e[0:I] x,  u = W13_e[I:2I] x          (gate/up GEMM, fp32 accum)
+ *     h = bf16(silu(g) * u)                          (fused epilogue)
+ *     y = W2_e h                                     (down GEMM, fp32 accum)
+ *   and per token: out = bf16(sum over its local slots of weight * y).
+ *
+ * Storage conventions shared by every entry point:
+ *   bf16 values are passed as uint16_t bit patterns;
+ *   weight codes: int32 words, 8 codes per word along K, element c = 8w+i in
+ *     bits [4i, 4i+4) (low nibble first); W13 codes [E_local, 2I, H/8] (rows
+ *     0..I-1 gate, I..2I-1 up), W2 codes [E_local, H, I/8];
+ *   scales: bf16 [E_local, 2I, H/32] and [E_local, H, I/32];
+ *   all matrices row-major and densely packed.
+ *
+ * Ownership and execution:
+ *   every pointer argument marked "device" must point to device memory that the
+ *   caller allocated and keeps alive until the work on `stream` completes;
+ *   `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Calls enqueue work on the stream and return without waiting,
+ *   except where CHORD_FLAG_VALIDATE is set.  No call allocates device memory:
+ *   scratch lives in a caller-provided workspace whose size the *_workspace_size
+ *   queries return.  Without CHORD_FLAG_VALIDATE no call copies anything back
+ *   to the host, so a sequence of calls can be captured in a CUDA graph.
+ *
+ * Errors: each call returns a chord_status.  Argument, shape and capacity
+ * checks happen on the host before anything is launched; nothing is launched
+ * when they fail.  Faults the device detects (a routing id out of range, a
+ * bounded wait that expired) set bits in a device error word inside the
+ * workspace; chord_get_device_error() reads it.  There is no CPU fallback and
+ * no silent alternative path: an unsupported case is an error.
+ */
+#ifndef CHORD_W4A16_H
+#define CHORD_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CHORD_OK = 0,
+    CHORD_ERR_INVALID_ARG = -1,       /* null pointer, negative size, bad flag or mode */
+    CHORD_ERR_UNSUPPORTED_SHAPE = -2, /* a size the kernels do not handle (see each call) */
+    CHORD_ERR_CAPACITY = -3,          /* routing buffers smaller than the required capacity */
+    CHORD_ERR_LAYOUT_MODE = -4,       /* grouped mode / layout combination not allowed */
+    CHORD_ERR_CUDA = -5,              /* a CUDA runtime call or launch failed */
+    CHORD_ERR_TIMEOUT = -6,           /* a device-side bounded wait expired (validate / query) */
+    CHORD_ERR_ROUTING = -7,           /* device found invalid routing data (validate / query) */
+    CHORD_ERR_WORKSPACE = -8,         /* workspace missing, misaligned or too small */
+    CHORD_ERR_NO_DEVICE = -9          /* no sm_103a device is current */
+} chord_status;
+
+/* grouped layouts (page: "grouped SM90 kernels", Fig. 3) */
+#define CHORD_GROUPED_CONTIGUOUS 0
+#define CHORD_GROUPED_MASKED 1
+
+/* flags */
+#define CHORD_FLAG_VALIDATE 1      /* synchronise the stream after the call and turn the
+                                      device error word into the status (not capturable) */
+#define CHORD_FLAG_DETERMINISTIC 2 /* per-pair fp32 down outputs + ordered combine instead of
+                                      fp32 reductions into the token rows */
+
+/* bits of the device error word */
+#define CHORD_DEVERR_TIMEOUT 1
+#define CHORD_DEVERR_ROUTING 2
+#define CHORD_DEVERR_CAPACITY 4
+
+/* Human-readable name of a status. */
+const char* chord_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int chord_version(void);
+
+/* ------------------------------------------------------------------------- */
+/* Host-side queries (pure functions of their arguments)                      */
+/* ------------------------------------------------------------------------- */
+
+/* Capacity of the aligned routing buffers (page: "vLLM integration": the
+ * moe_align_block_size buffers are over-allocated): the worst case of
+ * sum_e ceil(c_e / block_m) * block_m over any routing of T*k pairs, i.e.
+ * T*k + E_local*(block_m-1) rounded up to a multiple of block_m.
+ * sorted_ids has `capacity` entries, expert_ids capacity/block_m.
+ * Returns -1 for non-positive block_m or negative sizes. */
+int64_t chord_moe_align_capacity(int64_t T, int k, int E_local, int block_m);
+
+/* Padding granularity to use for the indexed path (page: "Kernel optimisation",
+ * block-M selection by routed tokens per expert).  Here the token tile of the
+ * tensor-core MMA is chosen per expert segment at run time, so block_m only
+ * sets padding; it is 16, the MMA's N granularity, for every shape. */
+int chord_select_block_m(int64_t T, int k, int E_global, int E_local, int H, int I);
+
+/* Writes a one-line description of the schedule the indexed path picks for a
+ * shape (token tile, pipeline, combine form) into buf; returns its length. */
+int chord_describe_schedule(int64_t T, int k, int E_global, int E_local, int H, int I, int flags,
+                            char* buf, size_t buf_len);
+
+/* Workspace bytes for chord_moe_align. */
+size_t chord_moe_align_workspace_size(int64_t T, int k, int E_local);
+
+/* Workspace bytes for chord_w4a16_moe_indexed with these sizes and flags. */
+size_t chord_w4a16_moe_workspace_size(int64_t T, int k, int E_global, int E_local, int H, int I,
+                                      int block_m, int64_t capacity, int flags);
+
+/* Workspace bytes for chord_w4a16_moe_grouped. M = rows of the grouped input
+ * (contiguous: m; masked: E_local*max_m); T, k only matter with out_tokens. */
+size_t chord_w4a16_grouped_workspace_size(int mode, int64_t M, int H, int I, int E_local,
+                                          int64_t T, int k, int with_tokens, int expected_m);
+
+/* ------------------------------------------------------------------------- */
+/* moe_align: routing -> indexed layout                                       */
+/* ------------------------------------------------------------------------- */
+/*
+ * Groups the (token, slot) pairs routed to local experts by expert (page:
+ * "Two kernel families": the indexed family consumes vLLM's sorted_ids /
+ * expert_ids / num_tokens_padded; Fig. 3: activations are not padded, the
+ * padding lives in the index as a sentinel).  Result, fully defined over the
+ * whole capacity so that it compares bit-exactly:
+ *   experts in ascending local id; inside an expert the pair ids p = t*k + j in
+ *   ascending order; each expert padded to a multiple of block_m with the
+ *   sentinel T*k; experts without pairs get no block; sorted_ids[ntp..cap) =
+ *   T*k and expert_ids[ntp/block_m..cap/block_m) = -1, where ntp =
+ *   *num_tokens_padded = sum_e ceil(c_e/block_m)*block_m.
+ *
+ *   topk_ids     device int32 [T, k]   global expert ids
+ *   expert_map   device int32 [E_global] or NULL; local id of each global id,
+ *                -1 for experts held elsewhere (NULL: identity, E_local ==
+ *                E_global).  Pairs whose expert is not local are dropped; an id
+ *                outside [0, E_global) is dropped and sets CHORD_DEVERR_ROUTING.
+ *   sorted_ids   device int32 [capacity]         (output)
+ *   expert_ids   device int32 [capacity/block_m] (output)
+ *   num_tokens_padded device int32 [1]           (output)
+ *   capacity     entries of sorted_ids; must be >= chord_moe_align_capacity().
+ *   workspace    device, >= chord_moe_align_workspace_size() bytes, 256-aligned.
+ * Limits: 1 <= k <= 32, 1 <= E_local <= 1024, 1 <= block_m <= 256,
+ *   T*k < 2^31.  T = 0 is allowed (everything becomes padding/tail).
+ */
+chord_status chord_moe_align(const int32_t* topk_ids, int64_t T, int k, int E_global,
+                             const int32_t* expert_map, int E_local, int block_m,
+                             int32_t* sorted_ids, int32_t* expert_ids,
+                             int32_t* num_tokens_padded, int64_t capacity, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* the MoE layer on the indexed layout                                        */
+/* ------------------------------------------------------------------------- */
+/*
+ * out[T, H] = the layer above, reading the pairs from the aligned layout
+ * (page: "Two kernel families": the indexed path; "vLLM integration": the
+ * over-allocated buffers are consumed without reading counts back to the
+ * host, so the call is CUDA-graph capturable).
+ *
+ *   x            device bf16 [T, H]
+ *   E_global     experts the router chose from; with T*k it gives the expected
+ *                rows per local expert that steers the schedule (must match the
+ *                value given to chord_w4a16_moe_workspace_size)
+ *   w13_q, w13_s, w2_q, w2_s  device weights as in the header comment
+ *   topk_weights device float [T, k]; weight of pair p = t*k+j is topk_weights[p]
+ *   sorted_ids, expert_ids, num_tokens_padded  device, the chord_moe_align
+ *                layout (any producer of the same layout works)
+ *   capacity, block_m  the sizes the layout was built with
+ *   workspace    device, >= chord_w4a16_moe_workspace_size() bytes, 256-aligned
+ *   out          device bf16 [T, H] (output; every element written)
+ *   h_out        device bf16 [capacity, I] or NULL: when given, the gate/up
+ *                stage writes its output h = bf16(silu(g) * u) here (rows
+ *                < num_tokens_padded; sentinel rows get 0) instead of into the
+ *                workspace, so a caller can inspect or reuse it
+ *   flags        CHORD_FLAG_* ; CHORD_FLAG_DETERMINISTIC gives run-to-run
+ *                bit-identical outputs (slots summed in a fixed order)
+ * Limits (CHORD_ERR_UNSUPPORTED_SHAPE otherwise): H % 256 == 0, I % 128 == 0,
+ *   1 <= k <= 32, E_local >= 1, T*k < 2^31, block_m in [1, 256].
+ */
+chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I, int E_global,
+                                     int E_local, int k, const int32_t* w13_q,
+                                     const uint16_t* w13_s, const int32_t* w2_q,
+                                     const uint16_t* w2_s, const float* topk_weights,
+                                     const int32_t* sorted_ids, const int32_t* expert_ids,
+                                     const int32_t* num_tokens_padded, int64_t capacity,
+                                     int block_m, void* workspace, size_t workspace_bytes,
+                                     uint16_t* out, uint16_t* h_out, int flags, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* the MoE layer on a grouped layout                                          */
+/* ------------------------------------------------------------------------- */
+/*
+ * Same expert MLP on the grouped layouts (page: "grouped SM90 kernels",
+ * Fig. 3, and the grouped operator entry points contiguous(a2, w, m_indices)
+ * / masked(a3, w, masked_m, expected_m)).
+ *
+ * mode CHORD_GROUPED_CONTIGUOUS: a is [M, H]; row r belongs to expert
+ *   m_indices[r], or is padding when m_indices[r] < 0.  Each expert's rows are
+ *   contiguous and start on a multiple of 16 rows (the page pads each expert
+ *   to 128); M % 16 == 0.  masked_m must be NULL.
+ * mode CHORD_GROUPED_MASKED: a is [E_local, max_m, H] (M = E_local*max_m);
+ *   rows e*max_m + i with i < masked_m[e] are valid, the rest are never read.
+ *   expected_m (> 0) is the host-side launch hint (expected valid rows per
+ *   expert); masked_m (device int32 [E_local]) is authoritative.  m_indices
+ *   must be NULL.
+ *
+ *   out_rows     device bf16 [M, H]: bf16(y) for every valid row.  Rows that
+ *                are padding (contiguous) or past masked_m (masked) carry no
+ *                result; consumers ignore them, as on the page.
+ *   row_to_pair, topk_weights, out_tokens: optional token combine.  When
+ *                out_tokens is not NULL, row_to_pair (device int32 [M], pair id
+ *                t*k+j of each valid row or -1) and topk_weights (device float
+ *                [T, k]) are required and out_tokens (device bf16 [T, H]) gets
+ *                the same combine as the indexed layer.
+ *   h_out        device bf16 [M, I] or NULL: the gate/up output of every row
+ *                the call computes (as for the indexed call).
+ * Limits as for the indexed call, plus max_m >= 1.
+ */
+chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int H, int I,
+                                     int E_local, const int32_t* m_indices,
+                                     const int32_t* masked_m, int64_t max_m, int expected_m,
+                                     const int32_t* w13_q, const uint16_t* w13_s,
+                                     const int32_t* w2_q, const uint16_t* w2_s,
+                                     const int32_t* row_to_pair, const float* topk_weights,
+                                     int64_t T, int k, void* workspace, size_t workspace_bytes,
+                                     uint16_t* out_rows, uint16_t* out_tokens, uint16_t* h_out,
+                                     int flags, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* device error word                                                          */
+/* ------------------------------------------------------------------------- */
+/* Synchronises `stream`, copies the error word of `workspace` (of a layer or
+ * align call) to *error_bits, clears it when `clear` is non-zero, and returns
+ * CHORD_ERR_TIMEOUT / CHORD_ERR_ROUTING / CHORD_ERR_CAPACITY for the first bit
+ * set, else CHORD_OK.  Not capturable. */
+chord_status chord_get_device_error(void* workspace, int* error_bits, int clear, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* stage timing (profiling aid)                                               */
+/* ------------------------------------------------------------------------- */
+/* When enabled, each indexed / grouped layer call records CUDA events around
+ * its stages (prepare, gate_up, down, combine) on its stream.  read() waits for
+ * the recorded events and returns the summed milliseconds per stage over all
+ * calls since enable, and the number of calls.  Stage events are skipped while
+ * a stream is being captured. */
+chord_status chord_stage_timing_enable(int enable);
+chord_status chord_stage_timing_read(float* ms_per_stage /* [4] */, int* calls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CHORD_W4A16_H */

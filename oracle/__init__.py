@@ -84,8 +84,14 @@ def _load():
         lib.oracle_expert_mlp.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, vp, vp, vp]
         lib.oracle_expert_mlp.restype = i32
         lib.oracle_moe_indexed.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
-                                           vp, vp, vp, i64, i64, vp, vp, vp]
+                                           vp, vp, vp, i64, i64, vp, vp, vp, vp, vp]
         lib.oracle_moe_indexed.restype = i32
+        lib.oracle_moe_indexed_down.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
+                                                vp, i64, i64, vp]
+        lib.oracle_moe_indexed_down.restype = i32
+        lib.oracle_moe_grouped_down.argtypes = [i32, vp, i64, i64, i64, i64, vp, vp, i64, vp, vp,
+                                                vp, vp, i64, i64, vp, vp]
+        lib.oracle_moe_grouped_down.restype = i32
         lib.oracle_moe_grouped.argtypes = [i32, vp, i64, i64, i64, i64, vp, vp, i64, vp, vp,
                                            vp, vp, vp, vp, i64, i64, vp, vp, vp, vp]
         lib.oracle_moe_grouped.restype = i32
@@ -193,8 +199,9 @@ def expert_mlp(w13_q, w13_s, w2_q, w2_s, e, x_rows):
 
 
 def moe_indexed(x, w13_q, w13_s, w2_q, w2_s, topk_weights, sorted_ids, expert_ids, ntp,
-                block_m, k, want_h=False, want_y=False):
-    """Whole layer on the indexed layout.  Returns out bits [T, H] (and h, y)."""
+                block_m, k, want_h=False, want_y=False, want_gu=False):
+    """Whole layer on the indexed layout.  Returns out bits [T, H] (and h, y,
+    and the pre-rounding gate/up values g, u [capacity, I] when asked)."""
     x = _c(x, np.uint16)
     T, H = x.shape
     E = w13_q.shape[0]
@@ -209,14 +216,59 @@ def moe_indexed(x, w13_q, w13_s, w2_q, w2_s, topk_weights, sorted_ids, expert_id
     out = np.empty((T, H), np.uint16)
     h = np.empty((cap, I), np.uint16) if want_h else None
     y = np.empty((T * k, H), np.float32) if want_y else None
+    g = np.empty((cap, I), np.float32) if want_gu else None
+    u = np.empty((cap, I), np.float32) if want_gu else None
     rc = _load().oracle_moe_indexed(_p(x), T, H, I, E, k, _p(w13_q), _p(w13_s), _p(w2_q),
                                     _p(w2_s), _p(tw), _p(sorted_ids), _p(expert_ids),
-                                    _p(ntp_a), cap, block_m, _p(out), _p(h), _p(y))
+                                    _p(ntp_a), cap, block_m, _p(out), _p(h), _p(y), _p(g), _p(u))
     if rc != 0:
         raise ValueError("oracle_moe_indexed failed")
+    if want_gu:
+        return out, h, y, g, u
     if want_h or want_y:
         return out, h, y
     return out
+
+
+def moe_indexed_down(h_rows, w2_q, w2_s, topk_weights, sorted_ids, expert_ids, ntp, block_m,
+                     T, k):
+    """Down GEMM + combine of the indexed layer on given bf16 rows h_rows
+    [capacity, I].  Returns out bits [T, H]."""
+    h_rows = _c(h_rows, np.uint16)
+    E, H = w2_q.shape[0], w2_q.shape[1]
+    I = w2_q.shape[2] * 8
+    w2_q, w2_s = _c(w2_q, np.int32), _c(w2_s, np.uint16)
+    tw = _c(topk_weights, np.float32)
+    sorted_ids = _c(sorted_ids, np.int32)
+    expert_ids = _c(expert_ids, np.int32)
+    ntp_a = np.array([ntp], dtype=np.int32)
+    out = np.empty((T, H), np.uint16)
+    rc = _load().oracle_moe_indexed_down(_p(h_rows), T, H, I, E, k, _p(w2_q), _p(w2_s), _p(tw),
+                                         _p(sorted_ids), _p(expert_ids), _p(ntp_a),
+                                         sorted_ids.size, block_m, _p(out))
+    if rc != 0:
+        raise ValueError("oracle_moe_indexed_down failed")
+    return out
+
+
+def moe_grouped_down(mode, h_rows, w2_q, w2_s, m_indices=None, masked_m=None, max_m=0,
+                     row_to_pair=None, topk_weights=None, T=0, k=0):
+    """Down GEMM + outputs of the grouped layer on given rows h_rows [M, I]."""
+    m = {"contiguous": 0, "masked": 1}[mode]
+    h_rows = _c(h_rows, np.uint16)
+    M, I = h_rows.shape
+    E, H = w2_q.shape[0], w2_q.shape[1]
+    w2_q, w2_s = _c(w2_q, np.int32), _c(w2_s, np.uint16)
+    mi, mm = _c(m_indices, np.int32), _c(masked_m, np.int32)
+    r2p, tw = _c(row_to_pair, np.int32), _c(topk_weights, np.float32)
+    out_rows = np.empty((M, H), np.uint16)
+    out_tok = np.empty((T, H), np.uint16) if r2p is not None else None
+    rc = _load().oracle_moe_grouped_down(m, _p(h_rows), M, H, I, E, _p(mi), _p(mm), max_m,
+                                         _p(w2_q), _p(w2_s), _p(r2p), _p(tw), T, k,
+                                         _p(out_rows), _p(out_tok))
+    if rc != 0:
+        raise ValueError("oracle_moe_grouped_down failed")
+    return (out_rows, out_tok) if out_tok is not None else out_rows
 
 
 def moe_grouped(mode, a, w13_q, w13_s, w2_q, w2_s, m_indices=None, masked_m=None,
@@ -262,12 +314,13 @@ def moe_grouped(mode, a, w13_q, w13_s, w2_q, w2_s, m_indices=None, masked_m=None
     return res[0] if len(res) == 1 else tuple(res)
 
 
-def run_workload(inp, block_m=None, want_h=False, want_y=False):
+def run_workload(inp, block_m=None, want_h=False, want_y=False, want_gu=False):
     """Align + indexed layer for a synth.MoEInputs draw."""
     s = inp.shape
     bm = s.block_m if block_m is None else block_m
     sorted_ids, expert_ids, ntp = moe_align(inp.topk_ids, s.E_global, inp.expert_map,
                                             s.E_local, bm)
     res = moe_indexed(inp.x, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, inp.topk_weights,
-                      sorted_ids, expert_ids, ntp, bm, s.k, want_h=want_h, want_y=want_y)
+                      sorted_ids, expert_ids, ntp, bm, s.k, want_h=want_h, want_y=want_y,
+                      want_gu=want_gu)
     return (sorted_ids, expert_ids, ntp), res

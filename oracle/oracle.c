@@ -443,7 +443,8 @@ int oracle_moe_indexed(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64
                        const int32_t* w2_q, const uint16_t* w2_s, const float* topk_weights,
                        const int32_t* sorted_ids, const int32_t* expert_ids,
                        const int32_t* num_tokens_padded, int64_t capacity, int64_t block_m,
-                       uint16_t* out, uint16_t* h_rows, float* y_pairs_out)
+                       uint16_t* out, uint16_t* h_rows, float* y_pairs_out, float* g_rows,
+                       float* u_rows)
 {
     const int64_t P = T * k;
     const int64_t ntp = num_tokens_padded[0];
@@ -460,6 +461,10 @@ int oracle_moe_indexed(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64
     }
     if (h_rows)
         memset(h_rows, 0, sizeof(uint16_t) * (size_t)(capacity * I));
+    if (g_rows)
+        memset(g_rows, 0, sizeof(float) * (size_t)(capacity * I));
+    if (u_rows)
+        memset(u_rows, 0, sizeof(float) * (size_t)(capacity * I));
     for (int64_t e = 0; e < E_local && rc == 0; ++e) {
         int64_t n = 0;
         for (int64_t r = 0; r < ntp; ++r) {
@@ -489,6 +494,10 @@ int oracle_moe_indexed(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64
                 memcpy(y_pairs + p * H, y + i * H, sizeof(float) * (size_t)H);
                 if (h_rows)
                     memcpy(h_rows + r * I, h + i * I, sizeof(uint16_t) * (size_t)I);
+                if (g_rows)
+                    memcpy(g_rows + r * I, g + i * I, sizeof(float) * (size_t)I);
+                if (u_rows)
+                    memcpy(u_rows + r * I, u + i * I, sizeof(float) * (size_t)I);
             }
         }
         free(g);
@@ -506,6 +515,141 @@ done:
     free(is_local);
     free(rows_of);
     free(xrows);
+    return rc;
+}
+
+/*
+ * The second half of the indexed layer on given intermediate rows: for each
+ * padded row r < num_tokens_padded with pair p = sorted_ids[r] (not the
+ * sentinel), y_p = W2_e h_rows[r] (e = expert_ids[r / block_m]), then the
+ * combine.  Checks a down GEMM + combine against the same intermediate that a
+ * gate/up implementation produced (the bf16 rounding of h is a decision two
+ * fp32 implementations may take differently).
+ */
+int oracle_moe_indexed_down(const uint16_t* h_rows, int64_t T, int64_t H, int64_t I,
+                            int64_t E_local, int64_t k, const int32_t* w2_q, const uint16_t* w2_s,
+                            const float* topk_weights, const int32_t* sorted_ids,
+                            const int32_t* expert_ids, const int32_t* num_tokens_padded,
+                            int64_t capacity, int64_t block_m, uint16_t* out)
+{
+    const int64_t P = T * k;
+    const int64_t ntp = num_tokens_padded[0];
+    if (ntp < 0 || ntp > capacity || block_m <= 0)
+        return -1;
+    float* y_pairs = (float*)calloc((size_t)(P > 0 ? P : 1) * (size_t)H, sizeof(float));
+    uint8_t* is_local = (uint8_t*)calloc((size_t)(P > 0 ? P : 1), 1);
+    int64_t* rows_of = (int64_t*)malloc(sizeof(int64_t) * (size_t)(ntp > 0 ? ntp : 1));
+    uint16_t* hbuf = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)((ntp > 0 ? ntp : 1) * I));
+    float* W2 = (float*)malloc(sizeof(float) * (size_t)(H * I));
+    float* y = (float*)malloc(sizeof(float) * (size_t)((ntp > 0 ? ntp : 1) * H));
+    int rc = 0;
+    if (!y_pairs || !is_local || !rows_of || !hbuf || !W2 || !y) {
+        rc = -1;
+        goto done;
+    }
+    for (int64_t e = 0; e < E_local; ++e) {
+        int64_t n = 0;
+        for (int64_t r = 0; r < ntp; ++r) {
+            int32_t p = sorted_ids[r];
+            if (p < 0 || p >= P || expert_ids[r / block_m] != e)
+                continue;
+            rows_of[n] = r;
+            memcpy(hbuf + n * I, h_rows + r * I, sizeof(uint16_t) * (size_t)I);
+            ++n;
+        }
+        if (n == 0)
+            continue;
+        oracle_dequant(w2_q + e * H * (I / 8), w2_s + e * H * (I / 32), H, I, W2);
+        mlp_ctx m = {NULL, W2, H, I, n, NULL, NULL, NULL, hbuf, y};
+        parallel_for(H, mlp_down, &m);
+        for (int64_t i = 0; i < n; ++i) {
+            int64_t p = sorted_ids[rows_of[i]];
+            is_local[p] = 1;
+            memcpy(y_pairs + p * H, y + i * H, sizeof(float) * (size_t)H);
+        }
+    }
+    combine(y_pairs, is_local, topk_weights, T, k, H, out);
+done:
+    free(y_pairs);
+    free(is_local);
+    free(rows_of);
+    free(hbuf);
+    free(W2);
+    free(y);
+    return rc;
+}
+
+/* Down GEMM + outputs of the grouped layer on given intermediate rows h_rows [M, I]. */
+int oracle_moe_grouped_down(int mode, const uint16_t* h_rows, int64_t M, int64_t H, int64_t I,
+                            int64_t E_local, const int32_t* m_indices, const int32_t* masked_m,
+                            int64_t max_m, const int32_t* w2_q, const uint16_t* w2_s,
+                            const int32_t* row_to_pair, const float* topk_weights, int64_t T,
+                            int64_t k, uint16_t* out_rows, uint16_t* out_tokens)
+{
+    if ((mode != 0 && mode != 1) || (mode == 1 && M != E_local * max_m))
+        return -1;
+    float* yall = (float*)calloc((size_t)(M > 0 ? M : 1) * (size_t)H, sizeof(float));
+    int64_t* rows_of = (int64_t*)malloc(sizeof(int64_t) * (size_t)(M > 0 ? M : 1));
+    uint16_t* hbuf = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)((M > 0 ? M : 1) * I));
+    float* W2 = (float*)malloc(sizeof(float) * (size_t)(H * I));
+    float* y = (float*)malloc(sizeof(float) * (size_t)((M > 0 ? M : 1) * H));
+    int rc = 0;
+    if (!yall || !rows_of || !hbuf || !W2 || !y) {
+        rc = -1;
+        goto done;
+    }
+    for (int64_t r = 0; r < M * H; ++r)
+        out_rows[r] = 0;
+    for (int64_t e = 0; e < E_local; ++e) {
+        int64_t n = 0;
+        for (int64_t r = 0; r < M; ++r) {
+            int valid = (mode == 0) ? (m_indices[r] == e)
+                                    : ((r / max_m == e) && (r % max_m) < masked_m[e]);
+            if (!valid)
+                continue;
+            rows_of[n] = r;
+            memcpy(hbuf + n * I, h_rows + r * I, sizeof(uint16_t) * (size_t)I);
+            ++n;
+        }
+        if (n == 0)
+            continue;
+        oracle_dequant(w2_q + e * H * (I / 8), w2_s + e * H * (I / 32), H, I, W2);
+        mlp_ctx m = {NULL, W2, H, I, n, NULL, NULL, NULL, hbuf, y};
+        parallel_for(H, mlp_down, &m);
+        for (int64_t i = 0; i < n; ++i) {
+            int64_t r = rows_of[i];
+            for (int64_t c = 0; c < H; ++c)
+                out_rows[r * H + c] = oracle_f32_to_bf16(y[i * H + c]);
+            memcpy(yall + r * H, y + i * H, sizeof(float) * (size_t)H);
+        }
+    }
+    if (out_tokens && row_to_pair && topk_weights) {
+        const int64_t P = T * k;
+        float* y_pairs = (float*)calloc((size_t)(P > 0 ? P : 1) * (size_t)H, sizeof(float));
+        uint8_t* is_local = (uint8_t*)calloc((size_t)(P > 0 ? P : 1), 1);
+        if (!y_pairs || !is_local) {
+            rc = -1;
+        } else {
+            for (int64_t r = 0; r < M; ++r) {
+                int valid = (mode == 0) ? (m_indices[r] >= 0)
+                                        : ((r % max_m) < masked_m[r / max_m]);
+                int64_t p = row_to_pair[r];
+                if (!valid || p < 0 || p >= P)
+                    continue;
+                is_local[p] = 1;
+                memcpy(y_pairs + p * H, yall + r * H, sizeof(float) * (size_t)H);
+            }
+            combine(y_pairs, is_local, topk_weights, T, k, H, out_tokens);
+        }
+        free(y_pairs);
+        free(is_local);
+    }
+done:
+    free(yall);
+    free(rows_of);
+    free(hbuf);
+    free(W2);
+    free(y);
     return rc;
 }
 

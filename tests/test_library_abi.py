@@ -1,0 +1,116 @@
+"""The C-ABI library: builds, loads, exports every symbol include/chord.h
+declares, and its host-side checks reject bad arguments before any launch
+(no GPU needed for any of this)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "chord.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a16_int4_mixture_gb300 import _binding, _build
+    _build.build()
+    return _binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(chord_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for need in ("chord_moe_align", "chord_w4a16_moe_indexed", "chord_w4a16_moe_grouped",
+                 "chord_moe_align_capacity", "chord_select_block_m",
+                 "chord_w4a16_moe_workspace_size", "chord_get_device_error"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from w4a16_int4_mixture_gb300 import _binding
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} missing from the library"
+        assert name in _binding.SIGNATURES, f"{name} has no binding signature"
+
+
+def test_capacity_and_block_m(lib):
+    assert lib.chord_moe_align_capacity(512, 8, 48, 16) == 4816
+    assert lib.chord_moe_align_capacity(16, 2, 8, 16) == 160
+    assert lib.chord_moe_align_capacity(0, 8, 4, 16) == 64
+    assert lib.chord_moe_align_capacity(3, 2, 3, 2) == 10
+    assert lib.chord_moe_align_capacity(3, 2, 3, 0) == -1
+    assert lib.chord_select_block_m(512, 8, 384, 48, 7168, 2048) == 16
+
+
+def test_schedule_selection_by_rows_per_expert():
+    import w4a16_int4_mixture_gb300 as m
+    assert "decode-tile32" in m.describe_schedule(512, 8, 384, 48, 7168, 2048)
+    assert "prefill-tile256" in m.describe_schedule(8192, 8, 384, 48, 7168, 2048)
+    assert "decode-tile64" in m.describe_schedule(2048, 8, 384, 384, 7168, 256)
+    assert "ordered-pairs" in m.describe_schedule(512, 8, 384, 48, 7168, 2048, 2)
+    assert "fp32-reduce" in m.describe_schedule(512, 8, 384, 48, 7168, 2048, 0)
+    assert "ordered-pairs" in m.describe_schedule(8192, 8, 384, 48, 7168, 2048, 0)
+
+
+def test_workspace_sizes_are_positive_and_monotone(lib):
+    a = lib.chord_w4a16_moe_workspace_size(512, 8, 384, 48, 7168, 2048, 16, 4816, 0)
+    b = lib.chord_w4a16_moe_workspace_size(1024, 8, 384, 48, 7168, 2048, 16, 9616, 0)
+    assert 0 < a < b
+    assert lib.chord_moe_align_workspace_size(512, 8, 48) >= 256 + 16 * 48 * 4
+
+
+def test_host_checks_reject_before_launch(lib):
+    vp = ctypes.c_void_p
+    fake = vp(0x1000)
+    # unsupported hidden size (not a multiple of 256)
+    st = lib.chord_w4a16_moe_indexed(fake, 4, 200, 128, 8, 8, 2, fake, fake, fake, fake, fake,
+                                     fake, fake, fake, 1024, 16, fake, 1 << 20, fake, None, 0, None)
+    assert st == -2
+    # k too large
+    st = lib.chord_w4a16_moe_indexed(fake, 4, 256, 128, 8, 8, 33, fake, fake, fake, fake, fake,
+                                     fake, fake, fake, 1024, 16, fake, 1 << 20, fake, None, 0, None)
+    assert st == -2
+    # capacity too small
+    st = lib.chord_w4a16_moe_indexed(fake, 4, 256, 128, 8, 8, 2, fake, fake, fake, fake, fake,
+                                     fake, fake, fake, 16, 16, fake, 1 << 20, fake, None, 0, None)
+    assert st == -3
+    # null pointer
+    st = lib.chord_w4a16_moe_indexed(None, 4, 256, 128, 8, 8, 2, fake, fake, fake, fake, fake,
+                                     fake, fake, fake, 1024, 16, fake, 1 << 20, fake, None, 0, None)
+    assert st == -1
+    # T = 0 is a no-op
+    st = lib.chord_w4a16_moe_indexed(None, 0, 256, 128, 8, 8, 2, None, None, None, None, None,
+                                     None, None, None, 0, 16, None, 0, None, None, 0, None)
+    assert st == 0
+    # align: capacity not enough / bad block_m / map missing with E_local != E_global
+    assert lib.chord_moe_align(fake, 10, 2, 8, None, 8, 16, fake, fake, fake, 16, fake, 4096,
+                               None) == -3
+    assert lib.chord_moe_align(fake, 10, 2, 8, None, 8, 0, fake, fake, fake, 512, fake, 4096,
+                               None) == -1
+    assert lib.chord_moe_align(fake, 10, 2, 16, None, 8, 16, fake, fake, fake, 512, fake, 4096,
+                               None) == -1
+    # grouped: wrong layout combinations fail loudly
+    assert lib.chord_w4a16_moe_grouped(0, fake, 32, 256, 128, 4, None, None, 0, 1, fake, fake,
+                                       fake, fake, None, None, 0, 0, fake, 1 << 20, fake, None,
+                                       None, 0, None) == -4
+    assert lib.chord_w4a16_moe_grouped(1, fake, 32, 256, 128, 4, fake, fake, 8, 1, fake, fake,
+                                       fake, fake, None, None, 0, 0, fake, 1 << 20, fake, None,
+                                       None, 0, None) == -4
+    assert lib.chord_w4a16_moe_grouped(7, fake, 32, 256, 128, 4, None, fake, 8, 1, fake, fake,
+                                       fake, fake, None, None, 0, 0, fake, 1 << 20, fake, None,
+                                       None, 0, None) == -4
+    assert lib.chord_w4a16_moe_grouped(0, fake, 30, 256, 128, 4, fake, None, 0, 1, fake, fake,
+                                       fake, fake, None, None, 0, 0, fake, 1 << 20, fake, None,
+                                       None, 0, None) == -2
+
+
+def test_status_strings(lib):
+    for code in range(-9, 1):
+        assert lib.chord_status_string(code)

@@ -44,3 +44,25 @@ def test_bf16_bits_roundtrip():
     fin = np.isfinite(f)
     back = np.array([oracle.f32_to_bf16(float(v)) for v in f[fin][:2000]], np.uint16)
     assert np.array_equal(back, b[fin][:2000])
+
+
+def test_downstream_entry_reproduces_the_layer():
+    """Down + combine on the oracle's own h reproduces the whole layer bit-exactly
+    (indexed and grouped): the split entries are the same arithmetic."""
+    inp = pins.small_random_inputs(3)
+    s = inp.shape
+    (si, ei, ntp), (out, h, _) = oracle.run_workload(inp, want_h=True)
+    out2 = oracle.moe_indexed_down(h, inp.w2_q, inp.w2_s, inp.topk_weights, si, ei, ntp,
+                                   s.block_m, s.T, s.k)
+    assert np.array_equal(out, out2)
+    from w4a16_int4_mixture_gb300 import synth
+    a3, mm, r2p = synth.grouped_masked_layout(inp)
+    rows, toks, hg = oracle.moe_grouped("masked", a3, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s,
+                                        masked_m=mm, row_to_pair=r2p,
+                                        topk_weights=inp.topk_weights, T=s.T, k=s.k,
+                                        want_h=True)
+    rows2, toks2 = oracle.moe_grouped_down("masked", hg, inp.w2_q, inp.w2_s, masked_m=mm,
+                                           max_m=a3.shape[1], row_to_pair=r2p,
+                                           topk_weights=inp.topk_weights, T=s.T, k=s.k)
+    assert np.array_equal(rows, rows2) and np.array_equal(toks, toks2)
+    assert np.array_equal(toks, out)

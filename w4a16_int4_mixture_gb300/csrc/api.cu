@@ -1,0 +1,806 @@
+// api.cu -- the C ABI (include/chord.h): argument checks, schedule selection,
+// workspace layout, tensor-map memo and the launch sequence of each call.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "chord.h"
+#include "kernels.h"
+
+namespace chord {
+
+cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const GemmArgs& a, int grid,
+                                cudaStream_t s);
+cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const GemmArgs& a, int grid,
+                             cudaStream_t s);
+int gemm_cfg_smem_gate_up(int cfg);
+int gemm_cfg_smem_down(int cfg);
+
+cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& map, const GemmArgs& a, int grid,
+                        cudaStream_t s)
+{
+    return gate_up ? launch_gemm_gate_up(cfg, map, a, grid, s) : launch_gemm_down(cfg, map, a, grid, s);
+}
+
+int gemm_cfg_smem(int cfg, bool gate_up)
+{
+    return gate_up ? gemm_cfg_smem_gate_up(cfg) : gemm_cfg_smem_down(cfg);
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// device properties
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    bool ok = false;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+chord_status device_info(DeviceInfo* out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return CHORD_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (d.device != dev) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return CHORD_ERR_NO_DEVICE;
+        d.device = dev;
+        d.sms = sms;
+        d.ok = (major == 10 && minor == 3);
+    }
+    *out = d;
+    return d.ok ? CHORD_OK : CHORD_ERR_NO_DEVICE;
+}
+
+// ---------------------------------------------------------------------------
+// tensor maps over the packed codes, memoised by (pointer, shape, box)
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct MapKey {
+    const void* ptr;
+    int64_t rows;
+    int64_t K;
+    int box_rows;
+    int bk;
+    int device;
+    bool operator==(const MapKey& o) const
+    {
+        return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows && bk == o.bk &&
+               device == o.device;
+    }
+};
+
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    uint64_t stamp;
+};
+
+std::mutex g_map_mu;
+std::vector<MapEntry> g_maps;
+uint64_t g_stamp = 0;
+
+chord_status codes_tensor_map(const int32_t* codes, int64_t rows, int64_t K, int box_rows, int bk,
+                              int device, CUtensorMap* out)
+{
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    const MapKey key{codes, rows, K, box_rows, bk, device};
+    for (auto& e : g_maps)
+        if (e.key == key) {
+            e.stamp = ++g_stamp;
+            *out = e.map;
+            return CHORD_OK;
+        }
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return CHORD_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    CUtensorMap m;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 8) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(bk / 8), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t es[2] = {1, 1};
+    const CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t*>(codes),
+                                dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return CHORD_ERR_CUDA;
+    if (g_maps.size() >= 32) {
+        size_t victim = 0;
+        for (size_t i = 1; i < g_maps.size(); ++i)
+            if (g_maps[i].stamp < g_maps[victim].stamp)
+                victim = i;
+        g_maps.erase(g_maps.begin() + static_cast<long>(victim));
+    }
+    g_maps.push_back({key, m, ++g_stamp});
+    *out = m;
+    return CHORD_OK;
+}
+
+// ---------------------------------------------------------------------------
+// schedule
+// ---------------------------------------------------------------------------
+struct Schedule {
+    int cfg_gate_up;
+    int cfg_down;
+    bool reduce;  // fp32 reductions into token rows (else per-pair store + ordered combine)
+};
+
+// Token tile by expected routed rows per expert (page: "Kernel optimisation":
+// the schedule is chosen from the routed tokens per expert, tok_e; prefill
+// switches above 80 rows per expert).  Below the switch the weight-streaming
+// decode pipeline with the smallest token tile that holds a typical expert
+// (mean + 3 sigma of a Poisson count) in one chunk; above it the deep-N
+// prefill tile of 256 tokens.
+int pick_cfg(double tok_e, int K)
+{
+    if (K % 256 != 0)
+        return kCfgP256;
+    if (tok_e >= 80.0)
+        return kCfgP256;
+    const double hi = tok_e + 3.0 * std::sqrt(tok_e > 0 ? tok_e : 0.0);
+    if (hi <= 32.0)
+        return kCfgD32;
+    if (hi <= 64.0)
+        return kCfgD64;
+    return kCfgD128;
+}
+
+// The reduction form keeps the fp32 token accumulators [T, H] L2-resident;
+// beyond that size the per-pair store + ordered combine moves fewer bytes.
+constexpr double kReduceMaxBytes = 96.0 * 1024 * 1024;
+
+Schedule pick_schedule(double tok_e, int64_t T, int H, int I, int flags)
+{
+    Schedule s;
+    s.cfg_gate_up = pick_cfg(tok_e, H);
+    s.cfg_down = pick_cfg(tok_e, I);
+    s.reduce = !(flags & CHORD_FLAG_DETERMINISTIC) &&
+               static_cast<double>(T) * H * 4.0 <= kReduceMaxBytes;
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+struct Workspace {
+    size_t off_hdr = 0;  // int err; int num_chunks[2]
+    size_t off_chunks[2] = {0, 0};
+    size_t off_h = 0;
+    size_t off_acc = 0;       // reduce: float [T, H]; store: float [T*k, H]
+    size_t off_pair_row = 0;  // store: int32 [T*k]
+    size_t total = 0;
+    int64_t max_chunks = 0;
+};
+
+Workspace layout_ws(int64_t max_chunks, int64_t h_rows, int I, int64_t T, int k, int H, bool reduce,
+                    bool with_tokens)
+{
+    Workspace w;
+    size_t o = 0;
+    w.off_hdr = o;
+    o += kAlign;
+    w.max_chunks = max_chunks;
+    for (int L = 0; L < 2; ++L) {
+        w.off_chunks[L] = o;
+        o = align_up(o + static_cast<size_t>(max_chunks) * sizeof(Chunk), kAlign);
+    }
+    w.off_h = o;
+    o = align_up(o + static_cast<size_t>(h_rows) * I * 2, kAlign);
+    if (with_tokens) {
+        w.off_acc = o;
+        if (reduce) {
+            o = align_up(o + static_cast<size_t>(T) * H * 4, kAlign);
+        } else {
+            o = align_up(o + static_cast<size_t>(T) * k * H * 4, kAlign);
+            w.off_pair_row = o;
+            o = align_up(o + static_cast<size_t>(T) * k * 4, kAlign);
+        }
+    }
+    w.total = o;
+    return w;
+}
+
+int64_t indexed_max_chunks(int E_local, int64_t capacity) { return E_local + capacity / 16 + 2; }
+
+int64_t grouped_max_chunks(int mode, int64_t M, int E_local, int64_t max_m)
+{
+    return mode == CHORD_GROUPED_MASKED ? E_local * ((max_m + 15) / 16) + 2 : M / 16 + 2;
+}
+
+// ---------------------------------------------------------------------------
+// stage timing
+// ---------------------------------------------------------------------------
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+struct ProfCall {
+    cudaEvent_t ev[5];
+};
+std::vector<ProfCall> g_prof;
+
+bool stream_capturing(cudaStream_t s)
+{
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess)
+        return true;
+    return st != cudaStreamCaptureStatusNone;
+}
+
+struct StageMarks {
+    ProfCall call{};
+    bool on = false;
+    cudaStream_t s = nullptr;
+    void begin(cudaStream_t st)
+    {
+        s = st;
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        if (!g_prof_on || stream_capturing(st))
+            return;
+        for (auto& e : call.ev)
+            if (cudaEventCreate(&e) != cudaSuccess)
+                return;
+        on = true;
+        cudaEventRecord(call.ev[0], s);
+    }
+    void mark(int i)
+    {
+        if (on)
+            cudaEventRecord(call.ev[i], s);
+    }
+    void end()
+    {
+        if (!on)
+            return;
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        g_prof.push_back(call);
+    }
+};
+
+chord_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CHORD_OK : CHORD_ERR_CUDA; }
+
+chord_status check_ws(void* ws, size_t bytes, size_t need)
+{
+    if (need > 0 && (ws == nullptr || bytes < need))
+        return CHORD_ERR_WORKSPACE;
+    if (ws && (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
+        return CHORD_ERR_WORKSPACE;
+    return CHORD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int zero_blocks_for(int64_t count, int sms)
+{
+    if (count <= 0)
+        return 0;
+    int64_t b = (count / 4 + 1023) / 1024;
+    if (b > 2LL * sms)
+        b = 2LL * sms;
+    return static_cast<int>(b < 1 ? 1 : b);
+}
+
+chord_status read_error_word(void* ws, cudaStream_t s, int* bits, bool clear)
+{
+    int v = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    if (clear && v != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    if (bits)
+        *bits = v;
+    if (v & CHORD_DEVERR_TIMEOUT)
+        return CHORD_ERR_TIMEOUT;
+    if (v & CHORD_DEVERR_ROUTING)
+        return CHORD_ERR_ROUTING;
+    if (v & CHORD_DEVERR_CAPACITY)
+        return CHORD_ERR_CAPACITY;
+    return CHORD_OK;
+}
+
+chord_status check_shape(int H, int I, int E_local, int k)
+{
+    if (H <= 0 || I <= 0 || E_local <= 0 || k <= 0)
+        return CHORD_ERR_INVALID_ARG;
+    if (H % 256 != 0 || I % 128 != 0 || k > 32)
+        return CHORD_ERR_UNSUPPORTED_SHAPE;
+    return CHORD_OK;
+}
+
+// The two GEMMs of one layer call, given a prepared chunk list.
+struct LayerIO {
+    int src_kind;
+    const uint16_t* src;
+    const int32_t* sorted_ids;
+    const int32_t* m_indices;
+    const int32_t* pair_of_row;
+    int k;
+    int64_t num_pairs;
+    int H, I, E_local;
+    const int32_t *w13_q, *w2_q;
+    const uint16_t *w13_s, *w2_s;
+    const float* topk_weights;
+    int64_t h_rows;
+    uint16_t* h_out;  // caller-provided intermediate, or null (workspace)
+    uint16_t* rows_out;
+    int down_epi;
+};
+
+chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w, uint8_t* ws,
+                       int* err, int32_t* pair_row, float* acc, const DeviceInfo& dev,
+                       cudaStream_t s, StageMarks& marks)
+{
+    CUtensorMap map13, map2;
+    chord_status st = codes_tensor_map(io.w13_q, static_cast<int64_t>(io.E_local) * 2 * io.I, io.H,
+                                       64, gemm_cfg_bk(sc.cfg_gate_up), dev.device, &map13);
+    if (st != CHORD_OK)
+        return st;
+    st = codes_tensor_map(io.w2_q, static_cast<int64_t>(io.E_local) * io.H, io.I, 128,
+                          gemm_cfg_bk(sc.cfg_down), dev.device, &map2);
+    if (st != CHORD_OK)
+        return st;
+    int32_t* num_chunks = reinterpret_cast<int32_t*>(ws + w.off_hdr) + 1;
+    uint16_t* h = io.h_out ? io.h_out : reinterpret_cast<uint16_t*>(ws + w.off_h);
+
+    GemmArgs g{};
+    g.src_kind = io.src_kind;
+    g.src = io.src;
+    g.ld_src = io.H;
+    g.sorted_ids = io.sorted_ids;
+    g.m_indices = io.m_indices;
+    g.topk = io.k;
+    g.num_pairs = static_cast<int>(io.num_pairs);
+    g.K = io.H;
+    g.N = 2 * io.I;
+    g.I = io.I;
+    g.n_tiles = io.I / 64;
+    g.scales = io.w13_s;
+    g.chunks = reinterpret_cast<const Chunk*>(ws + w.off_chunks[0]);
+    g.num_chunks = num_chunks;
+    g.epi = 0;
+    g.h_out = h;
+    g.ld_h = io.I;
+    g.pair_row = pair_row;
+    g.topk_weights = io.topk_weights;
+    g.pair_of_row = io.pair_of_row;
+    g.err = err;
+    marks.mark(1);
+    if (launch_gemm(sc.cfg_gate_up, true, map13, g, dev.sms, s) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    marks.mark(2);
+
+    GemmArgs d = g;
+    d.src_kind = kSrcDirect;
+    d.src = h;
+    d.ld_src = io.I;
+    d.K = io.I;
+    d.N = io.H;
+    d.n_tiles = io.H / 128;
+    d.scales = io.w2_s;
+    d.chunks = reinterpret_cast<const Chunk*>(ws + w.off_chunks[1]);
+    d.num_chunks = num_chunks + 1;
+    d.epi = io.down_epi;
+    d.h_out = nullptr;
+    d.pair_row = nullptr;
+    d.y_pairs = (io.down_epi & kEpiStorePair) ? acc : nullptr;
+    d.out_acc = (io.down_epi & kEpiReduceTok) ? acc : nullptr;
+    d.rows_out = io.rows_out;
+    if (launch_gemm(sc.cfg_down, false, map2, d, dev.sms, s) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    marks.mark(3);
+    return CHORD_OK;
+}
+
+}  // namespace
+}  // namespace chord
+
+using namespace chord;
+
+extern "C" {
+
+const char* chord_status_string(int status)
+{
+    switch (status) {
+    case CHORD_OK: return "ok";
+    case CHORD_ERR_INVALID_ARG: return "invalid argument";
+    case CHORD_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case CHORD_ERR_CAPACITY: return "routing capacity too small";
+    case CHORD_ERR_LAYOUT_MODE: return "layout mode mismatch";
+    case CHORD_ERR_CUDA: return "CUDA error";
+    case CHORD_ERR_TIMEOUT: return "device wait timed out";
+    case CHORD_ERR_ROUTING: return "invalid routing data";
+    case CHORD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case CHORD_ERR_NO_DEVICE: return "no sm_103a device current";
+    default: return "unknown status";
+    }
+}
+
+int chord_version(void) { return 100; }
+
+int64_t chord_moe_align_capacity(int64_t T, int k, int E_local, int block_m)
+{
+    if (block_m <= 0 || T < 0 || k <= 0 || E_local <= 0)
+        return -1;
+    const int64_t worst = T * k + static_cast<int64_t>(E_local) * (block_m - 1);
+    return (worst + block_m - 1) / block_m * block_m;
+}
+
+int chord_select_block_m(int64_t, int, int, int, int, int) { return 16; }
+
+int chord_describe_schedule(int64_t T, int k, int E_global, int E_local, int H, int I, int flags,
+                            char* buf, size_t buf_len)
+{
+    const double tok_e = E_global > 0 ? static_cast<double>(T) * k / E_global : 0.0;
+    const Schedule s = pick_schedule(tok_e, T, H, I, flags);
+    static const char* names[] = {"decode-tile32", "decode-tile64", "decode-tile128",
+                                  "prefill-tile256"};
+    char tmp[256];
+    const int n = snprintf(tmp, sizeof tmp,
+                           "tok_e=%.2f gate_up=%s(BK%d) down=%s(BK%d) combine=%s block_m=16 "
+                           "E_local=%d",
+                           tok_e, names[s.cfg_gate_up], gemm_cfg_bk(s.cfg_gate_up),
+                           names[s.cfg_down], gemm_cfg_bk(s.cfg_down),
+                           s.reduce ? "fp32-reduce" : "ordered-pairs", E_local);
+    if (buf && buf_len) {
+        strncpy(buf, tmp, buf_len - 1);
+        buf[buf_len - 1] = 0;
+    }
+    return n;
+}
+
+size_t chord_moe_align_workspace_size(int64_t T, int k, int E_local)
+{
+    const int64_t pairs = T * k;
+    const int64_t tiles = (pairs + 255) / 256;
+    return align_up(kAlign + static_cast<size_t>(tiles > 0 ? tiles : 1) * E_local * 4, kAlign);
+}
+
+size_t chord_w4a16_moe_workspace_size(int64_t T, int k, int E_global, int E_local, int H, int I,
+                                      int block_m, int64_t capacity, int flags)
+{
+    if (T < 0 || k <= 0 || E_local <= 0 || H <= 0 || I <= 0 || block_m <= 0 || capacity < 0)
+        return 0;
+    const double tok_e = E_global > 0 ? static_cast<double>(T) * k / E_global : 0.0;
+    const Schedule s = pick_schedule(tok_e, T, H, I, flags);
+    return layout_ws(indexed_max_chunks(E_local, capacity), capacity, I, T, k, H, s.reduce, true)
+        .total;
+}
+
+size_t chord_w4a16_grouped_workspace_size(int mode, int64_t M, int H, int I, int E_local, int64_t T,
+                                          int k, int with_tokens, int expected_m)
+{
+    (void)expected_m;
+    if (M < 0 || H <= 0 || I <= 0 || E_local <= 0)
+        return 0;
+    const int64_t max_m = mode == CHORD_GROUPED_MASKED ? M / E_local : 0;
+    return layout_ws(grouped_max_chunks(mode, M, E_local, max_m), M, I, T, k, H, true,
+                     with_tokens != 0)
+        .total;
+}
+
+chord_status chord_moe_align(const int32_t* topk_ids, int64_t T, int k, int E_global,
+                             const int32_t* expert_map, int E_local, int block_m,
+                             int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_tokens_padded,
+                             int64_t capacity, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (T < 0 || k < 1 || k > 32 || E_global < 1 || E_local < 1 || E_local > 1024 || block_m < 1 ||
+        block_m > 256)
+        return CHORD_ERR_INVALID_ARG;
+    if (!expert_map && E_local != E_global)
+        return CHORD_ERR_INVALID_ARG;
+    if (T * k >= (int64_t(1) << 31))
+        return CHORD_ERR_UNSUPPORTED_SHAPE;
+    if (!sorted_ids || !expert_ids || !num_tokens_padded || (T > 0 && !topk_ids))
+        return CHORD_ERR_INVALID_ARG;
+    if (capacity < chord_moe_align_capacity(T, k, E_local, block_m) || capacity % block_m != 0)
+        return CHORD_ERR_CAPACITY;
+    chord_status st =
+        check_ws(workspace, workspace_bytes, chord_moe_align_workspace_size(T, k, E_local));
+    if (st != CHORD_OK)
+        return st;
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != CHORD_OK)
+        return st;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    AlignArgs a{};
+    a.topk_ids = topk_ids;
+    a.num_pairs = T * k;
+    a.E_global = E_global;
+    a.expert_map = expert_map;
+    a.E_local = E_local;
+    a.block_m = block_m;
+    a.sorted_ids = sorted_ids;
+    a.expert_ids = expert_ids;
+    a.num_tokens_padded = num_tokens_padded;
+    a.capacity = capacity;
+    a.tile_hist = reinterpret_cast<int32_t*>(ws + kAlign);
+    a.n_tiles = static_cast<int>((T * k + 255) / 256);
+    a.err = reinterpret_cast<int*>(ws);
+    return from_cuda(launch_align(a, static_cast<cudaStream_t>(stream)));
+}
+
+chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I, int E_global,
+                                     int E_local, int k, const int32_t* w13_q,
+                                     const uint16_t* w13_s, const int32_t* w2_q,
+                                     const uint16_t* w2_s, const float* topk_weights,
+                                     const int32_t* sorted_ids, const int32_t* expert_ids,
+                                     const int32_t* num_tokens_padded, int64_t capacity,
+                                     int block_m, void* workspace, size_t workspace_bytes,
+                                     uint16_t* out, uint16_t* h_out, int flags, void* stream)
+{
+    chord_status st = check_shape(H, I, E_local, k);
+    if (st != CHORD_OK)
+        return st;
+    if (T < 0 || E_global < 1 || block_m < 1 || block_m > 256 || (flags & ~3))
+        return CHORD_ERR_INVALID_ARG;
+    if (T * k >= (int64_t(1) << 31))
+        return CHORD_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0)
+        return CHORD_OK;
+    if (!x || !w13_q || !w13_s || !w2_q || !w2_s || !topk_weights || !sorted_ids || !expert_ids ||
+        !num_tokens_padded || !out)
+        return CHORD_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w13_q) || !aligned16(w13_s) || !aligned16(w2_q) ||
+        !aligned16(w2_s) || !aligned16(out) || (h_out && !aligned16(h_out)))
+        return CHORD_ERR_INVALID_ARG;
+    if (capacity < chord_moe_align_capacity(T, k, E_local, block_m) || capacity % block_m != 0)
+        return CHORD_ERR_CAPACITY;
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != CHORD_OK)
+        return st;
+    const double tok_e = static_cast<double>(T) * k / E_global;
+    const Schedule sc = pick_schedule(tok_e, T, H, I, flags);
+    const Workspace w = layout_ws(indexed_max_chunks(E_local, capacity), capacity, I, T, k, H,
+                                  sc.reduce, true);
+    if ((st = check_ws(workspace, workspace_bytes, w.total)) != CHORD_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* err = reinterpret_cast<int*>(ws + w.off_hdr);
+    float* acc = reinterpret_cast<float*>(ws + w.off_acc);
+    int32_t* pair_row = sc.reduce ? nullptr : reinterpret_cast<int32_t*>(ws + w.off_pair_row);
+
+    StageMarks marks;
+    marks.begin(s);
+    PrepArgs pa{};
+    pa.layout = kLayoutIndexed;
+    pa.expert_ids = expert_ids;
+    pa.num_tokens_padded = num_tokens_padded;
+    pa.capacity = capacity;
+    pa.block_rows = block_m;
+    pa.E_local = E_local;
+    pa.maxn[0] = gemm_cfg_maxn(sc.cfg_gate_up);
+    pa.maxn[1] = gemm_cfg_maxn(sc.cfg_down);
+    pa.chunks[0] = reinterpret_cast<Chunk*>(ws + w.off_chunks[0]);
+    pa.chunks[1] = reinterpret_cast<Chunk*>(ws + w.off_chunks[1]);
+    pa.max_chunks = static_cast<int>(w.max_chunks);
+    pa.num_chunks = err + 1;
+    if (sc.reduce) {
+        pa.zero_f32 = acc;
+        pa.zero_count = T * H;
+    } else {
+        pa.fill_i32 = pair_row;
+        pa.fill_count = T * k;
+    }
+    pa.err = err;
+    if (launch_prep(pa, zero_blocks_for(sc.reduce ? T * H : T * k, dev.sms), s) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+
+    LayerIO io{};
+    io.src_kind = kSrcIndexed;
+    io.src = x;
+    io.sorted_ids = sorted_ids;
+    io.pair_of_row = sorted_ids;
+    io.k = k;
+    io.num_pairs = T * k;
+    io.H = H;
+    io.I = I;
+    io.E_local = E_local;
+    io.w13_q = w13_q;
+    io.w13_s = w13_s;
+    io.w2_q = w2_q;
+    io.w2_s = w2_s;
+    io.topk_weights = topk_weights;
+    io.h_rows = capacity;
+    io.h_out = h_out;
+    io.down_epi = sc.reduce ? kEpiReduceTok : kEpiStorePair;
+    if ((st = run_gemms(io, sc, w, ws, err, pair_row, acc, dev, s, marks)) != CHORD_OK)
+        return st;
+
+    cudaError_t e;
+    if (sc.reduce) {
+        e = launch_finalize(acc, out, T * H, dev.sms, s);
+    } else {
+        const CombineArgs ca{T, k, H, pair_row, topk_weights, acc, out};
+        e = launch_combine_pairs(ca, s);
+    }
+    if (e != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    marks.mark(4);
+    marks.end();
+    if (flags & CHORD_FLAG_VALIDATE)
+        return read_error_word(ws + w.off_hdr, s, nullptr, false);
+    return CHORD_OK;
+}
+
+chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int H, int I,
+                                     int E_local, const int32_t* m_indices,
+                                     const int32_t* masked_m, int64_t max_m, int expected_m,
+                                     const int32_t* w13_q, const uint16_t* w13_s,
+                                     const int32_t* w2_q, const uint16_t* w2_s,
+                                     const int32_t* row_to_pair, const float* topk_weights,
+                                     int64_t T, int k, void* workspace, size_t workspace_bytes,
+                                     uint16_t* out_rows, uint16_t* out_tokens, uint16_t* h_out,
+                                     int flags, void* stream)
+{
+    const bool with_tokens = out_tokens != nullptr;
+    chord_status st = check_shape(H, I, E_local, with_tokens ? k : 1);
+    if (st != CHORD_OK)
+        return st;
+    if (M < 0 || (flags & ~3))
+        return CHORD_ERR_INVALID_ARG;
+    if (mode == CHORD_GROUPED_CONTIGUOUS) {
+        if (masked_m != nullptr || (M > 0 && m_indices == nullptr))
+            return CHORD_ERR_LAYOUT_MODE;
+        if (M % 16 != 0)
+            return CHORD_ERR_UNSUPPORTED_SHAPE;
+    } else if (mode == CHORD_GROUPED_MASKED) {
+        if (m_indices != nullptr || masked_m == nullptr)
+            return CHORD_ERR_LAYOUT_MODE;
+        if (max_m < 1 || expected_m < 1 || M != E_local * max_m)
+            return CHORD_ERR_INVALID_ARG;
+    } else {
+        return CHORD_ERR_LAYOUT_MODE;
+    }
+    if (M >= (int64_t(1) << 31))
+        return CHORD_ERR_UNSUPPORTED_SHAPE;
+    if (with_tokens) {
+        if (!row_to_pair || !topk_weights || T < 0 || k < 1 || T * k >= (int64_t(1) << 31))
+            return CHORD_ERR_INVALID_ARG;
+    }
+    if (M == 0 && !with_tokens)
+        return CHORD_OK;
+    if (!a || !w13_q || !w13_s || !w2_q || !w2_s || !out_rows)
+        return CHORD_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(w13_q) || !aligned16(w13_s) || !aligned16(w2_q) ||
+        !aligned16(w2_s) || !aligned16(out_rows) || (out_tokens && !aligned16(out_tokens)) ||
+        (h_out && !aligned16(h_out)))
+        return CHORD_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != CHORD_OK)
+        return st;
+    const double tok_e = mode == CHORD_GROUPED_MASKED ? static_cast<double>(expected_m)
+                                                      : static_cast<double>(M) / E_local;
+    Schedule sc = pick_schedule(tok_e, T, H, I, 0);
+    sc.reduce = true;
+    const Workspace w = layout_ws(grouped_max_chunks(mode, M, E_local, max_m), M, I, T, k, H, true,
+                                  with_tokens);
+    if ((st = check_ws(workspace, workspace_bytes, w.total)) != CHORD_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* err = reinterpret_cast<int*>(ws + w.off_hdr);
+    float* acc = with_tokens ? reinterpret_cast<float*>(ws + w.off_acc) : nullptr;
+
+    StageMarks marks;
+    marks.begin(s);
+    PrepArgs pa{};
+    pa.layout = mode == CHORD_GROUPED_MASKED ? kLayoutMasked : kLayoutContiguous;
+    pa.block_rows = 16;
+    pa.m_indices = m_indices;
+    pa.M = M;
+    pa.masked_m = masked_m;
+    pa.max_m = max_m;
+    pa.E_local = E_local;
+    pa.maxn[0] = gemm_cfg_maxn(sc.cfg_gate_up);
+    pa.maxn[1] = gemm_cfg_maxn(sc.cfg_down);
+    pa.chunks[0] = reinterpret_cast<Chunk*>(ws + w.off_chunks[0]);
+    pa.chunks[1] = reinterpret_cast<Chunk*>(ws + w.off_chunks[1]);
+    pa.max_chunks = static_cast<int>(w.max_chunks);
+    pa.num_chunks = err + 1;
+    if (with_tokens) {
+        pa.zero_f32 = acc;
+        pa.zero_count = T * H;
+    }
+    pa.err = err;
+    if (launch_prep(pa, zero_blocks_for(with_tokens ? T * H : 0, dev.sms), s) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+
+    LayerIO io{};
+    io.src_kind = mode == CHORD_GROUPED_MASKED ? kSrcDirect : kSrcContiguous;
+    io.src = a;
+    io.m_indices = m_indices;
+    io.pair_of_row = with_tokens ? row_to_pair : nullptr;
+    io.k = with_tokens ? k : 1;
+    io.num_pairs = with_tokens ? T * k : 0;
+    io.H = H;
+    io.I = I;
+    io.E_local = E_local;
+    io.w13_q = w13_q;
+    io.w13_s = w13_s;
+    io.w2_q = w2_q;
+    io.w2_s = w2_s;
+    io.topk_weights = topk_weights;
+    io.h_rows = M;
+    io.h_out = h_out;
+    io.rows_out = out_rows;
+    io.down_epi = kEpiStoreRows | (with_tokens ? kEpiReduceTok : 0);
+    if ((st = run_gemms(io, sc, w, ws, err, nullptr, acc, dev, s, marks)) != CHORD_OK)
+        return st;
+    if (with_tokens && launch_finalize(acc, out_tokens, T * H, dev.sms, s) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    marks.mark(4);
+    marks.end();
+    if (flags & CHORD_FLAG_VALIDATE)
+        return read_error_word(ws + w.off_hdr, s, nullptr, false);
+    return CHORD_OK;
+}
+
+chord_status chord_get_device_error(void* workspace, int* error_bits, int clear, void* stream)
+{
+    if (!workspace)
+        return CHORD_ERR_INVALID_ARG;
+    return read_error_word(workspace, static_cast<cudaStream_t>(stream), error_bits, clear != 0);
+}
+
+chord_status chord_stage_timing_enable(int enable)
+{
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_on = enable != 0;
+    for (auto& c : g_prof)
+        for (auto& e : c.ev)
+            cudaEventDestroy(e);
+    g_prof.clear();
+    return CHORD_OK;
+}
+
+chord_status chord_stage_timing_read(float* ms_per_stage, int* calls)
+{
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    float sum[4] = {0, 0, 0, 0};
+    for (auto& c : g_prof) {
+        if (cudaEventSynchronize(c.ev[4]) != cudaSuccess)
+            return CHORD_ERR_CUDA;
+        for (int i = 0; i < 4; ++i) {
+            float ms = 0;
+            if (cudaEventElapsedTime(&ms, c.ev[i], c.ev[i + 1]) != cudaSuccess)
+                return CHORD_ERR_CUDA;
+            sum[i] += ms;
+        }
+    }
+    if (ms_per_stage)
+        for (int i = 0; i < 4; ++i)
+            ms_per_stage[i] = sum[i];
+    if (calls)
+        *calls = static_cast<int>(g_prof.size());
+    return CHORD_OK;
+}
+
+}  // extern "C"

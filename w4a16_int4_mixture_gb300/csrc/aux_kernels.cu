@@ -1,0 +1,437 @@
+// aux_kernels.cu -- routing alignment, per-call preparation and the top-k combine.
+//
+// moe_align (page: "Two kernel families" / "vLLM integration": the indexed
+// family consumes moe_align_block_size's sorted_ids / expert_ids /
+// num_tokens_padded; Fig. 3: the padding lives in the index as a sentinel).
+// Deterministic, three launches, no atomics on the output positions:
+//   1. align_hist:    per 256-pair tile, a histogram of local experts;
+//   2. align_scan:    one CTA: padded segment offsets, ntp, expert_ids, per-tile
+//                     bases, sentinel fill of sorted_ids;
+//   3. align_scatter: per tile, the stable rank of each pair among the pairs of
+//                     its expert (warp match + per-warp counts) -> sorted_ids.
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "kernels.h"
+
+namespace chord {
+
+constexpr int kAlignTile = 256;
+
+__device__ __forceinline__ int local_expert_of(int32_t gid, int E_global, const int32_t* expert_map,
+                                               int E_local, int* err)
+{
+    if (gid < 0 || gid >= E_global) {
+        raise_error(err, CHORD_DEVERR_ROUTING);
+        return -1;
+    }
+    const int l = expert_map ? expert_map[gid] : gid;
+    return (l >= 0 && l < E_local) ? l : -1;
+}
+
+__global__ void __launch_bounds__(kAlignTile) align_hist_kernel(AlignArgs a)
+{
+    extern __shared__ int cnt[];  // [E_local]
+    for (int e = threadIdx.x; e < a.E_local; e += blockDim.x)
+        cnt[e] = 0;
+    __syncthreads();
+    const int64_t p = static_cast<int64_t>(blockIdx.x) * kAlignTile + threadIdx.x;
+    if (p < a.num_pairs) {
+        const int l = local_expert_of(a.topk_ids[p], a.E_global, a.expert_map, a.E_local, nullptr);
+        if (l >= 0)
+            atomicAdd(&cnt[l], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E_local; e += blockDim.x)
+        a.tile_hist[static_cast<int64_t>(blockIdx.x) * a.E_local + e] = cnt[e];
+}
+
+// block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32)
+__device__ int block_exclusive_scan(int v, int* total)
+{
+    __shared__ int warp_sums[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o)
+                w += y;
+        }
+        warp_sums[lane] = w;  // inclusive
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+    *total = warp_sums[(blockDim.x >> 5) - 1];
+    __syncthreads();
+    return before;
+}
+
+__global__ void __launch_bounds__(1024) align_scan_kernel(AlignArgs a)
+{
+    const int sentinel = static_cast<int>(a.num_pairs);
+    const int bm = a.block_m;
+    // this call's error word starts clear (the scatter reports bad ids after us)
+    if (threadIdx.x == 0)
+        *a.err = 0;
+    // sentinel everywhere first; the scatter overwrites the real entries
+    for (int64_t i = threadIdx.x; i < a.capacity; i += blockDim.x)
+        a.sorted_ids[i] = sentinel;
+    __shared__ int s_base;
+    if (threadIdx.x == 0)
+        s_base = 0;
+    __syncthreads();
+    const int n_tiles = a.n_tiles;
+    for (int e0 = 0; e0 < a.E_local; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        int count = 0;
+        if (e < a.E_local)
+            for (int t = 0; t < n_tiles; ++t)
+                count += a.tile_hist[static_cast<int64_t>(t) * a.E_local + e];
+        const int padded = (count + bm - 1) / bm * bm;
+        int total;
+        const int off = s_base + block_exclusive_scan(padded, &total);
+        if (e < a.E_local) {
+            // per-tile bases (in place over the histogram)
+            int run = off;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int64_t idx = static_cast<int64_t>(t) * a.E_local + e;
+                const int c = a.tile_hist[idx];
+                a.tile_hist[idx] = run;
+                run += c;
+            }
+            if (off + padded <= a.capacity)
+                for (int b = off / bm; b < (off + padded) / bm; ++b)
+                    a.expert_ids[b] = e;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0)
+            s_base += total;
+        __syncthreads();
+    }
+    const int ntp = s_base;
+    if (ntp > a.capacity && threadIdx.x == 0)
+        raise_error(a.err, CHORD_DEVERR_CAPACITY);
+    const int64_t nblocks = a.capacity / bm;
+    for (int64_t b = ntp / bm + threadIdx.x; b < nblocks; b += blockDim.x)
+        a.expert_ids[b] = -1;
+    if (threadIdx.x == 0)
+        a.num_tokens_padded[0] = ntp <= a.capacity ? ntp : 0;
+}
+
+__global__ void __launch_bounds__(kAlignTile) align_scatter_kernel(AlignArgs a)
+{
+    extern __shared__ int wcnt[];  // [kAlignTile/32][E_local]
+    constexpr int W = kAlignTile / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < W * a.E_local; i += blockDim.x)
+        wcnt[i] = 0;
+    __syncthreads();
+    const int64_t p = static_cast<int64_t>(blockIdx.x) * kAlignTile + threadIdx.x;
+    int l = -1;
+    if (p < a.num_pairs)
+        l = local_expert_of(a.topk_ids[p], a.E_global, a.expert_map, a.E_local, a.err);
+    // pairs of the same expert inside this warp, and my rank among them
+    const unsigned peers = __match_any_sync(0xffffffffu, l);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    const int rank_in_warp = __popc(lower);
+    if (l >= 0 && lower == 0)
+        wcnt[warp * a.E_local + l] = __popc(peers);
+    __syncthreads();
+    if (l >= 0) {
+        int rank = rank_in_warp;
+        for (int w = 0; w < warp; ++w)
+            rank += wcnt[w * a.E_local + l];
+        const int64_t pos = a.tile_hist[static_cast<int64_t>(blockIdx.x) * a.E_local + l] + rank;
+        if (pos < a.capacity)
+            a.sorted_ids[pos] = static_cast<int32_t>(p);
+    }
+}
+
+cudaError_t launch_align(const AlignArgs& a, cudaStream_t s)
+{
+    const int tiles = a.n_tiles;
+    if (tiles > 0) {
+        align_hist_kernel<<<tiles, kAlignTile, a.E_local * sizeof(int), s>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    align_scan_kernel<<<1, 1024, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || tiles == 0)
+        return e;
+    align_scatter_kernel<<<tiles, kAlignTile, (kAlignTile / 32) * a.E_local * sizeof(int), s>>>(a);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// per-call preparation: chunk lists for the GEMMs, zeroed / initialised buffers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int chunks_for(int rows, int maxn) { return (rows + maxn - 1) / maxn; }
+
+// Splits a segment of `rows` rows starting at row0 into chunks of at most maxn
+// rows (balanced, each but the last a multiple of 16).  False when the list
+// would overflow (only reachable with a malformed layout).
+__device__ bool emit_chunks(Chunk* out, int slot, int row0, int rows, int expert, int maxn,
+                            int max_chunks, int* err)
+{
+    const int n = chunks_for(rows, maxn);
+    if (slot + n > max_chunks) {
+        raise_error(err, CHORD_DEVERR_ROUTING);
+        return false;
+    }
+    int cs = (rows + n - 1) / n;
+    cs = (cs + 15) & ~15;
+    if (cs > maxn)
+        cs = maxn;
+    for (int c = 0, r = 0; c < n; ++c, r += cs) {
+        Chunk ch;
+        ch.row0 = row0 + r;
+        ch.nrows = min(cs, rows - r);
+        ch.expert = expert;
+        ch.seg0 = row0;
+        out[slot + c] = ch;
+    }
+    return true;
+}
+
+// expert of block b (block_m rows indexed, 16 rows contiguous): -1 for padding
+// or an invalid id, -2 outside [0, nblocks)
+__device__ __forceinline__ int block_expert(const PrepArgs& a, int b, int nblocks)
+{
+    if (b < 0 || b >= nblocks)
+        return -2;
+    if (a.layout == kLayoutIndexed) {
+        const int e = a.expert_ids[b];
+        if (e < 0 || e >= a.E_local) {
+            raise_error(a.err, CHORD_DEVERR_ROUTING);
+            return -1;
+        }
+        return e;
+    }
+    const int e = a.m_indices[static_cast<int64_t>(b) * a.block_rows];
+    return (e >= 0 && e < a.E_local) ? e : -1;
+}
+
+__device__ void build_chunk_lists(const PrepArgs& a)
+{
+    __shared__ int s_off[2];
+    __shared__ int s_bad;
+    if (threadIdx.x == 0) {
+        s_off[0] = 0;
+        s_off[1] = 0;
+        s_bad = 0;
+        *a.err = 0;  // this call's error word starts clear
+    }
+    __syncthreads();
+    if (a.layout == kLayoutMasked) {
+        for (int e0 = 0; e0 < a.E_local; e0 += blockDim.x) {
+            const int e = e0 + threadIdx.x;
+            int rows = 0;
+            if (e < a.E_local) {
+                rows = a.masked_m[e];
+                if (rows < 0 || rows > a.max_m) {
+                    raise_error(a.err, CHORD_DEVERR_ROUTING);
+                    rows = rows < 0 ? 0 : static_cast<int>(a.max_m);
+                }
+            }
+            for (int L = 0; L < 2; ++L) {
+                const int n = rows > 0 ? chunks_for(rows, a.maxn[L]) : 0;
+                int total;
+                const int off = s_off[L] + block_exclusive_scan(n, &total);
+                if (n > 0 && !emit_chunks(a.chunks[L], off, static_cast<int>(e * a.max_m), rows, e,
+                                          a.maxn[L], a.max_chunks, a.err))
+                    s_bad = 1;
+                __syncthreads();
+                if (threadIdx.x == 0)
+                    s_off[L] += total;
+                __syncthreads();
+            }
+        }
+    } else {
+        int nblocks;
+        if (a.layout == kLayoutIndexed) {
+            const int ntp = a.num_tokens_padded[0];
+            nblocks = (ntp >= 0 && ntp <= a.capacity) ? ntp / a.block_rows : 0;
+        } else {
+            nblocks = static_cast<int>(a.M / a.block_rows);
+        }
+        for (int b0 = 0; b0 < nblocks; b0 += blockDim.x) {
+            const int b = b0 + threadIdx.x;
+            int rows = 0, e = -1;
+            if (b < nblocks) {
+                e = block_expert(a, b, nblocks);
+                if (e >= 0 && block_expert(a, b - 1, nblocks) != e) {
+                    int end = b + 1;
+                    while (end < nblocks && block_expert(a, end, nblocks) == e)
+                        ++end;
+                    rows = (end - b) * a.block_rows;
+                }
+            }
+            for (int L = 0; L < 2; ++L) {
+                const int n = rows > 0 ? chunks_for(rows, a.maxn[L]) : 0;
+                int total;
+                const int off = s_off[L] + block_exclusive_scan(n, &total);
+                if (n > 0 && !emit_chunks(a.chunks[L], off, b * a.block_rows, rows, e, a.maxn[L],
+                                          a.max_chunks, a.err))
+                    s_bad = 1;
+                __syncthreads();
+                if (threadIdx.x == 0)
+                    s_off[L] += total;
+                __syncthreads();
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // a malformed layout that overflows the list runs nothing rather than
+        // reading entries this call did not write
+        a.num_chunks[0] = s_bad ? 0 : s_off[0];
+        a.num_chunks[1] = s_bad ? 0 : s_off[1];
+    }
+}
+
+__global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
+{
+    if (blockIdx.x == 0) {
+        build_chunk_lists(a);
+        return;
+    }
+    const int64_t tid = static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+    const int64_t nth = static_cast<int64_t>(gridDim.x - 1) * blockDim.x;
+    if (a.zero_f32 != nullptr) {
+        float4* z = reinterpret_cast<float4*>(a.zero_f32);
+        const int64_t n4 = a.zero_count / 4;
+        for (int64_t i = tid; i < n4; i += nth)
+            z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t i = n4 * 4 + tid; i < a.zero_count; i += nth)
+            a.zero_f32[i] = 0.f;
+    }
+    if (a.fill_i32 != nullptr)
+        for (int64_t i = tid; i < a.fill_count; i += nth)
+            a.fill_i32[i] = -1;
+}
+
+cudaError_t launch_prep(const PrepArgs& a, int zero_blocks, cudaStream_t s)
+{
+    prep_kernel<<<1 + zero_blocks, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// combine
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// out[i] = bf16(acc[i]) for the fp32 token accumulators of the reduction form.
+__global__ void finalize_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out, int64_t n)
+{
+    const int64_t n8 = n / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+        uint4 o;
+        o.x = pack_bf16x2(a.x, a.y);
+        o.y = pack_bf16x2(a.z, a.w);
+        o.z = pack_bf16x2(b.x, b.y);
+        o.w = pack_bf16x2(b.z, b.w);
+        reinterpret_cast<uint4*>(out)[i] = o;
+    }
+    for (int64_t i = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += stride)
+        out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i]));
+}
+
+// Ordered top-k combine of per-pair fp32 outputs.  One warp per (token,
+// 16-column chunk).  Lane = (slot group j8 = lane/4, column quad cq = lane%4);
+// each lane weights its slot's float4, then the 8 slot groups are summed with a
+// fixed warp-shuffle tree (xor 4, 8, 16), so the result is bit-identical run to
+// run.  Slots are visited in ascending order in groups of 8 (k <= 32).
+__global__ void combine_pairs_kernel(CombineArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int chunks_per_tok = a.H / 16;
+    if (gw >= a.T * chunks_per_tok)
+        return;
+    const int64_t t = gw / chunks_per_tok;
+    const int col0 = static_cast<int>(gw % chunks_per_tok) * 16;
+    // routing metadata of this token, one slot per lane, broadcast by shuffles
+    int valid = 0;
+    float w = 0.f;
+    if (lane < a.k) {
+        const int64_t p = t * a.k + lane;
+        valid = a.pair_row[p] >= 0;
+        w = a.topk_weights[p];
+    }
+    const int j8 = lane >> 2, cq = lane & 3;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int jb = 0; jb < a.k; jb += 8) {
+        const int j = jb + j8;
+        const int vj = __shfl_sync(0xffffffffu, valid, j & 31);
+        const float wj = __shfl_sync(0xffffffffu, w, j & 31);
+        if (j < a.k && vj) {
+            const float4 y =
+                *reinterpret_cast<const float4*>(a.y_pairs + (t * a.k + j) * a.H + col0 + cq * 4);
+            acc.x += wj * y.x;
+            acc.y += wj * y.y;
+            acc.z += wj * y.z;
+            acc.w += wj * y.w;
+        }
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+    }
+    if (j8 == 0) {
+        uint2 o;
+        o.x = pack_bf16x2(acc.x, acc.y);
+        o.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(a.out + t * a.H + col0 + cq * 4) = o;
+    }
+}
+
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int sms, cudaStream_t s)
+{
+    if (n <= 0)
+        return cudaSuccess;
+    int64_t blocks = (n / 8 + 255) / 256;
+    if (blocks < 1)
+        blocks = 1;
+    if (blocks > 4LL * sms)
+        blocks = 4LL * sms;
+    finalize_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(acc, out, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_pairs(const CombineArgs& a, cudaStream_t s)
+{
+    const int64_t warps = a.T * (a.H / 16);
+    if (warps <= 0)
+        return cudaSuccess;
+    const int64_t blocks = (warps * 32 + 255) / 256;
+    combine_pairs_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace chord

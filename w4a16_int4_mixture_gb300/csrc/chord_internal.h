@@ -1,0 +1,64 @@
+// chord_internal.h -- definitions shared by the host side and the kernels.
+#pragma once
+
+#include <stdint.h>
+
+#include "chord.h"
+
+namespace chord {
+
+// One run of padded rows that share an expert, at most one MMA token tile long.
+struct Chunk {
+    int32_t row0;    // first padded row
+    int32_t nrows;   // rows in this chunk (the token tile is nrows rounded up to 16)
+    int32_t expert;  // local expert
+    int32_t seg0;    // first row of the expert's segment (unused by the GEMMs)
+};
+
+// How rows of the B operand (activations) are found.
+enum BSource : int {
+    kSrcIndexed = 0,     // row r -> token sorted_ids[r] / k of x; sentinel -> zero row
+    kSrcContiguous = 1,  // row r of a; m_indices[r] < 0 -> zero row
+    kSrcDirect = 2,      // row r of src (masked layout, or h for the down GEMM)
+};
+
+// Down-GEMM epilogue forms (bit set).
+enum Epilogue : int {
+    kEpiStorePair = 1,   // y_pairs[p, n] = y (fp32) for the pair of each row
+    kEpiReduceTok = 2,   // out_acc[t, n] += w_p * y (fp32 reductions)
+    kEpiStoreRows = 4,   // rows_out[r, n] = bf16(y)
+};
+
+struct GemmArgs {
+    // B operand
+    int src_kind;
+    const uint16_t* src;      // x, a or h
+    int64_t ld_src;           // elements between rows of src
+    const int32_t* sorted_ids;
+    const int32_t* m_indices;
+    int topk;
+    int num_pairs;            // T*k, the sentinel
+    // problem
+    int K;                    // reduction length
+    int N;                    // rows of one expert's weight
+    int I;                    // intermediate size (gate_up: up rows start at I)
+    int n_tiles;              // output tiles per chunk
+    const uint16_t* scales;   // [E, N, K/32]
+    const Chunk* chunks;
+    const int32_t* num_chunks;
+    // epilogue
+    int epi;
+    uint16_t* h_out;          // gate_up: [rows, I]
+    int64_t ld_h;
+    int32_t* pair_row;        // gate_up: pair -> padded row (ordered combine), or null
+    float* y_pairs;           // down: [T*k, N]
+    float* out_acc;           // down: [T, N]
+    uint16_t* rows_out;       // down: [rows, N]
+    const float* topk_weights;
+    const int32_t* pair_of_row;  // pair id t*k+j of each padded row (or -1 / sentinel)
+    int* err;
+};
+
+constexpr int kGemmThreads = 512;  // 16 warps
+
+}  // namespace chord

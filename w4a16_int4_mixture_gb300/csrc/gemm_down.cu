@@ -1,0 +1,42 @@
+// gemm_down.cu -- down GEMM instances (per-pair store / token reduction / row store).
+#include "gemm_instances.cuh"
+
+namespace chord {
+
+cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const GemmArgs& a, int grid,
+                             cudaStream_t s)
+{
+    switch (cfg) {
+    case kCfgD32: return launch_gemm_cfg<CfgD32<false>>(map, a, grid, s);
+    case kCfgD64: return launch_gemm_cfg<CfgD64<false>>(map, a, grid, s);
+    case kCfgD128: return launch_gemm_cfg<CfgD128<false>>(map, a, grid, s);
+    case kCfgP256: return launch_gemm_cfg<CfgP256<false>>(map, a, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int gemm_cfg_smem_down(int cfg)
+{
+    switch (cfg) {
+    case kCfgD32: return CfgD32<false>::SMEM_BYTES;
+    case kCfgD64: return CfgD64<false>::SMEM_BYTES;
+    case kCfgD128: return CfgD128<false>::SMEM_BYTES;
+    case kCfgP256: return CfgP256<false>::SMEM_BYTES;
+    default: return 0;
+    }
+}
+
+int gemm_cfg_bk(int cfg) { return cfg == kCfgP256 ? 128 : 256; }
+
+int gemm_cfg_maxn(int cfg)
+{
+    switch (cfg) {
+    case kCfgD32: return 32;
+    case kCfgD64: return 64;
+    case kCfgD128: return 128;
+    case kCfgP256: return 256;
+    default: return 0;
+    }
+}
+
+}  // namespace chord

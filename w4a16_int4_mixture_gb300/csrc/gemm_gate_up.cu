@@ -1,0 +1,29 @@
+// gemm_gate_up.cu -- gate/up GEMM instances (fused SiLU(gate) * up epilogue).
+#include "gemm_instances.cuh"
+
+namespace chord {
+
+cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const GemmArgs& a, int grid,
+                                cudaStream_t s)
+{
+    switch (cfg) {
+    case kCfgD32: return launch_gemm_cfg<CfgD32<true>>(map, a, grid, s);
+    case kCfgD64: return launch_gemm_cfg<CfgD64<true>>(map, a, grid, s);
+    case kCfgD128: return launch_gemm_cfg<CfgD128<true>>(map, a, grid, s);
+    case kCfgP256: return launch_gemm_cfg<CfgP256<true>>(map, a, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int gemm_cfg_smem_gate_up(int cfg)
+{
+    switch (cfg) {
+    case kCfgD32: return CfgD32<true>::SMEM_BYTES;
+    case kCfgD64: return CfgD64<true>::SMEM_BYTES;
+    case kCfgD128: return CfgD128<true>::SMEM_BYTES;
+    case kCfgP256: return CfgP256<true>::SMEM_BYTES;
+    default: return 0;
+    }
+}
+
+}  // namespace chord

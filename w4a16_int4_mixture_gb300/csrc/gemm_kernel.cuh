@@ -1,0 +1,526 @@
+// gemm_kernel.cuh -- the W4A16 expert GEMM for sm_103a (tcgen05 + TMEM + TMA).
+//
+// One persistent CTA per SM walks work units (chunk of padded rows that share
+// an expert) x (128-row tile of that expert's weight).  Per unit it computes
+//   D[128 weight rows, ntok tokens] = W_tile[128, K] * X_rows[ntok, K]^T
+// with the dequantised weights as the MMA's M operand (held in tensor memory)
+// and the routed tokens as its N operand (in shared memory).  This is the
+// Blackwell form of the swap-AB decode schedule of the Chord page ("Kernel
+// optimisation / H200 and Blackwell indexed decode": dequantised weights take
+// the MMA-M operand), used here for every token count.
+//
+// Roles (16 warps):
+//   warp 0      TMA producer: packed INT4 codes (TMA tile, L2 evict-first) and
+//               the group-32 scales (cp.async) of each K stage into a ring.
+//   warp 1      token producer: gathers the unit's activation rows (cp.async,
+//               zero-fill for sentinel / padding rows) into a 128B-swizzled
+//               K-major ring that is the MMA's B operand.
+//   warp 2      MMA issuer (one thread) and TMEM owner.
+//   warp 3      idle.
+//   warps 4-7   epilogue: TMEM -> registers; gate_up: SiLU(gate)*up -> bf16 h;
+//               down: per-pair fp32 store, fp32 reductions into token rows,
+//               or bf16 row store.
+//   warps 8-15  dequant, two groups taking alternate K stages: codes + scales
+//               from shared memory -> w = (q - 8) * s in bf16 (subtract, then
+//               scale: the page's unfused rounding order) -> tcgen05.st into
+//               the A-operand stage in TMEM.
+// Every wait is bounded (2 s); on expiry the CTA records CHORD_DEVERR_TIMEOUT,
+// every role leaves its loop, in-flight tensor-core work is drained and TMEM
+// is freed.
+#pragma once
+
+#include "device.cuh"
+
+namespace chord {
+
+template <int BK_, int KS_, int BS_, int AS_, int MAXN_, int ACCB_, bool GATE_UP_>
+struct GemmCfg {
+    static constexpr int BK = BK_;        // K elements per stage
+    static constexpr int KS = KS_;        // code/scale stages in shared memory
+    static constexpr int BS = BS_;        // token stages in shared memory
+    static constexpr int AS = AS_;        // A-operand stages in TMEM
+    static constexpr int MAXN = MAXN_;    // largest token tile
+    static constexpr int ACCB = ACCB_;    // accumulator buffers in TMEM
+    static constexpr bool GATE_UP = GATE_UP_;
+
+    static constexpr int CODE_ROW = BK / 2;                 // bytes of codes per weight row
+    static constexpr int CODE_STAGE = 128 * CODE_ROW;
+    static constexpr int SCALE_ROW = BK / 16;               // bytes of scales per weight row
+    static constexpr int SCALE_STAGE = 128 * SCALE_ROW;
+    static constexpr int B_KBLK = BK / 64;                  // 128B swizzle atoms along K
+    static constexpr int B_REGION = MAXN * 128;             // one atom column of the tile
+    static constexpr int B_STAGE = B_KBLK * B_REGION;
+    static constexpr int HS_BYTES = GATE_UP ? MAXN * 128 : 0;  // 64 channels of bf16 per row
+
+    static constexpr int OFF_CODES = 0;
+    static constexpr int OFF_B = OFF_CODES + KS * CODE_STAGE;
+    static constexpr int OFF_SCALES = OFF_B + BS * B_STAGE;
+    static constexpr int OFF_HS = OFF_SCALES + KS * SCALE_STAGE;
+    static constexpr int OFF_ROWSRC = OFF_HS + HS_BYTES;
+    static constexpr int OFF_BARS = OFF_ROWSRC + MAXN * 8;
+    static constexpr int NBARS = 2 * KS + 2 * AS + 2 * BS + 2 * ACCB + 2;
+    static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+
+    static constexpr int A_COLS = BK / 2;                   // TMEM columns per A stage
+    static constexpr int D_COL0 = AS * A_COLS;
+    static constexpr int TMEM_COLS = 512;
+
+    static_assert(BK == 128 || BK == 256, "stage depth");
+    static_assert(MAXN % 16 == 0 && MAXN >= 16 && MAXN <= 256, "token tile");
+    static_assert(D_COL0 + ACCB * MAXN <= TMEM_COLS, "tensor memory budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM keeps the 512-column TMEM alloc safe");
+    static_assert(OFF_B % 1024 == 0 && B_REGION % 1024 == 0, "swizzle atoms need 1024B alignment");
+    static_assert(CODE_STAGE % 1024 == 0, "TMA destinations");
+};
+
+// 16-byte chunk c of row r of a TMA tile with 128B (BK=256) or 64B (BK=128) rows.
+template <int BK>
+__device__ __forceinline__ int code_chunk_swizzle(int c, int r)
+{
+    if constexpr (BK == 256)
+        return c ^ (r & 7);
+    else
+        return c ^ ((r >> 1) & 3);
+}
+
+// bf16x2 helpers (single rounding each, round to nearest even)
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Dequantise one word of 8 codes (elements 8w..8w+7, low nibble first) with the
+// bf16x2 scale pair s2 = (s, s) into 4 bf16x2 columns (elements (0,1) .. (6,7)).
+// For each element pair: place the two nibbles in the low 4 bits of each half
+// (byte permute of w and w>>4), OR in the bf16 exponent of 128 so each half
+// reads 128 + q exactly, subtract 136 (exact: q - 8), multiply by the scale
+// (one rounding).
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t* o)
+{
+    const uint32_t w4 = w >> 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t t = __byte_perm(w, w4, static_cast<uint32_t>(j | ((4 + j) << 8)));
+        t = (t & 0x000F000Fu) | 0x43004300u;
+        o[j] = bf16x2_mul(bf16x2_sub(t, 0x43084308u), s2);
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap codes_map, const GemmArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - raw_u32);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // barriers
+    const uint32_t bar0 = sbase + C::OFF_BARS;
+    auto codes_full = [&](int s) { return bar0 + 8u * s; };
+    auto codes_empty = [&](int s) { return bar0 + 8u * (C::KS + s); };
+    auto a_full = [&](int s) { return bar0 + 8u * (2 * C::KS + s); };
+    auto a_empty = [&](int s) { return bar0 + 8u * (2 * C::KS + C::AS + s); };
+    auto b_full = [&](int s) { return bar0 + 8u * (2 * C::KS + 2 * C::AS + s); };
+    auto b_empty = [&](int s) { return bar0 + 8u * (2 * C::KS + 2 * C::AS + C::BS + s); };
+    auto d_full = [&](int s) { return bar0 + 8u * (2 * C::KS + 2 * C::AS + 2 * C::BS + s); };
+    auto d_empty = [&](int s) {
+        return bar0 + 8u * (2 * C::KS + 2 * C::AS + 2 * C::BS + C::ACCB + s);
+    };
+    const uint32_t epi_bar = bar0 + 8u * (C::NBARS - 2);
+    const uint32_t drain_bar = bar0 + 8u * (C::NBARS - 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::KS; ++s) {
+            mbar_init(codes_full(s), 1 + 32);  // expect_tx arrive + 32 cp.async arrivals
+            mbar_init(codes_empty(s), 4);      // the 4 warps of one dequant group
+        }
+        for (int s = 0; s < C::AS; ++s) {
+            mbar_init(a_full(s), 4);
+            mbar_init(a_empty(s), 1);          // tcgen05.commit
+        }
+        for (int s = 0; s < C::BS; ++s) {
+            mbar_init(b_full(s), 32);          // 32 cp.async arrivals
+            mbar_init(b_empty(s), 1);
+        }
+        for (int s = 0; s < C::ACCB; ++s) {
+            mbar_init(d_full(s), 1);
+            mbar_init(d_empty(s), 4);          // 4 epilogue warps
+        }
+        mbar_init(epi_bar, 4);                 // epilogue group rendezvous
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0)
+        prefetch_tensormap(&codes_map);
+    if (warp == 2)
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_tiles = args.n_tiles;
+    const int total_units = args.num_chunks[0] * n_tiles;
+    const int KT = args.K / C::BK;
+    int* err = args.err;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        const uint64_t pol = policy_evict_first();
+        int g = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const Chunk ch = args.chunks[u / n_tiles];
+            const int nt = u % n_tiles;
+            const int e = ch.expert;
+            int grow_a, grow_b;
+            if constexpr (C::GATE_UP) {
+                grow_a = e * args.N + nt * 64;
+                grow_b = e * args.N + args.I + nt * 64;
+            } else {
+                grow_a = e * args.N + nt * 128;
+                grow_b = grow_a + 64;
+            }
+            for (int ks = 0; ks < KT; ++ks, ++g) {
+                const int s = g % C::KS;
+                if (!mbar_wait(codes_empty(s), ((g / C::KS) & 1) ^ 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = sbase + C::OFF_CODES + s * C::CODE_STAGE;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(codes_full(s), C::CODE_STAGE);
+                    const int x = ks * (C::BK / 8);
+                    if constexpr (C::GATE_UP) {
+                        tma_load_2d(dst, &codes_map, x, grow_a, codes_full(s), pol);
+                        tma_load_2d(dst + 64 * C::CODE_ROW, &codes_map, x, grow_b, codes_full(s), pol);
+                    } else {
+                        tma_load_2d(dst, &codes_map, x, grow_a, codes_full(s), pol);
+                    }
+                }
+                const uint32_t sdst = sbase + C::OFF_SCALES + s * C::SCALE_STAGE;
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int r = lane + 32 * rr;
+                    const int grow = (r < 64) ? grow_a + r : grow_b + (r - 64);
+                    const uint16_t* src = args.scales + static_cast<int64_t>(grow) * (args.K / 32) +
+                                          ks * (C::BK / 32);
+                    if constexpr (C::BK == 256)
+                        cp_async_16(sdst + r * C::SCALE_ROW, src, 16);
+                    else
+                        cp_async_8(sdst + r * C::SCALE_ROW, src);
+                }
+                cp_async_arrive_noinc(codes_full(s));
+            }
+        }
+        if (!ok)  // let the copies already issued land before the CTA goes away
+            asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- token producer
+        int64_t* rowsrc = reinterpret_cast<int64_t*>(smem + C::OFF_ROWSRC);
+        constexpr int CPR = C::BK / 8;  // 16-byte chunks per row per stage
+        int g = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const Chunk ch = args.chunks[u / n_tiles];
+            const int ntok = ch.nrows;
+            const int ntok16 = (ntok + 15) & ~15;
+            __syncwarp();
+            for (int r = lane; r < ntok16; r += 32) {
+                int64_t off = -1;
+                if (r < ntok) {
+                    const int row = ch.row0 + r;
+                    if (args.src_kind == kSrcIndexed) {
+                        const int p = args.sorted_ids[row];
+                        if (p >= 0 && p < args.num_pairs)
+                            off = static_cast<int64_t>(p / args.topk) * args.ld_src;
+                    } else if (args.src_kind == kSrcContiguous) {
+                        if (args.m_indices[row] >= 0)
+                            off = static_cast<int64_t>(row) * args.ld_src;
+                    } else {
+                        off = static_cast<int64_t>(row) * args.ld_src;
+                    }
+                }
+                rowsrc[r] = off;
+            }
+            __syncwarp();
+            for (int ks = 0; ks < KT; ++ks, ++g) {
+                const int s = g % C::BS;
+                if (!mbar_wait(b_empty(s), ((g / C::BS) & 1) ^ 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t bst = sbase + C::OFF_B + s * C::B_STAGE;
+                for (int idx = lane; idx < ntok16 * CPR; idx += 32) {
+                    const int r = idx / CPR;
+                    const int c = idx % CPR;
+                    const int64_t off = rowsrc[r];
+                    const uint32_t dst = bst + (c >> 3) * C::B_REGION + r * 128 +
+                                         (((c & 7) ^ (r & 7)) << 4);
+                    const uint16_t* srcp = off >= 0 ? args.src + off + ks * C::BK + c * 8 : args.src;
+                    cp_async_16(dst, srcp, off >= 0 ? 16u : 0u);
+                }
+                cp_async_arrive_noinc(b_full(s));
+            }
+        }
+        if (!ok)
+            asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == 2) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int g = 0;
+            int issued = 0;
+            bool ok = true;
+            int i = 0;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++i) {
+                const Chunk ch = args.chunks[u / n_tiles];
+                const int ntok16 = (ch.nrows + 15) & ~15;
+                const uint32_t idesc = idesc_bf16_f32(128, ntok16);
+                const int acc = i % C::ACCB;
+                if (!mbar_wait(d_empty(acc), ((i / C::ACCB) & 1) ^ 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + C::D_COL0 + acc * C::MAXN;
+                for (int ks = 0; ks < KT; ++ks, ++g) {
+                    const int sa = g % C::AS;
+                    const int sb = g % C::BS;
+                    if (!mbar_wait(a_full(sa), (g / C::AS) & 1, abort_flag, err) ||
+                        !mbar_wait(b_full(sb), (g / C::BS) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();  // cp.async (generic proxy) -> tensor core reads
+                    tc_fence_after();
+                    const uint32_t a_base = tmem + sa * C::A_COLS;
+                    const uint32_t b_base = sbase + C::OFF_B + sb * C::B_STAGE;
+#pragma unroll
+                    for (int j = 0; j < C::BK / 16; ++j) {
+                        const uint64_t bdesc =
+                            smem_desc_sw128(b_base + (j >> 2) * C::B_REGION + (j & 3) * 32);
+                        mma_ts(d_tmem, a_base + j * 8, bdesc, idesc, (ks | j) != 0 ? 1u : 0u);
+                    }
+                    issued = 1;
+                    mma_commit(a_empty(sa));
+                    mma_commit(b_empty(sb));
+                }
+                if (!ok)
+                    break;
+                mma_commit(d_full(acc));
+            }
+            if (!ok && issued) {
+                // drain tensor-core work in flight before TMEM is released
+                mma_commit(drain_bar);
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // --------------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int et = threadIdx.x - 128;  // 0..127 inside the epilogue group
+        int esync = 0;
+        // all four epilogue warps meet here (bounded, unlike bar.sync)
+        auto epi_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(epi_bar);
+            const bool r = mbar_wait(epi_bar, esync & 1, abort_flag, err);
+            ++esync;
+            return r;
+        };
+        int i = 0;
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++i) {
+            const Chunk ch = args.chunks[u / n_tiles];
+            const int nt = u % n_tiles;
+            const int ntok = ch.nrows;
+            const int ntok16 = (ntok + 15) & ~15;
+            const int acc = i % C::ACCB;
+            if (!mbar_wait(d_full(acc), (i / C::ACCB) & 1, abort_flag, err))
+                break;
+            tc_fence_after();
+            const uint32_t dbase =
+                tmem + (static_cast<uint32_t>(q * 32) << 16) + C::D_COL0 + acc * C::MAXN;
+            if constexpr (C::GATE_UP) {
+                // lanes (l, l^8): gate and up of channel 16q + 8(l>>4) + (l&7)
+                __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_HS);
+                const int chl = 16 * q + 8 * (lane >> 4) + (lane & 7);
+                const bool is_gate = (lane & 15) < 8;
+                for (int c0 = 0; c0 < ntok16; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld_x16(dbase + c0, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const float mine = __uint_as_float(v[jj]);
+                        const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
+                        if (is_gate) {
+                            const float silu = mine / (1.0f + expf(-mine));
+                            hs[(c0 + jj) * 64 + chl] = __float2bfloat16_rn(silu * other);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(d_empty(acc));
+                if (!epi_sync())
+                    break;
+                const int64_t col0 = static_cast<int64_t>(nt) * 64;
+                for (int idx = et; idx < ntok * 8; idx += 128) {
+                    const int c = idx >> 3;
+                    const int part = idx & 7;
+                    const uint4 val = *reinterpret_cast<const uint4*>(hs + c * 64 + part * 8);
+                    *reinterpret_cast<uint4*>(args.h_out + static_cast<int64_t>(ch.row0 + c) * args.ld_h +
+                                              col0 + part * 8) = val;
+                }
+                if (args.pair_row != nullptr && nt == 0) {
+                    for (int c = et; c < ntok; c += 128) {
+                        const int p = args.pair_of_row[ch.row0 + c];
+                        if (p >= 0 && p < args.num_pairs)
+                            args.pair_row[p] = ch.row0 + c;
+                    }
+                }
+                if (!epi_sync())
+                    break;
+            } else {
+                const int n = nt * 128 + q * 32 + lane;
+                const int N = args.N;
+                for (int c0 = 0; c0 < ntok16; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld_x16(dbase + c0, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int c = c0 + jj;
+                        if (c >= ntok)
+                            break;
+                        const int row = ch.row0 + c;
+                        const float y = __uint_as_float(v[jj]);
+                        if (args.epi & kEpiStoreRows)
+                            args.rows_out[static_cast<int64_t>(row) * N + n] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(y));
+                        if (args.epi & (kEpiStorePair | kEpiReduceTok)) {
+                            const int p = args.pair_of_row ? args.pair_of_row[row] : -1;
+                            if (p >= 0 && p < args.num_pairs) {
+                                if (args.epi & kEpiStorePair)
+                                    args.y_pairs[static_cast<int64_t>(p) * N + n] = y;
+                                if (args.epi & kEpiReduceTok)
+                                    red_add_f32(args.out_acc + static_cast<int64_t>(p / args.topk) * N + n,
+                                                args.topk_weights[p] * y);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(d_empty(acc));
+            }
+        }
+    } else if (warp >= 8) {
+        // ---------------------------------------------------------------- dequant
+        const int dg = (warp - 8) >> 2;
+        const int q = warp & 3;
+        int srow;
+        if constexpr (C::GATE_UP)
+            srow = (((lane & 15) >= 8) ? 64 : 0) + 16 * q + 8 * (lane >> 4) + (lane & 7);
+        else
+            srow = q * 32 + lane;
+        const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
+        int g = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            for (int ks = 0; ks < KT; ++ks, ++g) {
+                if ((g & 1) != dg)
+                    continue;
+                const int s = g % C::KS;
+                if (!mbar_wait(codes_full(s), (g / C::KS) & 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t w[C::BK / 8];
+                const uint8_t* crow = smem + C::OFF_CODES + s * C::CODE_STAGE + srow * C::CODE_ROW;
+#pragma unroll
+                for (int c = 0; c < C::CODE_ROW / 16; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        crow + (code_chunk_swizzle<C::BK>(c, srow) << 4));
+                    w[4 * c + 0] = v.x;
+                    w[4 * c + 1] = v.y;
+                    w[4 * c + 2] = v.z;
+                    w[4 * c + 3] = v.w;
+                }
+                uint32_t sc[C::BK / 64];  // two bf16 scales per 32-bit word
+                {
+                    const uint8_t* sp = smem + C::OFF_SCALES + s * C::SCALE_STAGE + srow * C::SCALE_ROW;
+                    if constexpr (C::BK == 256) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(sp);
+                        sc[0] = v.x;
+                        sc[1] = v.y;
+                        sc[2] = v.z;
+                        sc[3] = v.w;
+                    } else {
+                        const uint2 v = *reinterpret_cast<const uint2*>(sp);
+                        sc[0] = v.x;
+                        sc[1] = v.y;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(codes_empty(s));
+                const int sa = g % C::AS;
+                if (!mbar_wait(a_empty(sa), ((g / C::AS) & 1) ^ 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c32 = 0; c32 < C::BK / 64; ++c32) {
+                    // 64 elements = 2 scale groups: 2*c32 and 2*c32+1
+                    const uint32_t spair = sc[c32];
+                    const uint32_t s_lo = __byte_perm(spair, 0, 0x1010);  // (s0, s0)
+                    const uint32_t s_hi = __byte_perm(spair, 0, 0x3232);  // (s1, s1)
+                    uint32_t o[32];
+#pragma unroll
+                    for (int wi = 0; wi < 8; ++wi)
+                        dequant_word(w[8 * c32 + wi], wi < 4 ? s_lo : s_hi, &o[4 * wi]);
+                    tmem_st_x32(tmem + tlane + sa * C::A_COLS + c32 * 32, o);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(a_full(sa));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace chord

@@ -1,0 +1,91 @@
+// kernels.h -- launch interfaces of the device code (host side of the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "chord_internal.h"
+
+namespace chord {
+
+struct AlignArgs {
+    const int32_t* topk_ids;
+    int64_t num_pairs;  // T*k, also the sentinel
+    int E_global;
+    const int32_t* expert_map;
+    int E_local;
+    int block_m;
+    int32_t* sorted_ids;
+    int32_t* expert_ids;
+    int32_t* num_tokens_padded;
+    int64_t capacity;
+    int32_t* tile_hist;  // [n_tiles, E_local] scratch
+    int n_tiles;         // ceil(num_pairs / 256)
+    int* err;
+};
+
+enum Layout : int { kLayoutIndexed = 0, kLayoutContiguous = 1, kLayoutMasked = 2 };
+
+struct PrepArgs {
+    int layout;
+    // indexed
+    const int32_t* expert_ids;
+    const int32_t* num_tokens_padded;
+    int64_t capacity;
+    int block_rows;  // block_m (indexed) or 16 (contiguous)
+    // contiguous
+    const int32_t* m_indices;
+    int64_t M;
+    // masked
+    const int32_t* masked_m;
+    int64_t max_m;
+    int E_local;
+    // outputs: two chunk lists (gate_up, down) with their token-tile limits
+    int maxn[2];
+    Chunk* chunks[2];
+    int max_chunks;       // entries of each chunk list
+    int32_t* num_chunks;  // [2]
+    // buffers to clear
+    float* zero_f32;
+    int64_t zero_count;
+    int32_t* fill_i32;  // set to -1
+    int64_t fill_count;
+    int* err;
+};
+
+struct CombineArgs {
+    int64_t T;
+    int k;
+    int H;
+    const int32_t* pair_row;
+    const float* topk_weights;
+    const float* y_pairs;
+    uint16_t* out;
+};
+
+cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
+cudaError_t launch_prep(const PrepArgs& a, int zero_blocks, cudaStream_t s);
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int sms, cudaStream_t s);
+cudaError_t launch_combine_pairs(const CombineArgs& a, cudaStream_t s);
+
+// GEMM kernel configurations (token tile, stage depth, pipeline depths)
+enum GemmConfig : int {
+    kCfgD32 = 0,    // BK 256, token tile <= 32, deep code ring: weight-streaming decode
+    kCfgD64 = 1,    // BK 256, token tile <= 64
+    kCfgD128 = 2,   // BK 256, token tile <= 128
+    kCfgP256 = 3,   // BK 128, token tile <= 256: prefill / short K
+    kNumGemmConfigs = 4
+};
+
+int gemm_cfg_bk(int cfg);
+int gemm_cfg_maxn(int cfg);
+int gemm_cfg_smem(int cfg, bool gate_up);
+
+// Launch one GEMM (gate_up with fused SiLU*up, or down with its epilogue).
+// codes_map: 2-D tensor map over the codes, inner dim K/8 int32 words, outer
+// E*N rows, box {BK/8, gate_up ? 64 : 128}, 128B (BK 256) or 64B (BK 128) swizzle.
+cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& codes_map, const GemmArgs& a,
+                        int grid, cudaStream_t s);
+
+}  // namespace chord

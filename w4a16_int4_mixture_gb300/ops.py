@@ -1,0 +1,267 @@
+"""PyTorch-facing calls of the W4A16 INT4 MoE library.
+
+Thin wrappers over the C ABI (include/chord.h): they check dtypes / devices,
+allocate outputs and workspaces with torch (PyTorch only provides device
+memory and the current stream) and pass raw pointers to the CUDA library.
+
+Layouts (page: "vLLM x Novita AI: Chord W4A16 INT4 MoE kernels for Kimi
+K2.x", sections "Two kernel families", "grouped SM90 kernels", Fig. 3):
+  x            bf16 [T, H]
+  w13_q        int32 [E, 2I, H/8]  packed 4-bit codes, rows 0..I-1 gate, I..2I-1 up
+  w13_s        bf16  [E, 2I, H/32]
+  w2_q         int32 [E, H, I/8]
+  w2_s         bf16  [E, H, I/32]
+  topk_ids     int32 [T, k] global expert ids; topk_weights float32 [T, k]
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _binding as B
+
+ChordError = B.ChordError
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _req(t: torch.Tensor, name: str, dtypes, dev=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dev is not None and t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, expected {dev}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() not in (ndim if isinstance(ndim, tuple) else (ndim,)):
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+_BF16 = (torch.bfloat16,)
+_I32 = (torch.int32,)
+_F32 = (torch.float32,)
+
+
+class _WorkspacePool:
+    """Per-device scratch buffers, grown on demand and reused across calls."""
+
+    def __init__(self):
+        self.bufs = {}
+
+    def get(self, device: torch.device, nbytes: int, key: str) -> torch.Tensor:
+        k = (device.index, key)
+        b = self.bufs.get(k)
+        if b is None or b.numel() < nbytes:
+            b = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+            self.bufs[k] = b
+        return b
+
+
+_pool = _WorkspacePool()
+
+
+def lib():
+    return B.load()
+
+
+def moe_align_capacity(T: int, k: int, E_local: int, block_m: int) -> int:
+    return int(lib().chord_moe_align_capacity(T, k, E_local, block_m))
+
+
+def select_block_m(T: int, k: int, E_global: int, E_local: int, H: int, I: int) -> int:
+    return int(lib().chord_select_block_m(T, k, E_global, E_local, H, I))
+
+
+def describe_schedule(T, k, E_global, E_local, H, I, flags=0) -> str:
+    buf = ctypes.create_string_buffer(256)
+    lib().chord_describe_schedule(T, k, E_global, E_local, H, I, flags, buf, 256)
+    return buf.value.decode()
+
+
+def align_workspace_size(T: int, k: int, E_local: int) -> int:
+    return int(lib().chord_moe_align_workspace_size(T, k, E_local))
+
+
+def moe_align(topk_ids: torch.Tensor, E_global: int, E_local: int, block_m: int = 16,
+              expert_map: Optional[torch.Tensor] = None, capacity: Optional[int] = None,
+              workspace: Optional[torch.Tensor] = None, out=None):
+    """Routing -> (sorted_ids, expert_ids, num_tokens_padded), all device int32."""
+    _req(topk_ids, "topk_ids", _I32, ndim=2)
+    dev = topk_ids.device
+    T, k = topk_ids.shape
+    if expert_map is not None:
+        _req(expert_map, "expert_map", _I32, dev, 1)
+    if capacity is None:
+        capacity = moe_align_capacity(T, k, E_local, block_m)
+    if out is None:
+        sorted_ids = torch.empty(capacity, dtype=torch.int32, device=dev)
+        expert_ids = torch.empty(capacity // block_m, dtype=torch.int32, device=dev)
+        ntp = torch.empty(1, dtype=torch.int32, device=dev)
+    else:
+        sorted_ids, expert_ids, ntp = out
+    need = align_workspace_size(T, k, E_local)
+    ws = workspace if workspace is not None else _pool.get(dev, need, "align")
+    st = lib().chord_moe_align(_p(topk_ids), T, k, E_global, _p(expert_map), E_local, block_m,
+                               _p(sorted_ids), _p(expert_ids), _p(ntp), capacity, _p(ws),
+                               ws.numel(), _stream(dev))
+    B.check(st, "chord_moe_align")
+    return sorted_ids, expert_ids, ntp
+
+
+def _check_weights(w13_q, w13_s, w2_q, w2_s, dev):
+    _req(w13_q, "w13_q", _I32, dev, 3)
+    _req(w13_s, "w13_s", _BF16, dev, 3)
+    _req(w2_q, "w2_q", _I32, dev, 3)
+    _req(w2_s, "w2_s", _BF16, dev, 3)
+    E, N13, H8 = w13_q.shape
+    H = H8 * 8
+    I = N13 // 2
+    if w13_s.shape != (E, 2 * I, H // 32) or w2_q.shape != (E, H, I // 8) or \
+            w2_s.shape != (E, H, I // 32):
+        raise ValueError("weight shapes are not [E,2I,H/8], [E,2I,H/32], [E,H,I/8], [E,H,I/32]")
+    return E, H, I
+
+
+def moe_workspace_size(T, k, E_global, E_local, H, I, block_m, capacity, flags=0) -> int:
+    return int(lib().chord_w4a16_moe_workspace_size(T, k, E_global, E_local, H, I, block_m,
+                                                    capacity, flags))
+
+
+def w4a16_moe_indexed(x, w13_q, w13_s, w2_q, w2_s, topk_weights, sorted_ids, expert_ids,
+                      num_tokens_padded, block_m: int, E_global: int, out=None, workspace=None,
+                      flags: int = 0, h_out=None):
+    """The MoE layer on the moe_align layout; returns out bf16 [T, H].
+    h_out (bf16 [capacity, I]) optionally receives the gate/up output."""
+    _req(x, "x", _BF16, ndim=2)
+    dev = x.device
+    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, dev)
+    T = x.shape[0]
+    if x.shape[1] != H:
+        raise ValueError("x and weights disagree on H")
+    _req(topk_weights, "topk_weights", _F32, dev, 2)
+    k = topk_weights.shape[1]
+    for n, t in (("sorted_ids", sorted_ids), ("expert_ids", expert_ids),
+                 ("num_tokens_padded", num_tokens_padded)):
+        _req(t, n, _I32, dev, 1)
+    capacity = sorted_ids.numel()
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    else:
+        _req(out, "out", _BF16, dev, 2)
+    if h_out is not None:
+        _req(h_out, "h_out", _BF16, dev, 2)
+        if tuple(h_out.shape) != (capacity, I):
+            raise ValueError("h_out must be [capacity, I]")
+    need = moe_workspace_size(T, k, E_global, E, H, I, block_m, capacity, flags)
+    ws = workspace if workspace is not None else _pool.get(dev, need, "layer")
+    st = lib().chord_w4a16_moe_indexed(_p(x), T, H, I, E_global, E, k, _p(w13_q), _p(w13_s),
+                                       _p(w2_q), _p(w2_s), _p(topk_weights), _p(sorted_ids),
+                                       _p(expert_ids), _p(num_tokens_padded), capacity, block_m,
+                                       _p(ws), ws.numel(), _p(out), _p(h_out), flags,
+                                       _stream(dev))
+    B.check(st, "chord_w4a16_moe_indexed")
+    return out
+
+
+def grouped_workspace_size(mode, M, H, I, E_local, T=0, k=0, with_tokens=False, expected_m=1):
+    return int(lib().chord_w4a16_grouped_workspace_size(mode, M, H, I, E_local, T, k,
+                                                        int(with_tokens), expected_m))
+
+
+def w4a16_moe_grouped(mode: str, a, w13_q, w13_s, w2_q, w2_s, m_indices=None, masked_m=None,
+                      expected_m: Optional[int] = None, row_to_pair=None, topk_weights=None,
+                      T: int = 0, out_rows=None, out_tokens=None, workspace=None, flags: int = 0,
+                      h_out=None):
+    """The MoE layer on a grouped layout.
+
+    mode "contiguous": a [M, H] bf16, m_indices int32 [M] (-1 on padding).
+    mode "masked":     a [E, max_m, H] bf16, masked_m int32 [E], expected_m int.
+    Returns out_rows [M, H] (and out_tokens [T, H] when row_to_pair /
+    topk_weights are given)."""
+    dev = a.device
+    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, dev)
+    if mode == "contiguous":
+        _req(a, "a", _BF16, dev, 2)
+        _req(m_indices, "m_indices", _I32, dev, 1)
+        M = a.shape[0]
+        max_m = 0
+        mcode = B.GROUPED_CONTIGUOUS
+        exp_m = expected_m or max(1, M // max(E, 1))
+    elif mode == "masked":
+        _req(a, "a", _BF16, dev, 3)
+        _req(masked_m, "masked_m", _I32, dev, 1)
+        if expected_m is None or expected_m < 1:
+            raise ValueError("masked mode needs a positive expected_m")
+        max_m = a.shape[1]
+        M = a.shape[0] * max_m
+        mcode = B.GROUPED_MASKED
+        exp_m = int(expected_m)
+    else:
+        raise ValueError(f"unknown grouped mode {mode!r}")
+    with_tokens = row_to_pair is not None
+    k = 0
+    if with_tokens:
+        _req(row_to_pair, "row_to_pair", _I32, dev, 1)
+        _req(topk_weights, "topk_weights", _F32, dev, 2)
+        k = topk_weights.shape[1]
+        T = topk_weights.shape[0]
+        if out_tokens is None:
+            out_tokens = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if out_rows is None:
+        out_rows = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    if h_out is not None:
+        _req(h_out, "h_out", _BF16, dev, 2)
+        if tuple(h_out.shape) != (M, I):
+            raise ValueError("h_out must be [M, I]")
+    need = grouped_workspace_size(mcode, M, H, I, E, T, k, with_tokens, exp_m)
+    ws = workspace if workspace is not None else _pool.get(dev, need, "grouped")
+    st = lib().chord_w4a16_moe_grouped(mcode, _p(a), M, H, I, E, _p(m_indices), _p(masked_m),
+                                       max_m, exp_m, _p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s),
+                                       _p(row_to_pair), _p(topk_weights), T, k, _p(ws),
+                                       ws.numel(), _p(out_rows), _p(out_tokens), _p(h_out),
+                                       flags, _stream(dev))
+    B.check(st, "chord_w4a16_moe_grouped")
+    return (out_rows, out_tokens) if with_tokens else out_rows
+
+
+def w4a16_moe(x, topk_ids, topk_weights, w13_q, w13_s, w2_q, w2_s, E_global: int,
+              expert_map=None, block_m: Optional[int] = None, flags: int = 0, out=None):
+    """Align + indexed layer in one call (both graph-capturable)."""
+    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, x.device)
+    T, k = topk_ids.shape
+    bm = block_m or select_block_m(T, k, E_global, E, H, I)
+    si, ei, ntp = moe_align(topk_ids, E_global, E, bm, expert_map=expert_map)
+    return w4a16_moe_indexed(x, w13_q, w13_s, w2_q, w2_s, topk_weights, si, ei, ntp, bm,
+                             E_global, out=out, flags=flags)
+
+
+def get_device_error(workspace: torch.Tensor, clear: bool = False) -> int:
+    """Synchronise and read the device error word of a workspace."""
+    bits = ctypes.c_int(0)
+    lib().chord_get_device_error(_p(workspace), ctypes.byref(bits), int(clear),
+                                 _stream(workspace.device))
+    return bits.value
+
+
+def stage_timing_enable(on: bool = True) -> None:
+    B.check(lib().chord_stage_timing_enable(int(on)), "chord_stage_timing_enable")
+
+
+def stage_timing_read():
+    """Summed ms per stage (prepare, gate_up, down, combine) and the call count."""
+    ms = (ctypes.c_float * 4)()
+    n = ctypes.c_int(0)
+    B.check(lib().chord_stage_timing_read(ms, ctypes.byref(n)), "chord_stage_timing_read")
+    return [float(v) for v in ms], n.value
