@@ -1,0 +1,414 @@
+"""Benchmark of the W4A16 INT4 MoE layer (align + gate/up + SiLU + down + combine).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--T T]
+                    [--impl ours|reference] [--flags F]
+
+Prints ONE JSON line.  A step is one pass of the whole hot path (moe_align +
+the indexed layer) over one batch of synthetic inputs already resident in HBM,
+replayed from a CUDA graph; the weights (1.19 GB for the EP8 workloads) are
+far larger than L2, so every step streams them from HBM.  `value` is
+microseconds per layer call (lower is better).
+
+--impl reference times the CPU oracle (test infrastructure, plain C) on the
+host cores on the same workload: the reference arm of this benchmark.
+Under torchrun each rank runs an independent replica (the layer has no
+cross-GPU step); rank 0 prints the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MoE layer us/call; decode HBM TB/s and prefill BF16 TFLOPS as % of roofline"
+UNIT = "us/call"
+KERNEL_SOURCES = ["gemm_kernel.cuh", "gemm_instances.cuh", "device.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload_bytes_flops(inp):
+    """Algorithmic work of one layer call: each touched expert's codes + scales
+    once, each distinct routed token read once, each token output written once;
+    FLOPs 2 * pairs * (2I*H + H*I)."""
+    from w4a16_int4_mixture_gb300 import synth
+    s = inp.shape
+    lid = synth.local_ids(inp)
+    touched = np.unique(lid[lid >= 0])
+    pairs = int(np.count_nonzero(lid >= 0))
+    tokens = int(np.count_nonzero((lid >= 0).any(axis=1)))
+    w13 = 2 * s.I * s.H // 2 + 2 * s.I * (s.H // 32) * 2
+    w2 = s.H * s.I // 2 + s.H * (s.I // 32) * 2
+    n = len(touched)
+    gate_up = {"weights": n * w13, "x": tokens * s.H * 2, "h": pairs * s.I * 2,
+               "flops": 2 * pairs * 2 * s.I * s.H}
+    down = {"weights": n * w2, "h": pairs * s.I * 2, "flops": 2 * pairs * s.H * s.I}
+    layer = {"bytes": n * (w13 + w2) + tokens * s.H * 2 + s.T * s.H * 2,
+             "flops": gate_up["flops"] + down["flops"]}
+    return {"touched": n, "pairs": pairs, "tokens": tokens, "gate_up": gate_up, "down": down,
+            "layer": layer}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "w4a16_int4_mixture_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, workload: str, src_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, when it was taken on
+    the current kernel source (its hash) and this workload; else None."""
+    pat = re.compile(r"traffic_per_launch\s+kernel=(\S+)\s+workload=(\S+)\s+source=(\S+)\s+"
+                     r"bytes=(\d+)")
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        with open(path) as f:
+            for m in pat.finditer(f.read()):
+                if m.group(1) == kernel and m.group(2) == workload and m.group(3) == src_hash:
+                    return int(m.group(4))
+    return None
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def device_inputs(inp, torch, dev):
+    def t(a, bf16=False):
+        a = np.ascontiguousarray(a)
+        x = torch.from_numpy(a.view(np.int16) if bf16 else a)
+        return (x.view(torch.bfloat16) if bf16 else x).to(dev)
+    d = {"x": t(inp.x, True), "w13_q": t(inp.w13_q), "w13_s": t(inp.w13_s, True),
+         "w2_q": t(inp.w2_q), "w2_s": t(inp.w2_s, True), "ids": t(inp.topk_ids),
+         "tw": t(inp.topk_weights)}
+    d["emap"] = None if inp.expert_map is None else t(inp.expert_map)
+    return d
+
+
+def run_ours(args, rank, world, dev_index):
+    import torch
+    import w4a16_int4_mixture_gb300 as chord
+    from w4a16_int4_mixture_gb300 import synth
+
+    chord.build()
+    torch.cuda.set_device(dev_index)
+    dev = torch.device("cuda", dev_index)
+    s = synth.config(args.config, T=args.T)
+    inp = synth.make_inputs(s)
+    work = workload_bytes_flops(inp)
+    d = device_inputs(inp, torch, dev)
+    bm = chord.select_block_m(s.T, s.k, s.E_global, s.E_local, s.H, s.I)
+    cap = chord.moe_align_capacity(s.T, s.k, s.E_local, bm)
+    si = torch.empty(cap, dtype=torch.int32, device=dev)
+    ei = torch.empty(cap // bm, dtype=torch.int32, device=dev)
+    ntp = torch.empty(1, dtype=torch.int32, device=dev)
+    out = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=dev)
+    ws_a = torch.empty(chord.ops.align_workspace_size(s.T, s.k, s.E_local), dtype=torch.uint8,
+                       device=dev)
+    ws_l = torch.empty(chord.moe_workspace_size(s.T, s.k, s.E_global, s.E_local, s.H, s.I, bm,
+                                                cap, args.flags), dtype=torch.uint8, device=dev)
+    w = (d["w13_q"], d["w13_s"], d["w2_q"], d["w2_s"])
+
+    def step(x=d["x"], ids=d["ids"], tw=d["tw"], o=out):
+        chord.moe_align(ids, s.E_global, s.E_local, bm, expert_map=d["emap"], capacity=cap,
+                        workspace=ws_a, out=(si, ei, ntp))
+        chord.w4a16_moe_indexed(x, *w, tw, si, ei, ntp, bm, s.E_global, out=o, workspace=ws_l,
+                                flags=args.flags)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    torch.cuda.synchronize()
+    launches_per_step = 3 + 4  # align: hist, scan, scatter; layer: prep, gate_up, down, combine
+    if s.T * s.k == 0:
+        launches_per_step = 1
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # warm-up, then the timed region: K graph replays on `stream`
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(dev_index) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # per-stage times (eager launches with stage events on the same stream)
+    chord.stage_timing_enable(True)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            step()
+    stage_ms, calls = chord.stage_timing_read()
+    chord.stage_timing_enable(False)
+    stage = [v / max(calls, 1) for v in stage_ms]
+
+    # end to end through the public API with host buffers
+    hx = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hids = torch.from_numpy(inp.topk_ids).pin_memory()
+    htw = torch.from_numpy(inp.topk_weights).pin_memory()
+    hout = torch.empty((s.T, s.H), dtype=torch.bfloat16).pin_memory()
+    dx, dids, dtw = torch.empty_like(d["x"]), torch.empty_like(d["ids"]), torch.empty_like(d["tw"])
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            if i == args.warmup:
+                e0.record(stream)
+            dx.copy_(hx, non_blocking=True)
+            dids.copy_(hids, non_blocking=True)
+            dtw.copy_(htw, non_blocking=True)
+            chord.w4a16_moe(dx, dids, dtw, *w, s.E_global, expert_map=d["emap"], block_m=bm,
+                            flags=args.flags, out=out)
+            hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = hx.numel() * 2 + hids.numel() * 4 + htw.numel() * 4
+    d2h = hout.numel() * 2
+
+    hbm, tfl, tfl_sus, src = peaks()
+    gu = work["gate_up"]
+    gu_bytes = gu["weights"] + gu["x"] + gu["h"]
+    gu_s = stage[1] / 1e3
+    layer_s = ms / 1e3
+    decode = work["pairs"] / max(work["touched"], 1) < 80
+    src_hash = kernel_source_hash()
+    if decode:
+        ach = gu_bytes / gu_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4)}
+    else:
+        ach = gu["flops"] / gu_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tfl, "unit": "TFLOP/s",
+                "frac": round(ach / tfl, 4)}
+    roof["traffic"] = ncu_traffic("gate_up", s.name, src_hash)
+    roof["kernel"] = "w4a16_gemm_kernel (gate_up, fused SiLU*up)"
+    roof["peak_source"] = f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else src
+    roof["algorithmic_bytes_per_launch"] = int(gu_bytes)
+    roof["launch_ms"] = round(stage[1], 5)
+    layer_tbs = work["layer"]["bytes"] / layer_s / 1e12
+    layer_tflops = work["layer"]["flops"] / layer_s / 1e12
+    res = {
+        "metric": METRIC, "value": round(ms * 1e3, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random INT4 codes / bf16 scales / bf16 activations; "
+                "routing per workload recipe)",
+        "config": {"workload": s.name, "T": s.T, "k": s.k, "E_global": s.E_global,
+                   "E_local": s.E_local, "H": s.H, "I": s.I, "block_m": bm,
+                   "routed_pairs": work["pairs"], "touched_experts": work["touched"],
+                   "schedule": chord.describe_schedule(s.T, s.k, s.E_global, s.E_local, s.H, s.I,
+                                                       args.flags),
+                   "l2": "inputs larger than L2 (weights of the touched experts "
+                         f"{work['layer']['bytes'] / 1e9:.2f} GB per step)",
+                   "timing": "CUDA events over K CUDA-graph replays on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "layer": {"hbm_tbs": round(layer_tbs, 3), "hbm_frac": round(layer_tbs * 1e3 / hbm, 4),
+                  "tflops": round(layer_tflops, 2), "tensor_frac": round(layer_tflops / tfl, 4),
+                  "tensor_frac_sustained": round(layer_tflops / tfl_sus, 4),
+                  "algorithmic_bytes": int(work["layer"]["bytes"]),
+                  "algorithmic_flops": int(work["layer"]["flops"])},
+        "stages_ms": {"prepare": round(stage[0], 5), "gate_up": round(stage[1], 5),
+                      "down": round(stage[2], 5), "combine": round(stage[3], 5)},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "kernel_source": src_hash,
+    }
+    return res, inp
+
+
+def cpu_oracle_time(inp, max_tokens=None):
+    """Wall time of the CPU oracle on (a sample of) the workload: align + layer."""
+    import oracle
+    from w4a16_int4_mixture_gb300 import synth
+    s = inp.shape
+    T = s.T if max_tokens is None else min(s.T, max_tokens)
+    sub = inp
+    if T < s.T:
+        shp = synth.MoEShape(s.name, T=T, k=s.k, E_global=s.E_global, E_local=s.E_local,
+                             H=s.H, I=s.I, block_m=s.block_m)
+        sub = synth.MoEInputs(shp, inp.x[:T], inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s,
+                              inp.topk_ids[:T], inp.topk_weights[:T], inp.expert_map)
+    t0 = time.perf_counter()
+    oracle.run_workload(sub)
+    dt = time.perf_counter() - t0
+    return dt, T, oracle.num_threads()
+
+
+def cpu_baseline(inp):
+    """The oracle on the host cores, on the whole workload when it has at most
+    1024 tokens, else on its first 512 tokens scaled by tokens (a bounded sample
+    of about 10-30 s)."""
+    s = inp.shape
+    max_tok = s.T if s.T <= 1024 else 512
+    dt, T, cores = cpu_oracle_time(inp, max_tok)
+    per_call_us = dt * 1e6 * (s.T / T)
+    sample = (f"CPU oracle (plain C, fp32) on {T} of {s.T} tokens of {s.name}: align + "
+              f"gate/up + SiLU + down + combine, {dt:.2f} s wall; scaled by tokens to one call")
+    return {"value": round(per_call_us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": sample}
+
+
+def run_reference(args):
+    from w4a16_int4_mixture_gb300 import synth
+    import oracle
+    oracle.build()
+    s = synth.config(args.config, T=args.T)
+    inp = synth.make_inputs(s)
+    max_tok = s.T if s.T <= 1024 else 256
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, T, cores = cpu_oracle_time(inp, max_tok)
+        if i >= args.warmup:
+            times.append(dt * (s.T / T))
+    per_call_us = statistics.median(times) * 1e6
+    sample = (f"CPU oracle (plain C, fp32) on {T} of {s.T} tokens of {s.name} per step, scaled "
+              f"by tokens to one call")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(per_call_us, 1), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_call_us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32 (oracle)", "data": "synthetic",
+        "config": {"workload": s.name, "T": s.T, "k": s.k, "E_global": s.E_global,
+                   "E_local": s.E_local, "H": s.H, "I": s.I},
+        "cpu_baseline": {"value": round(per_call_us, 1), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(per_call_us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    res, inp = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(inp)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -356,3 +356,30 @@ def test_config3_tp8(chord, T):
     run = run_indexed_full(chord, inp)
     tokens = None if T <= 128 else np.random.default_rng(1).choice(T, 64, replace=False)
     verify_indexed(inp, run, tokens, label=f"TP8 T={T}")
+
+
+@pytest.mark.parametrize("shape", ["prefill-multiunit", "decode-multiunit"])
+def test_gate_up_bit_reproducible(chord, shape):
+    """The gate/up output is computed without atomics, so repeated runs must be
+    bit-identical.  Run many times on shapes where every CTA walks several work
+    units: this catches shared-memory / tensor-memory races between the roles
+    (it caught a missing async-proxy fence before a codes stage was reused)."""
+    if shape == "prefill-multiunit":
+        inp = small(2048, 8, 48, 48, 1024, 512, 40, emap=False)
+    else:
+        inp = small(512, 8, 64, 64, 2048, 1024, 41, emap=False)
+    s = inp.shape
+    w = weights_to(inp, DEV)
+    x = dev_tensor(inp.x, DEV, True)
+    si, ei, ntp = chord.moe_align(dev_tensor(inp.topk_ids, DEV), s.E_global, s.E_local, 16)
+    tw = dev_tensor(inp.topk_weights, DEV)
+    ref = None
+    for _ in range(12):
+        h = torch.full((si.numel(), s.I), float("nan"), dtype=torch.bfloat16, device=DEV)
+        chord.w4a16_moe_indexed(x, *w, tw, si, ei, ntp, 16, s.E_global, flags=1, h_out=h)
+        torch.cuda.synchronize()
+        cur = h[:int(ntp.item())].view(torch.int16).cpu()
+        if ref is None:
+            ref = cur
+        else:
+            assert torch.equal(cur, ref), "gate/up output changed between identical runs"

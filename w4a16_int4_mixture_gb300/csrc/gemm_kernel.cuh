@@ -485,6 +485,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         sc[1] = v.y;
                     }
                 }
+                // The next TMA into this stage writes through the async proxy;
+                // order these generic-proxy reads before it (without the fence a
+                // few lanes intermittently read the following stage's codes).
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(codes_empty(s));
