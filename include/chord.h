@@ -150,6 +150,32 @@ chord_status chord_moe_align(const int32_t* topk_ids, int64_t T, int k, int E_gl
                              int32_t* num_tokens_padded, int64_t capacity, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/*
+ * chord_moe_align without a workspace.  The page has no counterpart: this is
+ * for callers that cannot allocate device memory or pass a workspace (code
+ * running inside an allocator or memory-pool callback, a plugin whose host owns
+ * every device buffer and hands over only inputs and outputs, a runtime that
+ * forbids allocation once started).  Same arguments, result and limits as
+ * chord_moe_align, minus the workspace; it allocates nothing.
+ *
+ * Its scratch (a per-256-pair-tile expert histogram and an error word) is a
+ * fixed 4 MiB device array inside the library, present on every GPU that
+ * loads it until the process exits.  Limit: ceil(T*k/256) * E_local must not
+ * exceed 1048512 (T*k up to 261888 pairs at the largest E_local of 1024, or
+ * up to about 5.5 million pairs at 48 local experts); larger problems return
+ * CHORD_ERR_UNSUPPORTED_SHAPE.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress), so make
+ * that first call before capturing a stream on that device.  All calls share
+ * the array: calls whose work overlaps on the GPU (different streams, or
+ * different host threads) race and must not be issued; each call rewrites all
+ * the scratch it reads.  Routing errors are recorded in the array and are not
+ * reported back.
+ */
+chord_status chord_moe_align_noalloc(const int32_t* topk_ids, int64_t T, int k, int E_global,
+                                     const int32_t* expert_map, int E_local, int block_m,
+                                     int32_t* sorted_ids, int32_t* expert_ids,
+                                     int32_t* num_tokens_padded, int64_t capacity, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* the MoE layer on the indexed layout                                        */
 /* ------------------------------------------------------------------------- */
