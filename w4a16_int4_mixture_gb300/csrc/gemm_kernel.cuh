@@ -12,11 +12,10 @@
 // Roles (16 warps):
 //   warp 0      TMA producer: packed INT4 codes (TMA tile, L2 evict-first) and
 //               the group-32 scales (cp.async) of each K stage into a ring.
-//   warp 1      token producer: gathers the unit's activation rows (cp.async,
+//   warps 1, 3  token producers: gather the unit's activation rows (cp.async,
 //               zero-fill for sentinel / padding rows) into a 128B-swizzled
 //               K-major ring that is the MMA's B operand.
 //   warp 2      MMA issuer (one thread) and TMEM owner.
-//   warp 3      idle.
 //   warps 4-7   epilogue: TMEM -> registers; gate_up: SiLU(gate)*up -> bf16 h;
 //               down: per-pair fp32 store, fp32 reductions into token rows,
 //               or bf16 row store.
@@ -155,7 +154,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(a_empty(s), 1);          // tcgen05.commit
         }
         for (int s = 0; s < C::BS; ++s) {
-            mbar_init(b_full(s), 32);          // 32 cp.async arrivals
+            mbar_init(b_full(s), 64);          // 2 producer warps x 32 cp.async arrivals
             mbar_init(b_empty(s), 1);
         }
         for (int s = 0; s < C::ACCB; ++s) {
@@ -232,10 +231,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (!ok)  // let the copies already issued land before the CTA goes away
             asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- token producer
+    } else if (warp == 1 || warp == 3) {
+        // ---------------------------------------------------------- token producers
+        // Two warps share the gather: warp 1 takes the even row groups, warp 3
+        // the odd ones.  A row group is the rows one warp-wide pass covers
+        // (CPR 16-byte chunks per row per stage, 32 lanes).
+        const int pw = warp == 1 ? 0 : 1;
         int64_t* rowsrc = reinterpret_cast<int64_t*>(smem + C::OFF_ROWSRC);
-        constexpr int CPR = C::BK / 8;  // 16-byte chunks per row per stage
+        constexpr int CPR = C::BK / 8;            // 16-byte chunks per row per stage
+        constexpr int RPI = 32 / CPR;             // rows per warp-wide pass
+        const int c = lane % CPR;                 // this lane's chunk of a row
+        const int rsub = lane / CPR;              // this lane's row inside a pass
+        const uint32_t lane_dst = (c >> 3) * C::B_REGION;
         int g = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
@@ -243,7 +250,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int ntok = ch.nrows;
             const int ntok16 = (ntok + 15) & ~15;
             __syncwarp();
+            // each warp fills (and later reads) only the entries of its own rows
             for (int r = lane; r < ntok16; r += 32) {
+                if (((r / RPI) & 1) != pw)
+                    continue;
                 int64_t off = -1;
                 if (r < ntok) {
                     const int row = ch.row0 + r;
@@ -267,15 +277,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t bst = sbase + C::OFF_B + s * C::B_STAGE;
-                for (int idx = lane; idx < ntok16 * CPR; idx += 32) {
-                    const int r = idx / CPR;
-                    const int c = idx % CPR;
+                const uint32_t bst = sbase + C::OFF_B + s * C::B_STAGE + lane_dst;
+                const uint16_t* src_k = args.src + ks * C::BK + c * 8;
+                for (int r = (pw * RPI) + rsub; r < ntok16; r += 2 * RPI) {
                     const int64_t off = rowsrc[r];
-                    const uint32_t dst = bst + (c >> 3) * C::B_REGION + r * 128 +
-                                         (((c & 7) ^ (r & 7)) << 4);
-                    const uint16_t* srcp = off >= 0 ? args.src + off + ks * C::BK + c * 8 : args.src;
-                    cp_async_16(dst, srcp, off >= 0 ? 16u : 0u);
+                    const uint32_t dst = bst + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+                    cp_async_16(dst, off >= 0 ? src_k + off : args.src, off >= 0 ? 16u : 0u);
                 }
                 cp_async_arrive_noinc(b_full(s));
             }
@@ -499,16 +506,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int c32 = 0; c32 < C::BK / 64; ++c32) {
-                    // 64 elements = 2 scale groups: 2*c32 and 2*c32+1
-                    const uint32_t spair = sc[c32];
-                    const uint32_t s_lo = __byte_perm(spair, 0, 0x1010);  // (s0, s0)
-                    const uint32_t s_hi = __byte_perm(spair, 0, 0x3232);  // (s1, s1)
-                    uint32_t o[32];
+                for (int grp = 0; grp < C::BK / 32; ++grp) {
+                    // one scale group: 32 elements = 4 code words = 16 TMEM columns
+                    const uint32_t s2 = __byte_perm(sc[grp >> 1], 0, (grp & 1) ? 0x3232 : 0x1010);
+                    uint32_t o[16];
 #pragma unroll
-                    for (int wi = 0; wi < 8; ++wi)
-                        dequant_word(w[8 * c32 + wi], wi < 4 ? s_lo : s_hi, &o[4 * wi]);
-                    tmem_st_x32(tmem + tlane + sa * C::A_COLS + c32 * 32, o);
+                    for (int wi = 0; wi < 4; ++wi)
+                        dequant_word(w[4 * grp + wi], s2, &o[4 * wi]);
+                    tmem_st_x16(tmem + tlane + sa * C::A_COLS + grp * 16, o);
                 }
                 tmem_wait_st();
                 tc_fence_before();
