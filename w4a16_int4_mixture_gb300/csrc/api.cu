@@ -15,17 +15,18 @@
 
 namespace chord {
 
-cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const GemmArgs& a, int grid,
-                                cudaStream_t s);
-cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const GemmArgs& a, int grid,
-                             cudaStream_t s);
+cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const CUtensorMap& bmap,
+                                const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const CUtensorMap& bmap,
+                             const GemmArgs& a, int grid, cudaStream_t s);
 int gemm_cfg_smem_gate_up(int cfg);
 int gemm_cfg_smem_down(int cfg);
 
-cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& map, const GemmArgs& a, int grid,
-                        cudaStream_t s)
+cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& map, const CUtensorMap& bmap,
+                        const GemmArgs& a, int grid, cudaStream_t s)
 {
-    return gate_up ? launch_gemm_gate_up(cfg, map, a, grid, s) : launch_gemm_down(cfg, map, a, grid, s);
+    return gate_up ? launch_gemm_gate_up(cfg, map, bmap, a, grid, s)
+                   : launch_gemm_down(cfg, map, bmap, a, grid, s);
 }
 
 int gemm_cfg_smem(int cfg, bool gate_up)
@@ -72,11 +73,15 @@ chord_status device_info(DeviceInfo* out)
 }
 
 // ---------------------------------------------------------------------------
-// tensor maps over the packed codes, memoised by (pointer, shape, box)
+// tensor maps (packed codes; bf16 token rows), memoised by (kind, pointer,
+// shape, box)
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+enum MapKind : int { kMapCodes = 0, kMapRows = 1 };
+
 struct MapKey {
+    int kind;
     const void* ptr;
     int64_t rows;
     int64_t K;
@@ -85,8 +90,8 @@ struct MapKey {
     int device;
     bool operator==(const MapKey& o) const
     {
-        return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows && bk == o.bk &&
-               device == o.device;
+        return kind == o.kind && ptr == o.ptr && rows == o.rows && K == o.K &&
+               box_rows == o.box_rows && bk == o.bk && device == o.device;
     }
 };
 
@@ -100,11 +105,15 @@ std::mutex g_map_mu;
 std::vector<MapEntry> g_maps;
 uint64_t g_stamp = 0;
 
-chord_status codes_tensor_map(const int32_t* codes, int64_t rows, int64_t K, int box_rows, int bk,
-                              int device, CUtensorMap* out)
+// kMapCodes: int32 words [rows, K/8], box {bk/8, box_rows}, 128B (bk 256) or
+//            64B (bk 128) swizzle.
+// kMapRows:  bf16 [rows, K], box {64, box_rows}, 128B swizzle; rows past the
+//            end read as zero.
+chord_status tensor_map(int kind, const void* ptr, int64_t rows, int64_t K, int box_rows, int bk,
+                        int device, CUtensorMap* out)
 {
     std::lock_guard<std::mutex> lk(g_map_mu);
-    const MapKey key{codes, rows, K, box_rows, bk, device};
+    const MapKey key{kind, ptr, rows, K, box_rows, bk, device};
     for (auto& e : g_maps)
         if (e.key == key) {
             e.stamp = ++g_stamp;
@@ -121,14 +130,24 @@ chord_status codes_tensor_map(const int32_t* codes, int64_t rows, int64_t K, int
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     CUtensorMap m;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 8) * 4};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(bk / 8), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t es[2] = {1, 1};
-    const CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t*>(codes),
-                                dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (kind == kMapCodes) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 8) * 4};
+        cuuint32_t box[2] = {static_cast<cuuint32_t>(bk / 8), static_cast<cuuint32_t>(box_rows)};
+        r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(ptr), dims, strides, box,
+                     es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+        r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS)
         return CHORD_ERR_CUDA;
     if (g_maps.size() >= 32) {
@@ -192,6 +211,7 @@ Schedule pick_schedule(double tok_e, int64_t T, int H, int I, int flags)
 struct Workspace {
     size_t off_hdr = 0;  // int err; int num_chunks[2]
     size_t off_chunks[2] = {0, 0};
+    size_t off_xs = 0;   // indexed: bf16 [capacity, H], token rows in padded-row order
     size_t off_h = 0;
     size_t off_acc = 0;       // reduce: float [T, H]; store: float [T*k, H]
     size_t off_pair_row = 0;  // store: int32 [T*k]
@@ -200,7 +220,7 @@ struct Workspace {
 };
 
 Workspace layout_ws(int64_t max_chunks, int64_t h_rows, int I, int64_t T, int k, int H, bool reduce,
-                    bool with_tokens)
+                    bool with_tokens, int64_t xs_rows)
 {
     Workspace w;
     size_t o = 0;
@@ -211,6 +231,8 @@ Workspace layout_ws(int64_t max_chunks, int64_t h_rows, int I, int64_t T, int k,
         w.off_chunks[L] = o;
         o = align_up(o + static_cast<size_t>(max_chunks) * sizeof(Chunk), kAlign);
     }
+    w.off_xs = o;
+    o = align_up(o + static_cast<size_t>(xs_rows) * H * 2, kAlign);
     w.off_h = o;
     o = align_up(o + static_cast<size_t>(h_rows) * I * 2, kAlign);
     if (with_tokens) {
@@ -336,10 +358,8 @@ chord_status check_shape(int H, int I, int E_local, int k)
 
 // The two GEMMs of one layer call, given a prepared chunk list.
 struct LayerIO {
-    int src_kind;
-    const uint16_t* src;
-    const int32_t* sorted_ids;
-    const int32_t* m_indices;
+    const uint16_t* src;  // token rows in padded-row order: gathered x, or a
+    int64_t src_rows;
     const int32_t* pair_of_row;
     int k;
     int64_t num_pairs;
@@ -357,24 +377,26 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
                        int* err, int32_t* pair_row, float* acc, const DeviceInfo& dev,
                        cudaStream_t s, StageMarks& marks)
 {
-    CUtensorMap map13, map2;
-    chord_status st = codes_tensor_map(io.w13_q, static_cast<int64_t>(io.E_local) * 2 * io.I, io.H,
-                                       64, gemm_cfg_bk(sc.cfg_gate_up), dev.device, &map13);
-    if (st != CHORD_OK)
-        return st;
-    st = codes_tensor_map(io.w2_q, static_cast<int64_t>(io.E_local) * io.H, io.I, 128,
-                          gemm_cfg_bk(sc.cfg_down), dev.device, &map2);
+    uint16_t* h = io.h_out ? io.h_out : reinterpret_cast<uint16_t*>(ws + w.off_h);
+    CUtensorMap map13, map2, bmap13, bmap2;
+    chord_status st = tensor_map(kMapCodes, io.w13_q, static_cast<int64_t>(io.E_local) * 2 * io.I,
+                                 io.H, 64, gemm_cfg_bk(sc.cfg_gate_up), dev.device, &map13);
+    if (st == CHORD_OK)
+        st = tensor_map(kMapCodes, io.w2_q, static_cast<int64_t>(io.E_local) * io.H, io.I, 128,
+                        gemm_cfg_bk(sc.cfg_down), dev.device, &map2);
+    // (a call with no rows has no chunks, so no tile is ever read through these
+    // maps; one row keeps the encoding valid)
+    if (st == CHORD_OK)
+        st = tensor_map(kMapRows, io.src, io.src_rows > 0 ? io.src_rows : 1, io.H,
+                        gemm_cfg_maxn(sc.cfg_gate_up), 0, dev.device, &bmap13);
+    if (st == CHORD_OK)
+        st = tensor_map(kMapRows, h, io.h_rows > 0 ? io.h_rows : 1, io.I,
+                        gemm_cfg_maxn(sc.cfg_down), 0, dev.device, &bmap2);
     if (st != CHORD_OK)
         return st;
     int32_t* num_chunks = reinterpret_cast<int32_t*>(ws + w.off_hdr) + 1;
-    uint16_t* h = io.h_out ? io.h_out : reinterpret_cast<uint16_t*>(ws + w.off_h);
 
     GemmArgs g{};
-    g.src_kind = io.src_kind;
-    g.src = io.src;
-    g.ld_src = io.H;
-    g.sorted_ids = io.sorted_ids;
-    g.m_indices = io.m_indices;
     g.topk = io.k;
     g.num_pairs = static_cast<int>(io.num_pairs);
     g.K = io.H;
@@ -392,14 +414,11 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.pair_of_row = io.pair_of_row;
     g.err = err;
     marks.mark(1);
-    if (launch_gemm(sc.cfg_gate_up, true, map13, g, dev.sms, s) != cudaSuccess)
+    if (launch_gemm(sc.cfg_gate_up, true, map13, bmap13, g, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(2);
 
     GemmArgs d = g;
-    d.src_kind = kSrcDirect;
-    d.src = h;
-    d.ld_src = io.I;
     d.K = io.I;
     d.N = io.H;
     d.n_tiles = io.H / 128;
@@ -412,7 +431,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     d.y_pairs = (io.down_epi & kEpiStorePair) ? acc : nullptr;
     d.out_acc = (io.down_epi & kEpiReduceTok) ? acc : nullptr;
     d.rows_out = io.rows_out;
-    if (launch_gemm(sc.cfg_down, false, map2, d, dev.sms, s) != cudaSuccess)
+    if (launch_gemm(sc.cfg_down, false, map2, bmap2, d, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(3);
     return CHORD_OK;
@@ -489,7 +508,8 @@ size_t chord_w4a16_moe_workspace_size(int64_t T, int k, int E_global, int E_loca
         return 0;
     const double tok_e = E_global > 0 ? static_cast<double>(T) * k / E_global : 0.0;
     const Schedule s = pick_schedule(tok_e, T, H, I, flags);
-    return layout_ws(indexed_max_chunks(E_local, capacity), capacity, I, T, k, H, s.reduce, true)
+    return layout_ws(indexed_max_chunks(E_local, capacity), capacity, I, T, k, H, s.reduce, true,
+                     capacity)
         .total;
 }
 
@@ -501,7 +521,7 @@ size_t chord_w4a16_grouped_workspace_size(int mode, int64_t M, int H, int I, int
         return 0;
     const int64_t max_m = mode == CHORD_GROUPED_MASKED ? M / E_local : 0;
     return layout_ws(grouped_max_chunks(mode, M, E_local, max_m), M, I, T, k, H, true,
-                     with_tokens != 0)
+                     with_tokens != 0, 0)
         .total;
 }
 
@@ -578,7 +598,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     const double tok_e = static_cast<double>(T) * k / E_global;
     const Schedule sc = pick_schedule(tok_e, T, H, I, flags);
     const Workspace w = layout_ws(indexed_max_chunks(E_local, capacity), capacity, I, T, k, H,
-                                  sc.reduce, true);
+                                  sc.reduce, true, capacity);
     if ((st = check_ws(workspace, workspace_bytes, w.total)) != CHORD_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -609,14 +629,23 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
         pa.fill_i32 = pair_row;
         pa.fill_count = T * k;
     }
+    uint16_t* xs = reinterpret_cast<uint16_t*>(ws + w.off_xs);
+    pa.gx_src = x;
+    pa.gx_out = xs;
+    pa.gx_ids = sorted_ids;
+    pa.gx_topk = k;
+    pa.gx_pairs = T * k;
+    pa.gx_H = H;
     pa.err = err;
-    if (launch_prep(pa, zero_blocks_for(sc.reduce ? T * H : T * k, dev.sms), s) != cudaSuccess)
+    int work_blocks = zero_blocks_for(sc.reduce ? T * H : T * k, dev.sms);
+    if (work_blocks < dev.sms)
+        work_blocks = dev.sms;
+    if (launch_prep(pa, work_blocks, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
 
     LayerIO io{};
-    io.src_kind = kSrcIndexed;
-    io.src = x;
-    io.sorted_ids = sorted_ids;
+    io.src = xs;
+    io.src_rows = capacity;
     io.pair_of_row = sorted_ids;
     io.k = k;
     io.num_pairs = T * k;
@@ -701,7 +730,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     Schedule sc = pick_schedule(tok_e, T, H, I, 0);
     sc.reduce = true;
     const Workspace w = layout_ws(grouped_max_chunks(mode, M, E_local, max_m), M, I, T, k, H, true,
-                                  with_tokens);
+                                  with_tokens, 0);
     if ((st = check_ws(workspace, workspace_bytes, w.total)) != CHORD_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -734,9 +763,8 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
         return CHORD_ERR_CUDA;
 
     LayerIO io{};
-    io.src_kind = mode == CHORD_GROUPED_MASKED ? kSrcDirect : kSrcContiguous;
     io.src = a;
-    io.m_indices = m_indices;
+    io.src_rows = M;
     io.pair_of_row = with_tokens ? row_to_pair : nullptr;
     io.k = with_tokens ? k : 1;
     io.num_pairs = with_tokens ? T * k : 0;

@@ -178,6 +178,7 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t s)
 
 // ---------------------------------------------------------------------------
 // per-call preparation: chunk lists for the GEMMs, zeroed / initialised buffers
+// and (indexed layout) the routed token rows gathered into padded-row order
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int chunks_for(int rows, int maxn) { return (rows + maxn - 1) / maxn; }
 
@@ -322,11 +323,42 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
     if (a.fill_i32 != nullptr)
         for (int64_t i = tid; i < a.fill_count; i += nth)
             a.fill_i32[i] = -1;
+    if (a.gx_out != nullptr) {
+        // one warp per padded row, 16-byte vectors, four loads in flight per lane
+        const int lane = threadIdx.x & 31;
+        const int64_t w0 = static_cast<int64_t>(blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+        const int64_t nw = static_cast<int64_t>(gridDim.x - 1) * (blockDim.x >> 5);
+        const int ntp = a.num_tokens_padded[0];
+        const int64_t rows = (ntp >= 0 && ntp <= a.capacity) ? ntp : 0;
+        const int n16 = a.gx_H / 8;
+        for (int64_t r = w0; r < rows; r += nw) {
+            const int p = a.gx_ids[r];
+            if (p < 0 || p >= a.gx_pairs) {
+                // sentinel row: zeros, so its h row is exactly 0
+                uint4* dst = reinterpret_cast<uint4*>(a.gx_out + r * a.gx_H);
+                for (int i = lane; i < n16; i += 32)
+                    dst[i] = make_uint4(0u, 0u, 0u, 0u);
+                continue;
+            }
+            const uint4* src = reinterpret_cast<const uint4*>(a.gx_src + static_cast<int64_t>(p / a.gx_topk) * a.gx_H);
+            uint4* dst = reinterpret_cast<uint4*>(a.gx_out + r * a.gx_H);
+            int i = lane;
+            for (; i + 96 < n16; i += 128) {
+                const uint4 v0 = src[i], v1 = src[i + 32], v2 = src[i + 64], v3 = src[i + 96];
+                dst[i] = v0;
+                dst[i + 32] = v1;
+                dst[i + 64] = v2;
+                dst[i + 96] = v3;
+            }
+            for (; i < n16; i += 32)
+                dst[i] = src[i];
+        }
+    }
 }
 
-cudaError_t launch_prep(const PrepArgs& a, int zero_blocks, cudaStream_t s)
+cudaError_t launch_prep(const PrepArgs& a, int work_blocks, cudaStream_t s)
 {
-    prep_kernel<<<1 + zero_blocks, 1024, 0, s>>>(a);
+    prep_kernel<<<1 + work_blocks, 1024, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -15,13 +15,6 @@ struct Chunk {
     int32_t seg0;    // first row of the expert's segment (unused by the GEMMs)
 };
 
-// How rows of the B operand (activations) are found.
-enum BSource : int {
-    kSrcIndexed = 0,     // row r -> token sorted_ids[r] / k of x; sentinel -> zero row
-    kSrcContiguous = 1,  // row r of a; m_indices[r] < 0 -> zero row
-    kSrcDirect = 2,      // row r of src (masked layout, or h for the down GEMM)
-};
-
 // Down-GEMM epilogue forms (bit set).
 enum Epilogue : int {
     kEpiStorePair = 1,   // y_pairs[p, n] = y (fp32) for the pair of each row
@@ -30,12 +23,8 @@ enum Epilogue : int {
 };
 
 struct GemmArgs {
-    // B operand
-    int src_kind;
-    const uint16_t* src;      // x, a or h
-    int64_t ld_src;           // elements between rows of src
-    const int32_t* sorted_ids;
-    const int32_t* m_indices;
+    // B operand: the token rows of each chunk are contiguous in the tensor map
+    // passed next to the codes map (x gathered into padded-row order, a, or h)
     int topk;
     int num_pairs;            // T*k, the sentinel
     // problem

@@ -3,14 +3,14 @@
 
 namespace chord {
 
-cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const GemmArgs& a, int grid,
-                                cudaStream_t s)
+cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const CUtensorMap& bmap,
+                                const GemmArgs& a, int grid, cudaStream_t s)
 {
     switch (cfg) {
-    case kCfgD32: return launch_gemm_cfg<CfgD32<true>>(map, a, grid, s);
-    case kCfgD64: return launch_gemm_cfg<CfgD64<true>>(map, a, grid, s);
-    case kCfgD128: return launch_gemm_cfg<CfgD128<true>>(map, a, grid, s);
-    case kCfgP256: return launch_gemm_cfg<CfgP256<true>>(map, a, grid, s);
+    case kCfgD32: return launch_gemm_cfg<CfgD32<true>>(map, bmap, a, grid, s);
+    case kCfgD64: return launch_gemm_cfg<CfgD64<true>>(map, bmap, a, grid, s);
+    case kCfgD128: return launch_gemm_cfg<CfgD128<true>>(map, bmap, a, grid, s);
+    case kCfgP256: return launch_gemm_cfg<CfgP256<true>>(map, bmap, a, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }

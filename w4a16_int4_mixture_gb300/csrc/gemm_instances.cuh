@@ -13,17 +13,24 @@ template <bool G> using CfgD128 = GemmCfg<256, 4, 2, 2, 128, 2, G>;
 template <bool G> using CfgP256 = GemmCfg<128, 4, 2, 4, 256, 1, G>;
 
 template <class C>
-cudaError_t launch_gemm_cfg(const CUtensorMap& map, const GemmArgs& a, int grid, cudaStream_t s)
+cudaError_t launch_gemm_cfg(const CUtensorMap& map, const CUtensorMap& bmap, const GemmArgs& a,
+                            int grid, cudaStream_t s)
 {
-    static bool attr_set = false;  // set once per configuration (first launch)
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(w4a16_gemm_kernel<C>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    static bool attr_set[64] = {};  // per device, set on the first launch there
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(w4a16_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
-        attr_set = true;
+        attr_set[dev] = true;
     }
-    w4a16_gemm_kernel<C><<<grid, kGemmThreads, C::SMEM_BYTES, s>>>(map, a);
+    w4a16_gemm_kernel<C><<<grid, kGemmThreads, C::SMEM_BYTES, s>>>(map, bmap, a);
     return cudaGetLastError();
 }
 

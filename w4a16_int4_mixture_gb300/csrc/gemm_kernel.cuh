@@ -10,12 +10,14 @@
 // the MMA-M operand), used here for every token count.
 //
 // Roles (16 warps):
-//   warp 0      TMA producer: packed INT4 codes (TMA tile, L2 evict-first) and
+//   warp 0      code producer: packed INT4 codes (TMA tile, L2 evict-first) and
 //               the group-32 scales (cp.async) of each K stage into a ring.
-//   warps 1, 3  token producers: gather the unit's activation rows (cp.async,
-//               zero-fill for sentinel / padding rows) into a 128B-swizzled
-//               K-major ring that is the MMA's B operand.
-//   warp 2      MMA issuer (one thread) and TMEM owner.
+//   warp 1      token producer: the chunk's activation rows, contiguous in the
+//               B tensor map, as 128B-swizzled K-major TMA tiles of MAXN rows
+//               (the rows past the chunk only feed discarded columns).
+//   warp 2      MMA issuer (the whole warp walks the schedule; elect.sync picks
+//               the issuing lane) and TMEM owner.
+//   warp 3      idle.
 //   warps 4-7   epilogue: TMEM -> registers; gate_up: SiLU(gate)*up -> bf16 h;
 //               down: per-pair fp32 store, fp32 reductions into token rows,
 //               or bf16 row store.
@@ -55,8 +57,7 @@ struct GemmCfg {
     static constexpr int OFF_B = OFF_CODES + KS * CODE_STAGE;
     static constexpr int OFF_SCALES = OFF_B + BS * B_STAGE;
     static constexpr int OFF_HS = OFF_SCALES + KS * SCALE_STAGE;
-    static constexpr int OFF_ROWSRC = OFF_HS + HS_BYTES;
-    static constexpr int OFF_BARS = OFF_ROWSRC + MAXN * 8;
+    static constexpr int OFF_BARS = OFF_HS + HS_BYTES;
     static constexpr int NBARS = 2 * KS + 2 * AS + 2 * BS + 2 * ACCB + 2;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -117,7 +118,8 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t* 
 
 template <class C>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap codes_map, const GemmArgs args)
+    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap codes_map,
+                      const __grid_constant__ CUtensorMap b_map, const GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(a_empty(s), 1);          // tcgen05.commit
         }
         for (int s = 0; s < C::BS; ++s) {
-            mbar_init(b_full(s), 64);          // 2 producer warps x 32 cp.async arrivals
+            mbar_init(b_full(s), 1);           // expect_tx arrive
             mbar_init(b_empty(s), 1);
         }
         for (int s = 0; s < C::ACCB; ++s) {
@@ -168,6 +170,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (warp == 0 && lane == 0)
         prefetch_tensormap(&codes_map);
+    if (warp == 1 && lane == 0)
+        prefetch_tensormap(&b_map);
     if (warp == 2)
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tc_fence_before();
@@ -231,114 +235,81 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (!ok)  // let the copies already issued land before the CTA goes away
             asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == 1 || warp == 3) {
-        // ---------------------------------------------------------- token producers
-        // Two warps share the gather: warp 1 takes the even row groups, warp 3
-        // the odd ones.  A row group is the rows one warp-wide pass covers
-        // (CPR 16-byte chunks per row per stage, 32 lanes).
-        const int pw = warp == 1 ? 0 : 1;
-        int64_t* rowsrc = reinterpret_cast<int64_t*>(smem + C::OFF_ROWSRC);
-        constexpr int CPR = C::BK / 8;            // 16-byte chunks per row per stage
-        constexpr int RPI = 32 / CPR;             // rows per warp-wide pass
-        const int c = lane % CPR;                 // this lane's chunk of a row
-        const int rsub = lane / CPR;              // this lane's row inside a pass
-        const uint32_t lane_dst = (c >> 3) * C::B_REGION;
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- token producer
+        const uint64_t pol = policy_evict_last();
         int g = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            const Chunk ch = args.chunks[u / n_tiles];
-            const int ntok = ch.nrows;
-            const int ntok16 = (ntok + 15) & ~15;
-            __syncwarp();
-            // each warp fills (and later reads) only the entries of its own rows
-            for (int r = lane; r < ntok16; r += 32) {
-                if (((r / RPI) & 1) != pw)
-                    continue;
-                int64_t off = -1;
-                if (r < ntok) {
-                    const int row = ch.row0 + r;
-                    if (args.src_kind == kSrcIndexed) {
-                        const int p = args.sorted_ids[row];
-                        if (p >= 0 && p < args.num_pairs)
-                            off = static_cast<int64_t>(p / args.topk) * args.ld_src;
-                    } else if (args.src_kind == kSrcContiguous) {
-                        if (args.m_indices[row] >= 0)
-                            off = static_cast<int64_t>(row) * args.ld_src;
-                    } else {
-                        off = static_cast<int64_t>(row) * args.ld_src;
-                    }
-                }
-                rowsrc[r] = off;
-            }
-            __syncwarp();
+            const int row0 = args.chunks[u / n_tiles].row0;
             for (int ks = 0; ks < KT; ++ks, ++g) {
                 const int s = g % C::BS;
                 if (!mbar_wait(b_empty(s), ((g / C::BS) & 1) ^ 1, abort_flag, err)) {
                     ok = false;
                     break;
                 }
-                const uint32_t bst = sbase + C::OFF_B + s * C::B_STAGE + lane_dst;
-                const uint16_t* src_k = args.src + ks * C::BK + c * 8;
-                for (int r = (pw * RPI) + rsub; r < ntok16; r += 2 * RPI) {
-                    const int64_t off = rowsrc[r];
-                    const uint32_t dst = bst + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-                    cp_async_16(dst, off >= 0 ? src_k + off : args.src, off >= 0 ? 16u : 0u);
+                if (lane == 0) {
+                    const uint32_t dst = sbase + C::OFF_B + s * C::B_STAGE;
+                    mbar_arrive_expect_tx(b_full(s), C::B_STAGE);
+#pragma unroll
+                    for (int kb = 0; kb < C::B_KBLK; ++kb)
+                        tma_load_2d(dst + kb * C::B_REGION, &b_map, ks * C::BK + kb * 64, row0,
+                                    b_full(s), pol);
                 }
-                cp_async_arrive_noinc(b_full(s));
+                __syncwarp();
             }
         }
-        if (!ok)
-            asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == 2) {
         // ------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            int g = 0;
-            int issued = 0;
-            bool ok = true;
-            int i = 0;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++i) {
-                const Chunk ch = args.chunks[u / n_tiles];
-                const int ntok16 = (ch.nrows + 15) & ~15;
-                const uint32_t idesc = idesc_bf16_f32(128, ntok16);
-                const int acc = i % C::ACCB;
-                if (!mbar_wait(d_empty(acc), ((i / C::ACCB) & 1) ^ 1, abort_flag, err)) {
+        // The whole warp walks the schedule (so every operand stays warp-uniform)
+        // and elect.sync picks the lane that issues each MMA and commit.
+        int g = 0;
+        int issued = 0;
+        bool ok = true;
+        int i = 0;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++i) {
+            const Chunk ch = args.chunks[u / n_tiles];
+            const int ntok16 = (ch.nrows + 15) & ~15;
+            const uint32_t idesc = idesc_bf16_f32(128, ntok16);
+            const int acc = i % C::ACCB;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(d_empty(acc), ((i / C::ACCB) & 1) ^ 1, abort_flag, err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + C::D_COL0 + acc * C::MAXN;
+            for (int ks = 0; ks < KT; ++ks, ++g) {
+                const int sa = g % C::AS;
+                const int sb = g % C::BS;
+                const bool got = mbar_wait(a_full(sa), (g / C::AS) & 1, abort_flag, err) &&
+                                 mbar_wait(b_full(sb), (g / C::BS) & 1, abort_flag, err);
+                if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + C::D_COL0 + acc * C::MAXN;
-                for (int ks = 0; ks < KT; ++ks, ++g) {
-                    const int sa = g % C::AS;
-                    const int sb = g % C::BS;
-                    if (!mbar_wait(a_full(sa), (g / C::AS) & 1, abort_flag, err) ||
-                        !mbar_wait(b_full(sb), (g / C::BS) & 1, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async_smem();  // cp.async (generic proxy) -> tensor core reads
-                    tc_fence_after();
-                    const uint32_t a_base = tmem + sa * C::A_COLS;
-                    const uint32_t b_base = sbase + C::OFF_B + sb * C::B_STAGE;
+                const uint32_t a_base = tmem + sa * C::A_COLS;
+                const uint32_t b_base = sbase + C::OFF_B + sb * C::B_STAGE;
 #pragma unroll
-                    for (int j = 0; j < C::BK / 16; ++j) {
-                        const uint64_t bdesc =
-                            smem_desc_sw128(b_base + (j >> 2) * C::B_REGION + (j & 3) * 32);
-                        mma_ts(d_tmem, a_base + j * 8, bdesc, idesc, (ks | j) != 0 ? 1u : 0u);
-                    }
-                    issued = 1;
-                    mma_commit(a_empty(sa));
-                    mma_commit(b_empty(sb));
+                for (int j = 0; j < C::BK / 16; ++j) {
+                    const uint64_t bdesc =
+                        smem_desc_sw128(b_base + (j >> 2) * C::B_REGION + (j & 3) * 32);
+                    mma_ts_elect(d_tmem, a_base + j * 8, bdesc, idesc, (ks | j) != 0 ? 1u : 0u);
                 }
-                if (!ok)
-                    break;
-                mma_commit(d_full(acc));
+                issued = 1;
+                mma_commit_elect(a_empty(sa));
+                mma_commit_elect(b_empty(sb));
             }
-            if (!ok && issued) {
-                // drain tensor-core work in flight before TMEM is released
-                mma_commit(drain_bar);
-                const uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
-                }
+            if (!ok)
+                break;
+            mma_commit_elect(d_full(acc));
+        }
+        if (!ok && issued) {
+            // drain tensor-core work in flight before TMEM is released
+            mma_commit_elect(drain_bar);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
         __syncwarp();
@@ -466,17 +437,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     ok = false;
                     break;
                 }
-                uint32_t w[C::BK / 8];
                 const uint8_t* crow = smem + C::OFF_CODES + s * C::CODE_STAGE + srow * C::CODE_ROW;
-#pragma unroll
-                for (int c = 0; c < C::CODE_ROW / 16; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(
-                        crow + (code_chunk_swizzle<C::BK>(c, srow) << 4));
-                    w[4 * c + 0] = v.x;
-                    w[4 * c + 1] = v.y;
-                    w[4 * c + 2] = v.z;
-                    w[4 * c + 3] = v.w;
-                }
                 uint32_t sc[C::BK / 64];  // two bf16 scales per 32-bit word
                 {
                     const uint8_t* sp = smem + C::OFF_SCALES + s * C::SCALE_STAGE + srow * C::SCALE_ROW;
@@ -492,29 +453,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         sc[1] = v.y;
                     }
                 }
-                // The next TMA into this stage writes through the async proxy;
-                // order these generic-proxy reads before it (without the fence a
-                // few lanes intermittently read the following stage's codes).
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(codes_empty(s));
                 const int sa = g % C::AS;
                 if (!mbar_wait(a_empty(sa), ((g / C::AS) & 1) ^ 1, abort_flag, err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                // One scale group per step: 32 elements = one 16-byte chunk of codes =
+                // 16 TMEM columns.  Codes are read from shared memory group by group
+                // (not all up front) so the stores of one group overlap the
+                // arithmetic of the next without running out of registers.
 #pragma unroll
                 for (int grp = 0; grp < C::BK / 32; ++grp) {
-                    // one scale group: 32 elements = 4 code words = 16 TMEM columns
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        crow + (code_chunk_swizzle<C::BK>(grp, srow) << 4));
                     const uint32_t s2 = __byte_perm(sc[grp >> 1], 0, (grp & 1) ? 0x3232 : 0x1010);
                     uint32_t o[16];
-#pragma unroll
-                    for (int wi = 0; wi < 4; ++wi)
-                        dequant_word(w[4 * grp + wi], s2, &o[4 * wi]);
+                    dequant_word(v.x, s2, &o[0]);
+                    dequant_word(v.y, s2, &o[4]);
+                    dequant_word(v.z, s2, &o[8]);
+                    dequant_word(v.w, s2, &o[12]);
                     tmem_st_x16(tmem + tlane + sa * C::A_COLS + grp * 16, o);
                 }
+                // The next TMA into this code stage writes through the async proxy;
+                // order these generic-proxy reads before it (without the fence a
+                // few lanes intermittently read the following stage's codes).
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(codes_empty(s));
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();

@@ -46,6 +46,15 @@ struct PrepArgs {
     Chunk* chunks[2];
     int max_chunks;       // entries of each chunk list
     int32_t* num_chunks;  // [2]
+    // indexed layout: gather the routed token rows of x into padded-row order
+    // (gx_out[r] = x[sorted_ids[r] / topk] for r < num_tokens_padded and a valid
+    // pair, zeros for sentinel rows)
+    const uint16_t* gx_src;  // x [T, gx_H]
+    uint16_t* gx_out;        // [capacity, gx_H]
+    const int32_t* gx_ids;   // sorted_ids
+    int gx_topk;
+    int64_t gx_pairs;        // T*k, the sentinel
+    int gx_H;
     // buffers to clear
     float* zero_f32;
     int64_t zero_count;
@@ -65,7 +74,7 @@ struct CombineArgs {
 };
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
-cudaError_t launch_prep(const PrepArgs& a, int zero_blocks, cudaStream_t s);
+cudaError_t launch_prep(const PrepArgs& a, int work_blocks, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int sms, cudaStream_t s);
 cudaError_t launch_combine_pairs(const CombineArgs& a, cudaStream_t s);
 
@@ -85,7 +94,9 @@ int gemm_cfg_smem(int cfg, bool gate_up);
 // Launch one GEMM (gate_up with fused SiLU*up, or down with its epilogue).
 // codes_map: 2-D tensor map over the codes, inner dim K/8 int32 words, outer
 // E*N rows, box {BK/8, gate_up ? 64 : 128}, 128B (BK 256) or 64B (BK 128) swizzle.
-cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& codes_map, const GemmArgs& a,
-                        int grid, cudaStream_t s);
+// b_map: 2-D tensor map over the bf16 token rows (padded-row order), inner dim
+// K, box {64, token tile}, 128B swizzle, zero fill past the last row.
+cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& codes_map,
+                        const CUtensorMap& b_map, const GemmArgs& a, int grid, cudaStream_t s);
 
 }  // namespace chord
