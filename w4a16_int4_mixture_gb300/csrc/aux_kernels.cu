@@ -391,55 +391,58 @@ __global__ void finalize_kernel(const float* __restrict__ acc, uint16_t* __restr
         out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i]));
 }
 
-// Ordered top-k combine of per-pair fp32 outputs.  One warp per (token,
-// 16-column chunk).  Lane = (slot group j8 = lane/4, column quad cq = lane%4);
-// each lane weights its slot's float4, then the 8 slot groups are summed with a
-// fixed warp-shuffle tree (xor 4, 8, 16), so the result is bit-identical run to
-// run.  Slots are visited in ascending order in groups of 8 (k <= 32).
-__global__ void combine_pairs_kernel(CombineArgs a)
+// Ordered top-k combine of per-pair fp32 outputs.  One block per token
+// (grid-stride): the token's local slots are compacted once into shared memory
+// in ascending slot order, then each thread produces 8 output columns as
+// sum_j w_j * y_j over those slots in that order, so the result is
+// bit-identical run to run.  A token with no local slot gets zeros.
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_pairs_kernel(CombineArgs a)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int chunks_per_tok = a.H / 16;
-    if (gw >= a.T * chunks_per_tok)
-        return;
-    const int64_t t = gw / chunks_per_tok;
-    const int col0 = static_cast<int>(gw % chunks_per_tok) * 16;
-    // routing metadata of this token, one slot per lane, broadcast by shuffles
-    int valid = 0;
-    float w = 0.f;
-    if (lane < a.k) {
-        const int64_t p = t * a.k + lane;
-        valid = a.pair_row[p] >= 0;
-        w = a.topk_weights[p];
-    }
-    const int j8 = lane >> 2, cq = lane & 3;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int jb = 0; jb < a.k; jb += 8) {
-        const int j = jb + j8;
-        const int vj = __shfl_sync(0xffffffffu, valid, j & 31);
-        const float wj = __shfl_sync(0xffffffffu, w, j & 31);
-        if (j < a.k && vj) {
-            const float4 y =
-                *reinterpret_cast<const float4*>(a.y_pairs + (t * a.k + j) * a.H + col0 + cq * 4);
-            acc.x += wj * y.x;
-            acc.y += wj * y.y;
-            acc.z += wj * y.z;
-            acc.w += wj * y.w;
+    __shared__ int64_t s_pair[32];
+    __shared__ float s_w[32];
+    __shared__ int s_n;
+    const int H8 = a.H / 8;
+    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+        if (threadIdx.x < 32) {
+            const int j = threadIdx.x;
+            const int64_t p = t * a.k + j;
+            const bool valid = j < a.k && a.pair_row[p] >= 0;
+            const uint32_t m = __ballot_sync(0xffffffffu, valid);
+            if (valid) {
+                const int idx = __popc(m & ((1u << j) - 1u));
+                s_pair[idx] = p;
+                s_w[idx] = a.topk_weights[p];
+            }
+            if (j == 0)
+                s_n = __popc(m);
         }
-    }
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
-        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
-        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
-        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
-    }
-    if (j8 == 0) {
-        uint2 o;
-        o.x = pack_bf16x2(acc.x, acc.y);
-        o.y = pack_bf16x2(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(a.out + t * a.H + col0 + cq * 4) = o;
+        __syncthreads();
+        const int n = s_n;
+        for (int c = threadIdx.x; c < H8; c += blockDim.x) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int i = 0; i < n; ++i) {
+                const float4* y = reinterpret_cast<const float4*>(a.y_pairs + s_pair[i] * a.H) + 2 * c;
+                const float4 y0 = y[0], y1 = y[1];
+                const float w = s_w[i];
+                acc[0] += w * y0.x;
+                acc[1] += w * y0.y;
+                acc[2] += w * y0.z;
+                acc[3] += w * y0.w;
+                acc[4] += w * y1.x;
+                acc[5] += w * y1.y;
+                acc[6] += w * y1.z;
+                acc[7] += w * y1.w;
+            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            reinterpret_cast<uint4*>(a.out + t * a.H)[c] = o;
+        }
+        __syncthreads();
     }
 }
 
@@ -458,11 +461,10 @@ cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int sms,
 
 cudaError_t launch_combine_pairs(const CombineArgs& a, cudaStream_t s)
 {
-    const int64_t warps = a.T * (a.H / 16);
-    if (warps <= 0)
+    if (a.T <= 0)
         return cudaSuccess;
-    const int64_t blocks = (warps * 32 + 255) / 256;
-    combine_pairs_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    const int64_t blocks = a.T < 65535 ? a.T : 65535;
+    combine_pairs_kernel<<<static_cast<unsigned>(blocks), kCombineThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

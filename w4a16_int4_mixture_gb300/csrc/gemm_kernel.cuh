@@ -52,12 +52,15 @@ struct GemmCfg {
     static constexpr int B_REGION = MAXN * 128;             // one atom column of the tile
     static constexpr int B_STAGE = B_KBLK * B_REGION;
     static constexpr int HS_BYTES = GATE_UP ? MAXN * 128 : 0;  // 64 channels of bf16 per row
+    // down: per token column (pair, token, weight), double-buffered by unit
+    static constexpr int META_BYTES = GATE_UP ? 0 : 2 * 3 * MAXN * 4;
 
     static constexpr int OFF_CODES = 0;
     static constexpr int OFF_B = OFF_CODES + KS * CODE_STAGE;
     static constexpr int OFF_SCALES = OFF_B + BS * B_STAGE;
     static constexpr int OFF_HS = OFF_SCALES + KS * SCALE_STAGE;
-    static constexpr int OFF_BARS = OFF_HS + HS_BYTES;
+    static constexpr int OFF_META = OFF_HS + HS_BYTES;
+    static constexpr int OFF_BARS = OFF_META + META_BYTES;
     static constexpr int NBARS = 2 * KS + 2 * AS + 2 * BS + 2 * ACCB + 2;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -334,7 +337,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int ntok = ch.nrows;
             const int ntok16 = (ntok + 15) & ~15;
             const int acc = i % C::ACCB;
+            // down: pair, token and weight of each column, staged once per unit
+            // (before the accumulator wait, so the loads overlap the MMAs)
+            int32_t* m_pair = reinterpret_cast<int32_t*>(smem + C::OFF_META) + (i & 1) * 3 * C::MAXN;
+            int32_t* m_tok = m_pair + C::MAXN;
+            float* m_w = reinterpret_cast<float*>(m_pair + 2 * C::MAXN);
+            const bool per_pair = !C::GATE_UP && (args.epi & (kEpiStorePair | kEpiReduceTok)) != 0;
+            if (per_pair) {
+                for (int c = et; c < ntok; c += 128) {
+                    int p = args.pair_of_row ? args.pair_of_row[ch.row0 + c] : -1;
+                    if (p < 0 || p >= args.num_pairs)
+                        p = -1;
+                    m_pair[c] = p;
+                    m_tok[c] = p >= 0 ? p / args.topk : 0;
+                    m_w[c] = (p >= 0 && args.topk_weights) ? args.topk_weights[p] : 0.f;
+                }
+            }
             if (!mbar_wait(d_full(acc), (i / C::ACCB) & 1, abort_flag, err))
+                break;
+            if (per_pair && !epi_sync())
                 break;
             tc_fence_after();
             const uint32_t dbase =
@@ -393,19 +414,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const int c = c0 + jj;
                         if (c >= ntok)
                             break;
-                        const int row = ch.row0 + c;
                         const float y = __uint_as_float(v[jj]);
                         if (args.epi & kEpiStoreRows)
-                            args.rows_out[static_cast<int64_t>(row) * N + n] =
+                            args.rows_out[static_cast<int64_t>(ch.row0 + c) * N + n] =
                                 __bfloat16_as_ushort(__float2bfloat16_rn(y));
-                        if (args.epi & (kEpiStorePair | kEpiReduceTok)) {
-                            const int p = args.pair_of_row ? args.pair_of_row[row] : -1;
-                            if (p >= 0 && p < args.num_pairs) {
+                        if (per_pair) {
+                            const int p = m_pair[c];
+                            if (p >= 0) {
                                 if (args.epi & kEpiStorePair)
                                     args.y_pairs[static_cast<int64_t>(p) * N + n] = y;
                                 if (args.epi & kEpiReduceTok)
-                                    red_add_f32(args.out_acc + static_cast<int64_t>(p / args.topk) * N + n,
-                                                args.topk_weights[p] * y);
+                                    red_add_f32(args.out_acc + static_cast<int64_t>(m_tok[c]) * N + n,
+                                                m_w[c] * y);
                             }
                         }
                     }
