@@ -284,9 +284,12 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&v)[16])
         : "memory");
 }
 
+// Fire-and-forget fp32 reduction.  No "memory" clobber: nothing in the kernel
+// reads the target after it, and a clobber would serialise the caller's
+// independent loads behind every reduction.
 __device__ __forceinline__ void red_add_f32(float* addr, float v)
 {
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v));
 }
 
 }  // namespace chord

@@ -1,7 +1,7 @@
 // gemm_kernel.cuh -- the W4A16 expert GEMM for sm_103a (tcgen05 + TMEM + TMA).
 //
-// One persistent CTA per SM walks work units (chunk of padded rows that share
-// an expert) x (128-row tile of that expert's weight).  Per unit it computes
+// One persistent CTA per SM walks a contiguous range of work units (chunk of
+// padded rows that share an expert) x (128-row tile of that expert's weight).  Per unit it computes
 //   D[128 weight rows, ntok tokens] = W_tile[128, K] * X_rows[ntok, K]^T
 // with the dequantised weights as the MMA's M operand (held in tensor memory)
 // and the routed tokens as its N operand (in shared memory).  This is the
@@ -183,8 +183,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     const int n_tiles = args.n_tiles;
-    const int total_units = args.num_chunks[0] * n_tiles;
     const int KT = args.K / C::BK;
+    // Units are dealt to CTAs with a stride of the grid, so at any time the
+    // CTAs work on neighbouring units: a few chunks, whose token tiles stay hot
+    // in L2 across the CTAs that share them.  Each role loads the descriptor of
+    // its next unit one unit ahead.
+    const int total_units = args.num_chunks[0] * n_tiles;
+    auto chunk_of = [&](int u) -> Chunk {
+        return u < total_units ? args.chunks[u / n_tiles] : Chunk{};
+    };
     int* err = args.err;
 
     if (warp == 0) {
@@ -192,8 +199,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint64_t pol = policy_evict_first();
         int g = 0;
         bool ok = true;
+        Chunk next = chunk_of(blockIdx.x);
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            const Chunk ch = args.chunks[u / n_tiles];
+            const Chunk ch = next;
+            next = chunk_of(u + gridDim.x);
             const int nt = u % n_tiles;
             const int e = ch.expert;
             int grow_a, grow_b;
@@ -243,8 +252,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint64_t pol = policy_evict_last();
         int g = 0;
         bool ok = true;
+        Chunk next = chunk_of(blockIdx.x);
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            const int row0 = args.chunks[u / n_tiles].row0;
+            const int row0 = next.row0;
+            next = chunk_of(u + gridDim.x);
             for (int ks = 0; ks < KT; ++ks, ++g) {
                 const int s = g % C::BS;
                 if (!mbar_wait(b_empty(s), ((g / C::BS) & 1) ^ 1, abort_flag, err)) {
@@ -270,8 +281,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int issued = 0;
         bool ok = true;
         int i = 0;
+        Chunk next = chunk_of(blockIdx.x);
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++i) {
-            const Chunk ch = args.chunks[u / n_tiles];
+            const Chunk ch = next;
+            next = chunk_of(u + gridDim.x);
             const int ntok16 = (ch.nrows + 15) & ~15;
             const uint32_t idesc = idesc_bf16_f32(128, ntok16);
             const int acc = i % C::ACCB;
@@ -331,8 +344,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             return r;
         };
         int i = 0;
+        Chunk next = chunk_of(blockIdx.x);
         for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++i) {
-            const Chunk ch = args.chunks[u / n_tiles];
+            const Chunk ch = next;
+            next = chunk_of(u + gridDim.x);
             const int nt = u % n_tiles;
             const int ntok = ch.nrows;
             const int ntok16 = (ntok + 15) & ~15;
@@ -409,24 +424,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t v[16];
                     tmem_ld_x16(dbase + c0, v);
                     tmem_wait_ld();
+                    if (args.epi & kEpiStoreRows) {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int c = c0 + jj;
-                        if (c >= ntok)
-                            break;
-                        const float y = __uint_as_float(v[jj]);
-                        if (args.epi & kEpiStoreRows)
-                            args.rows_out[static_cast<int64_t>(ch.row0 + c) * N + n] =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(y));
-                        if (per_pair) {
-                            const int p = m_pair[c];
-                            if (p >= 0) {
-                                if (args.epi & kEpiStorePair)
-                                    args.y_pairs[static_cast<int64_t>(p) * N + n] = y;
-                                if (args.epi & kEpiReduceTok)
-                                    red_add_f32(args.out_acc + static_cast<int64_t>(m_tok[c]) * N + n,
-                                                m_w[c] * y);
-                            }
+                        for (int jj = 0; jj < 16; ++jj)
+                            if (c0 + jj < ntok)
+                                args.rows_out[static_cast<int64_t>(ch.row0 + c0 + jj) * N + n] =
+                                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[jj])));
+                    }
+                    if (per_pair) {
+                        // the 16 columns' metadata at once (broadcast reads), then 16
+                        // independent stores / reductions
+                        int pp[16], tt[16];
+                        float ww[16];
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const int4 a = reinterpret_cast<const int4*>(m_pair + c0)[k4];
+                            const int4 b = reinterpret_cast<const int4*>(m_tok + c0)[k4];
+                            const float4 w4 = reinterpret_cast<const float4*>(m_w + c0)[k4];
+                            pp[4 * k4] = a.x; pp[4 * k4 + 1] = a.y; pp[4 * k4 + 2] = a.z; pp[4 * k4 + 3] = a.w;
+                            tt[4 * k4] = b.x; tt[4 * k4 + 1] = b.y; tt[4 * k4 + 2] = b.z; tt[4 * k4 + 3] = b.w;
+                            ww[4 * k4] = w4.x; ww[4 * k4 + 1] = w4.y; ww[4 * k4 + 2] = w4.z; ww[4 * k4 + 3] = w4.w;
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            if (c0 + jj >= ntok || pp[jj] < 0)
+                                continue;
+                            const float y = __uint_as_float(v[jj]);
+                            if (args.epi & kEpiStorePair)
+                                args.y_pairs[static_cast<int64_t>(pp[jj]) * N + n] = y;
+                            if (args.epi & kEpiReduceTok)
+                                red_add_f32(args.out_acc + static_cast<int64_t>(tt[jj]) * N + n, ww[jj] * y);
                         }
                     }
                 }
