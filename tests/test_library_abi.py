@@ -52,7 +52,7 @@ def test_capacity_and_block_m(lib):
 def test_schedule_selection_by_rows_per_expert():
     import w4a16_int4_mixture_gb300 as m
     assert "decode-tile32" in m.describe_schedule(512, 8, 384, 48, 7168, 2048)
-    assert "prefill-tile256" in m.describe_schedule(8192, 8, 384, 48, 7168, 2048)
+    assert "prefill-tile192" in m.describe_schedule(8192, 8, 384, 48, 7168, 2048)
     assert "decode-tile64" in m.describe_schedule(2048, 8, 384, 384, 7168, 256)
     assert "ordered-pairs" in m.describe_schedule(512, 8, 384, 48, 7168, 2048, 2)
     assert "fp32-reduce" in m.describe_schedule(512, 8, 384, 48, 7168, 2048, 0)

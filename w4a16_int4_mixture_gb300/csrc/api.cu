@@ -176,13 +176,14 @@ struct Schedule {
 // switches above 80 rows per expert).  Below the switch the weight-streaming
 // decode pipeline with the smallest token tile that holds a typical expert
 // (mean + 3 sigma of a Poisson count) in one chunk; above it the deep-N
-// prefill tile of 256 tokens.
+// prefill tile of 192 tokens (two accumulator buffers, so the epilogue of one
+// unit overlaps the MMAs of the next; larger experts split into chunks).
 int pick_cfg(double tok_e, int K)
 {
     if (K % 256 != 0)
-        return kCfgP256;
+        return kCfgP192;
     if (tok_e >= 80.0)
-        return kCfgP256;
+        return kCfgP192;
     const double hi = tok_e + 3.0 * std::sqrt(tok_e > 0 ? tok_e : 0.0);
     if (hi <= 32.0)
         return kCfgD32;
@@ -388,10 +389,10 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     // maps; one row keeps the encoding valid)
     if (st == CHORD_OK)
         st = tensor_map(kMapRows, io.src, io.src_rows > 0 ? io.src_rows : 1, io.H,
-                        gemm_cfg_maxn(sc.cfg_gate_up), 0, dev.device, &bmap13);
+                        gemm_cfg_box_rows(sc.cfg_gate_up), 0, dev.device, &bmap13);
     if (st == CHORD_OK)
         st = tensor_map(kMapRows, h, io.h_rows > 0 ? io.h_rows : 1, io.I,
-                        gemm_cfg_maxn(sc.cfg_down), 0, dev.device, &bmap2);
+                        gemm_cfg_box_rows(sc.cfg_down), 0, dev.device, &bmap2);
     if (st != CHORD_OK)
         return st;
     int32_t* num_chunks = reinterpret_cast<int32_t*>(ws + w.off_hdr) + 1;
@@ -479,7 +480,7 @@ int chord_describe_schedule(int64_t T, int k, int E_global, int E_local, int H, 
     const double tok_e = E_global > 0 ? static_cast<double>(T) * k / E_global : 0.0;
     const Schedule s = pick_schedule(tok_e, T, H, I, flags);
     static const char* names[] = {"decode-tile32", "decode-tile64", "decode-tile128",
-                                  "prefill-tile256"};
+                                  "prefill-tile192"};
     char tmp[256];
     const int n = snprintf(tmp, sizeof tmp,
                            "tok_e=%.2f gate_up=%s(BK%d) down=%s(BK%d) combine=%s block_m=16 "

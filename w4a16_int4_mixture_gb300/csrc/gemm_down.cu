@@ -10,7 +10,7 @@ cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const CUtensorMap&
     case kCfgD32: return launch_gemm_cfg<CfgD32<false>>(map, bmap, a, grid, s);
     case kCfgD64: return launch_gemm_cfg<CfgD64<false>>(map, bmap, a, grid, s);
     case kCfgD128: return launch_gemm_cfg<CfgD128<false>>(map, bmap, a, grid, s);
-    case kCfgP256: return launch_gemm_cfg<CfgP256<false>>(map, bmap, a, grid, s);
+    case kCfgP192: return launch_gemm_cfg<CfgP192<false>>(map, bmap, a, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -21,12 +21,18 @@ int gemm_cfg_smem_down(int cfg)
     case kCfgD32: return CfgD32<false>::SMEM_BYTES;
     case kCfgD64: return CfgD64<false>::SMEM_BYTES;
     case kCfgD128: return CfgD128<false>::SMEM_BYTES;
-    case kCfgP256: return CfgP256<false>::SMEM_BYTES;
+    case kCfgP192: return CfgP192<false>::SMEM_BYTES;
     default: return 0;
     }
 }
 
-int gemm_cfg_bk(int cfg) { return cfg == kCfgP256 ? 128 : 256; }
+int gemm_cfg_bk(int cfg) { return cfg == kCfgP192 ? 128 : 256; }
+
+int gemm_cfg_box_rows(int cfg)
+{
+    const int m = gemm_cfg_maxn(cfg);
+    return m < 64 ? m : 64;
+}
 
 int gemm_cfg_maxn(int cfg)
 {
@@ -34,7 +40,7 @@ int gemm_cfg_maxn(int cfg)
     case kCfgD32: return 32;
     case kCfgD64: return 64;
     case kCfgD128: return 128;
-    case kCfgP256: return 256;
+    case kCfgP192: return 192;
     default: return 0;
     }
 }

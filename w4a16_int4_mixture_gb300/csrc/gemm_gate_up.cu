@@ -10,7 +10,7 @@ cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const CUtensorM
     case kCfgD32: return launch_gemm_cfg<CfgD32<true>>(map, bmap, a, grid, s);
     case kCfgD64: return launch_gemm_cfg<CfgD64<true>>(map, bmap, a, grid, s);
     case kCfgD128: return launch_gemm_cfg<CfgD128<true>>(map, bmap, a, grid, s);
-    case kCfgP256: return launch_gemm_cfg<CfgP256<true>>(map, bmap, a, grid, s);
+    case kCfgP192: return launch_gemm_cfg<CfgP192<true>>(map, bmap, a, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -21,7 +21,7 @@ int gemm_cfg_smem_gate_up(int cfg)
     case kCfgD32: return CfgD32<true>::SMEM_BYTES;
     case kCfgD64: return CfgD64<true>::SMEM_BYTES;
     case kCfgD128: return CfgD128<true>::SMEM_BYTES;
-    case kCfgP256: return CfgP256<true>::SMEM_BYTES;
+    case kCfgP192: return CfgP192<true>::SMEM_BYTES;
     default: return 0;
     }
 }

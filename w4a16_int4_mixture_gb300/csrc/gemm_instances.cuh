@@ -10,7 +10,7 @@ namespace chord {
 template <bool G> using CfgD32 = GemmCfg<256, 6, 4, 3, 32, 2, G>;
 template <bool G> using CfgD64 = GemmCfg<256, 6, 3, 3, 64, 2, G>;
 template <bool G> using CfgD128 = GemmCfg<256, 4, 2, 2, 128, 2, G>;
-template <bool G> using CfgP256 = GemmCfg<128, 4, 2, 4, 256, 1, G>;
+template <bool G> using CfgP192 = GemmCfg<128, 4, 3, 2, 192, 2, G>;
 
 template <class C>
 cudaError_t launch_gemm_cfg(const CUtensorMap& map, const CUtensorMap& bmap, const GemmArgs& a,

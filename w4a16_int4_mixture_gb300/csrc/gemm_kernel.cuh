@@ -50,6 +50,7 @@ struct GemmCfg {
     static constexpr int SCALE_STAGE = 128 * SCALE_ROW;
     static constexpr int B_KBLK = BK / 64;                  // 128B swizzle atoms along K
     static constexpr int B_REGION = MAXN * 128;             // one atom column of the tile
+    static constexpr int B_BOX_ROWS = MAXN < 64 ? MAXN : 64; // rows per token TMA box
     static constexpr int B_STAGE = B_KBLK * B_REGION;
     static constexpr int HS_BYTES = GATE_UP ? MAXN * 128 : 0;  // 64 channels of bf16 per row
     // down: per token column (pair, token, weight), double-buffered by unit
@@ -75,6 +76,7 @@ struct GemmCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM keeps the 512-column TMEM alloc safe");
     static_assert(OFF_B % 1024 == 0 && B_REGION % 1024 == 0, "swizzle atoms need 1024B alignment");
+    static_assert(MAXN % B_BOX_ROWS == 0 && (B_BOX_ROWS * 128) % 1024 == 0, "token boxes");
     static_assert(CODE_STAGE % 1024 == 0, "TMA destinations");
 };
 
@@ -255,6 +257,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         Chunk next = chunk_of(blockIdx.x);
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
             const int row0 = next.row0;
+            // boxes of B_BOX_ROWS rows, as many as the token tile needs
+            const int nbox = ((next.nrows + 15) / 16 * 16 + C::B_BOX_ROWS - 1) / C::B_BOX_ROWS;
             next = chunk_of(u + gridDim.x);
             for (int ks = 0; ks < KT; ++ks, ++g) {
                 const int s = g % C::BS;
@@ -264,11 +268,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 if (lane == 0) {
                     const uint32_t dst = sbase + C::OFF_B + s * C::B_STAGE;
-                    mbar_arrive_expect_tx(b_full(s), C::B_STAGE);
+                    mbar_arrive_expect_tx(b_full(s), C::B_KBLK * nbox * C::B_BOX_ROWS * 128);
 #pragma unroll
                     for (int kb = 0; kb < C::B_KBLK; ++kb)
-                        tma_load_2d(dst + kb * C::B_REGION, &b_map, ks * C::BK + kb * 64, row0,
-                                    b_full(s), pol);
+                        for (int ib = 0; ib < nbox; ++ib)
+                            tma_load_2d(dst + kb * C::B_REGION + ib * (C::B_BOX_ROWS * 128), &b_map,
+                                        ks * C::BK + kb * 64, row0 + ib * C::B_BOX_ROWS, b_full(s), pol);
                 }
                 __syncwarp();
             }
@@ -389,7 +394,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const float mine = __uint_as_float(v[jj]);
                         const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
                         if (is_gate) {
-                            const float silu = mine / (1.0f + expf(-mine));
+                            // fast exp / divide: a few fp32 ulp, far below the bf16 rounding of h
+                            const float silu = __fdividef(mine, 1.0f + __expf(-mine));
                             hs[(c0 + jj) * 64 + chl] = __float2bfloat16_rn(silu * other);
                         }
                     }

@@ -83,19 +83,20 @@ enum GemmConfig : int {
     kCfgD32 = 0,    // BK 256, token tile <= 32, deep code ring: weight-streaming decode
     kCfgD64 = 1,    // BK 256, token tile <= 64
     kCfgD128 = 2,   // BK 256, token tile <= 128
-    kCfgP256 = 3,   // BK 128, token tile <= 256: prefill / short K
+    kCfgP192 = 3,   // BK 128, token tile <= 192, two accumulators: prefill / short K
     kNumGemmConfigs = 4
 };
 
 int gemm_cfg_bk(int cfg);
 int gemm_cfg_maxn(int cfg);
+int gemm_cfg_box_rows(int cfg);  // rows of one token TMA box: min(token tile, 64)
 int gemm_cfg_smem(int cfg, bool gate_up);
 
 // Launch one GEMM (gate_up with fused SiLU*up, or down with its epilogue).
 // codes_map: 2-D tensor map over the codes, inner dim K/8 int32 words, outer
 // E*N rows, box {BK/8, gate_up ? 64 : 128}, 128B (BK 256) or 64B (BK 128) swizzle.
 // b_map: 2-D tensor map over the bf16 token rows (padded-row order), inner dim
-// K, box {64, token tile}, 128B swizzle, zero fill past the last row.
+// K, box {64, gemm_cfg_box_rows(cfg)}, 128B swizzle, zero fill past the last row.
 cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& codes_map,
                         const CUtensorMap& b_map, const GemmArgs& a, int grid, cudaStream_t s);
 
