@@ -22,8 +22,9 @@
 //               down: per-pair fp32 store, fp32 reductions into token rows,
 //               or bf16 row store.
 //   warps 8-15  dequant, two groups taking alternate K stages: codes + scales
-//               from shared memory -> w = (q - 8) * s in bf16 (subtract, then
-//               scale: the page's unfused rounding order) -> tcgen05.st into
+//               from shared memory -> w = bf16((q - 8) * s), one rounding of
+//               the exact product as in the page's order (exact q - 8, then
+//               the scale multiply) -> tcgen05.st into
 //               the A-operand stage in TMEM.
 // Every wait is bounded (2 s); on expiry the CTA records CHORD_DEVERR_TIMEOUT,
 // every role leaves its loop, in-flight tensor-core work is drained and TMEM
@@ -64,7 +65,8 @@ struct GemmCfg {
     static constexpr int OFF_BARS = OFF_META + META_BYTES;
     static constexpr int NBARS = 2 * KS + 2 * AS + 2 * BS + 2 * ACCB + 2;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+    // misc: TMEM base, abort flag, 2 spare words, 4 per-quadrant stage counters
+    static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;  // + alignment slack
 
     static constexpr int A_COLS = BK / 2;                   // TMEM columns per A stage
     static constexpr int D_COL0 = AS * A_COLS;
@@ -91,33 +93,55 @@ __device__ __forceinline__ int code_chunk_swizzle(int c, int r)
 }
 
 // bf16x2 helpers (single rounding each, round to nearest even)
-__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
 {
     uint32_t d;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
-
-// Dequantise one word of 8 codes (elements 8w..8w+7, low nibble first) with the
-// bf16x2 scale pair s2 = (s, s) into 4 bf16x2 columns (elements (0,1) .. (6,7)).
-// For each element pair: place the two nibbles in the low 4 bits of each half
-// (byte permute of w and w>>4), OR in the bf16 exponent of 128 so each half
-// reads 128 + q exactly, subtract 136 (exact: q - 8), multiply by the scale
-// (one rounding).
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t* o)
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c)
 {
-    const uint32_t w4 = w >> 4;
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// generic-mode byte permute: selector bit 3 of a byte replicates the sign bit
+// of the selected byte (0x00 for the code bytes here, which are 0..15)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Per scale group: the constants of the dequant fma, from the bf16x2 scale
+// pair s2 = (s, s): s * 2^6 and -8 * s (both exact: power-of-two multiples).
+struct ScalePair {
+    uint32_t s6;
+    uint32_t m8;
+};
+__device__ __forceinline__ ScalePair scale_pair(uint32_t s2)
+{
+    return {bf16x2_mul(s2, 0x42804280u) /* 64 */, bf16x2_mul(s2, 0xC100C100u) /* -8 */};
+}
+
+// Dequantise one word of 8 codes (element i in bits 4i..4i+3) into 4 bf16x2
+// columns (elements (0,1) .. (6,7)), each w = (q - 8) * s rounded once.
+//   lo / hi: the low / high nibble of each byte (elements 0,2,4,6 / 1,3,5,7);
+//   prmt:    bytes (q_2j, 0, q_2j+1, 0) = two bf16 subnormals q * 2^-133;
+//   * 2^127: q * 2^-6, exact;
+//   fma:     (q * 2^-6) * (s * 2^6) + (-8 s): the product q * s and the sum
+//            (q - 8) * s are exact before the one rounding, so the result is
+//            the bf16 rounding of (q - 8) * s.
+__device__ __forceinline__ void dequant_word(uint32_t w, ScalePair sp, uint32_t* o)
+{
+    const uint32_t lo = w & 0x0F0F0F0Fu;
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        uint32_t t = __byte_perm(w, w4, static_cast<uint32_t>(j | ((4 + j) << 8)));
-        t = (t & 0x000F000Fu) | 0x43004300u;
-        o[j] = bf16x2_mul(bf16x2_sub(t, 0x43084308u), s2);
+        const uint32_t sel = static_cast<uint32_t>(j | ((8 | j) << 4) | ((4 + j) << 8) | ((12 + j) << 12));
+        const uint32_t t = prmt(lo, hi, sel);
+        o[j] = bf16x2_fma(bf16x2_mul(t, 0x7F007F00u) /* 2^127 */, sp.s6, sp.m8);
     }
 }
 
@@ -150,6 +174,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t drain_bar = bar0 + 8u * (C::NBARS - 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    int* stage_ctr = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::KS; ++s) {
@@ -171,6 +196,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_init(epi_bar, 4);                 // epilogue group rendezvous
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
+        for (int qq = 0; qq < 4; ++qq)
+            stage_ctr[qq] = 0;
         mbar_fence_init();
     }
     if (warp == 0 && lane == 0)
@@ -471,7 +498,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else if (warp >= 8) {
         // ---------------------------------------------------------------- dequant
-        const int dg = (warp - 8) >> 2;
+        // The two warps of each TMEM lane quadrant (warps q+8 and q+12) take K
+        // stages in order from a shared counter, each the next one not yet
+        // taken, so neither waits for the other's turn.
         const int q = warp & 3;
         int srow;
         if constexpr (C::GATE_UP)
@@ -479,12 +508,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else
             srow = q * 32 + lane;
         const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
-        int g = 0;
+        const int my_units = static_cast<int>(blockIdx.x) < total_units
+                                 ? (total_units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                                 : 0;
+        const int total_stages = my_units * KT;
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            for (int ks = 0; ks < KT; ++ks, ++g) {
-                if ((g & 1) != dg)
-                    continue;
+        for (;;) {
+            {
+                int g = 0;
+                if (lane == 0)
+                    g = atomicAdd(&stage_ctr[q], 1);
+                g = __shfl_sync(0xffffffffu, g, 0);
+                if (g >= total_stages)
+                    break;
                 const int s = g % C::KS;
                 if (!mbar_wait(codes_full(s), (g / C::KS) & 1, abort_flag, err)) {
                     ok = false;
@@ -520,12 +556,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int grp = 0; grp < C::BK / 32; ++grp) {
                     const uint4 v = *reinterpret_cast<const uint4*>(
                         crow + (code_chunk_swizzle<C::BK>(grp, srow) << 4));
-                    const uint32_t s2 = __byte_perm(sc[grp >> 1], 0, (grp & 1) ? 0x3232 : 0x1010);
+                    const ScalePair sp =
+                        scale_pair(__byte_perm(sc[grp >> 1], 0, (grp & 1) ? 0x3232 : 0x1010));
                     uint32_t o[16];
-                    dequant_word(v.x, s2, &o[0]);
-                    dequant_word(v.y, s2, &o[4]);
-                    dequant_word(v.z, s2, &o[8]);
-                    dequant_word(v.w, s2, &o[12]);
+                    dequant_word(v.x, sp, &o[0]);
+                    dequant_word(v.y, sp, &o[4]);
+                    dequant_word(v.z, sp, &o[8]);
+                    dequant_word(v.w, sp, &o[12]);
                     tmem_st_x16(tmem + tlane + sa * C::A_COLS + grp * 16, o);
                 }
                 // The next TMA into this code stage writes through the async proxy;
