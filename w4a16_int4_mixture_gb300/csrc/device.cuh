@@ -232,6 +232,64 @@ __device__ __forceinline__ void mma_commit_elect(uint32_t bar)
         : "memory");
 }
 
+// One K stage of MMAs (BK / 16 of them, K = 16 each) issued from one asm
+// block: one elect.sync for the stage, operands as 32-bit adds on the
+// descriptor's address word (address >> 4 stays below 2^14, so the adds never
+// carry into the other fields).  The j-th MMA reads A columns a + 8 j and the
+// B descriptor of 16-element K step j: atom column j / 4 (REG16 = that
+// column's size in 16-byte units), 32-byte step j % 4 inside the swizzled row.
+// accumulate = 0 makes the first MMA overwrite D.
+template <int REG16>
+__device__ __forceinline__ void mma_stage16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 bq, bl, al;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "mov.b32 bq, %2;\n\tmov.b64 bd, {bq, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p0;\n\t"
+        "add.u32 bl, bq, 2;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 4;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 6;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bq, %2, %6;\n\tmov.b64 bd, {bq, %3};\n\tadd.u32 al, %1, 32;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 2;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 40;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 4;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 48;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 6;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 56;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bq, %2, %7;\n\tmov.b64 bd, {bq, %3};\n\tadd.u32 al, %1, 64;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 2;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 72;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 4;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 80;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 6;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 88;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bq, %2, %8;\n\tmov.b64 bd, {bq, %3};\n\tadd.u32 al, %1, 96;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 2;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 104;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 4;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 112;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 6;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 120;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(static_cast<uint32_t>(b_desc)),
+        "r"(static_cast<uint32_t>(b_desc >> 32)), "r"(idesc), "r"(accumulate), "n"(REG16),
+        "n"(2 * REG16), "n"(3 * REG16)
+        : "memory");
+}
+
+template <int REG16>
+__device__ __forceinline__ void mma_stage8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 bq, bl, al;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "mov.b32 bq, %2;\n\tmov.b64 bd, {bq, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p0;\n\t"
+        "add.u32 bl, bq, 2;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 4;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 6;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bq, %2, %6;\n\tmov.b64 bd, {bq, %3};\n\tadd.u32 al, %1, 32;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 2;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 40;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 4;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 48;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "add.u32 bl, bq, 6;\n\tmov.b64 bd, {bl, %3};\n\tadd.u32 al, %1, 56;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [al], bd, %4, pt;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(static_cast<uint32_t>(b_desc)),
+        "r"(static_cast<uint32_t>(b_desc >> 32)), "r"(idesc), "r"(accumulate), "n"(REG16)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile(

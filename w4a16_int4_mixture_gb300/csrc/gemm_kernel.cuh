@@ -339,12 +339,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_fence_after();
                 const uint32_t a_base = tmem + sa * C::A_COLS;
                 const uint32_t b_base = sbase + C::OFF_B + sb * C::B_STAGE;
-#pragma unroll
-                for (int j = 0; j < C::BK / 16; ++j) {
-                    const uint64_t bdesc =
-                        smem_desc_sw128(b_base + (j >> 2) * C::B_REGION + (j & 3) * 32);
-                    mma_ts_elect(d_tmem, a_base + j * 8, bdesc, idesc, (ks | j) != 0 ? 1u : 0u);
-                }
+                if constexpr (C::BK == 256)
+                    mma_stage16<C::B_REGION / 16>(d_tmem, a_base, smem_desc_sw128(b_base), idesc,
+                                                  ks != 0 ? 1u : 0u);
+                else
+                    mma_stage8<C::B_REGION / 16>(d_tmem, a_base, smem_desc_sw128(b_base), idesc,
+                                                 ks != 0 ? 1u : 0u);
                 issued = 1;
                 mma_commit_elect(a_empty(sa));
                 mma_commit_elect(b_empty(sb));
