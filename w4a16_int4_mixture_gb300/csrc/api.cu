@@ -15,18 +15,19 @@
 
 namespace chord {
 
-cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const CUtensorMap& bmap,
-                                const GemmArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const CUtensorMap& bmap,
-                             const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const CUtensorMap& smap,
+                                const CUtensorMap& bmap, const GemmArgs& a, int grid,
+                                cudaStream_t s);
+cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const CUtensorMap& smap,
+                             const CUtensorMap& bmap, const GemmArgs& a, int grid, cudaStream_t s);
 int gemm_cfg_smem_gate_up(int cfg);
 int gemm_cfg_smem_down(int cfg);
 
-cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& map, const CUtensorMap& bmap,
-                        const GemmArgs& a, int grid, cudaStream_t s)
+cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& map, const CUtensorMap& smap,
+                        const CUtensorMap& bmap, const GemmArgs& a, int grid, cudaStream_t s)
 {
-    return gate_up ? launch_gemm_gate_up(cfg, map, bmap, a, grid, s)
-                   : launch_gemm_down(cfg, map, bmap, a, grid, s);
+    return gate_up ? launch_gemm_gate_up(cfg, map, smap, bmap, a, grid, s)
+                   : launch_gemm_down(cfg, map, smap, bmap, a, grid, s);
 }
 
 int gemm_cfg_smem(int cfg, bool gate_up)
@@ -73,26 +74,20 @@ chord_status device_info(DeviceInfo* out)
 }
 
 // ---------------------------------------------------------------------------
-// tensor maps (packed codes; bf16 token rows), memoised by (kind, pointer,
-// shape, box)
+// tensor maps, memoised by everything that goes into the encoding
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-enum MapKind : int { kMapCodes = 0, kMapRows = 1 };
-
 struct MapKey {
-    int kind;
     const void* ptr;
-    int64_t rows;
-    int64_t K;
-    int box_rows;
-    int bk;
+    int dtype;
+    int rank;
+    uint64_t dims[3];
+    uint64_t strides[2];
+    uint32_t box[3];
+    int swizzle;
     int device;
-    bool operator==(const MapKey& o) const
-    {
-        return kind == o.kind && ptr == o.ptr && rows == o.rows && K == o.K &&
-               box_rows == o.box_rows && bk == o.bk && device == o.device;
-    }
+    bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 
 struct MapEntry {
@@ -105,15 +100,9 @@ std::mutex g_map_mu;
 std::vector<MapEntry> g_maps;
 uint64_t g_stamp = 0;
 
-// kMapCodes: int32 words [rows, K/8], box {bk/8, box_rows}, 128B (bk 256) or
-//            64B (bk 128) swizzle.
-// kMapRows:  bf16 [rows, K], box {64, box_rows}, 128B swizzle; rows past the
-//            end read as zero.
-chord_status tensor_map(int kind, const void* ptr, int64_t rows, int64_t K, int box_rows, int bk,
-                        int device, CUtensorMap* out)
+chord_status encode_map(MapKey key, CUtensorMap* out)
 {
     std::lock_guard<std::mutex> lk(g_map_mu);
-    const MapKey key{kind, ptr, rows, K, box_rows, bk, device};
     for (auto& e : g_maps)
         if (e.key == key) {
             e.stamp = ++g_stamp;
@@ -130,27 +119,22 @@ chord_status tensor_map(int kind, const void* ptr, int64_t rows, int64_t K, int 
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     CUtensorMap m;
-    cuuint32_t es[2] = {1, 1};
-    CUresult r;
-    if (kind == kMapCodes) {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(rows)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 8) * 4};
-        cuuint32_t box[2] = {static_cast<cuuint32_t>(bk / 8), static_cast<cuuint32_t>(box_rows)};
-        r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(ptr), dims, strides, box,
-                     es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-        r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < key.rank; ++i) {
+        dims[i] = key.dims[i];
+        box[i] = key.box[i];
     }
+    for (int i = 0; i + 1 < key.rank; ++i)
+        strides[i] = key.strides[i];
+    const CUresult r = g_encode(&m, static_cast<CUtensorMapDataType>(key.dtype), key.rank,
+                                const_cast<void*>(key.ptr), dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                static_cast<CUtensorMapSwizzle>(key.swizzle),
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return CHORD_ERR_CUDA;
-    if (g_maps.size() >= 32) {
+    if (g_maps.size() >= 48) {
         size_t victim = 0;
         for (size_t i = 1; i < g_maps.size(); ++i)
             if (g_maps[i].stamp < g_maps[victim].stamp)
@@ -160,6 +144,105 @@ chord_status tensor_map(int kind, const void* ptr, int64_t rows, int64_t K, int 
     g_maps.push_back({key, m, ++g_stamp});
     *out = m;
     return CHORD_OK;
+}
+
+MapKey blank_key(const void* ptr, int dtype, int rank, int swizzle, int device)
+{
+    MapKey k;
+    std::memset(&k, 0, sizeof k);
+    k.ptr = ptr;
+    k.dtype = dtype;
+    k.rank = rank;
+    k.swizzle = swizzle;
+    k.device = device;
+    return k;
+}
+
+// Packed codes of one GEMM: int32 words, rows of K/8.  gate_up (I > 0): a 3-D
+// map {K/8, E*N - I rows, 2 halves I rows apart}, box {bk/8, 64, 2}: gate rows
+// and the matching up rows in one box.  down: 2-D, box {bk/8, 128}.  128B
+// swizzle for bk 256, 64B for bk 128.
+chord_status codes_map(const int32_t* q, int64_t rows, int64_t K, int64_t I, int bk, int device,
+                       CUtensorMap* out)
+{
+    const int sw = bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const uint64_t row_bytes = static_cast<uint64_t>(K / 8) * 4;
+    if (I > 0) {
+        MapKey k = blank_key(q, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, sw, device);
+        k.dims[0] = K / 8;
+        k.dims[1] = rows - I;
+        k.dims[2] = 2;
+        k.strides[0] = row_bytes;
+        k.strides[1] = row_bytes * I;
+        k.box[0] = bk / 8;
+        k.box[1] = 64;
+        k.box[2] = 2;
+        return encode_map(k, out);
+    }
+    MapKey k = blank_key(q, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sw, device);
+    k.dims[0] = K / 8;
+    k.dims[1] = rows;
+    k.strides[0] = row_bytes;
+    k.box[0] = bk / 8;
+    k.box[1] = 128;
+    return encode_map(k, out);
+}
+
+// Group-32 scales of one GEMM: bf16 rows of K/32, boxes of 8 columns (16 bytes,
+// one BK = 256 stage); the same 3-D gate/up pairing as the codes.
+chord_status scales_map(const uint16_t* sc, int64_t rows, int64_t K, int64_t I, int device,
+                        CUtensorMap* out)
+{
+    const uint64_t row_bytes = static_cast<uint64_t>(K / 32) * 2;
+    if (I > 0) {
+        MapKey k = blank_key(sc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             device);
+        k.dims[0] = K / 32;
+        k.dims[1] = rows - I;
+        k.dims[2] = 2;
+        k.strides[0] = row_bytes;
+        k.strides[1] = row_bytes * I;
+        k.box[0] = 8;
+        k.box[1] = 64;
+        k.box[2] = 2;
+        return encode_map(k, out);
+    }
+    MapKey k = blank_key(sc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_NONE, device);
+    k.dims[0] = K / 32;
+    k.dims[1] = rows;
+    k.strides[0] = row_bytes;
+    k.box[0] = 8;
+    k.box[1] = 128;
+    return encode_map(k, out);
+}
+
+// Token rows (bf16 [rows, K], padded-row order), 128B swizzle, zero past the
+// last row.  Token tiles of at most 64 rows: a 3-D map {64 columns, rows, K/64
+// column blocks} with box {64, tile, bk/64}, one box per stage laid out as the
+// stage's column blocks one after another.  Larger tiles: 2-D boxes {64, 64}.
+chord_status rows_map(const uint16_t* x, int64_t rows, int64_t K, int tile, int bk, int device,
+                      CUtensorMap* out)
+{
+    if (tile <= 64) {
+        MapKey k = blank_key(x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, CU_TENSOR_MAP_SWIZZLE_128B,
+                             device);
+        k.dims[0] = 64;
+        k.dims[1] = rows;
+        k.dims[2] = K / 64;
+        k.strides[0] = static_cast<uint64_t>(K) * 2;
+        k.strides[1] = 128;
+        k.box[0] = 64;
+        k.box[1] = tile;
+        k.box[2] = bk / 64;
+        return encode_map(k, out);
+    }
+    MapKey k = blank_key(x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_128B, device);
+    k.dims[0] = K;
+    k.dims[1] = rows;
+    k.strides[0] = static_cast<uint64_t>(K) * 2;
+    k.box[0] = 64;
+    k.box[1] = 64;
+    return encode_map(k, out);
 }
 
 // ---------------------------------------------------------------------------
@@ -379,20 +462,28 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
                        cudaStream_t s, StageMarks& marks)
 {
     uint16_t* h = io.h_out ? io.h_out : reinterpret_cast<uint16_t*>(ws + w.off_h);
-    CUtensorMap map13, map2, bmap13, bmap2;
-    chord_status st = tensor_map(kMapCodes, io.w13_q, static_cast<int64_t>(io.E_local) * 2 * io.I,
-                                 io.H, 64, gemm_cfg_bk(sc.cfg_gate_up), dev.device, &map13);
+    CUtensorMap map13, map2, smap13, smap2, bmap13, bmap2;
+    const int bk13 = gemm_cfg_bk(sc.cfg_gate_up), bk2 = gemm_cfg_bk(sc.cfg_down);
+    const int64_t rows13 = static_cast<int64_t>(io.E_local) * 2 * io.I;
+    const int64_t rows2 = static_cast<int64_t>(io.E_local) * io.H;
+    chord_status st = codes_map(io.w13_q, rows13, io.H, io.I, bk13, dev.device, &map13);
     if (st == CHORD_OK)
-        st = tensor_map(kMapCodes, io.w2_q, static_cast<int64_t>(io.E_local) * io.H, io.I, 128,
-                        gemm_cfg_bk(sc.cfg_down), dev.device, &map2);
+        st = codes_map(io.w2_q, rows2, io.I, 0, bk2, dev.device, &map2);
+    // scales by TMA only for BK 256 stages; the kernel ignores the map otherwise
+    smap13 = map13;
+    smap2 = map2;
+    if (st == CHORD_OK && bk13 == 256)
+        st = scales_map(io.w13_s, rows13, io.H, io.I, dev.device, &smap13);
+    if (st == CHORD_OK && bk2 == 256)
+        st = scales_map(io.w2_s, rows2, io.I, 0, dev.device, &smap2);
     // (a call with no rows has no chunks, so no tile is ever read through these
     // maps; one row keeps the encoding valid)
     if (st == CHORD_OK)
-        st = tensor_map(kMapRows, io.src, io.src_rows > 0 ? io.src_rows : 1, io.H,
-                        gemm_cfg_box_rows(sc.cfg_gate_up), 0, dev.device, &bmap13);
+        st = rows_map(io.src, io.src_rows > 0 ? io.src_rows : 1, io.H,
+                      gemm_cfg_maxn(sc.cfg_gate_up), bk13, dev.device, &bmap13);
     if (st == CHORD_OK)
-        st = tensor_map(kMapRows, h, io.h_rows > 0 ? io.h_rows : 1, io.I,
-                        gemm_cfg_box_rows(sc.cfg_down), 0, dev.device, &bmap2);
+        st = rows_map(h, io.h_rows > 0 ? io.h_rows : 1, io.I, gemm_cfg_maxn(sc.cfg_down), bk2,
+                      dev.device, &bmap2);
     if (st != CHORD_OK)
         return st;
     int32_t* num_chunks = reinterpret_cast<int32_t*>(ws + w.off_hdr) + 1;
@@ -415,7 +506,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.pair_of_row = io.pair_of_row;
     g.err = err;
     marks.mark(1);
-    if (launch_gemm(sc.cfg_gate_up, true, map13, bmap13, g, dev.sms, s) != cudaSuccess)
+    if (launch_gemm(sc.cfg_gate_up, true, map13, smap13, bmap13, g, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(2);
 
@@ -432,7 +523,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     d.y_pairs = (io.down_epi & kEpiStorePair) ? acc : nullptr;
     d.out_acc = (io.down_epi & kEpiReduceTok) ? acc : nullptr;
     d.rows_out = io.rows_out;
-    if (launch_gemm(sc.cfg_down, false, map2, bmap2, d, dev.sms, s) != cudaSuccess)
+    if (launch_gemm(sc.cfg_down, false, map2, smap2, bmap2, d, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(3);
     return CHORD_OK;

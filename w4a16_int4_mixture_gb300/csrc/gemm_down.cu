@@ -3,14 +3,14 @@
 
 namespace chord {
 
-cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const CUtensorMap& bmap,
+cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const CUtensorMap& smap, const CUtensorMap& bmap,
                              const GemmArgs& a, int grid, cudaStream_t s)
 {
     switch (cfg) {
-    case kCfgD32: return launch_gemm_cfg<CfgD32<false>>(map, bmap, a, grid, s);
-    case kCfgD64: return launch_gemm_cfg<CfgD64<false>>(map, bmap, a, grid, s);
-    case kCfgD128: return launch_gemm_cfg<CfgD128<false>>(map, bmap, a, grid, s);
-    case kCfgP192: return launch_gemm_cfg<CfgP192<false>>(map, bmap, a, grid, s);
+    case kCfgD32: return launch_gemm_cfg<CfgD32<false>>(map, smap, bmap, a, grid, s);
+    case kCfgD64: return launch_gemm_cfg<CfgD64<false>>(map, smap, bmap, a, grid, s);
+    case kCfgD128: return launch_gemm_cfg<CfgD128<false>>(map, smap, bmap, a, grid, s);
+    case kCfgP192: return launch_gemm_cfg<CfgP192<false>>(map, smap, bmap, a, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -27,12 +27,6 @@ int gemm_cfg_smem_down(int cfg)
 }
 
 int gemm_cfg_bk(int cfg) { return cfg == kCfgP192 ? 128 : 256; }
-
-int gemm_cfg_box_rows(int cfg)
-{
-    const int m = gemm_cfg_maxn(cfg);
-    return m < 64 ? m : 64;
-}
 
 int gemm_cfg_maxn(int cfg)
 {

@@ -13,8 +13,8 @@ template <bool G> using CfgD128 = GemmCfg<256, 4, 2, 2, 128, 2, G>;
 template <bool G> using CfgP192 = GemmCfg<128, 4, 3, 2, 192, 2, G>;
 
 template <class C>
-cudaError_t launch_gemm_cfg(const CUtensorMap& map, const CUtensorMap& bmap, const GemmArgs& a,
-                            int grid, cudaStream_t s)
+cudaError_t launch_gemm_cfg(const CUtensorMap& map, const CUtensorMap& smap,
+                            const CUtensorMap& bmap, const GemmArgs& a, int grid, cudaStream_t s)
 {
     static bool attr_set[64] = {};  // per device, set on the first launch there
     int dev = 0;
@@ -30,7 +30,7 @@ cudaError_t launch_gemm_cfg(const CUtensorMap& map, const CUtensorMap& bmap, con
             return e;
         attr_set[dev] = true;
     }
-    w4a16_gemm_kernel<C><<<grid, kGemmThreads, C::SMEM_BYTES, s>>>(map, bmap, a);
+    w4a16_gemm_kernel<C><<<grid, kGemmThreads, C::SMEM_BYTES, s>>>(map, smap, bmap, a);
     return cudaGetLastError();
 }
 

@@ -10,11 +10,13 @@
 // the MMA-M operand), used here for every token count.
 //
 // Roles (16 warps):
-//   warp 0      code producer: packed INT4 codes (TMA tile, L2 evict-first) and
-//               the group-32 scales (cp.async) of each K stage into a ring.
+//   warp 0      code producer: packed INT4 codes of each K stage into a ring, one
+//               TMA box (gate and up halves as one 3-D box), L2 evict-first,
+//               and the group-32 scales (a TMA box, or cp.async for BK 128).
 //   warp 1      token producer: the chunk's activation rows, contiguous in the
-//               B tensor map, as 128B-swizzled K-major TMA tiles of MAXN rows
-//               (the rows past the chunk only feed discarded columns).
+//               B tensor map, as 128B-swizzled K-major TMA tiles (one 3-D box
+//               per stage for token tiles of up to 64 rows; the rows past the
+//               chunk only feed discarded columns).
 //   warp 2      MMA issuer (the whole warp walks the schedule; elect.sync picks
 //               the issuing lane) and TMEM owner.
 //   warp 3      idle.
@@ -52,6 +54,12 @@ struct GemmCfg {
     static constexpr int B_KBLK = BK / 64;                  // 128B swizzle atoms along K
     static constexpr int B_REGION = MAXN * 128;             // one atom column of the tile
     static constexpr int B_BOX_ROWS = MAXN < 64 ? MAXN : 64; // rows per token TMA box
+    // token tile of a stage as one 3-D TMA box {64 columns, MAXN rows, BK/64
+    // column blocks} when it fits one box of rows; else 2-D boxes of 64 rows
+    static constexpr bool B_3D = MAXN <= 64;
+    // the stage's scales as a TMA box (16-byte rows) when BK = 256; cp.async
+    // (8-byte rows) when BK = 128
+    static constexpr bool SCALES_TMA = BK == 256;
     static constexpr int B_STAGE = B_KBLK * B_REGION;
     static constexpr int HS_BYTES = GATE_UP ? MAXN * 128 : 0;  // 64 channels of bf16 per row
     // down: per token column (pair, token, weight), double-buffered by unit
@@ -148,6 +156,7 @@ __device__ __forceinline__ void dequant_word(uint32_t w, ScalePair sp, uint32_t*
 template <class C>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap codes_map,
+                      const __grid_constant__ CUtensorMap scales_map,
                       const __grid_constant__ CUtensorMap b_map, const GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -178,7 +187,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::KS; ++s) {
-            mbar_init(codes_full(s), 1 + 32);  // expect_tx arrive + 32 cp.async arrivals
+            // expect_tx arrive (+ 32 cp.async arrivals when scales come by cp.async)
+            mbar_init(codes_full(s), C::SCALES_TMA ? 1 : 1 + 32);
             mbar_init(codes_empty(s), 4);      // the 4 warps of one dequant group
         }
         for (int s = 0; s < C::AS; ++s) {
@@ -200,8 +210,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             stage_ctr[qq] = 0;
         mbar_fence_init();
     }
-    if (warp == 0 && lane == 0)
+    if (warp == 0 && lane == 0) {
         prefetch_tensormap(&codes_map);
+        if constexpr (C::SCALES_TMA)
+            prefetch_tensormap(&scales_map);
+    }
     if (warp == 1 && lane == 0)
         prefetch_tensormap(&b_map);
     if (warp == 2)
@@ -234,14 +247,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             next = chunk_of(u + gridDim.x);
             const int nt = u % n_tiles;
             const int e = ch.expert;
-            int grow_a, grow_b;
-            if constexpr (C::GATE_UP) {
-                grow_a = e * args.N + nt * 64;
-                grow_b = e * args.N + args.I + nt * 64;
-            } else {
-                grow_a = e * args.N + nt * 128;
-                grow_b = grow_a + 64;
-            }
+            // first weight row of the tile: gate_up takes rows [row0, row0 + 64)
+            // (gate) and the same 64 rows I further on (up) as one 3-D box
+            const int row0 = C::GATE_UP ? e * args.N + nt * 64 : e * args.N + nt * 128;
             for (int ks = 0; ks < KT; ++ks, ++g) {
                 const int s = g % C::KS;
                 if (!mbar_wait(codes_empty(s), ((g / C::KS) & 1) ^ 1, abort_flag, err)) {
@@ -249,29 +257,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 const uint32_t dst = sbase + C::OFF_CODES + s * C::CODE_STAGE;
+                const uint32_t sdst = sbase + C::OFF_SCALES + s * C::SCALE_STAGE;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(codes_full(s), C::CODE_STAGE);
+                    mbar_arrive_expect_tx(codes_full(s),
+                                          C::CODE_STAGE + (C::SCALES_TMA ? C::SCALE_STAGE : 0));
                     const int x = ks * (C::BK / 8);
-                    if constexpr (C::GATE_UP) {
-                        tma_load_2d(dst, &codes_map, x, grow_a, codes_full(s), pol);
-                        tma_load_2d(dst + 64 * C::CODE_ROW, &codes_map, x, grow_b, codes_full(s), pol);
-                    } else {
-                        tma_load_2d(dst, &codes_map, x, grow_a, codes_full(s), pol);
+                    if constexpr (C::GATE_UP)
+                        tma_load_3d(dst, &codes_map, x, row0, 0, codes_full(s), pol);
+                    else
+                        tma_load_2d(dst, &codes_map, x, row0, codes_full(s), pol);
+                    if constexpr (C::SCALES_TMA) {
+                        if constexpr (C::GATE_UP)
+                            tma_load_3d(sdst, &scales_map, ks * (C::BK / 32), row0, 0, codes_full(s), pol);
+                        else
+                            tma_load_2d(sdst, &scales_map, ks * (C::BK / 32), row0, codes_full(s), pol);
                     }
                 }
-                const uint32_t sdst = sbase + C::OFF_SCALES + s * C::SCALE_STAGE;
+                if constexpr (!C::SCALES_TMA) {
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                    const int r = lane + 32 * rr;
-                    const int grow = (r < 64) ? grow_a + r : grow_b + (r - 64);
-                    const uint16_t* src = args.scales + static_cast<int64_t>(grow) * (args.K / 32) +
-                                          ks * (C::BK / 32);
-                    if constexpr (C::BK == 256)
-                        cp_async_16(sdst + r * C::SCALE_ROW, src, 16);
-                    else
+                    for (int rr = 0; rr < 4; ++rr) {
+                        const int r = lane + 32 * rr;
+                        const int grow = C::GATE_UP ? row0 + (r < 64 ? r : args.I + r - 64) : row0 + r;
+                        const uint16_t* src = args.scales + static_cast<int64_t>(grow) * (args.K / 32) +
+                                              ks * (C::BK / 32);
                         cp_async_8(sdst + r * C::SCALE_ROW, src);
+                    }
+                    cp_async_arrive_noinc(codes_full(s));
                 }
-                cp_async_arrive_noinc(codes_full(s));
+                __syncwarp();
             }
         }
         if (!ok)  // let the copies already issued land before the CTA goes away
@@ -295,12 +308,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 if (lane == 0) {
                     const uint32_t dst = sbase + C::OFF_B + s * C::B_STAGE;
-                    mbar_arrive_expect_tx(b_full(s), C::B_KBLK * nbox * C::B_BOX_ROWS * 128);
+                    if constexpr (C::B_3D) {
+                        mbar_arrive_expect_tx(b_full(s), C::B_STAGE);
+                        tma_load_3d(dst, &b_map, 0, row0, ks * (C::BK / 64), b_full(s), pol);
+                    } else {
+                        mbar_arrive_expect_tx(b_full(s), C::B_KBLK * nbox * C::B_BOX_ROWS * 128);
 #pragma unroll
-                    for (int kb = 0; kb < C::B_KBLK; ++kb)
-                        for (int ib = 0; ib < nbox; ++ib)
-                            tma_load_2d(dst + kb * C::B_REGION + ib * (C::B_BOX_ROWS * 128), &b_map,
-                                        ks * C::BK + kb * 64, row0 + ib * C::B_BOX_ROWS, b_full(s), pol);
+                        for (int kb = 0; kb < C::B_KBLK; ++kb)
+                            for (int ib = 0; ib < nbox; ++ib)
+                                tma_load_2d(dst + kb * C::B_REGION + ib * (C::B_BOX_ROWS * 128), &b_map,
+                                            ks * C::BK + kb * 64, row0 + ib * C::B_BOX_ROWS, b_full(s),
+                                            pol);
+                    }
                 }
                 __syncwarp();
             }

@@ -89,15 +89,14 @@ enum GemmConfig : int {
 
 int gemm_cfg_bk(int cfg);
 int gemm_cfg_maxn(int cfg);
-int gemm_cfg_box_rows(int cfg);  // rows of one token TMA box: min(token tile, 64)
 int gemm_cfg_smem(int cfg, bool gate_up);
 
 // Launch one GEMM (gate_up with fused SiLU*up, or down with its epilogue).
-// codes_map: 2-D tensor map over the codes, inner dim K/8 int32 words, outer
-// E*N rows, box {BK/8, gate_up ? 64 : 128}, 128B (BK 256) or 64B (BK 128) swizzle.
-// b_map: 2-D tensor map over the bf16 token rows (padded-row order), inner dim
-// K, box {64, gemm_cfg_box_rows(cfg)}, 128B swizzle, zero fill past the last row.
+// codes_map / scales_map / b_map: the tensor maps of api.cu's codes_map(),
+// scales_map() (read only for BK 256 stages) and rows_map() for this
+// configuration's BK and token tile.
 cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& codes_map,
-                        const CUtensorMap& b_map, const GemmArgs& a, int grid, cudaStream_t s);
+                        const CUtensorMap& scales_map, const CUtensorMap& b_map, const GemmArgs& a,
+                        int grid, cudaStream_t s);
 
 }  // namespace chord
