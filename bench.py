@@ -41,7 +41,7 @@ KERNEL_SOURCES = ["gemm_kernel.cuh", "gemm_instances.cuh", "device.cuh"]
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--T", type=int, default=None)
@@ -105,54 +105,125 @@ def ncu_traffic(kernel: str, workload: str, src_hash: str):
 
 
 class Clocks:
-    """nvidia-smi samples during the timed region."""
+    """SM clock, power and clock-event reasons sampled every millisecond during
+    the timed region, read through NVML (libnvidia-ml via ctypes); nvidia-smi
+    at its fastest period when NVML cannot be loaded."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, uuid: str | None = None):
         self.index = index
-        self.p = None
+        self.uuid = uuid
+        self.samples = []  # (sm_mhz, reasons_mask, power_w)
+        self.max_mhz = None
+        self.source = None
+        self._stop = None
+        self._thread = None
+        self._smi = None
+
+    def _nvml_handle(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            for u in (self.uuid, "GPU-" + self.uuid):
+                if lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0:
+                    ok = True
+                    break
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return lib, h
 
     def __enter__(self):
+        import ctypes
+        import threading
         try:
-            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
-                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            lib, h = self._nvml_handle()
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._stop = threading.Event()
+            started = threading.Event()
+
+            def run():
+                mhz, rs, mw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+                while True:
+                    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                        r = rs.value if reasons_fn(h, ctypes.byref(rs)) == 0 else 0
+                        p = mw.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else None
+                        self.samples.append((float(mhz.value), r, p))
+                    started.set()
+                    if self._stop.wait(0.001):
+                        break
+
+            self._thread = threading.Thread(target=run, daemon=True)
+            self._thread.start()
+            started.wait(2.0)
+            self.source = "nvml, 1 ms"
         except Exception:
-            self.p = None
+            self._thread = None
+            try:
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.SMI_Q}",
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi, 20 ms"
+            except Exception:
+                self._smi = None
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.p is not None:
-            self.p.terminate()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(5.0)
+        if self._smi is not None:
+            self._smi.terminate()
             try:
-                out, _ = self.p.communicate(timeout=5)
+                out, _ = self._smi.communicate(timeout=5)
             except Exception:
-                self.p.kill()
+                self._smi.kill()
                 out = ""
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            bits = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+                    "sw_power_cap": 0x4}
+            for ln in out.splitlines():
+                f = [x.strip() for x in ln.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    mhz = float(f[1])
+                    self.max_mhz = float(f[2])
+                    pw = float(f[3])
+                except ValueError:
+                    continue
+                mask = 0
+                for nm, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        mask |= bits[nm]
+                self.samples.append((mhz, mask, pw))
         return False
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
+        sm = [m for m, _, _ in self.samples]
+        reasons = set()
+        for _, r, _ in self.samples:
+            for bit, nm in self.REASONS.items():
+                if r & bit:
                     reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        pw = [p for _, _, p in self.samples if p is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None, "sampler": self.source}
 
 
 def device_inputs(inp, torch, dev):
@@ -224,7 +295,11 @@ def run_ours(args, rank, world, dev_index):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    with Clocks(dev_index) as clk:
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev_index).uuid)
+    except Exception:
+        uuid = None
+    with Clocks(dev_index, uuid) as clk:
         with torch.cuda.stream(stream):
             ev0.record(stream)
             for _ in range(args.steps):
@@ -325,6 +400,9 @@ def run_ours(args, rank, world, dev_index):
     return res, inp
 
 
+REF_BUDGET_S = 150.0
+
+
 def cpu_oracle_time(inp, max_tokens=None):
     """Wall time of the CPU oracle on (a sample of) the workload: align + layer."""
     import oracle
@@ -358,20 +436,28 @@ def cpu_baseline(inp):
 
 
 def run_reference(args):
+    """The oracle timed on the host cores.  Each step is a bounded sample: the
+    first T' tokens of the workload, T' sized from one untimed calibration run
+    so that all warm-up and timed steps take about REF_BUDGET_S together; its
+    time is scaled by tokens to one call."""
     from w4a16_int4_mixture_gb300 import synth
     import oracle
     oracle.build()
     s = synth.config(args.config, T=args.T)
     inp = synth.make_inputs(s)
-    max_tok = s.T if s.T <= 1024 else 256
+    cap = s.T if s.T <= 1024 else 256
+    t_cal, T_cal, _ = cpu_oracle_time(inp, cap)
+    per_step = REF_BUDGET_S / max(1, args.warmup + args.steps)
+    T_step = max(1, min(T_cal, int(T_cal * per_step / max(t_cal, 1e-9))))
     times = []
     for i in range(args.warmup + args.steps):
-        dt, T, cores = cpu_oracle_time(inp, max_tok)
+        dt, T, cores = cpu_oracle_time(inp, T_step)
         if i >= args.warmup:
             times.append(dt * (s.T / T))
     per_call_us = statistics.median(times) * 1e6
-    sample = (f"CPU oracle (plain C, fp32) on {T} of {s.T} tokens of {s.name} per step, scaled "
-              f"by tokens to one call")
+    sample = (f"CPU oracle (plain C, fp32) on the first {T} of {s.T} tokens of {s.name} per step "
+              f"(sized for a {REF_BUDGET_S:.0f} s run; calibration {T_cal} tokens in "
+              f"{t_cal:.2f} s), scaled by tokens to one call")
     return {
         "impl": "reference", "metric": METRIC, "value": round(per_call_us, 1), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
