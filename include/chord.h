@@ -17,7 +17,14 @@
  *   weight codes: int32 words, 8 codes per word along K, element c = 8w+i in
  *     bits [4i, 4i+4) (low nibble first); W13 codes [E_local, 2I, H/8] (rows
  *     0..I-1 gate, I..2I-1 up), W2 codes [E_local, H, I/8];
- *   scales: bf16 [E_local, 2I, H/32] and [E_local, H, I/32];
+ *   scales: bf16 [E_local, 2I, H/32] and [E_local, H, I/32]; every scale is
+ *     +-0 or has magnitude in [2^-86, 2^35) (about 1.3e-26 to 3.4e10).  The
+ *     kernels form each weight as bf16((q - 8) * scale * 2^-40) with one
+ *     rounding and scale the fp32 accumulators by 2^40; inside this range
+ *     that equals bf16((q - 8) * scale) exactly.  With
+ *     CHORD_FLAG_VALIDATE the layer calls check every scale and return
+ *     CHORD_ERR_SCALE_RANGE (device error bit CHORD_DEVERR_SCALE_RANGE);
+ *     without it an out-of-range scale gives an inexact weight, not an error.
  *   all matrices row-major and densely packed.
  *
  * Ownership and execution:
@@ -57,7 +64,8 @@ typedef enum {
     CHORD_ERR_TIMEOUT = -6,           /* a device-side bounded wait expired (validate / query) */
     CHORD_ERR_ROUTING = -7,           /* device found invalid routing data (validate / query) */
     CHORD_ERR_WORKSPACE = -8,         /* workspace missing, misaligned or too small */
-    CHORD_ERR_NO_DEVICE = -9          /* no sm_103a device is current */
+    CHORD_ERR_NO_DEVICE = -9,         /* no sm_103a device is current */
+    CHORD_ERR_SCALE_RANGE = -10       /* a scale outside the supported range (validate / query) */
 } chord_status;
 
 /* grouped layouts (page: "grouped SM90 kernels", Fig. 3) */
@@ -74,6 +82,7 @@ typedef enum {
 #define CHORD_DEVERR_TIMEOUT 1
 #define CHORD_DEVERR_ROUTING 2
 #define CHORD_DEVERR_CAPACITY 4
+#define CHORD_DEVERR_SCALE_RANGE 8
 
 /* Human-readable name of a status. */
 const char* chord_status_string(int status);

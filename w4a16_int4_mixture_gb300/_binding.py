@@ -23,6 +23,7 @@ STATUS = {
     -4: "layout mode mismatch", -5: "CUDA error", -6: "device wait timed out",
     -7: "invalid routing data", -8: "workspace missing, misaligned or too small",
     -9: "no sm_103a device current",
+    -10: "scale outside the supported range",
 }
 GROUPED_CONTIGUOUS = 0
 GROUPED_MASKED = 1
@@ -31,6 +32,7 @@ FLAG_DETERMINISTIC = 2
 DEVERR_TIMEOUT = 1
 DEVERR_ROUTING = 2
 DEVERR_CAPACITY = 4
+DEVERR_SCALE_RANGE = 8
 
 # every symbol include/chord.h declares, with (restype, argtypes)
 _i64, _int, _sz, _vp, _cp = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p

@@ -428,6 +428,8 @@ chord_status read_error_word(void* ws, cudaStream_t s, int* bits, bool clear)
         return CHORD_ERR_ROUTING;
     if (v & CHORD_DEVERR_CAPACITY)
         return CHORD_ERR_CAPACITY;
+    if (v & CHORD_DEVERR_SCALE_RANGE)
+        return CHORD_ERR_SCALE_RANGE;
     return CHORD_OK;
 }
 
@@ -547,6 +549,7 @@ const char* chord_status_string(int status)
     case CHORD_ERR_CUDA: return "CUDA error";
     case CHORD_ERR_TIMEOUT: return "device wait timed out";
     case CHORD_ERR_ROUTING: return "invalid routing data";
+    case CHORD_ERR_SCALE_RANGE: return "scale outside the supported range";
     case CHORD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case CHORD_ERR_NO_DEVICE: return "no sm_103a device current";
     default: return "unknown status";
@@ -734,6 +737,11 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
         work_blocks = dev.sms;
     if (launch_prep(pa, work_blocks, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
+    if ((flags & CHORD_FLAG_VALIDATE) &&
+        launch_scale_check(w13_s, static_cast<int64_t>(E_local) * 2 * I * (H / 32), w2_s,
+                           static_cast<int64_t>(E_local) * H * (I / 32), err, dev.sms, s) !=
+            cudaSuccess)
+        return CHORD_ERR_CUDA;
 
     LayerIO io{};
     io.src = xs;
@@ -852,6 +860,11 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     }
     pa.err = err;
     if (launch_prep(pa, zero_blocks_for(with_tokens ? T * H : 0, dev.sms), s) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    if ((flags & CHORD_FLAG_VALIDATE) &&
+        launch_scale_check(w13_s, static_cast<int64_t>(E_local) * 2 * I * (H / 32), w2_s,
+                           static_cast<int64_t>(E_local) * H * (I / 32), err, dev.sms, s) !=
+            cudaSuccess)
         return CHORD_ERR_CUDA;
 
     LayerIO io{};

@@ -356,6 +356,39 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
     }
 }
 
+// CHORD_FLAG_VALIDATE: every scale is +-0 or has magnitude in [2^-86, 2^35)
+// (bf16 exponent field 41..161), the range in which the GEMMs' scaled weights
+// are exact; anything else sets CHORD_DEVERR_SCALE_RANGE.
+__device__ __forceinline__ bool scale_in_range(uint32_t bits16)
+{
+    const uint32_t mag = bits16 & 0x7FFFu;
+    const uint32_t e = mag >> 7;
+    return mag == 0 || (e >= 41 && e <= 161);
+}
+
+__global__ void scale_range_kernel(const uint16_t* __restrict__ a, int64_t na,
+                                   const uint16_t* __restrict__ b, int64_t nb, int* err)
+{
+    bool ok = true;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb;
+         i += stride) {
+        const uint32_t v = i < na ? a[i] : b[i - na];
+        ok = ok && scale_in_range(v);
+    }
+    if (!ok)
+        raise_error(err, CHORD_DEVERR_SCALE_RANGE);
+}
+
+cudaError_t launch_scale_check(const uint16_t* a, int64_t na, const uint16_t* b, int64_t nb,
+                               int* err, int sms, cudaStream_t s)
+{
+    if (na + nb <= 0)
+        return cudaSuccess;
+    scale_range_kernel<<<4 * sms, 256, 0, s>>>(a, na, b, nb, err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prep(const PrepArgs& a, int work_blocks, cudaStream_t s)
 {
     prep_kernel<<<1 + work_blocks, 1024, 0, s>>>(a);

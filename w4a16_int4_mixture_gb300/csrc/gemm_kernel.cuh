@@ -23,11 +23,12 @@
 //   warps 4-7   epilogue: TMEM -> registers; gate_up: SiLU(gate)*up -> bf16 h;
 //               down: per-pair fp32 store, fp32 reductions into token rows,
 //               or bf16 row store.
-//   warps 8-15  dequant, two groups taking alternate K stages: codes + scales
-//               from shared memory -> w = bf16((q - 8) * s), one rounding of
-//               the exact product as in the page's order (exact q - 8, then
-//               the scale multiply) -> tcgen05.st into
-//               the A-operand stage in TMEM.
+//   warps 8-15  dequant, two warps per TMEM lane quadrant taking K stages in
+//               order from a shared counter: codes + scales from shared memory
+//               -> w = bf16((q - 8) * s), one rounding of the exact product as
+//               in the page's order (exact q - 8, then the scale multiply),
+//               held as w * 2^-40 (undone on the fp32 accumulators) ->
+//               tcgen05.st into the A-operand stage in TMEM.
 // Every wait is bounded (2 s); on expiry the CTA records CHORD_DEVERR_TIMEOUT,
 // every role leaves its loop, in-flight tensor-core work is drained and TMEM
 // is freed.
@@ -122,34 +123,47 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
     return d;
 }
 
-// Per scale group: the constants of the dequant fma, from the bf16x2 scale
-// pair s2 = (s, s): s * 2^6 and -8 * s (both exact: power-of-two multiples).
+// The weights enter the MMA as w' = bf16((q - 8) * s * 2^-40); the epilogue
+// multiplies the fp32 accumulators by 2^40 (exact).  For +-0 scales and
+// |s| in [2^-86, 2^35) every step below is exact up to the one rounding and
+// (q - 8) * s * 2^-40 stays a normal bf16, so w' * 2^40 = bf16((q - 8) * s):
+// the page's value, one rounding of the exact product.  (2^-40 keeps the
+// products w' * x far above the fp32 subnormal range for any realistic scale
+// and activation.)
+constexpr float kWeightRescale = 1099511627776.0f;  // 2^40
+
+// Per scale group: the fma constants from the bf16x2 scale pair s2 = (s, s):
+// A = (s * 2^93, s * 2^89) (for the low / high element of a pair, whose codes
+// arrive scaled by 2^-133 / 2^-129) and B = -8 s * 2^-40 = -s * 2^-37; both are
+// power-of-two multiples of s, so exact inside the scale range.
 struct ScalePair {
-    uint32_t s6;
-    uint32_t m8;
+    uint32_t a;
+    uint32_t b;
 };
 __device__ __forceinline__ ScalePair scale_pair(uint32_t s2)
 {
-    return {bf16x2_mul(s2, 0x42804280u) /* 64 */, bf16x2_mul(s2, 0xC100C100u) /* -8 */};
+    return {bf16x2_mul(s2, 0x6C006E00u) /* (2^93, 2^89) */,
+            bf16x2_mul(s2, 0xAD00AD00u) /* -2^-37 */};
 }
 
 // Dequantise one word of 8 codes (element i in bits 4i..4i+3) into 4 bf16x2
-// columns (elements (0,1) .. (6,7)), each w = (q - 8) * s rounded once.
-//   lo / hi: the low / high nibble of each byte (elements 0,2,4,6 / 1,3,5,7);
-//   prmt:    bytes (q_2j, 0, q_2j+1, 0) = two bf16 subnormals q * 2^-133;
-//   * 2^127: q * 2^-6, exact;
-//   fma:     (q * 2^-6) * (s * 2^6) + (-8 s): the product q * s and the sum
-//            (q - 8) * s are exact before the one rounding, so the result is
-//            the bf16 rounding of (q - 8) * s.
+// columns (elements (0,1) .. (6,7)) of w' (see above).
+//   lo / hi: w & 0x0F0F0F0F / w & 0xF0F0F0F0: byte j holds q_2j / 16 q_2j+1;
+//   prmt:    bytes (q_2j, 0, 16 q_2j+1, 0) as two bf16 bit patterns: q_2j *
+//            2^-133 and q_2j+1 * 2^-129 (subnormal, or for 16 q >= 128 the
+//            first normal binade, which continues the subnormal spacing); the
+//            zero bytes replicate the sign bit of a lo byte (always 0);
+//   fma:     q * 2^-133 * (s * 2^93) + (-s * 2^-37) = (q - 8) * s * 2^-40
+//            (likewise for the high element): the product and the sum are
+//            exact before the one rounding.
 __device__ __forceinline__ void dequant_word(uint32_t w, ScalePair sp, uint32_t* o)
 {
     const uint32_t lo = w & 0x0F0F0F0Fu;
-    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+    const uint32_t hi = w & 0xF0F0F0F0u;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t sel = static_cast<uint32_t>(j | ((8 | j) << 4) | ((4 + j) << 8) | ((12 + j) << 12));
-        const uint32_t t = prmt(lo, hi, sel);
-        o[j] = bf16x2_fma(bf16x2_mul(t, 0x7F007F00u) /* 2^127 */, sp.s6, sp.m8);
+        const uint32_t sel = static_cast<uint32_t>(j | ((8 | j) << 4) | ((4 + j) << 8) | ((8 | j) << 12));
+        o[j] = bf16x2_fma(prmt(lo, hi, sel), sp.a, sp.b);
     }
 }
 
@@ -437,7 +451,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tmem_wait_ld();
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const float mine = __uint_as_float(v[jj]);
+                        const float mine = __uint_as_float(v[jj]) * kWeightRescale;
                         const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
                         if (is_gate) {
                             // fast exp / divide: a few fp32 ulp, far below the bf16 rounding of h
@@ -481,7 +495,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (int jj = 0; jj < 16; ++jj)
                             if (c0 + jj < ntok)
                                 args.rows_out[static_cast<int64_t>(ch.row0 + c0 + jj) * N + n] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[jj])));
+                                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[jj]) *
+                                                                             kWeightRescale));
                     }
                     if (per_pair) {
                         // the 16 columns' metadata at once (broadcast reads), then 16
@@ -501,7 +516,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (int jj = 0; jj < 16; ++jj) {
                             if (c0 + jj >= ntok || pp[jj] < 0)
                                 continue;
-                            const float y = __uint_as_float(v[jj]);
+                            const float y = __uint_as_float(v[jj]) * kWeightRescale;
                             if (args.epi & kEpiStorePair)
                                 args.y_pairs[static_cast<int64_t>(pp[jj]) * N + n] = y;
                             if (args.epi & kEpiReduceTok)

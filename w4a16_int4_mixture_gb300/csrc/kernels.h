@@ -75,6 +75,10 @@ struct CombineArgs {
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
 cudaError_t launch_prep(const PrepArgs& a, int work_blocks, cudaStream_t s);
+// Sets CHORD_DEVERR_SCALE_RANGE when a scale of a[0..na) or b[0..nb) (bf16
+// bits) is neither +-0 nor of magnitude in [2^-86, 2^35).
+cudaError_t launch_scale_check(const uint16_t* a, int64_t na, const uint16_t* b, int64_t nb,
+                               int* err, int sms, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int sms, cudaStream_t s);
 cudaError_t launch_combine_pairs(const CombineArgs& a, cudaStream_t s);
 
