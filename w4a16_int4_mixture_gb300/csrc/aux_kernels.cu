@@ -78,49 +78,62 @@ __device__ int block_exclusive_scan(int v, int* total)
     return before;
 }
 
+// One CTA, one thread per local expert (E_local <= 1024).  The per-tile
+// histogram is read through shared memory in chunks of whole tiles (coalesced
+// loads instead of one dependent load per tile and expert).
+constexpr int kScanSmemInts = 8192;
+
 __global__ void __launch_bounds__(1024) align_scan_kernel(AlignArgs a)
 {
+    __shared__ int sh[kScanSmemInts];
     const int sentinel = static_cast<int>(a.num_pairs);
     const int bm = a.block_m;
+    const int E = a.E_local;
+    const int e = threadIdx.x;
     // this call's error word starts clear (the scatter reports bad ids after us)
     if (threadIdx.x == 0)
         *a.err = 0;
     // sentinel everywhere first; the scatter overwrites the real entries
     for (int64_t i = threadIdx.x; i < a.capacity; i += blockDim.x)
         a.sorted_ids[i] = sentinel;
-    __shared__ int s_base;
-    if (threadIdx.x == 0)
-        s_base = 0;
-    __syncthreads();
     const int n_tiles = a.n_tiles;
-    for (int e0 = 0; e0 < a.E_local; e0 += blockDim.x) {
-        const int e = e0 + threadIdx.x;
-        int count = 0;
-        if (e < a.E_local)
-            for (int t = 0; t < n_tiles; ++t)
-                count += a.tile_hist[static_cast<int64_t>(t) * a.E_local + e];
-        const int padded = (count + bm - 1) / bm * bm;
-        int total;
-        const int off = s_base + block_exclusive_scan(padded, &total);
-        if (e < a.E_local) {
-            // per-tile bases (in place over the histogram)
-            int run = off;
-            for (int t = 0; t < n_tiles; ++t) {
-                const int64_t idx = static_cast<int64_t>(t) * a.E_local + e;
-                const int c = a.tile_hist[idx];
-                a.tile_hist[idx] = run;
-                run += c;
-            }
-            if (off + padded <= a.capacity)
-                for (int b = off / bm; b < (off + padded) / bm; ++b)
-                    a.expert_ids[b] = e;
-        }
+    const int tch = kScanSmemInts / E > 0 ? kScanSmemInts / E : 1;
+    // pass 1: routed pairs per expert
+    int count = 0;
+    for (int t0 = 0; t0 < n_tiles; t0 += tch) {
+        const int nt = n_tiles - t0 < tch ? n_tiles - t0 : tch;
+        for (int i = threadIdx.x; i < nt * E; i += blockDim.x)
+            sh[i] = a.tile_hist[static_cast<int64_t>(t0) * E + i];
         __syncthreads();
-        if (threadIdx.x == 0)
-            s_base += total;
+        if (e < E)
+            for (int t = 0; t < nt; ++t)
+                count += sh[t * E + e];
         __syncthreads();
     }
-    const int ntp = s_base;
+    const int padded = e < E ? (count + bm - 1) / bm * bm : 0;
+    int ntp;
+    const int off = block_exclusive_scan(padded, &ntp);
+    // pass 2: per-tile bases, in place over the histogram
+    int run = off;
+    for (int t0 = 0; t0 < n_tiles; t0 += tch) {
+        const int nt = n_tiles - t0 < tch ? n_tiles - t0 : tch;
+        for (int i = threadIdx.x; i < nt * E; i += blockDim.x)
+            sh[i] = a.tile_hist[static_cast<int64_t>(t0) * E + i];
+        __syncthreads();
+        if (e < E)
+            for (int t = 0; t < nt; ++t) {
+                const int c = sh[t * E + e];
+                sh[t * E + e] = run;
+                run += c;
+            }
+        __syncthreads();
+        for (int i = threadIdx.x; i < nt * E; i += blockDim.x)
+            a.tile_hist[static_cast<int64_t>(t0) * E + i] = sh[i];
+        __syncthreads();
+    }
+    if (e < E && off + padded <= a.capacity)
+        for (int b = off / bm; b < (off + padded) / bm; ++b)
+            a.expert_ids[b] = e;
     if (ntp > a.capacity && threadIdx.x == 0)
         raise_error(a.err, CHORD_DEVERR_CAPACITY);
     const int64_t nblocks = a.capacity / bm;
@@ -269,15 +282,29 @@ __device__ void build_chunk_lists(const PrepArgs& a)
         } else {
             nblocks = static_cast<int>(a.M / a.block_rows);
         }
+        // the experts of this tile of blocks (plus one on each side) in shared
+        // memory, read with one coalesced pass; a run that leaves the staged
+        // tile continues with direct reads
+        __shared__ int s_e[1024 + 2];
+        const int staged = static_cast<int>(blockDim.x) + 2;
         for (int b0 = 0; b0 < nblocks; b0 += blockDim.x) {
+            for (int i = threadIdx.x; i < staged; i += blockDim.x)
+                s_e[i] = block_expert(a, b0 - 1 + i, nblocks);
+            __syncthreads();
             const int b = b0 + threadIdx.x;
             int rows = 0, e = -1;
             if (b < nblocks) {
-                e = block_expert(a, b, nblocks);
-                if (e >= 0 && block_expert(a, b - 1, nblocks) != e) {
+                e = s_e[threadIdx.x + 1];
+                if (e >= 0 && s_e[threadIdx.x] != e) {
                     int end = b + 1;
-                    while (end < nblocks && block_expert(a, end, nblocks) == e)
+                    int li = threadIdx.x + 2;
+                    while (end < nblocks && li < staged && s_e[li] == e) {
                         ++end;
+                        ++li;
+                    }
+                    if (li == staged)
+                        while (end < nblocks && block_expert(a, end, nblocks) == e)
+                            ++end;
                     rows = (end - b) * a.block_rows;
                 }
             }
@@ -324,34 +351,34 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
         for (int64_t i = tid; i < a.fill_count; i += nth)
             a.fill_i32[i] = -1;
     if (a.gx_out != nullptr) {
-        // one warp per padded row, 16-byte vectors, four loads in flight per lane
-        const int lane = threadIdx.x & 31;
-        const int64_t w0 = static_cast<int64_t>(blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-        const int64_t nw = static_cast<int64_t>(gridDim.x - 1) * (blockDim.x >> 5);
+        // 128 threads per padded row, up to 8 16-byte loads in flight per
+        // thread before the stores
+        constexpr int kGroup = 128;
+        const int gl = static_cast<int>(tid % kGroup);
+        const int64_t ngrp = nth / kGroup;
         const int ntp = a.num_tokens_padded[0];
         const int64_t rows = (ntp >= 0 && ntp <= a.capacity) ? ntp : 0;
         const int n16 = a.gx_H / 8;
-        for (int64_t r = w0; r < rows; r += nw) {
+        for (int64_t r = tid / kGroup; r < rows; r += ngrp) {
             const int p = a.gx_ids[r];
-            if (p < 0 || p >= a.gx_pairs) {
-                // sentinel row: zeros, so its h row is exactly 0
-                uint4* dst = reinterpret_cast<uint4*>(a.gx_out + r * a.gx_H);
-                for (int i = lane; i < n16; i += 32)
-                    dst[i] = make_uint4(0u, 0u, 0u, 0u);
-                continue;
-            }
-            const uint4* src = reinterpret_cast<const uint4*>(a.gx_src + static_cast<int64_t>(p / a.gx_topk) * a.gx_H);
+            const bool valid = p >= 0 && p < a.gx_pairs;  // sentinel rows become zeros
+            const uint4* src =
+                reinterpret_cast<const uint4*>(a.gx_src + static_cast<int64_t>(valid ? p / a.gx_topk : 0) * a.gx_H);
             uint4* dst = reinterpret_cast<uint4*>(a.gx_out + r * a.gx_H);
-            int i = lane;
-            for (; i + 96 < n16; i += 128) {
-                const uint4 v0 = src[i], v1 = src[i + 32], v2 = src[i + 64], v3 = src[i + 96];
-                dst[i] = v0;
-                dst[i + 32] = v1;
-                dst[i + 64] = v2;
-                dst[i + 96] = v3;
+            for (int c0 = gl; c0 < n16; c0 += 8 * kGroup) {
+                uint4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c = c0 + j * kGroup;
+                    v[j] = (valid && c < n16) ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c = c0 + j * kGroup;
+                    if (c < n16)
+                        dst[c] = v[j];
+                }
             }
-            for (; i < n16; i += 32)
-                dst[i] = src[i];
         }
     }
 }
