@@ -296,6 +296,7 @@ struct Workspace {
     size_t off_hdr = 0;  // int err; int num_chunks[2]
     size_t off_chunks[2] = {0, 0};
     size_t off_xs = 0;   // indexed: bf16 [capacity, H], token rows in padded-row order
+    size_t off_meta = 0; // with tokens: int4 [h_rows] {pair, token, weight bits, 0} per row
     size_t off_h = 0;
     size_t off_acc = 0;       // reduce: float [T, H]; store: float [T*k, H]
     size_t off_pair_row = 0;  // store: int32 [T*k]
@@ -320,6 +321,8 @@ Workspace layout_ws(int64_t max_chunks, int64_t h_rows, int I, int64_t T, int k,
     w.off_h = o;
     o = align_up(o + static_cast<size_t>(h_rows) * I * 2, kAlign);
     if (with_tokens) {
+        w.off_meta = o;
+        o = align_up(o + static_cast<size_t>(h_rows) * 16, kAlign);
         w.off_acc = o;
         if (reduce) {
             o = align_up(o + static_cast<size_t>(T) * H * 4, kAlign);
@@ -453,6 +456,7 @@ struct LayerIO {
     const int32_t *w13_q, *w2_q;
     const uint16_t *w13_s, *w2_s;
     const float* topk_weights;
+    const int4* row_meta;
     int64_t h_rows;
     uint16_t* h_out;  // caller-provided intermediate, or null (workspace)
     uint16_t* rows_out;
@@ -504,8 +508,8 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.h_out = h;
     g.ld_h = io.I;
     g.pair_row = pair_row;
-    g.topk_weights = io.topk_weights;
     g.pair_of_row = io.pair_of_row;
+    g.row_meta = io.row_meta;
     g.err = err;
     marks.mark(1);
     if (launch_gemm(sc.cfg_gate_up, true, map13, smap13, bmap13, g, dev.sms, s) != cudaSuccess)
@@ -725,6 +729,13 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
         pa.fill_count = T * k;
     }
     uint16_t* xs = reinterpret_cast<uint16_t*>(ws + w.off_xs);
+    int4* meta = reinterpret_cast<int4*>(ws + w.off_meta);
+    pa.meta_out = meta;
+    pa.meta_pair = sorted_ids;
+    pa.meta_w = topk_weights;
+    pa.meta_topk = k;
+    pa.meta_pairs = T * k;
+    pa.meta_rows = -1;
     pa.gx_src = x;
     pa.gx_out = xs;
     pa.gx_ids = sorted_ids;
@@ -747,6 +758,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     io.src = xs;
     io.src_rows = capacity;
     io.pair_of_row = sorted_ids;
+    io.row_meta = meta;
     io.k = k;
     io.num_pairs = T * k;
     io.H = H;
@@ -857,9 +869,18 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     if (with_tokens) {
         pa.zero_f32 = acc;
         pa.zero_count = T * H;
+        pa.meta_out = reinterpret_cast<int4*>(ws + w.off_meta);
+        pa.meta_pair = row_to_pair;
+        pa.meta_w = topk_weights;
+        pa.meta_topk = k;
+        pa.meta_pairs = T * k;
+        pa.meta_rows = M;
     }
     pa.err = err;
-    if (launch_prep(pa, zero_blocks_for(with_tokens ? T * H : 0, dev.sms), s) != cudaSuccess)
+    int work_blocks = zero_blocks_for(with_tokens ? T * H : 0, dev.sms);
+    if (with_tokens && work_blocks < dev.sms)
+        work_blocks = dev.sms;  // the per-row records are written by the worker blocks
+    if (launch_prep(pa, work_blocks, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     if ((flags & CHORD_FLAG_VALIDATE) &&
         launch_scale_check(w13_s, static_cast<int64_t>(E_local) * 2 * I * (H / 32), w2_s,
@@ -870,6 +891,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     LayerIO io{};
     io.src = a;
     io.src_rows = M;
+    io.row_meta = with_tokens ? reinterpret_cast<const int4*>(ws + w.off_meta) : nullptr;
     io.pair_of_row = with_tokens ? row_to_pair : nullptr;
     io.k = with_tokens ? k : 1;
     io.num_pairs = with_tokens ? T * k : 0;

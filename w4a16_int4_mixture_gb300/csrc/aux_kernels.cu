@@ -350,6 +350,21 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
     if (a.fill_i32 != nullptr)
         for (int64_t i = tid; i < a.fill_count; i += nth)
             a.fill_i32[i] = -1;
+    if (a.meta_out != nullptr && a.gx_out == nullptr) {
+        // (with a gather, the gather loop below writes the records)
+        int64_t rows = a.meta_rows;
+        if (rows < 0) {
+            const int ntp = a.num_tokens_padded[0];
+            rows = (ntp >= 0 && ntp <= a.capacity) ? ntp : 0;
+        }
+        for (int64_t r = tid; r < rows; r += nth) {
+            const int p = a.meta_pair[r];
+            int4 m = make_int4(-1, 0, 0, 0);
+            if (p >= 0 && p < a.meta_pairs)
+                m = make_int4(p, p / a.meta_topk, __float_as_int(a.meta_w[p]), 0);
+            a.meta_out[r] = m;
+        }
+    }
     if (a.gx_out != nullptr) {
         // 128 threads per padded row, up to 8 16-byte loads in flight per
         // thread before the stores
@@ -362,6 +377,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
         for (int64_t r = tid / kGroup; r < rows; r += ngrp) {
             const int p = a.gx_ids[r];
             const bool valid = p >= 0 && p < a.gx_pairs;  // sentinel rows become zeros
+            if (gl == 0 && a.meta_out != nullptr)
+                a.meta_out[r] = valid ? make_int4(p, p / a.gx_topk, __float_as_int(a.meta_w[p]), 0)
+                                      : make_int4(-1, 0, 0, 0);
             const uint4* src =
                 reinterpret_cast<const uint4*>(a.gx_src + static_cast<int64_t>(valid ? p / a.gx_topk : 0) * a.gx_H);
             uint4* dst = reinterpret_cast<uint4*>(a.gx_out + r * a.gx_H);

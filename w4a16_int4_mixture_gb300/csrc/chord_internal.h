@@ -43,8 +43,8 @@ struct GemmArgs {
     float* y_pairs;           // down: [T*k, N]
     float* out_acc;           // down: [T, N]
     uint16_t* rows_out;       // down: [rows, N]
-    const float* topk_weights;
     const int32_t* pair_of_row;  // pair id t*k+j of each padded row (or -1 / sentinel)
+    const int4* row_meta;        // down: {pair, token, weight bits, 0} per padded row
     int* err;
 };
 

@@ -352,6 +352,19 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&v)[16])
         : "memory");
 }
 
+// Four consecutive fp32 reductions in one instruction (16-byte aligned address).
+__device__ __forceinline__ void red_add_v4_f32(float* addr, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_pack_rn(float lo, float hi)
+{
+    const __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&t);
+}
+
 // Fire-and-forget fp32 reduction.  No "memory" clobber: nothing in the kernel
 // reads the target after it, and a clobber would serialise the caller's
 // independent loads behind every reduction.

@@ -65,13 +65,17 @@ struct GemmCfg {
     static constexpr int HS_BYTES = GATE_UP ? MAXN * 128 : 0;  // 64 channels of bf16 per row
     // down: per token column (pair, token, weight), double-buffered by unit
     static constexpr int META_BYTES = GATE_UP ? 0 : 2 * 3 * MAXN * 4;
+    // down: per epilogue warp a 16-column x 32-row fp32 tile to transpose the
+    // accumulator so each lane owns four consecutive output rows of a column
+    static constexpr int EPIT_BYTES = GATE_UP ? 0 : 4 * 16 * 32 * 4;
 
     static constexpr int OFF_CODES = 0;
     static constexpr int OFF_B = OFF_CODES + KS * CODE_STAGE;
     static constexpr int OFF_SCALES = OFF_B + BS * B_STAGE;
     static constexpr int OFF_HS = OFF_SCALES + KS * SCALE_STAGE;
     static constexpr int OFF_META = OFF_HS + HS_BYTES;
-    static constexpr int OFF_BARS = OFF_META + META_BYTES;
+    static constexpr int OFF_EPIT = OFF_META + META_BYTES;
+    static constexpr int OFF_BARS = OFF_EPIT + EPIT_BYTES;
     static constexpr int NBARS = 2 * KS + 2 * AS + 2 * BS + 2 * ACCB + 2;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
     // misc: TMEM base, abort flag, 2 spare words, 4 per-quadrant stage counters
@@ -408,31 +412,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ++esync;
             return r;
         };
+        // down: the pair, token and weight of each column come from the
+        // per-row records prep wrote.  The records of the next unit are loaded
+        // into registers one unit ahead (their chunk descriptor two ahead), so
+        // no unit waits on a global load before its accumulator is read.
+        const bool per_pair = !C::GATE_UP && (args.epi & (kEpiStorePair | kEpiReduceTok)) != 0;
+        constexpr int MPT = (C::MAXN + 127) / 128;  // record columns per epilogue thread
+        int4 meta_next[MPT];
+        auto load_meta = [&](const Chunk& c_, int4* dst) {
+#pragma unroll
+            for (int k = 0; k < MPT; ++k) {
+                const int col = et + 128 * k;
+                dst[k] = (per_pair && col < c_.nrows) ? args.row_meta[c_.row0 + col]
+                                                      : make_int4(-1, 0, 0, 0);
+            }
+        };
         int i = 0;
-        Chunk next = chunk_of(blockIdx.x);
+        Chunk c_cur = chunk_of(blockIdx.x);
+        Chunk c_nxt = chunk_of(blockIdx.x + gridDim.x);
+        load_meta(c_cur, meta_next);
         for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++i) {
-            const Chunk ch = next;
-            next = chunk_of(u + gridDim.x);
+            const Chunk ch = c_cur;
+            int4 meta_cur[MPT];
+#pragma unroll
+            for (int k = 0; k < MPT; ++k)
+                meta_cur[k] = meta_next[k];
+            load_meta(c_nxt, meta_next);
+            const Chunk c_nn = chunk_of(u + 2 * gridDim.x);
             const int nt = u % n_tiles;
             const int ntok = ch.nrows;
             const int ntok16 = (ntok + 15) & ~15;
             const int acc = i % C::ACCB;
-            // down: pair, token and weight of each column, staged once per unit
-            // (before the accumulator wait, so the loads overlap the MMAs)
             int32_t* m_pair = reinterpret_cast<int32_t*>(smem + C::OFF_META) + (i & 1) * 3 * C::MAXN;
             int32_t* m_tok = m_pair + C::MAXN;
             float* m_w = reinterpret_cast<float*>(m_pair + 2 * C::MAXN);
-            const bool per_pair = !C::GATE_UP && (args.epi & (kEpiStorePair | kEpiReduceTok)) != 0;
             if (per_pair) {
-                for (int c = et; c < ntok; c += 128) {
-                    int p = args.pair_of_row ? args.pair_of_row[ch.row0 + c] : -1;
-                    if (p < 0 || p >= args.num_pairs)
-                        p = -1;
-                    m_pair[c] = p;
-                    m_tok[c] = p >= 0 ? p / args.topk : 0;
-                    m_w[c] = (p >= 0 && args.topk_weights) ? args.topk_weights[p] : 0.f;
+#pragma unroll
+                for (int k = 0; k < MPT; ++k) {
+                    const int col = et + 128 * k;
+                    if (col < ntok) {
+                        m_pair[col] = meta_cur[k].x;
+                        m_tok[col] = meta_cur[k].y;
+                        m_w[col] = __int_as_float(meta_cur[k].z);
+                    }
                 }
             }
+            c_cur = c_nxt;
+            c_nxt = c_nn;
             if (!mbar_wait(d_full(acc), (i / C::ACCB) & 1, abort_flag, err))
                 break;
             if (per_pair && !epi_sync())
@@ -484,50 +510,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (!epi_sync())
                     break;
             } else {
-                const int n = nt * 128 + q * 32 + lane;
+                // Each 32-row x 16-column block goes through a shared tile so that
+                // lane l owns rows 4 (l % 8) .. +3 of columns l / 8 + {0, 4, 8, 12}:
+                // 16-byte stores and vector reductions instead of one 4-byte
+                // access per lane and column.
                 const int N = args.N;
+                const int nq = nt * 128 + q * 32;
+                float* tile = reinterpret_cast<float*>(smem + C::OFF_EPIT) + q * 16 * 32;
+                const int m4 = (lane & 7) * 4;
+                const int cg = lane >> 3;
                 for (int c0 = 0; c0 < ntok16; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld_x16(dbase + c0, v);
                     tmem_wait_ld();
-                    if (args.epi & kEpiStoreRows) {
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            if (c0 + jj < ntok)
-                                args.rows_out[static_cast<int64_t>(ch.row0 + c0 + jj) * N + n] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[jj]) *
-                                                                             kWeightRescale));
+                    if (c0 + 16 >= ntok16) {
+                        // last block read: the accumulator goes back to the MMA
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(d_empty(acc));
                     }
-                    if (per_pair) {
-                        // the 16 columns' metadata at once (broadcast reads), then 16
-                        // independent stores / reductions
-                        int pp[16], tt[16];
-                        float ww[16];
 #pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4) {
-                            const int4 a = reinterpret_cast<const int4*>(m_pair + c0)[k4];
-                            const int4 b = reinterpret_cast<const int4*>(m_tok + c0)[k4];
-                            const float4 w4 = reinterpret_cast<const float4*>(m_w + c0)[k4];
-                            pp[4 * k4] = a.x; pp[4 * k4 + 1] = a.y; pp[4 * k4 + 2] = a.z; pp[4 * k4 + 3] = a.w;
-                            tt[4 * k4] = b.x; tt[4 * k4 + 1] = b.y; tt[4 * k4 + 2] = b.z; tt[4 * k4 + 3] = b.w;
-                            ww[4 * k4] = w4.x; ww[4 * k4 + 1] = w4.y; ww[4 * k4 + 2] = w4.z; ww[4 * k4 + 3] = w4.w;
+                    for (int j = 0; j < 16; ++j)
+                        tile[j * 32 + lane] = __uint_as_float(v[j]) * kWeightRescale;
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int j = cg + 4 * i;
+                        const int c = c0 + j;
+                        if (c >= ntok)
+                            continue;
+                        const float4 y = *reinterpret_cast<const float4*>(tile + j * 32 + m4);
+                        if (args.epi & kEpiStoreRows) {
+                            uint2 o;
+                            o.x = bf16x2_pack_rn(y.x, y.y);
+                            o.y = bf16x2_pack_rn(y.z, y.w);
+                            *reinterpret_cast<uint2*>(args.rows_out + static_cast<int64_t>(ch.row0 + c) * N +
+                                                      nq + m4) = o;
                         }
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            if (c0 + jj >= ntok || pp[jj] < 0)
-                                continue;
-                            const float y = __uint_as_float(v[jj]) * kWeightRescale;
-                            if (args.epi & kEpiStorePair)
-                                args.y_pairs[static_cast<int64_t>(pp[jj]) * N + n] = y;
-                            if (args.epi & kEpiReduceTok)
-                                red_add_f32(args.out_acc + static_cast<int64_t>(tt[jj]) * N + n, ww[jj] * y);
+                        if (per_pair) {
+                            const int p = m_pair[c];
+                            if (p >= 0) {
+                                if (args.epi & kEpiStorePair)
+                                    *reinterpret_cast<float4*>(args.y_pairs + static_cast<int64_t>(p) * N +
+                                                               nq + m4) = y;
+                                if (args.epi & kEpiReduceTok) {
+                                    const float w = m_w[c];
+                                    red_add_v4_f32(args.out_acc + static_cast<int64_t>(m_tok[c]) * N + nq + m4,
+                                                   w * y.x, w * y.y, w * y.z, w * y.w);
+                                }
+                            }
                         }
                     }
+                    __syncwarp();  // the tile is rewritten by the next block
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(d_empty(acc));
             }
         }
     } else if (warp >= 8) {

@@ -55,6 +55,15 @@ struct PrepArgs {
     int gx_topk;
     int64_t gx_pairs;        // T*k, the sentinel
     int gx_H;
+    // per padded row r: {pair p, token p / topk, bits of topk_weights[p], 0},
+    // or {-1, 0, 0, 0} for a row with no pair; rows r < meta_rows, or
+    // r < num_tokens_padded when meta_rows < 0
+    int4* meta_out;
+    const int32_t* meta_pair;  // pair id of each padded row (sorted_ids / row_to_pair)
+    const float* meta_w;       // topk_weights [T * topk]
+    int meta_topk;
+    int64_t meta_pairs;
+    int64_t meta_rows;
     // buffers to clear
     float* zero_f32;
     int64_t zero_count;
