@@ -172,8 +172,96 @@ __global__ void __launch_bounds__(kAlignTile) align_scatter_kernel(AlignArgs a)
     }
 }
 
+// The whole align in one CTA for small routing batches (the three kernels above
+// cost three launches and a single-CTA scan in between): histogram in shared
+// memory (each pair's local expert kept there too), padded offsets, then the
+// same stable scatter as align_scatter_kernel in rounds of kSmallThreads pairs,
+// each pair ranked by warp match + per-warp counts + the counts of earlier
+// rounds.  Same output, bit for bit.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallMaxPairs = 4096;
+constexpr int kSmallMaxExperts = 128;
+
+__global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
+{
+    __shared__ int cnt[kSmallMaxExperts];   // pass 1 counts, then pairs placed by earlier rounds
+    __shared__ int base[kSmallMaxExperts];  // first padded row of each expert
+    __shared__ int wcnt[kSmallThreads / 32][kSmallMaxExperts];  // per warp of a round
+    __shared__ short lexp[kSmallMaxPairs];  // local expert of each pair (-1: not local)
+    const int E = a.E_local;
+    constexpr int W = kSmallThreads / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int npairs = static_cast<int>(a.num_pairs);
+    const int sentinel = npairs;
+    const int bm = a.block_m;
+    if (threadIdx.x == 0)
+        *a.err = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        cnt[e] = 0;
+    for (int64_t i = threadIdx.x; i < a.capacity; i += blockDim.x)
+        a.sorted_ids[i] = sentinel;
+    __syncthreads();
+    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+        const int l = local_expert_of(a.topk_ids[p], a.E_global, a.expert_map, E, a.err);
+        lexp[p] = static_cast<short>(l);
+        if (l >= 0)
+            atomicAdd(&cnt[l], 1);
+    }
+    __syncthreads();
+    const int e = threadIdx.x;
+    const int padded = e < E ? (cnt[e] + bm - 1) / bm * bm : 0;
+    int ntp;
+    const int off = block_exclusive_scan(padded, &ntp);
+    if (e < E) {
+        base[e] = off;
+        cnt[e] = 0;
+        if (off + padded <= a.capacity)
+            for (int b = off / bm; b < (off + padded) / bm; ++b)
+                a.expert_ids[b] = e;
+    }
+    if (ntp > a.capacity && threadIdx.x == 0)
+        raise_error(a.err, CHORD_DEVERR_CAPACITY);
+    const int64_t nblocks = a.capacity / bm;
+    for (int64_t b = ntp / bm + threadIdx.x; b < nblocks; b += blockDim.x)
+        a.expert_ids[b] = -1;
+    if (threadIdx.x == 0)
+        a.num_tokens_padded[0] = ntp <= a.capacity ? ntp : 0;
+    for (int r0 = 0; r0 < npairs; r0 += blockDim.x) {
+        for (int i = threadIdx.x; i < W * kSmallMaxExperts; i += blockDim.x)
+            (&wcnt[0][0])[i] = 0;
+        __syncthreads();
+        const int p = r0 + threadIdx.x;
+        const int l = p < npairs ? lexp[p] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, l);
+        const unsigned lower = peers & ((1u << lane) - 1u);
+        if (l >= 0 && lower == 0)
+            wcnt[warp][l] = __popc(peers);
+        __syncthreads();
+        if (l >= 0) {
+            int rank = cnt[l] + __popc(lower);
+            for (int w = 0; w < warp; ++w)
+                rank += wcnt[w][l];
+            const int64_t pos = static_cast<int64_t>(base[l]) + rank;
+            if (pos < a.capacity)
+                a.sorted_ids[pos] = p;
+        }
+        __syncthreads();
+        for (int x = threadIdx.x; x < E; x += blockDim.x) {
+            int add = 0;
+            for (int w = 0; w < W; ++w)
+                add += wcnt[w][x];
+            cnt[x] += add;
+        }
+        __syncthreads();
+    }
+}
+
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s)
 {
+    if (a.num_pairs <= kSmallMaxPairs && a.E_local <= kSmallMaxExperts) {
+        align_small_kernel<<<1, kSmallThreads, 0, s>>>(a);
+        return cudaGetLastError();
+    }
     const int tiles = a.n_tiles;
     if (tiles > 0) {
         align_hist_kernel<<<tiles, kAlignTile, a.E_local * sizeof(int), s>>>(a);
