@@ -63,8 +63,7 @@ struct GemmCfg {
     static constexpr bool SCALES_TMA = BK == 256;
     static constexpr int B_STAGE = B_KBLK * B_REGION;
     static constexpr int HS_BYTES = GATE_UP ? MAXN * 128 : 0;  // 64 channels of bf16 per row
-    // down: per token column (pair, token, weight), double-buffered by unit
-    static constexpr int META_BYTES = GATE_UP ? 0 : 2 * 3 * MAXN * 4;
+    static constexpr int META_BYTES = 0;  // (column records live in registers)
     // down: per epilogue warp a 16-column x 32-row fp32 tile to transpose the
     // accumulator so each lane owns four consecutive output rows of a column
     static constexpr int EPIT_BYTES = GATE_UP ? 0 : 4 * 16 * 32 * 4;
@@ -413,16 +412,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             return r;
         };
         // down: the pair, token and weight of each column come from the
-        // per-row records prep wrote.  The records of the next unit are loaded
-        // into registers one unit ahead (their chunk descriptor two ahead), so
-        // no unit waits on a global load before its accumulator is read.
+        // per-row records prep wrote.  Every epilogue warp holds the unit's
+        // records itself (lane l: columns l, l + 32, ...) and takes them by
+        // warp shuffle, so the down path needs no cross-warp rendezvous.  The
+        // records of the next unit are loaded one unit ahead (their chunk
+        // descriptor two ahead), so no unit waits on a global load.
         const bool per_pair = !C::GATE_UP && (args.epi & (kEpiStorePair | kEpiReduceTok)) != 0;
-        constexpr int MPT = (C::MAXN + 127) / 128;  // record columns per epilogue thread
+        constexpr int MPT = C::MAXN / 32;  // record columns per lane
         int4 meta_next[MPT];
         auto load_meta = [&](const Chunk& c_, int4* dst) {
 #pragma unroll
             for (int k = 0; k < MPT; ++k) {
-                const int col = et + 128 * k;
+                const int col = lane + 32 * k;
                 dst[k] = (per_pair && col < c_.nrows) ? args.row_meta[c_.row0 + col]
                                                       : make_int4(-1, 0, 0, 0);
             }
@@ -443,25 +444,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int ntok = ch.nrows;
             const int ntok16 = (ntok + 15) & ~15;
             const int acc = i % C::ACCB;
-            int32_t* m_pair = reinterpret_cast<int32_t*>(smem + C::OFF_META) + (i & 1) * 3 * C::MAXN;
-            int32_t* m_tok = m_pair + C::MAXN;
-            float* m_w = reinterpret_cast<float*>(m_pair + 2 * C::MAXN);
-            if (per_pair) {
-#pragma unroll
-                for (int k = 0; k < MPT; ++k) {
-                    const int col = et + 128 * k;
-                    if (col < ntok) {
-                        m_pair[col] = meta_cur[k].x;
-                        m_tok[col] = meta_cur[k].y;
-                        m_w[col] = __int_as_float(meta_cur[k].z);
-                    }
-                }
-            }
             c_cur = c_nxt;
             c_nxt = c_nn;
             if (!mbar_wait(d_full(acc), (i / C::ACCB) & 1, abort_flag, err))
-                break;
-            if (per_pair && !epi_sync())
                 break;
             tc_fence_after();
             const uint32_t dbase =
@@ -519,7 +504,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 float* tile = reinterpret_cast<float*>(smem + C::OFF_EPIT) + q * 16 * 32;
                 const int m4 = (lane & 7) * 4;
                 const int cg = lane >> 3;
-                for (int c0 = 0; c0 < ntok16; c0 += 16) {
+#pragma unroll
+                for (int c0 = 0; c0 < C::MAXN; c0 += 16) {
+                    if (c0 >= ntok16)
+                        break;
                     uint32_t v[16];
                     tmem_ld_x16(dbase + c0, v);
                     tmem_wait_ld();
@@ -534,10 +522,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int j = 0; j < 16; ++j)
                         tile[j * 32 + lane] = __uint_as_float(v[j]) * kWeightRescale;
                     __syncwarp();
+                    const int4 mrec = meta_cur[c0 / 32];  // columns c0 .. c0 + 15 sit in one lane group
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int j = cg + 4 * i;
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const int j = cg + 4 * ii;
                         const int c = c0 + j;
+                        const int src = c & 31;
+                        const int p = __shfl_sync(0xffffffffu, mrec.x, src);
+                        const int tok = __shfl_sync(0xffffffffu, mrec.y, src);
+                        const float w = __int_as_float(__shfl_sync(0xffffffffu, mrec.z, src));
                         if (c >= ntok)
                             continue;
                         const float4 y = *reinterpret_cast<const float4*>(tile + j * 32 + m4);
@@ -548,18 +541,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             *reinterpret_cast<uint2*>(args.rows_out + static_cast<int64_t>(ch.row0 + c) * N +
                                                       nq + m4) = o;
                         }
-                        if (per_pair) {
-                            const int p = m_pair[c];
-                            if (p >= 0) {
-                                if (args.epi & kEpiStorePair)
-                                    *reinterpret_cast<float4*>(args.y_pairs + static_cast<int64_t>(p) * N +
-                                                               nq + m4) = y;
-                                if (args.epi & kEpiReduceTok) {
-                                    const float w = m_w[c];
-                                    red_add_v4_f32(args.out_acc + static_cast<int64_t>(m_tok[c]) * N + nq + m4,
-                                                   w * y.x, w * y.y, w * y.z, w * y.w);
-                                }
-                            }
+                        if (per_pair && p >= 0) {
+                            if (args.epi & kEpiStorePair)
+                                *reinterpret_cast<float4*>(args.y_pairs + static_cast<int64_t>(p) * N + nq + m4) = y;
+                            if (args.epi & kEpiReduceTok)
+                                red_add_v4_f32(args.out_acc + static_cast<int64_t>(tok) * N + nq + m4,
+                                               w * y.x, w * y.y, w * y.z, w * y.w);
                         }
                     }
                     __syncwarp();  // the tile is rewritten by the next block
