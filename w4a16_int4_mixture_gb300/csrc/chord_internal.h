@@ -48,6 +48,6 @@ struct GemmArgs {
     int* err;
 };
 
-constexpr int kGemmThreads = 512;  // 16 warps
+constexpr int kGemmThreads = 512;  // 16 warps (the GEMM configurations may add a warp group)
 
 }  // namespace chord

@@ -9,7 +9,7 @@
 // optimisation / H200 and Blackwell indexed decode": dequantised weights take
 // the MMA-M operand), used here for every token count.
 //
-// Roles (16 warps):
+// Roles (16 warps, 20 for the down GEMM with token tiles <= 64):
 //   warp 0      code producer: packed INT4 codes of each K stage into a ring, one
 //               TMA box (gate and up halves as one 3-D box), L2 evict-first,
 //               and the group-32 scales (a TMA box, or cp.async for BK 128).
@@ -23,6 +23,8 @@
 //   warps 4-7   epilogue: TMEM -> registers; gate_up: SiLU(gate)*up -> bf16 h;
 //               down: per-pair fp32 store, fp32 reductions into token rows,
 //               or bf16 row store.
+//   warps 16-19 (down GEMM with token tiles <= 64 only) a second epilogue
+//               group taking every other unit.
 //   warps 8-15  dequant, two warps per TMEM lane quadrant taking K stages in
 //               order from a shared counter: codes + scales from shared memory
 //               -> w = bf16((q - 8) * s), one rounding of the exact product as
@@ -64,9 +66,14 @@ struct GemmCfg {
     static constexpr int B_STAGE = B_KBLK * B_REGION;
     static constexpr int HS_BYTES = GATE_UP ? MAXN * 128 : 0;  // 64 channels of bf16 per row
     static constexpr int META_BYTES = 0;  // (column records live in registers)
+    // down with token tiles of at most 64 rows (short units when K is small):
+    // a second group of four epilogue warps (warps 16-19) takes every other
+    // unit, each group owning one accumulator buffer
+    static constexpr int EPI_GROUPS = (!GATE_UP && MAXN <= 64) ? 2 : 1;
+    static constexpr int THREADS = 512 + 128 * (EPI_GROUPS - 1);
     // down: per epilogue warp a 16-column x 32-row fp32 tile to transpose the
     // accumulator so each lane owns four consecutive output rows of a column
-    static constexpr int EPIT_BYTES = GATE_UP ? 0 : 4 * 16 * 32 * 4;
+    static constexpr int EPIT_BYTES = GATE_UP ? 0 : EPI_GROUPS * 4 * 16 * 32 * 4;
 
     static constexpr int OFF_CODES = 0;
     static constexpr int OFF_B = OFF_CODES + KS * CODE_STAGE;
@@ -91,6 +98,7 @@ struct GemmCfg {
     static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM keeps the 512-column TMEM alloc safe");
     static_assert(OFF_B % 1024 == 0 && B_REGION % 1024 == 0, "swizzle atoms need 1024B alignment");
     static_assert(MAXN % B_BOX_ROWS == 0 && (B_BOX_ROWS * 128) % 1024 == 0, "token boxes");
+    static_assert(ACCB % EPI_GROUPS == 0, "each epilogue group owns whole accumulator buffers");
     static_assert(CODE_STAGE % 1024 == 0, "TMA destinations");
 };
 
@@ -171,7 +179,7 @@ __device__ __forceinline__ void dequant_word(uint32_t w, ScalePair sp, uint32_t*
 }
 
 template <class C>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap codes_map,
                       const __grid_constant__ CUtensorMap scales_map,
                       const __grid_constant__ CUtensorMap b_map, const GemmArgs args)
@@ -397,10 +405,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
+    } else if ((warp >= 4 && warp < 8) || warp >= 16) {
         // --------------------------------------------------------------- epilogue
         const int q = warp & 3;
-        const int et = threadIdx.x - 128;  // 0..127 inside the epilogue group
+        const int egrp = warp >= 16 ? 1 : 0;  // epilogue group: units i with i % EPI_GROUPS == egrp
+        const int et = threadIdx.x - (egrp ? 512 : 128);  // 0..127 inside the epilogue group
         int esync = 0;
         // all four epilogue warps meet here (bounded, unlike bar.sync)
         auto epi_sync = [&]() -> bool {
@@ -428,18 +437,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                                       : make_int4(-1, 0, 0, 0);
             }
         };
-        int i = 0;
-        Chunk c_cur = chunk_of(blockIdx.x);
-        Chunk c_nxt = chunk_of(blockIdx.x + gridDim.x);
+        constexpr int EG = C::EPI_GROUPS;
+        int i = egrp;
+        Chunk c_cur = chunk_of(blockIdx.x + egrp * gridDim.x);
+        Chunk c_nxt = chunk_of(blockIdx.x + (egrp + EG) * gridDim.x);
         load_meta(c_cur, meta_next);
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++i) {
+        for (int u = blockIdx.x + egrp * gridDim.x; u < total_units; u += EG * gridDim.x, i += EG) {
             const Chunk ch = c_cur;
             int4 meta_cur[MPT];
 #pragma unroll
             for (int k = 0; k < MPT; ++k)
                 meta_cur[k] = meta_next[k];
             load_meta(c_nxt, meta_next);
-            const Chunk c_nn = chunk_of(u + 2 * gridDim.x);
+            const Chunk c_nn = chunk_of(u + 2 * EG * gridDim.x);
             const int nt = u % n_tiles;
             const int ntok = ch.nrows;
             const int ntok16 = (ntok + 15) & ~15;
@@ -501,7 +511,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 // access per lane and column.
                 const int N = args.N;
                 const int nq = nt * 128 + q * 32;
-                float* tile = reinterpret_cast<float*>(smem + C::OFF_EPIT) + q * 16 * 32;
+                float* tile = reinterpret_cast<float*>(smem + C::OFF_EPIT) + (egrp * 4 + q) * 16 * 32;
                 const int m4 = (lane & 7) * 4;
                 const int cg = lane >> 3;
 #pragma unroll
