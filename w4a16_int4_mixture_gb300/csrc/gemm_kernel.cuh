@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // Units are dealt to CTAs with a stride of the grid, so at any time the
     // CTAs work on neighbouring units: a few chunks, whose token tiles stay hot
     // in L2 across the CTAs that share them.  Each role loads the descriptor of
-    // its next unit one unit ahead.
+    // a unit two units ahead (one unit of a short-K GEMM is shorter than a
+    // global load).
     const int total_units = args.num_chunks[0] * n_tiles;
     auto chunk_of = [&](int u) -> Chunk {
         return u < total_units ? args.chunks[u / n_tiles] : Chunk{};
@@ -267,9 +268,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int g = 0;
         bool ok = true;
         Chunk next = chunk_of(blockIdx.x);
+        Chunk next2 = chunk_of(blockIdx.x + gridDim.x);
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
             const Chunk ch = next;
-            next = chunk_of(u + gridDim.x);
+            next = next2;
+            next2 = chunk_of(u + 2 * gridDim.x);
             const int nt = u % n_tiles;
             const int e = ch.expert;
             // first weight row of the tile: gate_up takes rows [row0, row0 + 64)
@@ -320,11 +323,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int g = 0;
         bool ok = true;
         Chunk next = chunk_of(blockIdx.x);
+        Chunk next2 = chunk_of(blockIdx.x + gridDim.x);
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
             const int row0 = next.row0;
             // boxes of B_BOX_ROWS rows, as many as the token tile needs
             const int nbox = ((next.nrows + 15) / 16 * 16 + C::B_BOX_ROWS - 1) / C::B_BOX_ROWS;
-            next = chunk_of(u + gridDim.x);
+            next = next2;
+            next2 = chunk_of(u + 2 * gridDim.x);
             for (int ks = 0; ks < KT; ++ks, ++g) {
                 const int s = g % C::BS;
                 if (!mbar_wait(b_empty(s), ((g / C::BS) & 1) ^ 1, abort_flag, err)) {
@@ -358,9 +363,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         bool ok = true;
         int i = 0;
         Chunk next = chunk_of(blockIdx.x);
+        Chunk next2 = chunk_of(blockIdx.x + gridDim.x);
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++i) {
             const Chunk ch = next;
-            next = chunk_of(u + gridDim.x);
+            next = next2;
+            next2 = chunk_of(u + 2 * gridDim.x);
             const int ntok16 = (ch.nrows + 15) & ~15;
             const uint32_t idesc = idesc_bf16_f32(128, ntok16);
             const int acc = i % C::ACCB;
