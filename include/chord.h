@@ -79,6 +79,11 @@ typedef enum {
                                       fp32 reductions into the token rows */
 
 /* bits of the device error word */
+#define CHORD_FLAG_TEST_SKIP_ARRIVE 4 /* test hook: the gate/up GEMM drops one mbarrier arrival
+                                         (first K stage, CTA 0), so that a bounded device wait
+                                         expires; the call's outputs are then undefined and, with
+                                         CHORD_FLAG_VALIDATE, it returns CHORD_ERR_TIMEOUT.  Exists
+                                         to show that an expired wait ends the kernel cleanly. */
 #define CHORD_DEVERR_TIMEOUT 1
 #define CHORD_DEVERR_ROUTING 2
 #define CHORD_DEVERR_CAPACITY 4

@@ -461,6 +461,7 @@ struct LayerIO {
     uint16_t* h_out;  // caller-provided intermediate, or null (workspace)
     uint16_t* rows_out;
     int down_epi;
+    int flags;
 };
 
 chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w, uint8_t* ws,
@@ -512,11 +513,13 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.row_meta = io.row_meta;
     g.err = err;
     marks.mark(1);
+    g.test_skip_arrive = (io.flags & CHORD_FLAG_TEST_SKIP_ARRIVE) ? 1 : 0;
     if (launch_gemm(sc.cfg_gate_up, true, map13, smap13, bmap13, g, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(2);
 
     GemmArgs d = g;
+    d.test_skip_arrive = 0;
     d.K = io.I;
     d.N = io.H;
     d.n_tiles = io.H / 128;
@@ -677,7 +680,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     chord_status st = check_shape(H, I, E_local, k);
     if (st != CHORD_OK)
         return st;
-    if (T < 0 || E_global < 1 || block_m < 1 || block_m > 256 || (flags & ~3))
+    if (T < 0 || E_global < 1 || block_m < 1 || block_m > 256 || (flags & ~7))
         return CHORD_ERR_INVALID_ARG;
     if (T * k >= (int64_t(1) << 31))
         return CHORD_ERR_UNSUPPORTED_SHAPE;
@@ -772,6 +775,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     io.h_rows = capacity;
     io.h_out = h_out;
     io.down_epi = sc.reduce ? kEpiReduceTok : kEpiStorePair;
+    io.flags = flags;
     if ((st = run_gemms(io, sc, w, ws, err, pair_row, acc, dev, s, marks)) != CHORD_OK)
         return st;
 
@@ -805,7 +809,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     chord_status st = check_shape(H, I, E_local, with_tokens ? k : 1);
     if (st != CHORD_OK)
         return st;
-    if (M < 0 || (flags & ~3))
+    if (M < 0 || (flags & ~7))
         return CHORD_ERR_INVALID_ARG;
     if (mode == CHORD_GROUPED_CONTIGUOUS) {
         if (masked_m != nullptr || (M > 0 && m_indices == nullptr))
@@ -907,6 +911,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     io.h_out = h_out;
     io.rows_out = out_rows;
     io.down_epi = kEpiStoreRows | (with_tokens ? kEpiReduceTok : 0);
+    io.flags = flags;
     if ((st = run_gemms(io, sc, w, ws, err, nullptr, acc, dev, s, marks)) != CHORD_OK)
         return st;
     if (with_tokens && launch_finalize(acc, out_tokens, T * H, dev.sms, s) != cudaSuccess)

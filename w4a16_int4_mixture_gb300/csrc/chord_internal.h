@@ -46,6 +46,7 @@ struct GemmArgs {
     const int32_t* pair_of_row;  // pair id t*k+j of each padded row (or -1 / sentinel)
     const int4* row_meta;        // down: {pair, token, weight bits, 0} per padded row
     int* err;
+    int test_skip_arrive;  // CHORD_FLAG_TEST_SKIP_ARRIVE (gate_up only)
 };
 
 constexpr int kGemmThreads = 512;  // 16 warps (the GEMM configurations may add a warp group)

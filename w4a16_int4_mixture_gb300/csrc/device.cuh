@@ -96,6 +96,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Bounded wait for a phase that copies this thread issued will complete, used on
+// the way out of an aborted CTA (so ignores the abort flag): the CTA must not
+// end while the TMA engine still writes its shared memory.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tiled tensor copies, global -> shared) and cp.async
 // ---------------------------------------------------------------------------

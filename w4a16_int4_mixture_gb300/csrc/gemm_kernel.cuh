@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     const int n_tiles = args.n_tiles;
     const int KT = args.K / C::BK;
+    int issued_stages = 0;  // code / token producers: K stages whose copies were issued
     // Units are dealt to CTAs with a stride of the grid, so at any time the
     // CTAs work on neighbouring units: a few chunks, whose token tiles stay hot
     // in L2 across the CTAs that share them.  Each role loads the descriptor of
@@ -315,8 +316,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 __syncwarp();
             }
         }
-        if (!ok)  // let the copies already issued land before the CTA goes away
-            asm volatile("cp.async.wait_all;" ::: "memory");
+        issued_stages = g;
     } else if (warp == 1) {
         // ----------------------------------------------------------- token producer
         const uint64_t pol = policy_evict_last();
@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 __syncwarp();
             }
         }
+        issued_stages = g;
     } else if (warp == 2) {
         // ------------------------------------------------------------- MMA issuer
         // The whole warp walks the schedule (so every operand stays warp-uniform)
@@ -649,7 +650,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
+                // (test hook: one arrival dropped so that the MMA's bounded wait expires)
+                const bool drop = args.test_skip_arrive && blockIdx.x == 0 && q == 0 && g == 0;
+                if (lane == 0 && !drop)
                     mbar_arrive(a_full(sa));
             }
         }
@@ -657,6 +660,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (*abort_flag) {
+        // An aborted CTA may leave copies it issued but nobody consumed: the
+        // producers wait (bounded) for the last stages they issued to land, so
+        // the CTA does not end while the TMA engine still writes its shared
+        // memory.
+        if (warp == 0 || warp == 1) {
+            const int depth = warp == 0 ? C::KS : C::BS;
+            if (lane == 0)
+                for (int gg = issued_stages > depth ? issued_stages - depth : 0; gg < issued_stages; ++gg)
+                    mbar_drain(warp == 0 ? codes_full(gg % C::KS) : b_full(gg % C::BS),
+                               (gg / depth) & 1);
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            __syncwarp();
+        }
+    }
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
