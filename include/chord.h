@@ -78,12 +78,15 @@ typedef enum {
 #define CHORD_FLAG_DETERMINISTIC 2 /* per-pair fp32 down outputs + ordered combine instead of
                                       fp32 reductions into the token rows */
 
-/* bits of the device error word */
 #define CHORD_FLAG_TEST_SKIP_ARRIVE 4 /* test hook: the gate/up GEMM drops one mbarrier arrival
                                          (first K stage, CTA 0), so that a bounded device wait
                                          expires; the call's outputs are then undefined and, with
                                          CHORD_FLAG_VALIDATE, it returns CHORD_ERR_TIMEOUT.  Exists
                                          to show that an expired wait ends the kernel cleanly. */
+#define CHORD_FLAG_NO_SPLIT_K 8 /* keep every work unit whole: no K-split of the last, partly
+                                   filled round of units (see chord_w4a16_moe_indexed) */
+
+/* bits of the device error word */
 #define CHORD_DEVERR_TIMEOUT 1
 #define CHORD_DEVERR_ROUTING 2
 #define CHORD_DEVERR_CAPACITY 4
@@ -218,6 +221,14 @@ chord_status chord_moe_align_noalloc(const int32_t* topk_ids, int64_t T, int k, 
  *                bit-identical outputs (slots summed in a fixed order)
  * Limits (CHORD_ERR_UNSUPPORTED_SHAPE otherwise): H % 256 == 0, I % 128 == 0,
  *   1 <= k <= 32, E_local >= 1, T*k < 2^31, block_m in [1, 256].
+ * Work schedule of both GEMMs: one CTA per SM takes (chunk of rows, weight
+ *   tile) units in turn.  When the last round of units would leave at least
+ *   half of the SMs idle, each of its units is cut along K into pieces of two
+ *   or more K stages, one per otherwise idle SM; every piece leaves its fp32
+ *   partial sum in the workspace and the last piece of a unit to finish adds
+ *   the pieces in piece order (a fixed order: results stay bit-identical from
+ *   run to run) and runs the unit's epilogue.  CHORD_FLAG_NO_SPLIT_K turns
+ *   this off.
  */
 chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I, int E_global,
                                      int E_local, int k, const int32_t* w13_q,

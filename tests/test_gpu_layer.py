@@ -182,9 +182,7 @@ def test_poisoned_workspace_does_not_leak(chord):
 
 
 # ---------------------------------------------------------------- grouped
-@pytest.mark.parametrize("align", [16, 128])
-def test_grouped_contiguous(chord, align):
-    inp = small(80, 3, 10, 6, 512, 256, 21)
+def contiguous_layer_check(chord, inp, align, label, flags=0):
     s = inp.shape
     a2, m_idx, r2p = synth.grouped_contiguous_layout(inp, align=align)
     w = weights_to(inp, DEV)
@@ -192,8 +190,8 @@ def test_grouped_contiguous(chord, align):
     rows, toks = chord.w4a16_moe_grouped("contiguous", dev_tensor(a2, DEV, True), *w,
                                          m_indices=dev_tensor(m_idx, DEV),
                                          row_to_pair=dev_tensor(r2p, DEV),
-                                         topk_weights=dev_tensor(inp.topk_weights, DEV), flags=1,
-                                         h_out=h)
+                                         topk_weights=dev_tensor(inp.topk_weights, DEV),
+                                         flags=flags | 1, h_out=h)
     torch.cuda.synchronize()
     ref_rows, ref_tok, ref_h = oracle.moe_grouped("contiguous", a2, inp.w13_q, inp.w13_s,
                                                   inp.w2_q, inp.w2_s, m_indices=m_idx,
@@ -202,13 +200,20 @@ def test_grouped_contiguous(chord, align):
     valid = m_idx >= 0
     hg = bf16_to_np(h)
     hg[~valid] = 0
-    check_h(hg[valid], ref_h[valid], "contiguous h")
+    check_h(hg[valid], ref_h[valid], f"{label} h")
     d_rows, d_tok = oracle.moe_grouped_down("contiguous", hg, inp.w2_q, inp.w2_s,
                                             m_indices=m_idx, row_to_pair=r2p,
                                             topk_weights=inp.topk_weights, T=s.T, k=s.k)
-    assert_close_bf16(bf16_to_np(rows)[valid], d_rows[valid], "contiguous rows given h")
-    assert_close_bf16(bf16_to_np(toks), d_tok, "contiguous tokens given h")
-    print(f"[contiguous align={align}] end-to-end tokens {e2e_ratio(bf16_to_np(toks), ref_tok):.3f}x")
+    assert_close_bf16(bf16_to_np(rows)[valid], d_rows[valid], f"{label} rows given h")
+    assert_close_bf16(bf16_to_np(toks), d_tok, f"{label} tokens given h")
+    print(f"[{label}] end-to-end tokens {e2e_ratio(bf16_to_np(toks), ref_tok):.3f}x")
+    return bf16_to_np(rows)[valid], bf16_to_np(toks)
+
+
+@pytest.mark.parametrize("align", [16, 128])
+def test_grouped_contiguous(chord, align):
+    contiguous_layer_check(chord, small(80, 3, 10, 6, 512, 256, 21), align,
+                           f"contiguous align={align}")
 
 
 def masked_layer_check(chord, inp, a3, mm, r2p, w, label):

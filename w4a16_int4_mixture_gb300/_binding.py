@@ -30,6 +30,7 @@ GROUPED_MASKED = 1
 FLAG_VALIDATE = 1
 FLAG_DETERMINISTIC = 2
 FLAG_TEST_SKIP_ARRIVE = 4
+FLAG_NO_SPLIT_K = 8
 DEVERR_TIMEOUT = 1
 DEVERR_ROUTING = 2
 DEVERR_CAPACITY = 4

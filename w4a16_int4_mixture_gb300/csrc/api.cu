@@ -300,17 +300,25 @@ struct Workspace {
     size_t off_h = 0;
     size_t off_acc = 0;       // reduce: float [T, H]; store: float [T*k, H]
     size_t off_pair_row = 0;  // store: int32 [T*k]
+    size_t off_split_cnt = 0;   // int32 [2][kSplitSlots]: K-split piece counters per GEMM
+    size_t off_split_part = 0;  // fp32 [kSplitSlots][split_maxn][128]: K-split partial sums
+    int split_maxn = 0;
     size_t total = 0;
     int64_t max_chunks = 0;
 };
 
 Workspace layout_ws(int64_t max_chunks, int64_t h_rows, int I, int64_t T, int k, int H, bool reduce,
-                    bool with_tokens, int64_t xs_rows)
+                    bool with_tokens, int64_t xs_rows, int split_maxn)
 {
     Workspace w;
     size_t o = 0;
     w.off_hdr = o;
     o += kAlign;
+    w.off_split_cnt = o;
+    o = align_up(o + 2 * kSplitSlots * sizeof(int32_t), kAlign);
+    w.off_split_part = o;
+    w.split_maxn = split_maxn;
+    o = align_up(o + static_cast<size_t>(kSplitSlots) * split_maxn * 128 * sizeof(float), kAlign);
     w.max_chunks = max_chunks;
     for (int L = 0; L < 2; ++L) {
         w.off_chunks[L] = o;
@@ -337,6 +345,22 @@ Workspace layout_ws(int64_t max_chunks, int64_t h_rows, int I, int64_t T, int k,
 }
 
 int64_t indexed_max_chunks(int E_local, int64_t capacity) { return E_local + capacity / 16 + 2; }
+
+// Token tile that sizes the K-split slots: the larger of the two GEMMs'
+// tiles, or (grouped calls, whose schedule the size query does not fix) the
+// largest tile of any configuration.
+int split_maxn_of(const Schedule& sc)
+{
+    const int a = gemm_cfg_maxn(sc.cfg_gate_up), b = gemm_cfg_maxn(sc.cfg_down);
+    return a > b ? a : b;
+}
+int split_maxn_any()
+{
+    int m = 0;
+    for (int c = 0; c < kNumGemmConfigs; ++c)
+        m = gemm_cfg_maxn(c) > m ? gemm_cfg_maxn(c) : m;
+    return m;
+}
 
 int64_t grouped_max_chunks(int mode, int64_t M, int E_local, int64_t max_m)
 {
@@ -512,6 +536,17 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.pair_of_row = io.pair_of_row;
     g.row_meta = io.row_meta;
     g.err = err;
+    // K-split slots: as many as the workspace holds for this token tile, at
+    // most one per CTA
+    const bool split = !(io.flags & CHORD_FLAG_NO_SPLIT_K);
+    auto slots_for = [&](int cfg) {
+        const int n = kSplitSlots * w.split_maxn / gemm_cfg_maxn(cfg);
+        return split ? (n < dev.sms ? n : dev.sms) : 0;
+    };
+    int32_t* split_cnt = reinterpret_cast<int32_t*>(ws + w.off_split_cnt);
+    g.split_part = reinterpret_cast<float*>(ws + w.off_split_part);
+    g.split_cnt = split_cnt;
+    g.split_slots = slots_for(sc.cfg_gate_up);
     marks.mark(1);
     g.test_skip_arrive = (io.flags & CHORD_FLAG_TEST_SKIP_ARRIVE) ? 1 : 0;
     if (launch_gemm(sc.cfg_gate_up, true, map13, smap13, bmap13, g, dev.sms, s) != cudaSuccess)
@@ -532,6 +567,8 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     d.y_pairs = (io.down_epi & kEpiStorePair) ? acc : nullptr;
     d.out_acc = (io.down_epi & kEpiReduceTok) ? acc : nullptr;
     d.rows_out = io.rows_out;
+    d.split_cnt = split_cnt + kSplitSlots;
+    d.split_slots = slots_for(sc.cfg_down);
     if (launch_gemm(sc.cfg_down, false, map2, smap2, bmap2, d, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(3);
@@ -611,7 +648,7 @@ size_t chord_w4a16_moe_workspace_size(int64_t T, int k, int E_global, int E_loca
     const double tok_e = E_global > 0 ? static_cast<double>(T) * k / E_global : 0.0;
     const Schedule s = pick_schedule(tok_e, T, H, I, flags);
     return layout_ws(indexed_max_chunks(E_local, capacity), capacity, I, T, k, H, s.reduce, true,
-                     capacity)
+                     capacity, split_maxn_of(s))
         .total;
 }
 
@@ -623,7 +660,7 @@ size_t chord_w4a16_grouped_workspace_size(int mode, int64_t M, int H, int I, int
         return 0;
     const int64_t max_m = mode == CHORD_GROUPED_MASKED ? M / E_local : 0;
     return layout_ws(grouped_max_chunks(mode, M, E_local, max_m), M, I, T, k, H, true,
-                     with_tokens != 0, 0)
+                     with_tokens != 0, 0, split_maxn_any())
         .total;
 }
 
@@ -680,7 +717,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     chord_status st = check_shape(H, I, E_local, k);
     if (st != CHORD_OK)
         return st;
-    if (T < 0 || E_global < 1 || block_m < 1 || block_m > 256 || (flags & ~7))
+    if (T < 0 || E_global < 1 || block_m < 1 || block_m > 256 || (flags & ~15))
         return CHORD_ERR_INVALID_ARG;
     if (T * k >= (int64_t(1) << 31))
         return CHORD_ERR_UNSUPPORTED_SHAPE;
@@ -700,7 +737,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     const double tok_e = static_cast<double>(T) * k / E_global;
     const Schedule sc = pick_schedule(tok_e, T, H, I, flags);
     const Workspace w = layout_ws(indexed_max_chunks(E_local, capacity), capacity, I, T, k, H,
-                                  sc.reduce, true, capacity);
+                                  sc.reduce, true, capacity, split_maxn_of(sc));
     if ((st = check_ws(workspace, workspace_bytes, w.total)) != CHORD_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -724,6 +761,8 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     pa.chunks[1] = reinterpret_cast<Chunk*>(ws + w.off_chunks[1]);
     pa.max_chunks = static_cast<int>(w.max_chunks);
     pa.num_chunks = err + 1;
+    pa.zero_i32 = reinterpret_cast<int32_t*>(ws + w.off_split_cnt);
+    pa.zero_i32_count = 2 * kSplitSlots;
     if (sc.reduce) {
         pa.zero_f32 = acc;
         pa.zero_count = T * H;
@@ -809,7 +848,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     chord_status st = check_shape(H, I, E_local, with_tokens ? k : 1);
     if (st != CHORD_OK)
         return st;
-    if (M < 0 || (flags & ~7))
+    if (M < 0 || (flags & ~15))
         return CHORD_ERR_INVALID_ARG;
     if (mode == CHORD_GROUPED_CONTIGUOUS) {
         if (masked_m != nullptr || (M > 0 && m_indices == nullptr))
@@ -846,7 +885,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     Schedule sc = pick_schedule(tok_e, T, H, I, 0);
     sc.reduce = true;
     const Workspace w = layout_ws(grouped_max_chunks(mode, M, E_local, max_m), M, I, T, k, H, true,
-                                  with_tokens, 0);
+                                  with_tokens, 0, split_maxn_any());
     if ((st = check_ws(workspace, workspace_bytes, w.total)) != CHORD_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -870,6 +909,8 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     pa.chunks[1] = reinterpret_cast<Chunk*>(ws + w.off_chunks[1]);
     pa.max_chunks = static_cast<int>(w.max_chunks);
     pa.num_chunks = err + 1;
+    pa.zero_i32 = reinterpret_cast<int32_t*>(ws + w.off_split_cnt);
+    pa.zero_i32_count = 2 * kSplitSlots;
     if (with_tokens) {
         pa.zero_f32 = acc;
         pa.zero_count = T * H;

@@ -422,6 +422,8 @@ __device__ void build_chunk_lists(const PrepArgs& a)
 __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
 {
     if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < a.zero_i32_count; i += blockDim.x)
+            a.zero_i32[i] = 0;
         build_chunk_lists(a);
         return;
     }

@@ -47,7 +47,16 @@ struct GemmArgs {
     const int4* row_meta;        // down: {pair, token, weight bits, 0} per padded row
     int* err;
     int test_skip_arrive;  // CHORD_FLAG_TEST_SKIP_ARRIVE (gate_up only)
+    // K-split of the last, partly filled round of units (0 slots: never split)
+    float* split_part;     // [split_slots][MAXN columns][128 rows] fp32 partial sums
+    int32_t* split_cnt;    // [split_slots] finished pieces per split unit, zero on entry
+    int split_slots;
 };
+
+// Partial-sum slots of the K-split per GEMM (at least the SM count of the part).
+constexpr int kSplitSlots = 160;
+// Fewest K stages in one piece of a split unit.
+constexpr int kSplitMinStages = 2;
 
 constexpr int kGemmThreads = 512;  // 16 warps (the GEMM configurations may add a warp group)
 

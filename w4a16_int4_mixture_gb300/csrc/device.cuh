@@ -75,11 +75,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 // never spins forever.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, uint64_t limit_ns = kWaitLimitNs)
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, uint64_t limit_ns)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity))
@@ -94,6 +92,30 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, uint64_t limit_ns = kWaitLimitNs)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    return mbar_spin(bar, parity, abort_flag, err, limit_ns);
+}
+
+// The same wait with the spin loop out of line, for the waits off the
+// critical path (producers, epilogue): one try_wait inline keeps those loops
+// small for the instruction cache; a wait that spins pays a call.
+static __device__ __noinline__ bool mbar_spin_ool(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, int* err)
+{
+    return mbar_spin(bar, parity, abort_flag, err, kWaitLimitNs);
+}
+__device__ __forceinline__ bool mbar_wait_cold(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               int* err)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    return mbar_spin_ool(bar, parity, abort_flag, err);
 }
 
 // Bounded wait for a phase that copies this thread issued will complete, used on

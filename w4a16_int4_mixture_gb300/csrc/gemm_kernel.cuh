@@ -82,14 +82,21 @@ struct GemmCfg {
     static constexpr int OFF_META = OFF_HS + HS_BYTES;
     static constexpr int OFF_EPIT = OFF_META + META_BYTES;
     static constexpr int OFF_BARS = OFF_EPIT + EPIT_BYTES;
-    static constexpr int NBARS = 2 * KS + 2 * AS + 2 * BS + 2 * ACCB + 2;
+    // rings, then one rendezvous per epilogue group and the drain barrier
+    static constexpr int NBARS = 2 * KS + 2 * AS + 2 * BS + 2 * ACCB + 3;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
-    // misc: TMEM base, abort flag, 2 spare words, 4 per-quadrant stage counters
+    // misc: TMEM base, abort flag, a split-unit verdict per epilogue group,
+    // 4 per-quadrant stage counters
     static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;  // + alignment slack
 
     static constexpr int A_COLS = BK / 2;                   // TMEM columns per A stage
     static constexpr int D_COL0 = AS * A_COLS;
     static constexpr int TMEM_COLS = 512;
+
+    // producers and epilogue wait with the spin loop out of line (smaller hot
+    // code; measured faster for the BK 256 decode tiles, slower for the
+    // prefill tile, whose producers wake on every one of its short stages)
+    static constexpr bool COLD_WAITS = BK == 256;
 
     static_assert(BK == 128 || BK == 256, "stage depth");
     static_assert(MAXN % 16 == 0 && MAXN >= 16 && MAXN <= 256, "token tile");
@@ -178,6 +185,15 @@ __device__ __forceinline__ void dequant_word(uint32_t w, ScalePair sp, uint32_t*
     }
 }
 
+// One work item of a GEMM CTA: a whole unit, or one K piece of a split unit.
+struct WorkItem {
+    int unit;   // chunk * n_tiles + weight tile
+    int k0;     // K stages [k0, k1)
+    int k1;
+    int piece;  // -1 for a whole unit, else the piece index
+    int tail;   // split units: index of the unit among the split ones
+};
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap codes_map,
@@ -204,10 +220,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     auto d_empty = [&](int s) {
         return bar0 + 8u * (2 * C::KS + 2 * C::AS + 2 * C::BS + C::ACCB + s);
     };
-    const uint32_t epi_bar = bar0 + 8u * (C::NBARS - 2);
+    const uint32_t epi_bar0 = bar0 + 8u * (C::NBARS - 3);  // + 8 * epilogue group
     const uint32_t drain_bar = bar0 + 8u * (C::NBARS - 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    volatile int* split_last = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // [2]
     int* stage_ctr = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);
 
     if (threadIdx.x == 0) {
@@ -228,7 +245,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(d_full(s), 1);
             mbar_init(d_empty(s), 4);          // 4 epilogue warps
         }
-        mbar_init(epi_bar, 4);                 // epilogue group rendezvous
+        mbar_init(epi_bar0, 4);                // epilogue group rendezvous
+        mbar_init(epi_bar0 + 8u, 4);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         for (int qq = 0; qq < 4; ++qq)
@@ -261,27 +279,76 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     auto chunk_of = [&](int u) -> Chunk {
         return u < total_units ? args.chunks[u / n_tiles] : Chunk{};
     };
+    // The work items are those units, except that when the last round of
+    // units (rem = units mod grid) would leave at least half of the CTAs idle,
+    // each of its units is cut along K into split_p pieces of at least
+    // kSplitMinStages stages, items split_base + t * split_p + j (piece j of
+    // tail unit t), one per CTA.  Every role derives the same schedule.
+    int split_base = total_units;
+    int split_p = 1;
+    {
+        const int grid = static_cast<int>(gridDim.x);
+        const int rem = total_units % grid;
+        const int slots = args.split_slots < grid ? args.split_slots : grid;
+        if (rem > 0 && slots >= 2 * rem) {
+            int p = slots / rem;
+            if (p > KT / kSplitMinStages)
+                p = KT / kSplitMinStages;
+            if (p >= 2) {
+                split_base = total_units - rem;
+                split_p = p;
+            }
+        }
+    }
+    const int total_items = split_base + (total_units - split_base) * split_p;
+    auto item_of = [&](int v) -> WorkItem {
+        WorkItem it;
+        if (v < split_base) {
+            it.unit = v;
+            it.k0 = 0;
+            it.k1 = KT;
+            it.piece = -1;
+            it.tail = 0;
+        } else {
+            const int r = v - split_base;
+            it.tail = r / split_p;
+            it.piece = r - it.tail * split_p;
+            it.unit = split_base + it.tail;
+            it.k0 = it.piece * KT / split_p;
+            it.k1 = (it.piece + 1) * KT / split_p;
+        }
+        return it;
+    };
+    auto chunk_of_item = [&](int v) -> Chunk { return chunk_of(item_of(v).unit); };
     int* err = args.err;
+    // waits off the critical path (producers, epilogue)
+    auto wait_side = [&](uint32_t bar, uint32_t parity) -> bool {
+        if constexpr (C::COLD_WAITS)
+            return mbar_wait_cold(bar, parity, abort_flag, err);
+        else
+            return mbar_wait(bar, parity, abort_flag, err);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         const uint64_t pol = policy_evict_first();
         int g = 0;
         bool ok = true;
-        Chunk next = chunk_of(blockIdx.x);
-        Chunk next2 = chunk_of(blockIdx.x + gridDim.x);
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        Chunk next = chunk_of_item(blockIdx.x);
+        Chunk next2 = chunk_of_item(blockIdx.x + gridDim.x);
+        for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x) {
+            const WorkItem it = item_of(v);
             const Chunk ch = next;
             next = next2;
-            next2 = chunk_of(u + 2 * gridDim.x);
-            const int nt = u % n_tiles;
+            next2 = chunk_of_item(v + 2 * gridDim.x);
+            const int nt = it.unit % n_tiles;
             const int e = ch.expert;
             // first weight row of the tile: gate_up takes rows [row0, row0 + 64)
             // (gate) and the same 64 rows I further on (up) as one 3-D box
             const int row0 = C::GATE_UP ? e * args.N + nt * 64 : e * args.N + nt * 128;
-            for (int ks = 0; ks < KT; ++ks, ++g) {
+            for (int ks = it.k0; ks < it.k1; ++ks, ++g) {
                 const int s = g % C::KS;
-                if (!mbar_wait(codes_empty(s), ((g / C::KS) & 1) ^ 1, abort_flag, err)) {
+                if (!wait_side(codes_empty(s), ((g / C::KS) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
@@ -322,17 +389,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint64_t pol = policy_evict_last();
         int g = 0;
         bool ok = true;
-        Chunk next = chunk_of(blockIdx.x);
-        Chunk next2 = chunk_of(blockIdx.x + gridDim.x);
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        Chunk next = chunk_of_item(blockIdx.x);
+        Chunk next2 = chunk_of_item(blockIdx.x + gridDim.x);
+        for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x) {
+            const WorkItem it = item_of(v);
             const int row0 = next.row0;
             // boxes of B_BOX_ROWS rows, as many as the token tile needs
             const int nbox = ((next.nrows + 15) / 16 * 16 + C::B_BOX_ROWS - 1) / C::B_BOX_ROWS;
             next = next2;
-            next2 = chunk_of(u + 2 * gridDim.x);
-            for (int ks = 0; ks < KT; ++ks, ++g) {
+            next2 = chunk_of_item(v + 2 * gridDim.x);
+            for (int ks = it.k0; ks < it.k1; ++ks, ++g) {
                 const int s = g % C::BS;
-                if (!mbar_wait(b_empty(s), ((g / C::BS) & 1) ^ 1, abort_flag, err)) {
+                if (!wait_side(b_empty(s), ((g / C::BS) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
@@ -363,12 +431,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int issued = 0;
         bool ok = true;
         int i = 0;
-        Chunk next = chunk_of(blockIdx.x);
-        Chunk next2 = chunk_of(blockIdx.x + gridDim.x);
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++i) {
+        Chunk next = chunk_of_item(blockIdx.x);
+        Chunk next2 = chunk_of_item(blockIdx.x + gridDim.x);
+        for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x, ++i) {
+            const WorkItem it = item_of(v);
             const Chunk ch = next;
             next = next2;
-            next2 = chunk_of(u + 2 * gridDim.x);
+            next2 = chunk_of_item(v + 2 * gridDim.x);
             const int ntok16 = (ch.nrows + 15) & ~15;
             const uint32_t idesc = idesc_bf16_f32(128, ntok16);
             const int acc = i % C::ACCB;
@@ -379,7 +448,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem + C::D_COL0 + acc * C::MAXN;
-            for (int ks = 0; ks < KT; ++ks, ++g) {
+            for (int ks = it.k0; ks < it.k1; ++ks, ++g) {
                 const int sa = g % C::AS;
                 const int sb = g % C::BS;
                 const bool got = mbar_wait(a_full(sa), (g / C::AS) & 1, abort_flag, err) &&
@@ -393,10 +462,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const uint32_t b_base = sbase + C::OFF_B + sb * C::B_STAGE;
                 if constexpr (C::BK == 256)
                     mma_stage16<C::B_REGION / 16>(d_tmem, a_base, smem_desc_sw128(b_base), idesc,
-                                                  ks != 0 ? 1u : 0u);
+                                                  ks != it.k0 ? 1u : 0u);
                 else
                     mma_stage8<C::B_REGION / 16>(d_tmem, a_base, smem_desc_sw128(b_base), idesc,
-                                                 ks != 0 ? 1u : 0u);
+                                                 ks != it.k0 ? 1u : 0u);
                 issued = 1;
                 mma_commit_elect(a_empty(sa));
                 mma_commit_elect(b_empty(sb));
@@ -419,12 +488,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int egrp = warp >= 16 ? 1 : 0;  // epilogue group: units i with i % EPI_GROUPS == egrp
         const int et = threadIdx.x - (egrp ? 512 : 128);  // 0..127 inside the epilogue group
         int esync = 0;
-        // all four epilogue warps meet here (bounded, unlike bar.sync)
+        const uint32_t epi_bar = epi_bar0 + 8u * egrp;
+        // the four warps of the group meet here (bounded, unlike bar.sync)
         auto epi_sync = [&]() -> bool {
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(epi_bar);
-            const bool r = mbar_wait(epi_bar, esync & 1, abort_flag, err);
+            const bool r = wait_side(epi_bar, esync & 1);
             ++esync;
             return r;
         };
@@ -447,28 +517,83 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         };
         constexpr int EG = C::EPI_GROUPS;
         int i = egrp;
-        Chunk c_cur = chunk_of(blockIdx.x + egrp * gridDim.x);
-        Chunk c_nxt = chunk_of(blockIdx.x + (egrp + EG) * gridDim.x);
+        Chunk c_cur = chunk_of_item(blockIdx.x + egrp * gridDim.x);
+        Chunk c_nxt = chunk_of_item(blockIdx.x + (egrp + EG) * gridDim.x);
         load_meta(c_cur, meta_next);
-        for (int u = blockIdx.x + egrp * gridDim.x; u < total_units; u += EG * gridDim.x, i += EG) {
+        constexpr int kSlotFloats = 128 * C::MAXN;
+        for (int v = blockIdx.x + egrp * gridDim.x; v < total_items; v += EG * gridDim.x, i += EG) {
+            const WorkItem it = item_of(v);
             const Chunk ch = c_cur;
             int4 meta_cur[MPT];
 #pragma unroll
             for (int k = 0; k < MPT; ++k)
                 meta_cur[k] = meta_next[k];
             load_meta(c_nxt, meta_next);
-            const Chunk c_nn = chunk_of(u + 2 * EG * gridDim.x);
-            const int nt = u % n_tiles;
+            const Chunk c_nn = chunk_of_item(v + 2 * EG * gridDim.x);
+            const int nt = it.unit % n_tiles;
             const int ntok = ch.nrows;
             const int ntok16 = (ntok + 15) & ~15;
             const int acc = i % C::ACCB;
             c_cur = c_nxt;
             c_nxt = c_nn;
-            if (!mbar_wait(d_full(acc), (i / C::ACCB) & 1, abort_flag, err))
+            if (!wait_side(d_full(acc), (i / C::ACCB) & 1))
                 break;
             tc_fence_after();
             const uint32_t dbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + C::D_COL0 + acc * C::MAXN;
+            // A piece of a split unit: the accumulator goes to the piece's slot
+            // (column-major, so a warp stores 128 contiguous bytes per column).
+            // The last piece of the unit to get here adds the unit's slots in
+            // piece order back into its accumulator and runs the epilogue below
+            // on it; the other pieces hand their accumulator back to the MMA.
+            if (it.piece >= 0) {
+                const float* slots = args.split_part + static_cast<int64_t>(it.tail * split_p) * kSlotFloats +
+                                     q * 32 + lane;
+                float* mine = args.split_part + static_cast<int64_t>(it.tail * split_p + it.piece) * kSlotFloats +
+                              q * 32 + lane;
+                for (int c0 = 0; c0 < ntok16; c0 += 16) {
+                    uint32_t vv[16];
+                    tmem_ld_x16(dbase + c0, vv);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        __stcg(mine + (c0 + jj) * 128, __uint_as_float(vv[jj]));
+                }
+                __threadfence();  // the slot is visible before the count says so
+                if (!epi_sync())
+                    break;
+                if (et == 0) {
+                    const int before = atomicAdd(args.split_cnt + it.tail, 1);
+                    __threadfence();  // the other pieces' slots are read after their counts
+                    split_last[egrp] = before == split_p - 1;
+                }
+                if (!epi_sync())
+                    break;
+                if (!split_last[egrp]) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(d_empty(acc));
+                    continue;
+                }
+                for (int c0 = 0; c0 < ntok16; c0 += 16) {
+                    float sum[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        sum[jj] = __ldcg(slots + (c0 + jj) * 128);
+                    for (int j = 1; j < split_p; ++j) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            sum[jj] += __ldcg(slots + static_cast<int64_t>(j) * kSlotFloats + (c0 + jj) * 128);
+                    }
+                    uint32_t vv[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        vv[jj] = __float_as_uint(sum[jj]);
+                    tmem_st_x16(dbase + c0, vv);
+                }
+                tmem_wait_st();
+            }
             if constexpr (C::GATE_UP) {
                 // lanes (l, l^8): gate and up of channel 16q + 8(l>>4) + (l&7)
                 __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_HS);
@@ -522,10 +647,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 float* tile = reinterpret_cast<float*>(smem + C::OFF_EPIT) + (egrp * 4 + q) * 16 * 32;
                 const int m4 = (lane & 7) * 4;
                 const int cg = lane >> 3;
-#pragma unroll
-                for (int c0 = 0; c0 < C::MAXN; c0 += 16) {
-                    if (c0 >= ntok16)
-                        break;
+                // (a rolled loop: the epilogue runs once per unit, and its code
+                // competes for the instruction cache with every other role's)
+#pragma unroll 1
+                for (int c0 = 0; c0 < ntok16; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld_x16(dbase + c0, v);
                     tmem_wait_ld();
@@ -540,7 +665,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     for (int j = 0; j < 16; ++j)
                         tile[j * 32 + lane] = __uint_as_float(v[j]) * kWeightRescale;
                     __syncwarp();
-                    const int4 mrec = meta_cur[c0 / 32];  // columns c0 .. c0 + 15 sit in one lane group
+                    // columns c0 .. c0 + 15 sit in one lane group: records meta_cur[c0 / 32]
+                    int4 mrec = meta_cur[0];
+#pragma unroll
+                    for (int k = 1; k < MPT; ++k)
+                        if (c0 >= 32 * k)
+                            mrec = meta_cur[k];
 #pragma unroll
                     for (int ii = 0; ii < 4; ++ii) {
                         const int j = cg + 4 * ii;
@@ -583,10 +713,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         else
             srow = q * 32 + lane;
         const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
-        const int my_units = static_cast<int>(blockIdx.x) < total_units
-                                 ? (total_units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                                 : 0;
-        const int total_stages = my_units * KT;
+        int total_stages = 0;
+        for (int v = blockIdx.x; v < total_items; v += gridDim.x) {
+            const WorkItem it = item_of(v);
+            total_stages += it.k1 - it.k0;
+        }
         bool ok = true;
         for (;;) {
             {

@@ -65,6 +65,8 @@ struct PrepArgs {
     int64_t meta_pairs;
     int64_t meta_rows;
     // buffers to clear
+    int32_t* zero_i32;  // (the K-split piece counters; cleared by block 0)
+    int zero_i32_count;
     float* zero_f32;
     int64_t zero_count;
     int32_t* fill_i32;  // set to -1
