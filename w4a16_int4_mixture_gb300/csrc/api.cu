@@ -486,7 +486,27 @@ struct LayerIO {
     uint16_t* rows_out;
     int down_epi;
     int flags;
+    double tok_e;  // expected rows per local expert
 };
+
+// Weight tiles per unit of the down GEMM: with a one-stage K (I = BK) each
+// unit is short, and its fixed costs (waits, commits, the token tile) are
+// shared by several tiles of a short-K configuration, as long as the units
+// still give every SM several.  Returns the tiles per unit and sets *cfg to
+// the configuration that runs them.
+int pick_tpu(int* cfg, int K, int n_tiles, int E_local, double tok_e, int sms)
+{
+    const int s_cfg = *cfg == kCfgD32 ? kCfgS32 : *cfg == kCfgD64 ? kCfgS64 : -1;
+    if (s_cfg < 0 || K != gemm_cfg_bk(s_cfg))
+        return 1;
+    const double chunks = E_local * (1.0 - std::exp(-(tok_e > 0 ? tok_e : 0.0)));
+    int tpu = gemm_cfg_tpu_max_down(s_cfg);
+    while (tpu > 1 && (n_tiles % tpu != 0 || chunks * n_tiles / tpu < 4.0 * sms))
+        tpu /= 2;
+    if (tpu > 1)
+        *cfg = s_cfg;
+    return tpu;
+}
 
 chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w, uint8_t* ws,
                        int* err, int32_t* pair_row, float* acc, const DeviceInfo& dev,
@@ -526,6 +546,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.N = 2 * io.I;
     g.I = io.I;
     g.n_tiles = io.I / 64;
+    g.tpu = 1;
     g.scales = io.w13_s;
     g.chunks = reinterpret_cast<const Chunk*>(ws + w.off_chunks[0]);
     g.num_chunks = num_chunks;
@@ -558,6 +579,8 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     d.K = io.I;
     d.N = io.H;
     d.n_tiles = io.H / 128;
+    int cfg_down = sc.cfg_down;
+    d.tpu = pick_tpu(&cfg_down, io.I, d.n_tiles, io.E_local, io.tok_e, dev.sms);
     d.scales = io.w2_s;
     d.chunks = reinterpret_cast<const Chunk*>(ws + w.off_chunks[1]);
     d.num_chunks = num_chunks + 1;
@@ -569,7 +592,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     d.rows_out = io.rows_out;
     d.split_cnt = split_cnt + kSplitSlots;
     d.split_slots = slots_for(sc.cfg_down);
-    if (launch_gemm(sc.cfg_down, false, map2, smap2, bmap2, d, dev.sms, s) != cudaSuccess)
+    if (launch_gemm(cfg_down, false, map2, smap2, bmap2, d, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(3);
     return CHORD_OK;
@@ -618,7 +641,7 @@ int chord_describe_schedule(int64_t T, int k, int E_global, int E_local, int H, 
     const double tok_e = E_global > 0 ? static_cast<double>(T) * k / E_global : 0.0;
     const Schedule s = pick_schedule(tok_e, T, H, I, flags);
     static const char* names[] = {"decode-tile32", "decode-tile64", "decode-tile128",
-                                  "prefill-tile192"};
+                                  "prefill-tile192", "short-k-tile32", "short-k-tile64"};
     char tmp[256];
     const int n = snprintf(tmp, sizeof tmp,
                            "tok_e=%.2f gate_up=%s(BK%d) down=%s(BK%d) combine=%s block_m=16 "
@@ -815,6 +838,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     io.h_out = h_out;
     io.down_epi = sc.reduce ? kEpiReduceTok : kEpiStorePair;
     io.flags = flags;
+    io.tok_e = tok_e;
     if ((st = run_gemms(io, sc, w, ws, err, pair_row, acc, dev, s, marks)) != CHORD_OK)
         return st;
 
@@ -953,6 +977,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     io.rows_out = out_rows;
     io.down_epi = kEpiStoreRows | (with_tokens ? kEpiReduceTok : 0);
     io.flags = flags;
+    io.tok_e = tok_e;
     if ((st = run_gemms(io, sc, w, ws, err, nullptr, acc, dev, s, marks)) != CHORD_OK)
         return st;
     if (with_tokens && launch_finalize(acc, out_tokens, T * H, dev.sms, s) != cudaSuccess)

@@ -32,6 +32,7 @@ struct GemmArgs {
     int N;                    // rows of one expert's weight
     int I;                    // intermediate size (gate_up: up rows start at I)
     int n_tiles;              // output tiles per chunk
+    int tpu;                  // tiles per work unit (n_tiles % tpu == 0; > 1 only when K is one stage)
     const uint16_t* scales;   // [E, N, K/32]
     const Chunk* chunks;
     const int32_t* num_chunks;

@@ -6,9 +6,14 @@
 
 namespace chord {
 
-// template <BK, code stages, token stages, A stages in TMEM, token tile, accum buffers, gate_up>
+// template <BK, code stages, token stages, A stages in TMEM, token tile, accum buffers, gate_up
+//           [, accumulator columns: several weight tiles per unit for a one-stage K]>
 template <bool G> using CfgD32 = GemmCfg<256, 6, 4, 3, 32, 2, G>;
 template <bool G> using CfgD64 = GemmCfg<256, 6, 3, 3, 64, 2, G>;
+// down GEMMs with a one-stage K: four (32) or two (64) weight tiles per
+// unit, at the cost of one A stage
+using CfgS32 = GemmCfg<256, 6, 4, 2, 32, 2, false, 128>;
+using CfgS64 = GemmCfg<256, 6, 3, 2, 64, 2, false, 128>;
 template <bool G> using CfgD128 = GemmCfg<256, 4, 2, 2, 128, 2, G>;
 template <bool G> using CfgP192 = GemmCfg<128, 4, 3, 2, 192, 2, G>;
 

@@ -40,7 +40,7 @@
 
 namespace chord {
 
-template <int BK_, int KS_, int BS_, int AS_, int MAXN_, int ACCB_, bool GATE_UP_>
+template <int BK_, int KS_, int BS_, int AS_, int MAXN_, int ACCB_, bool GATE_UP_, int ACCW_ = MAXN_>
 struct GemmCfg {
     static constexpr int BK = BK_;        // K elements per stage
     static constexpr int KS = KS_;        // code/scale stages in shared memory
@@ -48,6 +48,10 @@ struct GemmCfg {
     static constexpr int AS = AS_;        // A-operand stages in TMEM
     static constexpr int MAXN = MAXN_;    // largest token tile
     static constexpr int ACCB = ACCB_;    // accumulator buffers in TMEM
+    // columns of one accumulator buffer: ACCW / MAXN weight tiles of a unit
+    // (one-stage K: several tiles share the unit's token tile)
+    static constexpr int ACCW = ACCW_;
+    static constexpr int TPU_MAX = ACCW / MAXN;
     static constexpr bool GATE_UP = GATE_UP_;
 
     static constexpr int CODE_ROW = BK / 2;                 // bytes of codes per weight row
@@ -100,7 +104,8 @@ struct GemmCfg {
 
     static_assert(BK == 128 || BK == 256, "stage depth");
     static_assert(MAXN % 16 == 0 && MAXN >= 16 && MAXN <= 256, "token tile");
-    static_assert(D_COL0 + ACCB * MAXN <= TMEM_COLS, "tensor memory budget");
+    static_assert(D_COL0 + ACCB * ACCW <= TMEM_COLS, "tensor memory budget");
+    static_assert(ACCW % MAXN == 0 && (TPU_MAX == 1 || (!GATE_UP && BK == 256)), "tiles per unit");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM keeps the 512-column TMEM alloc safe");
     static_assert(OFF_B % 1024 == 0 && B_REGION % 1024 == 0, "swizzle atoms need 1024B alignment");
@@ -187,7 +192,7 @@ __device__ __forceinline__ void dequant_word(uint32_t w, ScalePair sp, uint32_t*
 
 // One work item of a GEMM CTA: a whole unit, or one K piece of a split unit.
 struct WorkItem {
-    int unit;   // chunk * n_tiles + weight tile
+    int unit;   // chunk * units_per_chunk + tile group
     int k0;     // K stages [k0, k1)
     int k1;
     int piece;  // -1 for a whole unit, else the piece index
@@ -269,15 +274,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     const int n_tiles = args.n_tiles;
     const int KT = args.K / C::BK;
+    // weight tiles per unit (1, or up to TPU_MAX for a one-stage K): a unit
+    // covers tiles nt0 .. nt0 + tpu - 1 of one chunk, K stage by K stage, each
+    // tile into its own MAXN columns of the accumulator
+    const int tpu = C::TPU_MAX == 1 ? 1 : args.tpu;
+    const int units_per_chunk = n_tiles / tpu;
     int issued_stages = 0;  // code / token producers: K stages whose copies were issued
     // Units are dealt to CTAs with a stride of the grid, so at any time the
     // CTAs work on neighbouring units: a few chunks, whose token tiles stay hot
     // in L2 across the CTAs that share them.  Each role loads the descriptor of
     // a unit two units ahead (one unit of a short-K GEMM is shorter than a
     // global load).
-    const int total_units = args.num_chunks[0] * n_tiles;
+    const int total_units = args.num_chunks[0] * units_per_chunk;
     auto chunk_of = [&](int u) -> Chunk {
-        return u < total_units ? args.chunks[u / n_tiles] : Chunk{};
+        return u < total_units ? args.chunks[u / units_per_chunk] : Chunk{};
     };
     // The work items are those units, except that when the last round of
     // units (rem = units mod grid) would leave at least half of the CTAs idle,
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int grid = static_cast<int>(gridDim.x);
         const int rem = total_units % grid;
         const int slots = args.split_slots < grid ? args.split_slots : grid;
-        if (rem > 0 && slots >= 2 * rem) {
+        if (rem > 0 && slots >= 2 * rem && tpu == 1) {
             int p = slots / rem;
             if (p > KT / kSplitMinStages)
                 p = KT / kSplitMinStages;
@@ -341,12 +351,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const Chunk ch = next;
             next = next2;
             next2 = chunk_of_item(v + 2 * gridDim.x);
-            const int nt = it.unit % n_tiles;
+            const int nt0 = (it.unit % units_per_chunk) * tpu;
             const int e = ch.expert;
-            // first weight row of the tile: gate_up takes rows [row0, row0 + 64)
-            // (gate) and the same 64 rows I further on (up) as one 3-D box
-            const int row0 = C::GATE_UP ? e * args.N + nt * 64 : e * args.N + nt * 128;
-            for (int ks = it.k0; ks < it.k1; ++ks, ++g) {
+            // K stage by K stage, the unit's tiles in turn
+            for (int ks = it.k0, nt = nt0; ks < it.k1 && ok; ++g) {
+                // first weight row of the tile: gate_up takes rows [row0, row0 + 64)
+                // (gate) and the same 64 rows I further on (up) as one 3-D box
+                const int row0 = C::GATE_UP ? e * args.N + nt * 64 : e * args.N + nt * 128;
                 const int s = g % C::KS;
                 if (!wait_side(codes_empty(s), ((g / C::KS) & 1) ^ 1)) {
                     ok = false;
@@ -381,6 +392,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     cp_async_arrive_noinc(codes_full(s));
                 }
                 __syncwarp();
+                if (++nt == nt0 + tpu) {
+                    nt = nt0;
+                    ++ks;
+                }
             }
         }
         issued_stages = g;
@@ -427,7 +442,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ------------------------------------------------------------- MMA issuer
         // The whole warp walks the schedule (so every operand stays warp-uniform)
         // and elect.sync picks the lane that issues each MMA and commit.
-        int g = 0;
+        int ga = 0;  // A stages (one per K stage and tile)
+        int gb = 0;  // token stages (one per K stage)
         int issued = 0;
         bool ok = true;
         int i = 0;
@@ -447,28 +463,48 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem + C::D_COL0 + acc * C::MAXN;
-            for (int ks = it.k0; ks < it.k1; ++ks, ++g) {
-                const int sa = g % C::AS;
-                const int sb = g % C::BS;
-                const bool got = mbar_wait(a_full(sa), (g / C::AS) & 1, abort_flag, err) &&
-                                 mbar_wait(b_full(sb), (g / C::BS) & 1, abort_flag, err);
-                if (!__all_sync(0xffffffffu, got)) {
-                    ok = false;
-                    break;
+            const uint32_t d_tmem = tmem + C::D_COL0 + acc * C::ACCW;
+            for (int ks = it.k0; ks < it.k1 && ok; ++ks, ++gb) {
+                const int sb = gb % C::BS;
+                const uint64_t bdesc = smem_desc_sw128(sbase + C::OFF_B + sb * C::B_STAGE);
+                const uint32_t accum = ks != it.k0 ? 1u : 0u;
+                if constexpr (C::TPU_MAX == 1) {
+                    const int sa = ga % C::AS;
+                    const bool got = mbar_wait(a_full(sa), (ga / C::AS) & 1, abort_flag, err) &&
+                                     mbar_wait(b_full(sb), (gb / C::BS) & 1, abort_flag, err);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = tmem + sa * C::A_COLS;
+                    if constexpr (C::BK == 256)
+                        mma_stage16<C::B_REGION / 16>(d_tmem, a_base, bdesc, idesc, accum);
+                    else
+                        mma_stage8<C::B_REGION / 16>(d_tmem, a_base, bdesc, idesc, accum);
+                    issued = 1;
+                    mma_commit_elect(a_empty(sa));
+                    ++ga;
+                } else {
+                    if (!__all_sync(0xffffffffu, mbar_wait(b_full(sb), (gb / C::BS) & 1, abort_flag, err))) {
+                        ok = false;
+                        break;
+                    }
+                    for (int t = 0; t < tpu; ++t, ++ga) {
+                        const int sa = ga % C::AS;
+                        if (!__all_sync(0xffffffffu, mbar_wait(a_full(sa), (ga / C::AS) & 1, abort_flag, err))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_base = tmem + sa * C::A_COLS;
+                        mma_stage16<C::B_REGION / 16>(d_tmem + t * C::MAXN, a_base, bdesc, idesc, accum);
+                        issued = 1;
+                        mma_commit_elect(a_empty(sa));
+                    }
                 }
-                tc_fence_after();
-                const uint32_t a_base = tmem + sa * C::A_COLS;
-                const uint32_t b_base = sbase + C::OFF_B + sb * C::B_STAGE;
-                if constexpr (C::BK == 256)
-                    mma_stage16<C::B_REGION / 16>(d_tmem, a_base, smem_desc_sw128(b_base), idesc,
-                                                  ks != it.k0 ? 1u : 0u);
-                else
-                    mma_stage8<C::B_REGION / 16>(d_tmem, a_base, smem_desc_sw128(b_base), idesc,
-                                                 ks != it.k0 ? 1u : 0u);
-                issued = 1;
-                mma_commit_elect(a_empty(sa));
-                mma_commit_elect(b_empty(sb));
+                if (ok)
+                    mma_commit_elect(b_empty(sb));
             }
             if (!ok)
                 break;
@@ -530,7 +566,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 meta_cur[k] = meta_next[k];
             load_meta(c_nxt, meta_next);
             const Chunk c_nn = chunk_of_item(v + 2 * EG * gridDim.x);
-            const int nt = it.unit % n_tiles;
+            const int nt0 = (it.unit % units_per_chunk) * tpu;
             const int ntok = ch.nrows;
             const int ntok16 = (ntok + 15) & ~15;
             const int acc = i % C::ACCB;
@@ -540,7 +576,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 break;
             tc_fence_after();
             const uint32_t dbase =
-                tmem + (static_cast<uint32_t>(q * 32) << 16) + C::D_COL0 + acc * C::MAXN;
+                tmem + (static_cast<uint32_t>(q * 32) << 16) + C::D_COL0 + acc * C::ACCW;
             // A piece of a split unit: the accumulator goes to the piece's slot
             // (column-major, so a warp stores 128 contiguous bytes per column).
             // The last piece of the unit to get here adds the unit's slots in
@@ -620,7 +656,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     mbar_arrive(d_empty(acc));
                 if (!epi_sync())
                     break;
-                const int64_t col0 = static_cast<int64_t>(nt) * 64;
+                const int64_t col0 = static_cast<int64_t>(nt0) * 64;
                 for (int idx = et; idx < ntok * 8; idx += 128) {
                     const int c = idx >> 3;
                     const int part = idx & 7;
@@ -628,7 +664,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     *reinterpret_cast<uint4*>(args.h_out + static_cast<int64_t>(ch.row0 + c) * args.ld_h +
                                               col0 + part * 8) = val;
                 }
-                if (args.pair_row != nullptr && nt == 0) {
+                if (args.pair_row != nullptr && nt0 == 0) {
                     for (int c = et; c < ntok; c += 128) {
                         const int p = args.pair_of_row[ch.row0 + c];
                         if (p >= 0 && p < args.num_pairs)
@@ -643,61 +679,65 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // 16-byte stores and vector reductions instead of one 4-byte
                 // access per lane and column.
                 const int N = args.N;
-                const int nq = nt * 128 + q * 32;
                 float* tile = reinterpret_cast<float*>(smem + C::OFF_EPIT) + (egrp * 4 + q) * 16 * 32;
                 const int m4 = (lane & 7) * 4;
                 const int cg = lane >> 3;
-                // (a rolled loop: the epilogue runs once per unit, and its code
+                // (rolled loops: the epilogue runs once per unit, and its code
                 // competes for the instruction cache with every other role's)
 #pragma unroll 1
-                for (int c0 = 0; c0 < ntok16; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld_x16(dbase + c0, v);
-                    tmem_wait_ld();
-                    if (c0 + 16 >= ntok16) {
-                        // last block read: the accumulator goes back to the MMA
-                        tc_fence_before();
+                for (int t = 0; t < tpu; ++t) {
+                    const int nq = (nt0 + t) * 128 + q * 32;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < ntok16; c0 += 16) {
+                        uint32_t v[16];
+                        tmem_ld_x16(dbase + t * C::MAXN + c0, v);
+                        tmem_wait_ld();
+                        if (t == tpu - 1 && c0 + 16 >= ntok16) {
+                            // last block read: the accumulator goes back to the MMA
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(d_empty(acc));
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            tile[j * 32 + lane] = __uint_as_float(v[j]) * kWeightRescale;
                         __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(d_empty(acc));
-                    }
+                        // columns c0 .. c0 + 15 sit in one lane group: records meta_cur[c0 / 32]
+                        int4 mrec = meta_cur[0];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        tile[j * 32 + lane] = __uint_as_float(v[j]) * kWeightRescale;
-                    __syncwarp();
-                    // columns c0 .. c0 + 15 sit in one lane group: records meta_cur[c0 / 32]
-                    int4 mrec = meta_cur[0];
+                        for (int k = 1; k < MPT; ++k)
+                            if (c0 >= 32 * k)
+                                mrec = meta_cur[k];
 #pragma unroll
-                    for (int k = 1; k < MPT; ++k)
-                        if (c0 >= 32 * k)
-                            mrec = meta_cur[k];
-#pragma unroll
-                    for (int ii = 0; ii < 4; ++ii) {
-                        const int j = cg + 4 * ii;
-                        const int c = c0 + j;
-                        const int src = c & 31;
-                        const int p = __shfl_sync(0xffffffffu, mrec.x, src);
-                        const int tok = __shfl_sync(0xffffffffu, mrec.y, src);
-                        const float w = __int_as_float(__shfl_sync(0xffffffffu, mrec.z, src));
-                        if (c >= ntok)
-                            continue;
-                        const float4 y = *reinterpret_cast<const float4*>(tile + j * 32 + m4);
-                        if (args.epi & kEpiStoreRows) {
-                            uint2 o;
-                            o.x = bf16x2_pack_rn(y.x, y.y);
-                            o.y = bf16x2_pack_rn(y.z, y.w);
-                            *reinterpret_cast<uint2*>(args.rows_out + static_cast<int64_t>(ch.row0 + c) * N +
-                                                      nq + m4) = o;
+                        for (int ii = 0; ii < 4; ++ii) {
+                            const int j = cg + 4 * ii;
+                            const int c = c0 + j;
+                            const int src = c & 31;
+                            const int p = __shfl_sync(0xffffffffu, mrec.x, src);
+                            const int tok = __shfl_sync(0xffffffffu, mrec.y, src);
+                            const float w = __int_as_float(__shfl_sync(0xffffffffu, mrec.z, src));
+                            if (c >= ntok)
+                                continue;
+                            const float4 y = *reinterpret_cast<const float4*>(tile + j * 32 + m4);
+                            if (args.epi & kEpiStoreRows) {
+                                uint2 o;
+                                o.x = bf16x2_pack_rn(y.x, y.y);
+                                o.y = bf16x2_pack_rn(y.z, y.w);
+                                *reinterpret_cast<uint2*>(args.rows_out + static_cast<int64_t>(ch.row0 + c) * N +
+                                                          nq + m4) = o;
+                            }
+                            if (per_pair && p >= 0) {
+                                if (args.epi & kEpiStorePair)
+                                    *reinterpret_cast<float4*>(args.y_pairs + static_cast<int64_t>(p) * N + nq +
+                                                               m4) = y;
+                                if (args.epi & kEpiReduceTok)
+                                    red_add_v4_f32(args.out_acc + static_cast<int64_t>(tok) * N + nq + m4,
+                                                   w * y.x, w * y.y, w * y.z, w * y.w);
+                            }
                         }
-                        if (per_pair && p >= 0) {
-                            if (args.epi & kEpiStorePair)
-                                *reinterpret_cast<float4*>(args.y_pairs + static_cast<int64_t>(p) * N + nq + m4) = y;
-                            if (args.epi & kEpiReduceTok)
-                                red_add_v4_f32(args.out_acc + static_cast<int64_t>(tok) * N + nq + m4,
-                                               w * y.x, w * y.y, w * y.z, w * y.w);
-                        }
+                        __syncwarp();  // the tile is rewritten by the next block
                     }
-                    __syncwarp();  // the tile is rewritten by the next block
                 }
             }
         }
@@ -716,7 +756,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int total_stages = 0;
         for (int v = blockIdx.x; v < total_items; v += gridDim.x) {
             const WorkItem it = item_of(v);
-            total_stages += it.k1 - it.k0;
+            total_stages += (it.k1 - it.k0) * tpu;
         }
         bool ok = true;
         for (;;) {

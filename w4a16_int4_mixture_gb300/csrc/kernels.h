@@ -99,10 +99,14 @@ enum GemmConfig : int {
     kCfgD64 = 1,    // BK 256, token tile <= 64
     kCfgD128 = 2,   // BK 256, token tile <= 128
     kCfgP192 = 3,   // BK 128, token tile <= 192, two accumulators: prefill / short K
-    kNumGemmConfigs = 4
+    kCfgS32 = 4,    // down only, one-stage K: token tile <= 32, up to 4 weight tiles per unit
+    kCfgS64 = 5,    // down only, one-stage K: token tile <= 64, up to 2 weight tiles per unit
+    kNumGemmConfigs = 6
 };
 
 int gemm_cfg_bk(int cfg);
+// Most weight tiles one unit of the down GEMM may hold (one-stage K only).
+int gemm_cfg_tpu_max_down(int cfg);
 int gemm_cfg_maxn(int cfg);
 int gemm_cfg_smem(int cfg, bool gate_up);
 
