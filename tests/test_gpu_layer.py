@@ -179,6 +179,9 @@ def test_poisoned_workspace_does_not_leak(chord):
         run = Run(bf16_to_np(out), bf16_to_np(h), si.cpu().numpy(), ei.cpu().numpy(),
                   int(ntp.item()), 16)
         verify_indexed(inp, run, label=f"poisoned workspace flags={flags}")
+        # h rows of the layout's sentinel (padding) entries are zero
+        pad = np.nonzero(run.si[:run.ntp] >= s.T * s.k)[0]
+        assert pad.size > 0 and np.all(run.h[pad] == 0), "sentinel rows of h are not zero"
 
 
 # ---------------------------------------------------------------- grouped

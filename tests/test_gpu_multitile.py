@@ -4,7 +4,8 @@ With I = 256 the down GEMM's K is a single stage, and the library lets one
 work unit cover up to four 128-row weight tiles that share the unit's token
 tile, when the units still give every SM several.  The TP8 workload tests
 (test_gpu_layer) run this at their full sizes; these cases add the grouped
-entry points and a ragged expert mix, against the oracle."""
+entry points and a ragged expert mix, against the oracle.  The last case runs
+the 64-row token tile over many units of a long K."""
 
 import numpy as np
 import pytest
@@ -42,5 +43,15 @@ def test_multitile_contiguous(chord):
 def test_multitile_deterministic(chord):
     inp = tp8_like(40, 6, 48, 64)
     a = run_indexed_full(chord, inp, flags=2)
+    b = run_indexed_full(chord, inp, flags=2)
+    assert np.array_equal(a.out, b.out)
+
+
+def test_tile64_many_units(chord):
+    # 64 experts x ~20 rows (64-row token tile), I = 2048: 32 gate/up tiles and
+    # 4 down tiles per chunk, down K in 8 stages
+    inp = small(160, 8, 64, 64, 512, 2048, 65, emap=False)
+    a = run_indexed_full(chord, inp, flags=2)
+    verify_indexed(inp, a, label="64-row tile, many units")
     b = run_indexed_full(chord, inp, flags=2)
     assert np.array_equal(a.out, b.out)

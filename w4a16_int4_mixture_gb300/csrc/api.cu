@@ -487,6 +487,7 @@ struct LayerIO {
     int down_epi;
     int flags;
     double tok_e;  // expected rows per local expert
+    bool h_zero_unpaired;  // h rows without a pair are written as zeros (indexed layout)
 };
 
 // Weight tiles per unit of the down GEMM: with a one-stage K (I = BK) each
@@ -557,6 +558,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.pair_of_row = io.pair_of_row;
     g.row_meta = io.row_meta;
     g.err = err;
+    g.h_zero_unpaired = io.h_zero_unpaired ? 1 : 0;
     // K-split slots: as many as the workspace holds for this token tile, at
     // most one per CTA
     const bool split = !(io.flags & CHORD_FLAG_NO_SPLIT_K);
@@ -839,6 +841,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     io.down_epi = sc.reduce ? kEpiReduceTok : kEpiStorePair;
     io.flags = flags;
     io.tok_e = tok_e;
+    io.h_zero_unpaired = true;
     if ((st = run_gemms(io, sc, w, ws, err, pair_row, acc, dev, s, marks)) != CHORD_OK)
         return st;
 

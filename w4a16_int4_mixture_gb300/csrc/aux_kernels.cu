@@ -457,7 +457,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
     }
     if (a.gx_out != nullptr) {
         // 128 threads per padded row, up to 8 16-byte loads in flight per
-        // thread before the stores
+        // thread before the stores.  Rows with no pair (the block padding of
+        // the layout) are not written: they only feed MMA columns that no
+        // output reads, and the gate/up epilogue writes zeros for their h rows.
         constexpr int kGroup = 128;
         const int gl = static_cast<int>(tid % kGroup);
         const int64_t ngrp = nth / kGroup;
@@ -470,15 +472,16 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
             if (gl == 0 && a.meta_out != nullptr)
                 a.meta_out[r] = valid ? make_int4(p, p / a.gx_topk, __float_as_int(a.meta_w[p]), 0)
                                       : make_int4(-1, 0, 0, 0);
-            const uint4* src =
-                reinterpret_cast<const uint4*>(a.gx_src + static_cast<int64_t>(valid ? p / a.gx_topk : 0) * a.gx_H);
+            if (!valid)
+                continue;
+            const uint4* src = reinterpret_cast<const uint4*>(a.gx_src + static_cast<int64_t>(p / a.gx_topk) * a.gx_H);
             uint4* dst = reinterpret_cast<uint4*>(a.gx_out + r * a.gx_H);
             for (int c0 = gl; c0 < n16; c0 += 8 * kGroup) {
                 uint4 v[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int c = c0 + j * kGroup;
-                    v[j] = (valid && c < n16) ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                    v[j] = c < n16 ? src[c] : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {

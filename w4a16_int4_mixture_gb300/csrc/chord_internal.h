@@ -45,6 +45,7 @@ struct GemmArgs {
     float* out_acc;           // down: [T, N]
     uint16_t* rows_out;       // down: [rows, N]
     const int32_t* pair_of_row;  // pair id t*k+j of each padded row (or -1 / sentinel)
+    int h_zero_unpaired;         // gate_up: rows whose pair_of_row is not a pair get h = 0
     const int4* row_meta;        // down: {pair, token, weight bits, 0} per padded row
     int* err;
     int test_skip_arrive;  // CHORD_FLAG_TEST_SKIP_ARRIVE (gate_up only)

@@ -660,7 +660,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (int idx = et; idx < ntok * 8; idx += 128) {
                     const int c = idx >> 3;
                     const int part = idx & 7;
-                    const uint4 val = *reinterpret_cast<const uint4*>(hs + c * 64 + part * 8);
+                    uint4 val = *reinterpret_cast<const uint4*>(hs + c * 64 + part * 8);
+                    if (args.h_zero_unpaired) {
+                        // (an unpaired row's token row was never written: its h is
+                        // whatever the MMA made of it)
+                        const int p = args.pair_of_row[ch.row0 + c];
+                        if (p < 0 || p >= args.num_pairs)
+                            val = make_uint4(0u, 0u, 0u, 0u);
+                    }
                     *reinterpret_cast<uint4*>(args.h_out + static_cast<int64_t>(ch.row0 + c) * args.ld_h +
                                               col0 + part * 8) = val;
                 }

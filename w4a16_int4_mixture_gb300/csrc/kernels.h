@@ -48,7 +48,7 @@ struct PrepArgs {
     int32_t* num_chunks;  // [2]
     // indexed layout: gather the routed token rows of x into padded-row order
     // (gx_out[r] = x[sorted_ids[r] / topk] for r < num_tokens_padded and a valid
-    // pair, zeros for sentinel rows)
+    // pair; sentinel rows are left as they are)
     const uint16_t* gx_src;  // x [T, gx_H]
     uint16_t* gx_out;        // [capacity, gx_H]
     const int32_t* gx_ids;   // sorted_ids
