@@ -31,6 +31,8 @@ __device__ __forceinline__ int local_expert_of(int32_t gid, int E_global, const 
 
 __global__ void __launch_bounds__(kAlignTile) align_hist_kernel(AlignArgs a)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ int cnt[];  // [E_local]
     for (int e = threadIdx.x; e < a.E_local; e += blockDim.x)
         cnt[e] = 0;
@@ -85,6 +87,8 @@ constexpr int kScanSmemInts = 8192;
 
 __global__ void __launch_bounds__(1024) align_scan_kernel(AlignArgs a)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int sh[kScanSmemInts];
     const int sentinel = static_cast<int>(a.num_pairs);
     const int bm = a.block_m;
@@ -145,6 +149,8 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(AlignArgs a)
 
 __global__ void __launch_bounds__(kAlignTile) align_scatter_kernel(AlignArgs a)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ int wcnt[];  // [kAlignTile/32][E_local]
     constexpr int W = kAlignTile / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -184,6 +190,8 @@ constexpr int kSmallMaxExperts = 128;
 
 __global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int cnt[kSmallMaxExperts];   // pass 1 counts, then pairs placed by earlier rounds
     __shared__ int base[kSmallMaxExperts];  // first padded row of each expert
     __shared__ int wcnt[kSmallThreads / 32][kSmallMaxExperts];  // per warp of a round
@@ -259,22 +267,18 @@ __global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s)
 {
     if (a.num_pairs <= kSmallMaxPairs && a.E_local <= kSmallMaxExperts) {
-        align_small_kernel<<<1, kSmallThreads, 0, s>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(align_small_kernel, 1, kSmallThreads, 0, s, a);
     }
     const int tiles = a.n_tiles;
     if (tiles > 0) {
-        align_hist_kernel<<<tiles, kAlignTile, a.E_local * sizeof(int), s>>>(a);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(align_hist_kernel, tiles, kAlignTile, a.E_local * sizeof(int), s, a);
         if (e != cudaSuccess)
             return e;
     }
-    align_scan_kernel<<<1, 1024, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(align_scan_kernel, 1, 1024, 0, s, a);
     if (e != cudaSuccess || tiles == 0)
         return e;
-    align_scatter_kernel<<<tiles, kAlignTile, (kAlignTile / 32) * a.E_local * sizeof(int), s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(align_scatter_kernel, tiles, kAlignTile, (kAlignTile / 32) * a.E_local * sizeof(int), s, a);
 }
 
 // ---------------------------------------------------------------------------
@@ -421,6 +425,8 @@ __device__ void build_chunk_lists(const PrepArgs& a)
 
 __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i < a.zero_i32_count; i += blockDim.x)
             a.zero_i32[i] = 0;
@@ -507,6 +513,8 @@ __device__ __forceinline__ bool scale_in_range(uint32_t bits16)
 __global__ void scale_range_kernel(const uint16_t* __restrict__ a, int64_t na,
                                    const uint16_t* __restrict__ b, int64_t nb, int* err)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     bool ok = true;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb;
@@ -523,14 +531,12 @@ cudaError_t launch_scale_check(const uint16_t* a, int64_t na, const uint16_t* b,
 {
     if (na + nb <= 0)
         return cudaSuccess;
-    scale_range_kernel<<<4 * sms, 256, 0, s>>>(a, na, b, nb, err);
-    return cudaGetLastError();
+    return launch_pdl(scale_range_kernel, 4 * sms, 256, 0, s, a, na, b, nb, err);
 }
 
 cudaError_t launch_prep(const PrepArgs& a, int work_blocks, cudaStream_t s)
 {
-    prep_kernel<<<1 + work_blocks, 1024, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(prep_kernel, 1 + work_blocks, 1024, 0, s, a);
 }
 
 // ---------------------------------------------------------------------------
@@ -545,6 +551,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 // out[i] = bf16(acc[i]) for the fp32 token accumulators of the reduction form.
 __global__ void finalize_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out, int64_t n)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t n8 = n / 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
@@ -571,6 +579,8 @@ constexpr int kCombineThreads = 128;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_pairs_kernel(CombineArgs a)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int64_t s_pair[32];
     __shared__ float s_w[32];
     __shared__ int s_n;
@@ -626,8 +636,7 @@ cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int sms,
         blocks = 1;
     if (blocks > 4LL * sms)
         blocks = 4LL * sms;
-    finalize_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(acc, out, n);
-    return cudaGetLastError();
+    return launch_pdl(finalize_kernel, static_cast<int>(blocks), 256, 0, s, acc, out, n);
 }
 
 cudaError_t launch_combine_pairs(const CombineArgs& a, cudaStream_t s)
@@ -635,8 +644,7 @@ cudaError_t launch_combine_pairs(const CombineArgs& a, cudaStream_t s)
     if (a.T <= 0)
         return cudaSuccess;
     const int64_t blocks = a.T < 65535 ? a.T : 65535;
-    combine_pairs_kernel<<<static_cast<unsigned>(blocks), kCombineThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(combine_pairs_kernel, static_cast<unsigned>(blocks), kCombineThreads, 0, s, a);
 }
 
 }  // namespace chord

@@ -24,6 +24,19 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the kernel before it in the stream finishes; it
+// lets its own successor be scheduled as soon as all its CTAs run, and waits
+// for its predecessors (completed, their writes visible) before it touches
+// any memory they may read or write
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // error word (in the caller's workspace)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void raise_error(int* err, int bits)

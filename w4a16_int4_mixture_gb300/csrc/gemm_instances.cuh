@@ -35,8 +35,7 @@ cudaError_t launch_gemm_cfg(const CUtensorMap& map, const CUtensorMap& smap,
             return e;
         attr_set[dev] = true;
     }
-    w4a16_gemm_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(map, smap, bmap, a);
-    return cudaGetLastError();
+    return launch_pdl(w4a16_gemm_kernel<C>, grid, C::THREADS, C::SMEM_BYTES, s, map, smap, bmap, a);
 }
 
 }  // namespace chord

@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();
 
     // barriers
     const uint32_t bar0 = sbase + C::OFF_BARS;
@@ -271,6 +272,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // (barriers and tensor memory are set up while the previous kernel ends;
+    // everything after this reads or writes memory it may still use)
+    pdl_wait();
 
     const int n_tiles = args.n_tiles;
     const int KT = args.K / C::BK;
