@@ -240,9 +240,9 @@ def device_inputs(inp, torch, dev):
 
 def kernels_per_call(pairs: int, e_local: int) -> int:
     """Kernels of one align + indexed layer call: the align runs as one CTA up to
-    4096 pairs and 128 local experts (aux_kernels.cu), else as three kernels;
+    4096 pairs and 512 local experts (aux_kernels.cu), else as three kernels;
     the layer is prep, gate_up, down and the combine / finalize."""
-    align = 1 if (pairs <= 4096 and e_local <= 128) else 3
+    align = 1 if (pairs <= 4096 and e_local <= 512) else 3
     return align + 4
 
 

@@ -56,6 +56,8 @@ def test_single_rank_values():
     assert bench.max_over_ranks(2.0, 1, None) == 2.0
     assert bench.whole_job_us_per_call(0.2384, 1) == 238.4
     assert bench.kernels_per_call(4096, 48) == 5
+    assert bench.kernels_per_call(1024, 384) == 5
+    assert bench.kernels_per_call(1024, 513) == 7
     assert bench.kernels_per_call(65536, 48) == 7
 
 

@@ -63,6 +63,16 @@ def test_align_random_small(chord):
         _compare(chord, ids, Eg, emap, El, bm)
 
 
+@pytest.mark.parametrize("E", [129, 384, 512, 513, 1000])
+def test_align_many_local_experts(chord, E):
+    # one-CTA form up to 512 local experts and 4096 pairs, three kernels beyond
+    rng = np.random.default_rng(E)
+    T, k = 300, 8
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    for bm in (1, 16):
+        _compare(chord, ids, E, None, E, bm)
+
+
 def test_align_over_allocated_capacity(chord):
     s = synth.config(3, T=16)
     inp = synth.make_inputs(s, weights=False)

@@ -80,62 +80,70 @@ __device__ int block_exclusive_scan(int v, int* total)
     return before;
 }
 
-// One CTA, one thread per local expert (E_local <= 1024).  The per-tile
-// histogram is read through shared memory in chunks of whole tiles (coalesced
-// loads instead of one dependent load per tile and expert).
-constexpr int kScanSmemInts = 8192;
-
+// One CTA.  Each local expert (E_local <= 1024) gets tpe threads (a power of
+// two, tpe * E_local <= 1024), thread j of expert e taking a contiguous range
+// of tiles; threads j * E_local + e are adjacent in e, so every load of the
+// per-tile histogram is coalesced.  Pass 1 sums each range, pass 2 rewrites
+// the histogram in place as the first padded row of each (tile, expert).
 __global__ void __launch_bounds__(1024) align_scan_kernel(AlignArgs a)
 {
     pdl_launch_dependents();
     pdl_wait();
-    __shared__ int sh[kScanSmemInts];
+    __shared__ int part[1024];
+    __shared__ int offs[1024];
     const int sentinel = static_cast<int>(a.num_pairs);
     const int bm = a.block_m;
     const int E = a.E_local;
-    const int e = threadIdx.x;
     // this call's error word starts clear (the scatter reports bad ids after us)
     if (threadIdx.x == 0)
         *a.err = 0;
     // sentinel everywhere first; the scatter overwrites the real entries
     for (int64_t i = threadIdx.x; i < a.capacity; i += blockDim.x)
         a.sorted_ids[i] = sentinel;
+    int tpe = 1;
+    while (tpe < 32 && 2 * tpe * E <= static_cast<int>(blockDim.x))
+        tpe *= 2;
+    const bool act = static_cast<int>(threadIdx.x) < tpe * E;
+    const int e = act ? static_cast<int>(threadIdx.x) % E : 0;
+    const int j = act ? static_cast<int>(threadIdx.x) / E : 0;
     const int n_tiles = a.n_tiles;
-    const int tch = kScanSmemInts / E > 0 ? kScanSmemInts / E : 1;
-    // pass 1: routed pairs per expert
-    int count = 0;
-    for (int t0 = 0; t0 < n_tiles; t0 += tch) {
-        const int nt = n_tiles - t0 < tch ? n_tiles - t0 : tch;
-        for (int i = threadIdx.x; i < nt * E; i += blockDim.x)
-            sh[i] = a.tile_hist[static_cast<int64_t>(t0) * E + i];
-        __syncthreads();
-        if (e < E)
-            for (int t = 0; t < nt; ++t)
-                count += sh[t * E + e];
-        __syncthreads();
+    const int per = (n_tiles + tpe - 1) / tpe;
+    const int t0 = j * per;
+    const int t1 = t0 + per < n_tiles ? t0 + per : n_tiles;
+    int32_t* h = a.tile_hist;
+    int sum = 0;
+    if (act) {
+#pragma unroll 8
+        for (int t = t0; t < t1; ++t)
+            sum += h[static_cast<int64_t>(t) * E + e];
     }
-    const int padded = e < E ? (count + bm - 1) / bm * bm : 0;
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    int before = 0, count = 0;
+    if (act)
+        for (int jj = 0; jj < tpe; ++jj) {
+            const int v = part[jj * E + e];
+            before += jj < j ? v : 0;
+            count += v;
+        }
+    // padded rows per expert, scanned over the threads j = 0 (threads 0 .. E-1, in expert order)
+    const int padded = (act && j == 0) ? (count + bm - 1) / bm * bm : 0;
     int ntp;
     const int off = block_exclusive_scan(padded, &ntp);
-    // pass 2: per-tile bases, in place over the histogram
-    int run = off;
-    for (int t0 = 0; t0 < n_tiles; t0 += tch) {
-        const int nt = n_tiles - t0 < tch ? n_tiles - t0 : tch;
-        for (int i = threadIdx.x; i < nt * E; i += blockDim.x)
-            sh[i] = a.tile_hist[static_cast<int64_t>(t0) * E + i];
-        __syncthreads();
-        if (e < E)
-            for (int t = 0; t < nt; ++t) {
-                const int c = sh[t * E + e];
-                sh[t * E + e] = run;
-                run += c;
-            }
-        __syncthreads();
-        for (int i = threadIdx.x; i < nt * E; i += blockDim.x)
-            a.tile_hist[static_cast<int64_t>(t0) * E + i] = sh[i];
-        __syncthreads();
+    if (act && j == 0)
+        offs[e] = off;
+    __syncthreads();
+    if (act) {
+        int run = offs[e] + before;
+#pragma unroll 8
+        for (int t = t0; t < t1; ++t) {
+            const int64_t i = static_cast<int64_t>(t) * E + e;
+            const int c = h[i];
+            h[i] = run;
+            run += c;
+        }
     }
-    if (e < E && off + padded <= a.capacity)
+    if (act && j == 0 && off + padded <= a.capacity)
         for (int b = off / bm; b < (off + padded) / bm; ++b)
             a.expert_ids[b] = e;
     if (ntp > a.capacity && threadIdx.x == 0)
@@ -186,7 +194,7 @@ __global__ void __launch_bounds__(kAlignTile) align_scatter_kernel(AlignArgs a)
 // rounds.  Same output, bit for bit.
 constexpr int kSmallThreads = 1024;
 constexpr int kSmallMaxPairs = 4096;
-constexpr int kSmallMaxExperts = 128;
+constexpr int kSmallMaxExperts = 512;
 
 __global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
 {
@@ -194,7 +202,7 @@ __global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
     pdl_wait();
     __shared__ int cnt[kSmallMaxExperts];   // pass 1 counts, then pairs placed by earlier rounds
     __shared__ int base[kSmallMaxExperts];  // first padded row of each expert
-    __shared__ int wcnt[kSmallThreads / 32][kSmallMaxExperts];  // per warp of a round
+    __shared__ short wcnt[kSmallThreads / 32][kSmallMaxExperts];  // per warp of a round (<= 32)
     __shared__ short lexp[kSmallMaxPairs];  // local expert of each pair (-1: not local)
     const int E = a.E_local;
     constexpr int W = kSmallThreads / 32;
@@ -235,15 +243,15 @@ __global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
     if (threadIdx.x == 0)
         a.num_tokens_padded[0] = ntp <= a.capacity ? ntp : 0;
     for (int r0 = 0; r0 < npairs; r0 += blockDim.x) {
-        for (int i = threadIdx.x; i < W * kSmallMaxExperts; i += blockDim.x)
-            (&wcnt[0][0])[i] = 0;
+        for (int i = threadIdx.x; i < W * kSmallMaxExperts / 2; i += blockDim.x)
+            reinterpret_cast<int*>(&wcnt[0][0])[i] = 0;
         __syncthreads();
         const int p = r0 + threadIdx.x;
         const int l = p < npairs ? lexp[p] : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, l);
         const unsigned lower = peers & ((1u << lane) - 1u);
         if (l >= 0 && lower == 0)
-            wcnt[warp][l] = __popc(peers);
+            wcnt[warp][l] = static_cast<short>(__popc(peers));
         __syncthreads();
         if (l >= 0) {
             int rank = cnt[l] + __popc(lower);
