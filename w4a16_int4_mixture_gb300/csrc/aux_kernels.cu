@@ -557,21 +557,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 }
 
 // out[i] = bf16(acc[i]) for the fp32 token accumulators of the reduction form.
+// (four 8-element groups per thread and step, all loads before the stores)
+constexpr int kFinUnroll = 4;
+
 __global__ void finalize_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out, int64_t n)
 {
     pdl_launch_dependents();
     pdl_wait();
     const int64_t n8 = n / 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
-        const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-        const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-        uint4 o;
-        o.x = pack_bf16x2(a.x, a.y);
-        o.y = pack_bf16x2(a.z, a.w);
-        o.z = pack_bf16x2(b.x, b.y);
-        o.w = pack_bf16x2(b.z, b.w);
-        reinterpret_cast<uint4*>(out)[i] = o;
+    const float4* a4 = reinterpret_cast<const float4*>(acc);
+    uint4* o4 = reinterpret_cast<uint4*>(out);
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n8;
+         i0 += kFinUnroll * stride) {
+        float4 a[kFinUnroll], b[kFinUnroll];
+#pragma unroll
+        for (int u = 0; u < kFinUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n8) {
+                a[u] = a4[2 * i];
+                b[u] = a4[2 * i + 1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kFinUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n8) {
+                uint4 o;
+                o.x = pack_bf16x2(a[u].x, a[u].y);
+                o.y = pack_bf16x2(a[u].z, a[u].w);
+                o.z = pack_bf16x2(b[u].x, b[u].y);
+                o.w = pack_bf16x2(b[u].z, b[u].w);
+                o4[i] = o;
+            }
+        }
     }
     for (int64_t i = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += stride)
@@ -639,7 +658,7 @@ cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int sms,
 {
     if (n <= 0)
         return cudaSuccess;
-    int64_t blocks = (n / 8 + 255) / 256;
+    int64_t blocks = (n / 8 + 256 * kFinUnroll - 1) / (256 * kFinUnroll);
     if (blocks < 1)
         blocks = 1;
     if (blocks > 4LL * sms)
