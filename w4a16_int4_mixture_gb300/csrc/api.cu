@@ -354,6 +354,11 @@ int split_maxn_of(const Schedule& sc)
     const int a = gemm_cfg_maxn(sc.cfg_gate_up), b = gemm_cfg_maxn(sc.cfg_down);
     return a > b ? a : b;
 }
+// Masked layout: its valid rows are copied (by prep) to a gap-free block for
+// the gate/up GEMM, whose token tiles would otherwise read the rows past each
+// expert's count (max_m apart, so mostly never touched before) into every box.
+bool masked_compacts(int mode, int E_local) { return mode == CHORD_GROUPED_MASKED && E_local <= 1024; }
+
 int split_maxn_any()
 {
     int m = 0;
@@ -685,7 +690,7 @@ size_t chord_w4a16_grouped_workspace_size(int mode, int64_t M, int H, int I, int
         return 0;
     const int64_t max_m = mode == CHORD_GROUPED_MASKED ? M / E_local : 0;
     return layout_ws(grouped_max_chunks(mode, M, E_local, max_m), M, I, T, k, H, true,
-                     with_tokens != 0, 0, split_maxn_any())
+                     with_tokens != 0, masked_compacts(mode, E_local) ? M : 0, split_maxn_any())
         .total;
 }
 
@@ -911,8 +916,9 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
                                                       : static_cast<double>(M) / E_local;
     Schedule sc = pick_schedule(tok_e, T, H, I, 0);
     sc.reduce = true;
+    const bool compact = masked_compacts(mode, E_local);
     const Workspace w = layout_ws(grouped_max_chunks(mode, M, E_local, max_m), M, I, T, k, H, true,
-                                  with_tokens, 0, split_maxn_any());
+                                  with_tokens, compact ? M : 0, split_maxn_any());
     if ((st = check_ws(workspace, workspace_bytes, w.total)) != CHORD_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -948,10 +954,16 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
         pa.meta_pairs = T * k;
         pa.meta_rows = M;
     }
+    uint16_t* xs = compact ? reinterpret_cast<uint16_t*>(ws + w.off_xs) : nullptr;
+    if (compact) {
+        pa.mc_src = a;
+        pa.mc_out = xs;
+        pa.mc_H = H;
+    }
     pa.err = err;
     int work_blocks = zero_blocks_for(with_tokens ? T * H : 0, dev.sms);
-    if (with_tokens && work_blocks < dev.sms)
-        work_blocks = dev.sms;  // the per-row records are written by the worker blocks
+    if ((with_tokens || compact) && work_blocks < dev.sms)
+        work_blocks = dev.sms;  // the row records and the compacted rows come from the worker blocks
     if (launch_prep(pa, work_blocks, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     if ((flags & CHORD_FLAG_VALIDATE) &&
@@ -961,7 +973,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
         return CHORD_ERR_CUDA;
 
     LayerIO io{};
-    io.src = a;
+    io.src = compact ? xs : a;
     io.src_rows = M;
     io.row_meta = with_tokens ? reinterpret_cast<const int4*>(ws + w.off_meta) : nullptr;
     io.pair_of_row = with_tokens ? row_to_pair : nullptr;

@@ -299,7 +299,7 @@ __device__ __forceinline__ int chunks_for(int rows, int maxn) { return (rows + m
 // rows (balanced, each but the last a multiple of 16).  False when the list
 // would overflow (only reachable with a malformed layout).
 __device__ bool emit_chunks(Chunk* out, int slot, int row0, int rows, int expert, int maxn,
-                            int max_chunks, int* err)
+                            int max_chunks, int* err, int brow_base)
 {
     const int n = chunks_for(rows, maxn);
     if (slot + n > max_chunks) {
@@ -315,7 +315,7 @@ __device__ bool emit_chunks(Chunk* out, int slot, int row0, int rows, int expert
         ch.row0 = row0 + r;
         ch.nrows = min(cs, rows - r);
         ch.expert = expert;
-        ch.seg0 = row0;
+        ch.brow0 = brow_base + r;
         out[slot + c] = ch;
     }
     return true;
@@ -351,6 +351,10 @@ __device__ void build_chunk_lists(const PrepArgs& a)
     }
     __syncthreads();
     if (a.layout == kLayoutMasked) {
+        __shared__ int s_roff;  // compacted rows of the experts before this slice
+        if (threadIdx.x == 0)
+            s_roff = 0;
+        __syncthreads();
         for (int e0 = 0; e0 < a.E_local; e0 += blockDim.x) {
             const int e = e0 + threadIdx.x;
             int rows = 0;
@@ -361,18 +365,25 @@ __device__ void build_chunk_lists(const PrepArgs& a)
                     rows = rows < 0 ? 0 : static_cast<int>(a.max_m);
                 }
             }
+            int rtotal;
+            const int roff = s_roff + block_exclusive_scan(rows, &rtotal);
             for (int L = 0; L < 2; ++L) {
                 const int n = rows > 0 ? chunks_for(rows, a.maxn[L]) : 0;
                 int total;
                 const int off = s_off[L] + block_exclusive_scan(n, &total);
-                if (n > 0 && !emit_chunks(a.chunks[L], off, static_cast<int>(e * a.max_m), rows, e,
-                                          a.maxn[L], a.max_chunks, a.err))
+                const int row0 = static_cast<int>(e * a.max_m);
+                const int brow = (L == 0 && a.mc_out != nullptr) ? roff : row0;
+                if (n > 0 && !emit_chunks(a.chunks[L], off, row0, rows, e, a.maxn[L], a.max_chunks,
+                                          a.err, brow))
                     s_bad = 1;
                 __syncthreads();
                 if (threadIdx.x == 0)
                     s_off[L] += total;
                 __syncthreads();
             }
+            if (threadIdx.x == 0)
+                s_roff += rtotal;
+            __syncthreads();
         }
     } else {
         int nblocks;
@@ -413,7 +424,7 @@ __device__ void build_chunk_lists(const PrepArgs& a)
                 int total;
                 const int off = s_off[L] + block_exclusive_scan(n, &total);
                 if (n > 0 && !emit_chunks(a.chunks[L], off, b * a.block_rows, rows, e, a.maxn[L],
-                                          a.max_chunks, a.err))
+                                          a.max_chunks, a.err, b * a.block_rows))
                     s_bad = 1;
                 __syncthreads();
                 if (threadIdx.x == 0)
@@ -443,6 +454,56 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
     }
     const int64_t tid = static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x - 1) * blockDim.x;
+    if (a.mc_out != nullptr) {
+        // the experts' first compacted rows (the same scan as the chunk lists),
+        // then 128 threads per compacted row
+        __shared__ int s_mcoff[1025];
+        const int E = a.E_local;  // <= 1024 (the host compacts only then)
+        int rows = 0;
+        if (static_cast<int>(threadIdx.x) < E) {
+            rows = a.masked_m[threadIdx.x];
+            rows = rows < 0 ? 0 : (rows > a.max_m ? static_cast<int>(a.max_m) : rows);
+        }
+        int total;
+        const int off = block_exclusive_scan(rows, &total);
+        if (static_cast<int>(threadIdx.x) < E)
+            s_mcoff[threadIdx.x] = off;
+        if (threadIdx.x == 0)
+            s_mcoff[E] = total;
+        __syncthreads();
+        constexpr int kGroup = 128;
+        const int gl = static_cast<int>(tid % kGroup);
+        const int64_t ngrp = nth / kGroup;
+        const int n16 = a.mc_H / 8;
+        for (int64_t i = tid / kGroup; i < total; i += ngrp) {
+            // expert of compacted row i: the last e with s_mcoff[e] <= i
+            int lo = 0, hi = E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_mcoff[mid] <= i)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            const int64_t srow = static_cast<int64_t>(lo) * a.max_m + (i - s_mcoff[lo]);
+            const uint4* src = reinterpret_cast<const uint4*>(a.mc_src + srow * a.mc_H);
+            uint4* dst = reinterpret_cast<uint4*>(a.mc_out + i * a.mc_H);
+            for (int c0 = gl; c0 < n16; c0 += 8 * kGroup) {
+                uint4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c = c0 + j * kGroup;
+                    v[j] = c < n16 ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c = c0 + j * kGroup;
+                    if (c < n16)
+                        dst[c] = v[j];
+                }
+            }
+        }
+    }
     if (a.zero_f32 != nullptr) {
         float4* z = reinterpret_cast<float4*>(a.zero_f32);
         const int64_t n4 = a.zero_count / 4;

@@ -12,7 +12,8 @@ struct Chunk {
     int32_t row0;    // first padded row
     int32_t nrows;   // rows in this chunk (the token tile is nrows rounded up to 16)
     int32_t expert;  // local expert
-    int32_t seg0;    // first row of the expert's segment (unused by the GEMMs)
+    int32_t brow0;   // first row of the chunk in the GEMM's token-row source: row0, except
+                     // that the masked layout's gate/up reads its rows compacted
 };
 
 // Down-GEMM epilogue forms (bit set).

@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         Chunk next2 = chunk_of_item(blockIdx.x + gridDim.x);
         for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x) {
             const WorkItem it = item_of(v);
-            const int row0 = next.row0;
+            const int row0 = next.brow0;  // (token rows: compacted for the masked gate/up)
             // boxes of B_BOX_ROWS rows, as many as the token tile needs
             const int nbox = ((next.nrows + 15) / 16 * 16 + C::B_BOX_ROWS - 1) / C::B_BOX_ROWS;
             next = next2;

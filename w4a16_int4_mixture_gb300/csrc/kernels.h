@@ -83,6 +83,12 @@ struct PrepArgs {
     int meta_topk;
     int64_t meta_pairs;
     int64_t meta_rows;
+    // masked layout: its valid rows (row e * max_m + r, r < masked_m[e]) copied
+    // to mc_out in expert order with no gaps, the gate/up GEMM's token rows
+    // (its chunk list's brow0 points there)
+    const uint16_t* mc_src;
+    uint16_t* mc_out;
+    int mc_H;
     // buffers to clear
     int32_t* zero_i32;  // (the K-split piece counters; cleared by block 0)
     int zero_i32_count;
