@@ -301,7 +301,7 @@ struct Workspace {
     size_t off_acc = 0;       // reduce: float [T, H]; store: float [T*k, H]
     size_t off_pair_row = 0;  // store: int32 [T*k]
     size_t off_split_cnt = 0;   // int32 [2][kSplitSlots]: K-split piece counters per GEMM
-    size_t off_split_part = 0;  // fp32 [kSplitSlots][split_maxn][128]: K-split partial sums
+    size_t off_split_part = 0;  // fp32 [2][kSplitSlots][split_maxn][128]: K-split partial sums per GEMM
     int split_maxn = 0;
     size_t total = 0;
     int64_t max_chunks = 0;
@@ -318,7 +318,8 @@ Workspace layout_ws(int64_t max_chunks, int64_t h_rows, int I, int64_t T, int k,
     o = align_up(o + 2 * kSplitSlots * sizeof(int32_t), kAlign);
     w.off_split_part = o;
     w.split_maxn = split_maxn;
-    o = align_up(o + static_cast<size_t>(kSplitSlots) * split_maxn * 128 * sizeof(float), kAlign);
+    // (one region per GEMM: the down GEMM may start while the gate/up GEMM ends)
+    o = align_up(o + 2 * static_cast<size_t>(kSplitSlots) * split_maxn * 128 * sizeof(float), kAlign);
     w.max_chunks = max_chunks;
     for (int L = 0; L < 2; ++L) {
         w.off_chunks[L] = o;
@@ -598,6 +599,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     d.out_acc = (io.down_epi & kEpiReduceTok) ? acc : nullptr;
     d.rows_out = io.rows_out;
     d.split_cnt = split_cnt + kSplitSlots;
+    d.split_part = g.split_part + static_cast<size_t>(kSplitSlots) * w.split_maxn * 128;
     d.split_slots = slots_for(sc.cfg_down);
     if (launch_gemm(cfg_down, false, map2, smap2, bmap2, d, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;

@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    pdl_launch_dependents();
+    if constexpr (!C::GATE_UP)
+        pdl_launch_dependents();
 
     // barriers
     const uint32_t bar0 = sbase + C::OFF_BARS;
@@ -272,9 +273,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // (barriers and tensor memory are set up while the previous kernel ends;
-    // everything after this reads or writes memory it may still use)
-    pdl_wait();
+    // Barriers and tensor memory are set up while the previous kernel ends.
+    // gate_up reads prep's outputs everywhere, so it waits here, and only then
+    // lets the down GEMM be scheduled; the down GEMM, whose chunk lists, row
+    // records and weights are ready by then, waits only where it reads h (the
+    // token producer): on an SM the gate/up tail has freed it already streams
+    // and dequantises weights.
+    if constexpr (C::GATE_UP) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
 
     const int n_tiles = args.n_tiles;
     const int KT = args.K / C::BK;
@@ -405,6 +413,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         issued_stages = g;
     } else if (warp == 1) {
         // ----------------------------------------------------------- token producer
+        if constexpr (!C::GATE_UP)
+            pdl_wait();
         const uint64_t pol = policy_evict_last();
         int g = 0;
         bool ok = true;
