@@ -55,3 +55,15 @@ def test_tile64_many_units(chord):
     verify_indexed(inp, a, label="64-row tile, many units")
     b = run_indexed_full(chord, inp, flags=2)
     assert np.array_equal(a.out, b.out)
+
+
+@pytest.mark.parametrize("bm", [16, 32])
+def test_indexed_compacted_token_rows(chord, bm):
+    # 256 experts x ~2 rows: the layout's padding rows would pass 16 MB, so the
+    # gathered token rows are compacted (gate/up token boxes start at each
+    # chunk's compacted row); h rows of the padding stay zero
+    inp = small(128, 4, 256, 256, 7168, 256, 66 + bm, emap=False)
+    run = run_indexed_full(chord, inp, block_m=bm)
+    verify_indexed(inp, run, label=f"compacted token rows block_m={bm}")
+    pad = np.nonzero(run.si[:run.ntp] >= inp.shape.T * inp.shape.k)[0]
+    assert pad.size > 0 and np.all(run.h[pad] == 0)

@@ -812,6 +812,15 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     pa.meta_rows = -1;
     pa.gx_src = x;
     pa.gx_out = xs;
+    // compact the gathered rows when the layout's padding rows (about
+    // (block_m - 1) / 2 per touched expert) would otherwise put more than
+    // 16 MB of never-written rows into the token boxes (below that, the
+    // compaction scans cost prep more than the GEMM gains)
+    {
+        const double touched = E_local * (1.0 - std::exp(-tok_e));
+        const double pad_bytes = touched * (block_m - 1) * 0.5 * H * 2.0;
+        pa.gx_compact = (E_local <= 1024 && pad_bytes >= 16.0 * 1024 * 1024) ? 1 : 0;
+    }
     pa.gx_ids = sorted_ids;
     pa.gx_topk = k;
     pa.gx_pairs = T * k;

@@ -339,6 +339,65 @@ __device__ __forceinline__ int block_expert(const PrepArgs& a, int b, int nblock
     return (e >= 0 && e < a.E_local) ? e : -1;
 }
 
+// Indexed layout, compacted token rows: the rows of each expert's segment
+// that hold a pair come first (the layout pads each segment at its end), so
+// padded row r of expert e holds compacted row coff[e] + (r - seg[e]), where
+// seg[e] is the segment's first row and coff[e] the pairs of the experts
+// before it.  Needs E_local <= blockDim.x; every thread of the block calls it.
+struct CompactIdx {
+    int* seg;   // [E_local] first padded row, or -1
+    int* coff;  // [E_local] first compacted row
+};
+__device__ CompactIdx indexed_compaction(const PrepArgs& a)
+{
+    __shared__ int s_seg[1024];
+    __shared__ int s_end[1024];
+    __shared__ int s_coff[1024];
+    const int E = a.E_local;
+    const int bm = a.block_rows;
+    const int ntp = a.num_tokens_padded[0];
+    const int nblocks = (ntp >= 0 && ntp <= a.capacity) ? ntp / bm : 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        s_seg[e] = -1;
+        s_end[e] = -1;
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < nblocks; b += blockDim.x) {
+        const int e = a.expert_ids[b];
+        if (e < 0 || e >= E)
+            continue;
+        const int prev = b > 0 ? a.expert_ids[b - 1] : -1;
+        const int next = b + 1 < nblocks ? a.expert_ids[b + 1] : -1;
+        if (prev != e)
+            s_seg[e] = b * bm;
+        if (next != e) {
+            int v = 0;  // rows of the segment's last block that hold a pair
+            const int32_t* ids = a.gx_ids + static_cast<int64_t>(b) * bm;
+            for (int i0 = 0; i0 < bm; i0 += 16) {
+                int p[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    p[i] = i0 + i < bm ? ids[i0 + i] : -1;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v += (p[i] >= 0 && p[i] < a.gx_pairs) ? 1 : 0;
+            }
+            s_end[e] = b * bm + v;
+        }
+    }
+    __syncthreads();
+    const int e = threadIdx.x;
+    int cnt = 0;
+    if (e < E && s_seg[e] >= 0 && s_end[e] >= s_seg[e])
+        cnt = s_end[e] - s_seg[e];
+    int total;
+    const int off = block_exclusive_scan(cnt, &total);
+    if (e < E)
+        s_coff[e] = off;
+    __syncthreads();
+    return CompactIdx{s_seg, s_coff};
+}
+
 __device__ void build_chunk_lists(const PrepArgs& a)
 {
     __shared__ int s_off[2];
@@ -393,6 +452,10 @@ __device__ void build_chunk_lists(const PrepArgs& a)
         } else {
             nblocks = static_cast<int>(a.M / a.block_rows);
         }
+        // compacted token rows of the gate/up GEMM (indexed layout)
+        CompactIdx cx{nullptr, nullptr};
+        if (a.layout == kLayoutIndexed && a.gx_compact)
+            cx = indexed_compaction(a);
         // the experts of this tile of blocks (plus one on each side) in shared
         // memory, read with one coalesced pass; a run that leaves the staged
         // tile continues with direct reads
@@ -423,8 +486,11 @@ __device__ void build_chunk_lists(const PrepArgs& a)
                 const int n = rows > 0 ? chunks_for(rows, a.maxn[L]) : 0;
                 int total;
                 const int off = s_off[L] + block_exclusive_scan(n, &total);
+                const int brow = (L == 0 && cx.coff != nullptr)
+                                     ? cx.coff[e] + (b * a.block_rows - cx.seg[e])
+                                     : b * a.block_rows;
                 if (n > 0 && !emit_chunks(a.chunks[L], off, b * a.block_rows, rows, e, a.maxn[L],
-                                          a.max_chunks, a.err, b * a.block_rows))
+                                          a.max_chunks, a.err, brow))
                     s_bad = 1;
                 __syncthreads();
                 if (threadIdx.x == 0)
@@ -535,6 +601,11 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
         // thread before the stores.  Rows with no pair (the block padding of
         // the layout) are not written: they only feed MMA columns that no
         // output reads, and the gate/up epilogue writes zeros for their h rows.
+        // Compacted: row r of expert e goes to coff[e] + (r - seg[e]), so no
+        // token box reads a padding row.
+        CompactIdx cx{nullptr, nullptr};
+        if (a.gx_compact)
+            cx = indexed_compaction(a);
         constexpr int kGroup = 128;
         const int gl = static_cast<int>(tid % kGroup);
         const int64_t ngrp = nth / kGroup;
@@ -549,8 +620,15 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
                                       : make_int4(-1, 0, 0, 0);
             if (!valid)
                 continue;
+            int64_t drow = r;
+            if (cx.coff != nullptr) {
+                const int e = a.expert_ids[r / a.block_rows];
+                if (e < 0 || e >= a.E_local || cx.seg[e] < 0)
+                    continue;
+                drow = cx.coff[e] + (r - cx.seg[e]);
+            }
             const uint4* src = reinterpret_cast<const uint4*>(a.gx_src + static_cast<int64_t>(p / a.gx_topk) * a.gx_H);
-            uint4* dst = reinterpret_cast<uint4*>(a.gx_out + r * a.gx_H);
+            uint4* dst = reinterpret_cast<uint4*>(a.gx_out + drow * a.gx_H);
             for (int c0 = gl; c0 < n16; c0 += 8 * kGroup) {
                 uint4 v[8];
 #pragma unroll

@@ -74,6 +74,10 @@ struct PrepArgs {
     int gx_topk;
     int64_t gx_pairs;        // T*k, the sentinel
     int gx_H;
+    // compacted: only the rows holding a pair, in padded-row order with the
+    // padding left out (E_local <= 1024); the gate/up chunk list's brow0
+    // points into them
+    int gx_compact;
     // per padded row r: {pair p, token p / topk, bits of topk_weights[p], 0},
     // or {-1, 0, 0, 0} for a row with no pair; rows r < meta_rows, or
     // r < num_tokens_padded when meta_rows < 0
