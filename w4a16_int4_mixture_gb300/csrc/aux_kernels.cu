@@ -347,6 +347,7 @@ __device__ __forceinline__ int block_expert(const PrepArgs& a, int b, int nblock
 struct CompactIdx {
     int* seg;   // [E_local] first padded row, or -1
     int* coff;  // [E_local] first compacted row
+    int total;  // compacted rows
 };
 __device__ CompactIdx indexed_compaction(const PrepArgs& a)
 {
@@ -395,8 +396,10 @@ __device__ CompactIdx indexed_compaction(const PrepArgs& a)
     if (e < E)
         s_coff[e] = off;
     __syncthreads();
-    return CompactIdx{s_seg, s_coff};
+    return CompactIdx{s_seg, s_coff, total};
 }
+
+__device__ __forceinline__ int end_block_of(int b, int rows, int bm) { return b + rows / bm; }
 
 __device__ void build_chunk_lists(const PrepArgs& a)
 {
@@ -452,10 +455,12 @@ __device__ void build_chunk_lists(const PrepArgs& a)
         } else {
             nblocks = static_cast<int>(a.M / a.block_rows);
         }
-        // compacted token rows of the gate/up GEMM (indexed layout)
-        CompactIdx cx{nullptr, nullptr};
-        if (a.layout == kLayoutIndexed && a.gx_compact)
-            cx = indexed_compaction(a);
+        // compacted token rows of the gate/up GEMM (indexed layout): each run's
+        // paired rows counted from its last block, scanned like the chunks
+        const bool compact = a.layout == kLayoutIndexed && a.gx_compact;
+        __shared__ int s_roff;
+        if (threadIdx.x == 0)
+            s_roff = 0;
         // the experts of this tile of blocks (plus one on each side) in shared
         // memory, read with one coalesced pass; a run that leaves the staged
         // tile continues with direct reads
@@ -482,19 +487,40 @@ __device__ void build_chunk_lists(const PrepArgs& a)
                     rows = (end - b) * a.block_rows;
                 }
             }
+            int paired = 0;
+            if (compact && rows > 0) {
+                const int bm = a.block_rows;
+                const int32_t* ids = a.gx_ids + static_cast<int64_t>(end_block_of(b, rows, bm) - 1) * bm;
+                int v = 0;
+                for (int i0 = 0; i0 < bm; i0 += 16) {
+                    int p[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        p[i] = i0 + i < bm ? ids[i0 + i] : -1;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        v += (p[i] >= 0 && p[i] < a.gx_pairs) ? 1 : 0;
+                }
+                paired = rows - bm + v;
+            }
+            int rtotal = 0;
+            const int roff = compact ? s_roff + block_exclusive_scan(paired, &rtotal) : 0;
             for (int L = 0; L < 2; ++L) {
                 const int n = rows > 0 ? chunks_for(rows, a.maxn[L]) : 0;
                 int total;
                 const int off = s_off[L] + block_exclusive_scan(n, &total);
-                const int brow = (L == 0 && cx.coff != nullptr)
-                                     ? cx.coff[e] + (b * a.block_rows - cx.seg[e])
-                                     : b * a.block_rows;
+                const int brow = (L == 0 && compact) ? roff : b * a.block_rows;
                 if (n > 0 && !emit_chunks(a.chunks[L], off, b * a.block_rows, rows, e, a.maxn[L],
                                           a.max_chunks, a.err, brow))
                     s_bad = 1;
                 __syncthreads();
                 if (threadIdx.x == 0)
                     s_off[L] += total;
+                __syncthreads();
+            }
+            if (compact) {
+                if (threadIdx.x == 0)
+                    s_roff += rtotal;
                 __syncthreads();
             }
         }
@@ -602,31 +628,16 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
         // the layout) are not written: they only feed MMA columns that no
         // output reads, and the gate/up epilogue writes zeros for their h rows.
         // Compacted: row r of expert e goes to coff[e] + (r - seg[e]), so no
-        // token box reads a padding row.
-        CompactIdx cx{nullptr, nullptr};
-        if (a.gx_compact)
-            cx = indexed_compaction(a);
+        // token box reads a padding row; then the row records come from a
+        // loop of their own (one thread per padded row) and the copies walk
+        // the compacted rows, so no copy group waits on a padding row.
         constexpr int kGroup = 128;
         const int gl = static_cast<int>(tid % kGroup);
         const int64_t ngrp = nth / kGroup;
         const int ntp = a.num_tokens_padded[0];
         const int64_t rows = (ntp >= 0 && ntp <= a.capacity) ? ntp : 0;
         const int n16 = a.gx_H / 8;
-        for (int64_t r = tid / kGroup; r < rows; r += ngrp) {
-            const int p = a.gx_ids[r];
-            const bool valid = p >= 0 && p < a.gx_pairs;  // sentinel rows become zeros
-            if (gl == 0 && a.meta_out != nullptr)
-                a.meta_out[r] = valid ? make_int4(p, p / a.gx_topk, __float_as_int(a.meta_w[p]), 0)
-                                      : make_int4(-1, 0, 0, 0);
-            if (!valid)
-                continue;
-            int64_t drow = r;
-            if (cx.coff != nullptr) {
-                const int e = a.expert_ids[r / a.block_rows];
-                if (e < 0 || e >= a.E_local || cx.seg[e] < 0)
-                    continue;
-                drow = cx.coff[e] + (r - cx.seg[e]);
-            }
+        auto copy_row = [&](int p, int64_t drow) {
             const uint4* src = reinterpret_cast<const uint4*>(a.gx_src + static_cast<int64_t>(p / a.gx_topk) * a.gx_H);
             uint4* dst = reinterpret_cast<uint4*>(a.gx_out + drow * a.gx_H);
             for (int c0 = gl; c0 < n16; c0 += 8 * kGroup) {
@@ -643,6 +654,48 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
                         dst[c] = v[j];
                 }
             }
+        };
+        if (a.gx_compact) {
+            const CompactIdx cx = indexed_compaction(a);
+            if (a.meta_out != nullptr)
+                for (int64_t r = tid; r < rows; r += nth) {
+                    const int p = a.gx_ids[r];
+                    const bool valid = p >= 0 && p < a.gx_pairs;
+                    a.meta_out[r] = valid ? make_int4(p, p / a.gx_topk, __float_as_int(a.meta_w[p]), 0)
+                                          : make_int4(-1, 0, 0, 0);
+                }
+            const int E = a.E_local;
+            for (int64_t c = tid / kGroup; c < cx.total; c += ngrp) {
+                // expert of compacted row c: the last e with a segment and coff[e] <= c
+                int lo = 0, hi = E - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (cx.coff[mid] <= c)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
+                }
+                while (lo > 0 && cx.seg[lo] < 0)
+                    --lo;  // (experts without rows share the offset of the next one)
+                if (cx.seg[lo] < 0)
+                    continue;
+                const int64_t r = cx.seg[lo] + (c - cx.coff[lo]);
+                if (r >= rows)
+                    continue;
+                const int p = a.gx_ids[r];
+                if (p >= 0 && p < a.gx_pairs)
+                    copy_row(p, c);
+            }
+            return;
+        }
+        for (int64_t r = tid / kGroup; r < rows; r += ngrp) {
+            const int p = a.gx_ids[r];
+            const bool valid = p >= 0 && p < a.gx_pairs;  // sentinel rows become zeros
+            if (gl == 0 && a.meta_out != nullptr)
+                a.meta_out[r] = valid ? make_int4(p, p / a.gx_topk, __float_as_int(a.meta_w[p]), 0)
+                                      : make_int4(-1, 0, 0, 0);
+            if (valid)
+                copy_row(p, r);
         }
     }
 }
