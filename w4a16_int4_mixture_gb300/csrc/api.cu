@@ -734,6 +734,7 @@ chord_status chord_moe_align(const int32_t* topk_ids, int64_t T, int k, int E_gl
     a.tile_hist = reinterpret_cast<int32_t*>(ws + kAlign);
     a.n_tiles = static_cast<int>((T * k + 255) / 256);
     a.err = reinterpret_cast<int*>(ws);
+    PdlScope pdl(T * k <= kPdlMaxRows);
     return from_cuda(launch_align(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -778,6 +779,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     float* acc = reinterpret_cast<float*>(ws + w.off_acc);
     int32_t* pair_row = sc.reduce ? nullptr : reinterpret_cast<int32_t*>(ws + w.off_pair_row);
 
+    PdlScope pdl(T * k <= kPdlMaxRows);
     StageMarks marks;
     marks.begin(s);
     PrepArgs pa{};
@@ -937,6 +939,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     int* err = reinterpret_cast<int*>(ws + w.off_hdr);
     float* acc = with_tokens ? reinterpret_cast<float*>(ws + w.off_acc) : nullptr;
 
+    PdlScope pdl((with_tokens ? T * k : M) <= kPdlMaxRows);
     StageMarks marks;
     marks.begin(s);
     PrepArgs pa{};

@@ -703,61 +703,76 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 float* tile = reinterpret_cast<float*>(smem + C::OFF_EPIT) + (egrp * 4 + q) * 16 * 32;
                 const int m4 = (lane & 7) * 4;
                 const int cg = lane >> 3;
-                // (rolled loops: the epilogue runs once per unit, and its code
-                // competes for the instruction cache with every other role's)
-#pragma unroll 1
-                for (int t = 0; t < tpu; ++t) {
+                // one 16-column block of tile t: accumulator columns -> shared tile
+                // -> per-pair stores / token reductions / row stores
+                auto block = [&](int t, int c0, int4 mrec) {
                     const int nq = (nt0 + t) * 128 + q * 32;
-#pragma unroll 1
-                    for (int c0 = 0; c0 < ntok16; c0 += 16) {
-                        uint32_t v[16];
-                        tmem_ld_x16(dbase + t * C::MAXN + c0, v);
-                        tmem_wait_ld();
-                        if (t == tpu - 1 && c0 + 16 >= ntok16) {
-                            // last block read: the accumulator goes back to the MMA
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0)
-                                mbar_arrive(d_empty(acc));
-                        }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            tile[j * 32 + lane] = __uint_as_float(v[j]) * kWeightRescale;
+                    uint32_t v[16];
+                    tmem_ld_x16(dbase + t * C::MAXN + c0, v);
+                    tmem_wait_ld();
+                    if (t == tpu - 1 && c0 + 16 >= ntok16) {
+                        // last block read: the accumulator goes back to the MMA
+                        tc_fence_before();
                         __syncwarp();
-                        // columns c0 .. c0 + 15 sit in one lane group: records meta_cur[c0 / 32]
-                        int4 mrec = meta_cur[0];
+                        if (lane == 0)
+                            mbar_arrive(d_empty(acc));
+                    }
 #pragma unroll
-                        for (int k = 1; k < MPT; ++k)
-                            if (c0 >= 32 * k)
-                                mrec = meta_cur[k];
+                    for (int j = 0; j < 16; ++j)
+                        tile[j * 32 + lane] = __uint_as_float(v[j]) * kWeightRescale;
+                    __syncwarp();
 #pragma unroll
-                        for (int ii = 0; ii < 4; ++ii) {
-                            const int j = cg + 4 * ii;
-                            const int c = c0 + j;
-                            const int src = c & 31;
-                            const int p = __shfl_sync(0xffffffffu, mrec.x, src);
-                            const int tok = __shfl_sync(0xffffffffu, mrec.y, src);
-                            const float w = __int_as_float(__shfl_sync(0xffffffffu, mrec.z, src));
-                            if (c >= ntok)
-                                continue;
-                            const float4 y = *reinterpret_cast<const float4*>(tile + j * 32 + m4);
-                            if (args.epi & kEpiStoreRows) {
-                                uint2 o;
-                                o.x = bf16x2_pack_rn(y.x, y.y);
-                                o.y = bf16x2_pack_rn(y.z, y.w);
-                                *reinterpret_cast<uint2*>(args.rows_out + static_cast<int64_t>(ch.row0 + c) * N +
-                                                          nq + m4) = o;
-                            }
-                            if (per_pair && p >= 0) {
-                                if (args.epi & kEpiStorePair)
-                                    *reinterpret_cast<float4*>(args.y_pairs + static_cast<int64_t>(p) * N + nq +
-                                                               m4) = y;
-                                if (args.epi & kEpiReduceTok)
-                                    red_add_v4_f32(args.out_acc + static_cast<int64_t>(tok) * N + nq + m4,
-                                                   w * y.x, w * y.y, w * y.z, w * y.w);
-                            }
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const int j = cg + 4 * ii;
+                        const int c = c0 + j;
+                        const int src = c & 31;
+                        const int p = __shfl_sync(0xffffffffu, mrec.x, src);
+                        const int tok = __shfl_sync(0xffffffffu, mrec.y, src);
+                        const float w = __int_as_float(__shfl_sync(0xffffffffu, mrec.z, src));
+                        if (c >= ntok)
+                            continue;
+                        const float4 y = *reinterpret_cast<const float4*>(tile + j * 32 + m4);
+                        if (args.epi & kEpiStoreRows) {
+                            uint2 o;
+                            o.x = bf16x2_pack_rn(y.x, y.y);
+                            o.y = bf16x2_pack_rn(y.z, y.w);
+                            *reinterpret_cast<uint2*>(args.rows_out + static_cast<int64_t>(ch.row0 + c) * N + nq +
+                                                      m4) = o;
                         }
-                        __syncwarp();  // the tile is rewritten by the next block
+                        if (per_pair && p >= 0) {
+                            if (args.epi & kEpiStorePair)
+                                *reinterpret_cast<float4*>(args.y_pairs + static_cast<int64_t>(p) * N + nq + m4) = y;
+                            if (args.epi & kEpiReduceTok)
+                                red_add_v4_f32(args.out_acc + static_cast<int64_t>(tok) * N + nq + m4, w * y.x,
+                                               w * y.y, w * y.z, w * y.w);
+                        }
+                    }
+                    __syncwarp();  // the tile is rewritten by the next block
+                };
+                if constexpr (C::COLD_WAITS) {
+                    // (rolled loops for the BK 256 tiles: their epilogue runs once
+                    // per short unit, and its code competes for the instruction
+                    // cache with every other role's)
+#pragma unroll 1
+                    for (int t = 0; t < tpu; ++t) {
+#pragma unroll 1
+                        for (int c0 = 0; c0 < ntok16; c0 += 16) {
+                            // columns c0 .. c0 + 15 sit in one lane group: records meta_cur[c0 / 32]
+                            int4 mrec = meta_cur[0];
+#pragma unroll
+                            for (int k = 1; k < MPT; ++k)
+                                if (c0 >= 32 * k)
+                                    mrec = meta_cur[k];
+                            block(t, c0, mrec);
+                        }
+                    }
+                } else {
+                    // (the prefill tile's long units: unrolled over the token tile)
+#pragma unroll
+                    for (int c0 = 0; c0 < C::MAXN; c0 += 16) {
+                        if (c0 >= ntok16)
+                            break;
+                        block(0, c0, meta_cur[c0 / 32]);
                     }
                 }
             }

@@ -9,6 +9,19 @@
 
 namespace chord {
 
+// Whether launch_pdl asks for programmatic stream serialization on this host
+// thread, set per call: on for decode-sized calls (it hides the launch
+// gaps: config 1 237 -> 233 us), off for large ones (prefill measured 661 ->
+// 692 us with it).  The kernels are correct either way: griddepcontrol.wait
+// returns at once when the launch was serialized.
+inline thread_local bool g_launch_pdl = true;
+constexpr int64_t kPdlMaxRows = 4096;  // routed rows up to which a call uses it
+struct PdlScope {
+    bool prev;
+    explicit PdlScope(bool on) : prev(g_launch_pdl) { g_launch_pdl = on; }
+    ~PdlScope() { g_launch_pdl = prev; }
+};
+
 // Launch with programmatic stream serialization (the kernel waits for its
 // predecessor itself, with griddepcontrol.wait, before it touches memory).
 template <typename... KArgs, typename... Args>
@@ -22,7 +35,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].val.programmaticStreamSerializationAllowed = g_launch_pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);

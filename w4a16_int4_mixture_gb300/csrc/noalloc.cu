@@ -92,6 +92,7 @@ extern "C" chord_status chord_moe_align_noalloc(const int32_t* topk_ids, int64_t
     a.tile_hist = scratch + kErrInts;
     a.n_tiles = static_cast<int>(tiles);
     a.err = scratch;
+    PdlScope pdl(T * k <= kPdlMaxRows);
     return launch_align(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CHORD_OK
                                                                               : CHORD_ERR_CUDA;
 }
