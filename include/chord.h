@@ -223,7 +223,8 @@ chord_status chord_moe_align_noalloc(const int32_t* topk_ids, int64_t T, int k, 
  *   1 <= k <= 32, E_local >= 1, T*k < 2^31, block_m in [1, 256].
  * Work schedule of both GEMMs: one CTA per SM takes (chunk of rows, weight
  *   tile) units in turn.  When the last round of units would leave at least
- *   half of the SMs idle, each of its units is cut along K into pieces of two
+ *   half of the SMs idle (decode token tiles, K stages of 256), each of its
+ *   units is cut along K into pieces of two
  *   or more K stages, one per otherwise idle SM; every piece leaves its fp32
  *   partial sum in the workspace and the last piece of a unit to finish adds
  *   the pieces in piece order (a fixed order: results stay bit-identical from

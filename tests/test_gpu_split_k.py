@@ -34,7 +34,8 @@ CASES = {
     # 8 down tiles (4 stages) -> 2 pieces each
     "both": (1, 4, 16, 1024, 1024, 54),
     # prefill tile (BK 128): 4 experts x ~100 rows, 4 tiles, K = 2048 in 16
-    # stages -> 8 pieces
+    # stages; this tile is never split (its pieces' sums cost more than the
+    # split saves), so both runs take the whole-unit path
     "prefill-tile": (200, 2, 4, 2048, 256, 55),
 }
 

@@ -567,10 +567,12 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.h_zero_unpaired = io.h_zero_unpaired ? 1 : 0;
     // K-split slots: as many as the workspace holds for this token tile, at
     // most one per CTA
+    // (not for the prefill tile: summing pieces of up to 192 columns costs its
+    // last round more than the split saves, 215 -> 220 us on the prefill down)
     const bool split = !(io.flags & CHORD_FLAG_NO_SPLIT_K);
     auto slots_for = [&](int cfg) {
         const int n = kSplitSlots * w.split_maxn / gemm_cfg_maxn(cfg);
-        return split ? (n < dev.sms ? n : dev.sms) : 0;
+        return (split && gemm_cfg_bk(cfg) == 256) ? (n < dev.sms ? n : dev.sms) : 0;
     };
     int32_t* split_cnt = reinterpret_cast<int32_t*>(ws + w.off_split_cnt);
     g.split_part = reinterpret_cast<float*>(ws + w.off_split_part);
