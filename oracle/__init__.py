@@ -38,6 +38,8 @@ MUTATIONS = {
     "down_transposed": 10,
     "align_no_pad": 11,
     "code_offset": 12,
+    "route_tie_high": 13,
+    "route_no_renorm": 14,
 }
 
 
@@ -81,6 +83,8 @@ def _load():
         lib.oracle_align_capacity.restype = i64
         lib.oracle_moe_align.argtypes = [vp, i64, i64, i64, vp, i64, i64, vp, vp, vp, i64]
         lib.oracle_moe_align.restype = i32
+        lib.oracle_route_topk.argtypes = [vp, i64, i64, i64, i32, vp, vp]
+        lib.oracle_route_topk.restype = i32
         lib.oracle_expert_mlp.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, vp, vp, vp]
         lib.oracle_expert_mlp.restype = i32
         lib.oracle_moe_indexed.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
@@ -178,6 +182,18 @@ def moe_align(topk_ids, E_global, expert_map, E_local, block_m, capacity=None):
     if rc != 0:
         raise ValueError("oracle_moe_align: capacity too small or bad block_m")
     return sorted_ids, expert_ids, int(ntp[0])
+
+
+def route_topk(logits, k, renormalize=True):
+    """Router (oracle.c R12): logits float32 [T, E] -> (topk_ids int32 [T, k],
+    topk_weights float32 [T, k])."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    if _load().oracle_route_topk(_p(lg), T, E, k, 1 if renormalize else 0, _p(ids), _p(w)) != 0:
+        raise ValueError("oracle_route_topk: bad sizes")
+    return ids, w
 
 
 def expert_mlp(w13_q, w13_s, w2_q, w2_s, e, x_rows):

@@ -43,6 +43,10 @@
  *      sentinel T*k, empty experts get no block, sorted_ids tail = sentinel,
  *      expert_ids tail = -1.
  *   R11 pairs routed to a non-local expert (expert_map = -1) are dropped.
+ *   R12 router (the step before align, config 0's routing rule): per token
+ *      the k largest logits, ties to the lower expert id, in descending order;
+ *      weight of a selected expert = its softmax probability over all
+ *      E_global experts, renormalised over the k selected when asked.
  *
  * Every function below is pinned by the CPU tests (closed forms, exhaustive
  * dequant against exact rational rounding, brute-force fp64 evaluation,
@@ -76,6 +80,8 @@ enum {
     MUT_DOWN_TRANSPOSED = 10,  /* down weight read as [I, H] */
     MUT_ALIGN_NO_PAD = 11,     /* segments not padded to block_m */
     MUT_CODE_OFFSET = 12,      /* reads the code of element c+1 */
+    MUT_ROUTE_TIE_HIGH = 13,   /* R12 violated: equal logits go to the higher id */
+    MUT_ROUTE_NO_RENORM = 14,  /* R12 violated: weights not renormalised */
 };
 static int g_mutation = 0;
 void oracle_set_mutation(int m) { g_mutation = m; }
@@ -235,6 +241,56 @@ void oracle_dequant(const int32_t* wq, const uint16_t* ws, int64_t N, int64_t K,
 /* ------------------------------------------------------------------------- */
 /* align (R10, R11)                                                          */
 /* ------------------------------------------------------------------------- */
+/*
+ * Router (R12).  logits float [T, E]; writes ids int32 [T, k] (descending
+ * logit, ties to the lower id) and w float [T, k]:
+ *   w_j = exp(l_j - m) / D,  m = max_e l_e,
+ *   D = sum over the k selected of exp(l - m) when renorm, else over all E
+ * (the softmax probability, renormalised over the selected experts or not),
+ * evaluated in fp64 and rounded to fp32.  Returns -1 on bad sizes.
+ */
+int oracle_route_topk(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
+                      int32_t* ids, float* w)
+{
+    if (k < 1 || k > E || E < 1)
+        return -1;
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (!taken)
+        return -1;
+    const int do_renorm = renorm && g_mutation != MUT_ROUTE_NO_RENORM;
+    for (int64_t t = 0; t < T; ++t) {
+        const float* l = logits + t * E;
+        memset(taken, 0, (size_t)E);
+        for (int64_t j = 0; j < k; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                if (taken[e])
+                    continue;
+                if (best < 0 || l[e] > l[best] ||
+                    (g_mutation == MUT_ROUTE_TIE_HIGH && l[e] == l[best]))
+                    best = e;
+            }
+            taken[best] = 1;
+            ids[t * k + j] = (int32_t)best;
+        }
+        double m = l[0];
+        for (int64_t e = 1; e < E; ++e)
+            if (l[e] > m)
+                m = l[e];
+        double denom = 0.0;
+        if (do_renorm)
+            for (int64_t j = 0; j < k; ++j)
+                denom += exp((double)l[ids[t * k + j]] - m);
+        else
+            for (int64_t e = 0; e < E; ++e)
+                denom += exp((double)l[e] - m);
+        for (int64_t j = 0; j < k; ++j)
+            w[t * k + j] = (float)(exp((double)l[ids[t * k + j]] - m) / denom);
+    }
+    free(taken);
+    return 0;
+}
+
 int64_t oracle_align_capacity(int64_t T, int64_t k, int64_t E_local, int64_t block_m)
 {
     if (block_m <= 0)

@@ -497,7 +497,74 @@ def pin_silu():
     return worst <= 4.0, f"silu worst {worst:.2f} ulp"
 
 
+def _route_brute(logits, k, renormalize):
+    """Router by the definition, written differently from the oracle: the k
+    largest logits by a full sort on (-logit, id); the weights from Python
+    fp64 exponentials of the shifted logits."""
+    import math
+    T, E = logits.shape
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    for t in range(T):
+        row = [float(v) for v in logits[t]]
+        order = sorted(range(E), key=lambda e: (-row[e], e))[:k]
+        m = max(row)
+        ex = [math.exp(v - m) for v in row]
+        den = sum(ex[e] for e in order) if renormalize else math.fsum(ex)
+        ids[t] = order
+        w[t] = [ex[e] / den for e in order]
+    return ids, w
+
+
+def pin_route_brute_force(seed=51):
+    """Router vs a brute-force sort on small integer-valued logits (many ties),
+    with and without renormalisation: ids exactly, weights within 1 fp32 ulp of
+    the fp64 value."""
+    rng = np.random.default_rng(seed)
+    for E, k in [(6, 2), (9, 4), (16, 16), (40, 8), (1, 1)]:
+        lg = rng.integers(-3, 4, size=(17, E)).astype(np.float32)
+        lg[0, :] = 1.0  # one token with every logit equal
+        for renorm in (True, False):
+            ids, w = oracle.route_topk(lg, k, renorm)
+            bids, bw = _route_brute(lg, k, renorm)
+            if not np.array_equal(ids, bids):
+                return False, f"ids differ E={E} k={k} renorm={renorm}"
+            err = np.abs(w.astype(np.float64) - bw) / np.spacing(np.float32(bw)).astype(np.float64)
+            if err.max() > 1.0:
+                return False, f"weights off by {err.max():.2f} ulp E={E} k={k} renorm={renorm}"
+    return True, "ok"
+
+
+def pin_route_closed_forms():
+    """Closed forms: equal logits give the k lowest ids with weight 1/k
+    (renormalised) or 1/E (not); logits ln 2 / 0 give weights 2/3, 1/3 over a
+    pair; a constant shift of every logit changes nothing."""
+    E, k = 8, 3
+    lg = np.zeros((1, E), np.float32)
+    ids, w = oracle.route_topk(lg, k, True)
+    if list(ids[0]) != [0, 1, 2] or not np.allclose(w, 1.0 / k, rtol=0, atol=1e-7):
+        return False, f"equal logits renorm {ids} {w}"
+    ids, w = oracle.route_topk(lg, k, False)
+    if not np.allclose(w, 1.0 / E, rtol=0, atol=1e-8):
+        return False, f"equal logits softmax {w}"
+    lg = np.array([[0.0, np.log(2.0), -30.0, -30.0]], np.float32)
+    ids, w = oracle.route_topk(lg, 2, True)
+    l1 = float(np.float32(np.log(2.0)))
+    want = np.array([np.exp(l1) / (np.exp(l1) + 1.0), 1.0 / (np.exp(l1) + 1.0)])
+    if list(ids[0]) != [1, 0] or np.abs(w[0] - want).max() > 1e-7:
+        return False, f"two-level {ids} {w}"
+    rng = np.random.default_rng(7)
+    lg = rng.standard_normal((11, 24)).astype(np.float32)
+    a = oracle.route_topk(lg, 5, True)
+    b = oracle.route_topk(lg + np.float32(16.0), 5, True)
+    if not np.array_equal(a[0], b[0]) or np.abs(a[1] - b[1]).max() > 2e-6:
+        return False, "shift changed the routing"
+    return True, "ok"
+
+
 ALL_PINS = {
+    "route_brute_force": pin_route_brute_force,
+    "route_closed_forms": pin_route_closed_forms,
     "silu": pin_silu,
     "dequant_exhaustive": pin_dequant_exhaustive,
     "dequant_zero_code": pin_dequant_zero_code,
