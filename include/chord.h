@@ -194,6 +194,37 @@ chord_status chord_moe_align_noalloc(const int32_t* topk_ids, int64_t T, int k, 
                                      int32_t* num_tokens_padded, int64_t capacity, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* router + moe_align in one call                                             */
+/* ------------------------------------------------------------------------- */
+/*
+ * The router step before the layer, then chord_moe_align of its result, with
+ * no host round trip (graph capturable).  Per token t (page: "vLLM
+ * integration": top-k routing over the router's softmax; config 0's rule):
+ *   topk_ids[t, 0..k)     the k largest logits[t, :] in descending order, ties
+ *                         to the lower expert id (global ids);
+ *   topk_weights[t, j]    softmax probability of expert topk_ids[t, j] over all
+ *                         E_global logits, renormalised to sum 1 over the k
+ *                         chosen when renormalize != 0 (fp32; exp and the sums
+ *                         in fp32, within a few ulp of the fp64 value);
+ * then sorted_ids / expert_ids / num_tokens_padded exactly as chord_moe_align
+ * on those ids.  Up to 64 tokens (4096 pairs, 512 local experts) both steps
+ * run in one CTA (one launch), else as a router kernel and the align kernels.
+ *
+ *   logits       device float [T, E_global], finite
+ *   E_global     1..1024;  k in [1, min(32, E_global)]
+ *   topk_ids     device int32 [T, k] (output)
+ *   topk_weights device float [T, k] (output)
+ *   the other arguments as chord_moe_align; workspace >=
+ *   chord_moe_align_workspace_size(T, k, E_local) bytes.
+ */
+chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global, int k,
+                                   int renormalize, const int32_t* expert_map, int E_local,
+                                   int block_m, int32_t* topk_ids, float* topk_weights,
+                                   int32_t* sorted_ids, int32_t* expert_ids,
+                                   int32_t* num_tokens_padded, int64_t capacity, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* the MoE layer on the indexed layout                                        */
 /* ------------------------------------------------------------------------- */
 /*

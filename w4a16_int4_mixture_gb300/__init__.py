@@ -15,6 +15,7 @@ from .ops import (  # noqa: F401
     grouped_workspace_size,
     moe_align,
     moe_align_capacity,
+    moe_route_align,
     moe_workspace_size,
     select_block_m,
     stage_timing_enable,
@@ -27,7 +28,7 @@ from . import synth  # noqa: F401
 
 __all__ = [
     "build", "ChordError", "describe_schedule", "get_device_error", "grouped_workspace_size",
-    "moe_align", "moe_align_capacity", "moe_workspace_size", "select_block_m",
+    "moe_align", "moe_align_capacity", "moe_route_align", "moe_workspace_size", "select_block_m",
     "stage_timing_enable", "stage_timing_read", "w4a16_moe", "w4a16_moe_grouped",
     "w4a16_moe_indexed", "synth",
 ]

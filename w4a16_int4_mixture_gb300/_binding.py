@@ -52,6 +52,8 @@ SIGNATURES = {
                                _sz, _vp]),
     "chord_moe_align_noalloc": (_int, [_vp, _i64, _int, _int, _vp, _int, _int, _vp, _vp, _vp,
                                        _i64, _vp]),
+    "chord_moe_route_align": (_int, [_vp, _i64, _int, _int, _int, _vp, _int, _int, _vp, _vp, _vp,
+                                     _vp, _vp, _i64, _vp, _sz, _vp]),
     "chord_w4a16_moe_indexed": (_int, [_vp, _i64, _int, _int, _int, _int, _int, _vp, _vp, _vp,
                                        _vp, _vp, _vp, _vp, _vp, _i64, _int, _vp, _sz, _vp, _vp,
                                        _int, _vp]),

@@ -740,6 +740,61 @@ chord_status chord_moe_align(const int32_t* topk_ids, int64_t T, int k, int E_gl
     return from_cuda(launch_align(a, static_cast<cudaStream_t>(stream)));
 }
 
+chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global, int k,
+                                   int renormalize, const int32_t* expert_map, int E_local,
+                                   int block_m, int32_t* topk_ids, float* topk_weights,
+                                   int32_t* sorted_ids, int32_t* expert_ids,
+                                   int32_t* num_tokens_padded, int64_t capacity, void* workspace,
+                                   size_t workspace_bytes, void* stream)
+{
+    if (T < 0 || k < 1 || k > 32 || E_global < 1 || k > E_global || E_local < 1 ||
+        E_local > 1024 || block_m < 1 || block_m > 256)
+        return CHORD_ERR_INVALID_ARG;
+    if (E_global > 1024)
+        return CHORD_ERR_UNSUPPORTED_SHAPE;
+    if (!expert_map && E_local != E_global)
+        return CHORD_ERR_INVALID_ARG;
+    if (T * k >= (int64_t(1) << 31) || T * E_global >= (int64_t(1) << 40))
+        return CHORD_ERR_UNSUPPORTED_SHAPE;
+    if (!sorted_ids || !expert_ids || !num_tokens_padded ||
+        (T > 0 && (!logits || !topk_ids || !topk_weights)))
+        return CHORD_ERR_INVALID_ARG;
+    if (capacity < chord_moe_align_capacity(T, k, E_local, block_m) || capacity % block_m != 0)
+        return CHORD_ERR_CAPACITY;
+    chord_status st =
+        check_ws(workspace, workspace_bytes, chord_moe_align_workspace_size(T, k, E_local));
+    if (st != CHORD_OK)
+        return st;
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != CHORD_OK)
+        return st;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    RouteArgs r{};
+    r.logits = logits;
+    r.T = T;
+    r.E = E_global;
+    r.k = k;
+    r.renorm = renormalize ? 1 : 0;
+    r.ids = topk_ids;
+    r.w = topk_weights;
+    AlignArgs a{};
+    a.topk_ids = topk_ids;
+    a.num_pairs = T * k;
+    a.E_global = E_global;
+    a.expert_map = expert_map;
+    a.E_local = E_local;
+    a.block_m = block_m;
+    a.sorted_ids = sorted_ids;
+    a.expert_ids = expert_ids;
+    a.num_tokens_padded = num_tokens_padded;
+    a.capacity = capacity;
+    a.tile_hist = reinterpret_cast<int32_t*>(ws + kAlign);
+    a.n_tiles = static_cast<int>((T * k + 255) / 256);
+    a.err = reinterpret_cast<int*>(ws);
+    PdlScope pdl(T * k <= kPdlMaxRows);
+    return from_cuda(launch_route_align(r, a, static_cast<cudaStream_t>(stream)));
+}
+
 chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I, int E_global,
                                      int E_local, int k, const int32_t* w13_q,
                                      const uint16_t* w13_s, const int32_t* w2_q,

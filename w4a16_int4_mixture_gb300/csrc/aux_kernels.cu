@@ -196,10 +196,9 @@ constexpr int kSmallThreads = 1024;
 constexpr int kSmallMaxPairs = 4096;
 constexpr int kSmallMaxExperts = 512;
 
-__global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
+// The one-CTA align (called by every thread of a 1024-thread block).
+__device__ void align_small_run(const AlignArgs& a)
 {
-    pdl_launch_dependents();
-    pdl_wait();
     __shared__ int cnt[kSmallMaxExperts];   // pass 1 counts, then pairs placed by earlier rounds
     __shared__ int base[kSmallMaxExperts];  // first padded row of each expert
     __shared__ short wcnt[kSmallThreads / 32][kSmallMaxExperts];  // per warp of a round (<= 32)
@@ -270,6 +269,139 @@ __global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
         }
         __syncthreads();
     }
+}
+
+__global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    align_small_run(a);
+}
+
+// ---------------------------------------------------------------------------
+// router: per token the k largest logits (ties to the lower expert id), in
+// descending order, each weighted by its softmax probability over all experts,
+// renormalised over the k when asked.  One warp per token: lane l holds logits
+// l, l + 32, ...; k rounds of a warp argmax over (logit, lower id).
+// ---------------------------------------------------------------------------
+// NI logits per lane: E <= 32 * NI (NI = 4, 8, 16 or 32).
+template <int NI>
+__device__ void route_token_warp(const RouteArgs& r, int64_t t, int lane)
+{
+    const int E = r.E;
+    const float* row = r.logits + t * E;
+    float v[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? row[e] : -INFINITY;
+    }
+    uint32_t taken = 0u;  // bit i: logit lane + 32 i already chosen
+    float top = 0.f;      // the largest logit (the first one chosen)
+    int my_id = -1;       // lane j keeps the j-th choice
+    float my_v = 0.f;
+    for (int j = 0; j < r.k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (bi == 0x7fffffff || v[i] > bv)) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane)
+            taken |= 1u << (bi >> 5);
+        if (j == 0)
+            top = bv;
+        if (lane == j) {
+            my_id = bi;
+            my_v = bv;
+        }
+    }
+    // denominators: over the chosen k, or over every expert
+    float den = 0.f;
+    if (r.renorm) {
+        den = lane < r.k ? expf(my_v - top) : 0.f;
+    } else {
+#pragma unroll
+        for (int i = 0; i < NI; ++i)
+            if (lane + 32 * i < E)
+                den += expf(v[i] - top);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane < r.k) {
+        r.ids[t * r.k + lane] = my_id;
+        r.w[t * r.k + lane] = expf(my_v - top) / den;
+    }
+}
+
+template <int NI>
+__global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs r)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t t = warp; t < r.T; t += nwarps)
+        route_token_warp<NI>(r, t, lane);
+}
+
+// Router and align in one CTA (up to 64 tokens, 4096 pairs and 512 local
+// experts): the 32 warps route the tokens into topk_ids / topk_weights, then
+// the block aligns them.
+constexpr int kRouteFusedMaxT = 64;
+
+template <int NI>
+__global__ void __launch_bounds__(kSmallThreads) route_align_small_kernel(RouteArgs r, AlignArgs a)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t t = warp; t < r.T; t += kSmallThreads / 32)
+        route_token_warp<NI>(r, t, lane);
+    __syncthreads();  // (the block's writes of topk_ids are visible to it)
+    align_small_run(a);
+}
+
+template <int NI>
+cudaError_t launch_route_align_ni(const RouteArgs& r, const AlignArgs& a, cudaStream_t s)
+{
+    if (r.T <= kRouteFusedMaxT && a.num_pairs <= kSmallMaxPairs && a.E_local <= kSmallMaxExperts)
+        return launch_pdl(route_align_small_kernel<NI>, 1, kSmallThreads, 0, s, r, a);
+    if (r.T > 0) {
+        int64_t blocks = (r.T + 7) / 8;  // 8 warps per block, a token each
+        if (blocks > 65535)
+            blocks = 65535;
+        cudaError_t e = launch_pdl(route_topk_kernel<NI>, static_cast<int>(blocks), 256, 0, s, r);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return launch_align(a, s);
+}
+
+cudaError_t launch_route_align(const RouteArgs& r, const AlignArgs& a, cudaStream_t s)
+{
+    if (r.E <= 128)
+        return launch_route_align_ni<4>(r, a, s);
+    if (r.E <= 256)
+        return launch_route_align_ni<8>(r, a, s);
+    if (r.E <= 512)
+        return launch_route_align_ni<16>(r, a, s);
+    return launch_route_align_ni<32>(r, a, s);
 }
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s)

@@ -57,6 +57,17 @@ struct AlignArgs {
     int* err;
 };
 
+// Router: logits float [T, E] -> topk ids int32 [T, k] and weights float [T, k].
+struct RouteArgs {
+    const float* logits;
+    int64_t T;
+    int E;       // <= 1024
+    int k;       // <= min(E, 32)
+    int renorm;  // weights renormalised over the k chosen
+    int32_t* ids;
+    float* w;
+};
+
 enum Layout : int { kLayoutIndexed = 0, kLayoutContiguous = 1, kLayoutMasked = 2 };
 
 struct PrepArgs {
@@ -127,6 +138,9 @@ struct CombineArgs {
 };
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
+// Router, then align of its ids (a.topk_ids == r.ids): one CTA for both up to
+// 4096 pairs and 512 local experts, else a router kernel and launch_align.
+cudaError_t launch_route_align(const RouteArgs& r, const AlignArgs& a, cudaStream_t s);
 cudaError_t launch_prep(const PrepArgs& a, int work_blocks, cudaStream_t s);
 // Sets CHORD_DEVERR_SCALE_RANGE when a scale of a[0..na) or b[0..nb) (bf16
 // bits) is neither +-0 nor of magnitude in [2^-86, 2^35).

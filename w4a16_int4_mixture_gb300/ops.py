@@ -120,6 +120,38 @@ def moe_align(topk_ids: torch.Tensor, E_global: int, E_local: int, block_m: int 
     return sorted_ids, expert_ids, ntp
 
 
+def moe_route_align(logits: torch.Tensor, k: int, E_local: int, block_m: int = 16,
+                    expert_map: Optional[torch.Tensor] = None, renormalize: bool = True,
+                    capacity: Optional[int] = None, workspace: Optional[torch.Tensor] = None,
+                    out=None):
+    """Router logits float32 [T, E_global] -> (topk_ids, topk_weights, sorted_ids,
+    expert_ids, num_tokens_padded): the k largest logits per token (ties to the
+    lower id), softmax weights (renormalised over the k), and their aligned layout."""
+    _req(logits, "logits", _F32, ndim=2)
+    dev = logits.device
+    T, E_global = logits.shape
+    if expert_map is not None:
+        _req(expert_map, "expert_map", _I32, dev, 1)
+    if capacity is None:
+        capacity = moe_align_capacity(T, k, E_local, block_m)
+    if out is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        topk_weights = torch.empty((T, k), dtype=torch.float32, device=dev)
+        sorted_ids = torch.empty(capacity, dtype=torch.int32, device=dev)
+        expert_ids = torch.empty(capacity // block_m, dtype=torch.int32, device=dev)
+        ntp = torch.empty(1, dtype=torch.int32, device=dev)
+    else:
+        topk_ids, topk_weights, sorted_ids, expert_ids, ntp = out
+    need = align_workspace_size(T, k, E_local)
+    ws = workspace if workspace is not None else _pool.get(dev, need, "align")
+    st = lib().chord_moe_route_align(_p(logits), T, E_global, k, 1 if renormalize else 0,
+                                     _p(expert_map), E_local, block_m, _p(topk_ids),
+                                     _p(topk_weights), _p(sorted_ids), _p(expert_ids), _p(ntp),
+                                     capacity, _p(ws), ws.numel(), _stream(dev))
+    B.check(st, "chord_moe_route_align")
+    return topk_ids, topk_weights, sorted_ids, expert_ids, ntp
+
+
 def _check_weights(w13_q, w13_s, w2_q, w2_s, dev):
     _req(w13_q, "w13_q", _I32, dev, 3)
     _req(w13_s, "w13_s", _BF16, dev, 3)
