@@ -1,6 +1,6 @@
 """Benchmark of the W4A16 INT4 MoE layer (align + gate/up + SiLU + down + combine).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--T T]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T]
                     [--impl ours|reference] [--flags F]
 
 Prints ONE JSON line.  A step is one pass of the whole hot path (moe_align +
@@ -33,6 +33,8 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
+from w4a16_int4_mixture_gb300 import synth  # noqa: E402
+
 METRIC = "MoE layer us/call; decode HBM TB/s and prefill BF16 TFLOPS as % of roofline"
 UNIT = "us/call"
 KERNEL_SOURCES = ["gemm_kernel.cuh", "gemm_instances.cuh", "device.cuh"]
@@ -43,7 +45,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--workload", choices=synth.WORKLOADS, default="ep8-decode")
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flags", type=int, default=0)
@@ -270,7 +272,7 @@ def run_ours(args, rank, world, dev_index):
     chord.build()
     torch.cuda.set_device(dev_index)
     dev = torch.device("cuda", dev_index)
-    s = synth.config(args.config, T=args.T)
+    s = synth.workload(args.workload, T=args.T)
     inp = synth.make_inputs(s)
     work = workload_bytes_flops(inp)
     d = device_inputs(inp, torch, dev)
@@ -465,7 +467,7 @@ def run_reference(args):
     from w4a16_int4_mixture_gb300 import synth
     import oracle
     oracle.build()
-    s = synth.config(args.config, T=args.T)
+    s = synth.workload(args.workload, T=args.T)
     inp = synth.make_inputs(s)
     cap = s.T if s.T <= 1024 else 256
     t_cal, T_cal, _ = cpu_oracle_time(inp, cap)

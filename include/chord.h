@@ -199,7 +199,7 @@ chord_status chord_moe_align_noalloc(const int32_t* topk_ids, int64_t T, int k, 
 /*
  * The router step before the layer, then chord_moe_align of its result, with
  * no host round trip (graph capturable).  Per token t (page: "vLLM
- * integration": top-k routing over the router's softmax; config 0's rule):
+ * integration": top-k routing over the router's softmax):
  *   topk_ids[t, 0..k)     the k largest logits[t, :] in descending order, ties
  *                         to the lower expert id (global ids);
  *   topk_weights[t, j]    softmax probability of expert topk_ids[t, j] over all

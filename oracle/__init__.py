@@ -185,7 +185,7 @@ def moe_align(topk_ids, E_global, expert_map, E_local, block_m, capacity=None):
 
 
 def route_topk(logits, k, renormalize=True):
-    """Router (oracle.c R12): logits float32 [T, E] -> (topk_ids int32 [T, k],
+    """Router (oracle.c R14): logits float32 [T, E] -> (topk_ids int32 [T, k],
     topk_weights float32 [T, k])."""
     lg = _c(logits, np.float32)
     T, E = lg.shape

@@ -43,7 +43,7 @@
  *      sentinel T*k, empty experts get no block, sorted_ids tail = sentinel,
  *      expert_ids tail = -1.
  *   R11 pairs routed to a non-local expert (expert_map = -1) are dropped.
- *   R12 router (the step before align, config 0's routing rule): per token
+ *   R14 router (the step before align; the tiny workload's routing rule): per token
  *      the k largest logits, ties to the lower expert id, in descending order;
  *      weight of a selected expert = its softmax probability over all
  *      E_global experts, renormalised over the k selected when asked.
@@ -80,8 +80,8 @@ enum {
     MUT_DOWN_TRANSPOSED = 10,  /* down weight read as [I, H] */
     MUT_ALIGN_NO_PAD = 11,     /* segments not padded to block_m */
     MUT_CODE_OFFSET = 12,      /* reads the code of element c+1 */
-    MUT_ROUTE_TIE_HIGH = 13,   /* R12 violated: equal logits go to the higher id */
-    MUT_ROUTE_NO_RENORM = 14,  /* R12 violated: weights not renormalised */
+    MUT_ROUTE_TIE_HIGH = 13,   /* R14 violated: equal logits go to the higher id */
+    MUT_ROUTE_NO_RENORM = 14,  /* R14 violated: weights not renormalised */
 };
 static int g_mutation = 0;
 void oracle_set_mutation(int m) { g_mutation = m; }
@@ -242,7 +242,7 @@ void oracle_dequant(const int32_t* wq, const uint16_t* ws, int64_t N, int64_t K,
 /* align (R10, R11)                                                          */
 /* ------------------------------------------------------------------------- */
 /*
- * Router (R12).  logits float [T, E]; writes ids int32 [T, k] (descending
+ * Router (R14).  logits float [T, E]; writes ids int32 [T, k] (descending
  * logit, ties to the lower id) and w float [T, k]:
  *   w_j = exp(l_j - m) / D,  m = max_e l_e,
  *   D = sum over the k selected of exp(l - m) when renorm, else over all E

@@ -34,17 +34,18 @@ def _compare(chord, ids, E_global, emap, E_local, bm, capacity=None):
     assert np.array_equal(ei, rei), f"expert_ids differ at {np.nonzero(ei != rei)[0][:10]}"
 
 
-@pytest.mark.parametrize("cfg,T", [(0, None), (1, None), (2, None), (3, 1), (3, 16), (3, 128),
-                                   (3, 2048), (4, None)])
-def test_align_workloads(chord, cfg, T):
-    s = synth.config(cfg, T=T)
+@pytest.mark.parametrize("wl,T", [("tiny", None), ("ep8-decode", None), ("ep8-prefill", None),
+                                  ("tp8", 1), ("tp8", 16), ("tp8", 128), ("tp8", 2048),
+                                  ("skewed", None)])
+def test_align_workloads(chord, wl, T):
+    s = synth.workload(wl, T=T)
     inp = synth.make_inputs(s, weights=False)
     _compare(chord, inp.topk_ids, s.E_global, inp.expert_map, s.E_local, s.block_m)
 
 
 @pytest.mark.parametrize("bm", [1, 4, 8, 16, 32, 64, 128])
 def test_align_block_m(chord, bm):
-    s = synth.config(1, T=300)
+    s = synth.workload("ep8-decode", T=300)
     inp = synth.make_inputs(s, weights=False)
     _compare(chord, inp.topk_ids, s.E_global, inp.expert_map, s.E_local, bm)
 
@@ -74,7 +75,7 @@ def test_align_many_local_experts(chord, E):
 
 
 def test_align_over_allocated_capacity(chord):
-    s = synth.config(3, T=16)
+    s = synth.workload("tp8", T=16)
     inp = synth.make_inputs(s, weights=False)
     cap = chord.moe_align_capacity(2048, 8, 384, 16)
     _compare(chord, inp.topk_ids, s.E_global, None, s.E_local, 16, capacity=cap)

@@ -18,7 +18,7 @@ CHORD_ERR_TIMEOUT = -6
 
 
 def test_expired_wait_reports_timeout_and_context_survives(chord):
-    inp = synth.make_inputs(synth.config(0))
+    inp = synth.make_inputs(synth.workload("tiny"))
     with pytest.raises(chord.ChordError) as ei:
         run_indexed_full(chord, inp, flags=chord.ops.B.FLAG_TEST_SKIP_ARRIVE)
     assert ei.value.status == CHORD_ERR_TIMEOUT

@@ -113,7 +113,7 @@ def small(T, k, Eg, El, H, I, seed, bm=16, emap=True, sigma=0.05):
 
 
 SMALL = {
-    "cfg0": lambda: synth.make_inputs(synth.config(0)),
+    "tiny": lambda: synth.make_inputs(synth.workload("tiny")),
     "decode32-map": lambda: small(40, 3, 10, 6, 512, 256, 1),
     "decode64": lambda: small(64, 4, 8, 8, 512, 256, 2, emap=False),
     "decode128": lambda: small(100, 4, 8, 8, 256, 128, 3, emap=False),
@@ -315,26 +315,26 @@ def test_graph_capture_token_sweep(chord):
 # ---------------------------------------------------------------- full workloads
 @pytest.fixture(scope="module")
 def ep8_weights():
-    s = synth.config(1)
+    s = synth.workload("ep8-decode")
     inp = synth.make_inputs(s)
     return inp, weights_to(inp, DEV)
 
 
-def _with_weights(inp_w, cfg, T=None):
+def _with_weights(inp_w, wl, T=None):
     base, w = inp_w
-    s = synth.config(cfg, T=T)
+    s = synth.workload(wl, T=T)
     r = synth.make_inputs(s, weights=False)
     r.w13_q, r.w13_s, r.w2_q, r.w2_s = base.w13_q, base.w13_s, base.w2_q, base.w2_s
     return r, w
 
 
-def test_config1_decode_full(chord, ep8_weights):
-    inp, w = _with_weights(ep8_weights, 1)
+def test_ep8_decode_full(chord, ep8_weights):
+    inp, w = _with_weights(ep8_weights, "ep8-decode")
     verify_indexed(inp, run_indexed_full(chord, inp, weights=w), label="EP8 decode T=512")
 
 
-def test_config1_decode_deterministic(chord, ep8_weights):
-    inp, w = _with_weights(ep8_weights, 1)
+def test_ep8_decode_deterministic(chord, ep8_weights):
+    inp, w = _with_weights(ep8_weights, "ep8-decode")
     a = run_indexed_full(chord, inp, weights=w, flags=2)
     b = run_indexed_full(chord, inp, weights=w, flags=2)
     assert np.array_equal(a.out, b.out)
@@ -342,24 +342,24 @@ def test_config1_decode_deterministic(chord, ep8_weights):
     verify_indexed(inp, a, tokens, label="EP8 decode T=512 ordered combine")
 
 
-def test_config2_prefill_sampled(chord, ep8_weights):
-    inp, w = _with_weights(ep8_weights, 2)
+def test_ep8_prefill_sampled(chord, ep8_weights):
+    inp, w = _with_weights(ep8_weights, "ep8-prefill")
     run = run_indexed_full(chord, inp, weights=w)
     assert np.all(np.isfinite(oracle.bf16_to_f32(run.out)))
     tokens = np.random.default_rng(0).choice(inp.shape.T, 48, replace=False)
     verify_indexed(inp, run, tokens, label="EP8 prefill T=8192 (48 sampled tokens)")
 
 
-def test_config4_skewed_indexed_and_masked(chord, ep8_weights):
-    inp, w = _with_weights(ep8_weights, 4)
+def test_skewed_indexed_and_masked(chord, ep8_weights):
+    inp, w = _with_weights(ep8_weights, "skewed")
     verify_indexed(inp, run_indexed_full(chord, inp, weights=w), label="Zipf indexed")
     a3, mm, r2p = synth.grouped_masked_layout(inp)
     masked_layer_check(chord, inp, a3, mm, r2p, w, "Zipf masked")
 
 
 @pytest.mark.parametrize("T", [1, 16, 128, 2048])
-def test_config3_tp8(chord, T):
-    s = synth.config(3, T=T)
+def test_tp8(chord, T):
+    s = synth.workload("tp8", T=T)
     inp = synth.make_inputs(s)
     run = run_indexed_full(chord, inp)
     tokens = None if T <= 128 else np.random.default_rng(1).choice(T, 64, replace=False)

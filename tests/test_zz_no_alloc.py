@@ -27,7 +27,7 @@ def test_noalloc_align_matches_workspace_align():
     lib = chord.ops.lib()
     dev = torch.device("cuda:0")
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
-    draws = [(synth.config(1), 11), (synth.config(3, T=128), 12)]
+    draws = [(synth.workload("ep8-decode"), 11), (synth.workload("tp8", T=128), 12)]
     for shape, seed in draws:
         inp = synth.make_inputs(shape, seed=seed, weights=False)
         s = inp.shape

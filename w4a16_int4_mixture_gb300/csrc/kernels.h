@@ -11,7 +11,7 @@ namespace chord {
 
 // Whether launch_pdl asks for programmatic stream serialization on this host
 // thread, set per call: on for decode-sized calls (it hides the launch
-// gaps: config 1 237 -> 233 us), off for large ones (prefill measured 661 ->
+// gaps: EP8 decode, 512 tokens, 237 -> 233 us), off for large ones (prefill measured 661 ->
 // 692 us with it).  The kernels are correct either way: griddepcontrol.wait
 // returns at once when the launch was serialized.
 inline thread_local bool g_launch_pdl = true;

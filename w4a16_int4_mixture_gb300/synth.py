@@ -54,29 +54,32 @@ class MoEShape:
         return 0
 
 
-def config(index: int, T: int | None = None) -> MoEShape:
-    """The five workloads, by index (see the recipe in the module docstring)."""
-    if index == 0:
-        s = MoEShape("tiny-E8-k2-T16-H256-I128", T=16, k=2, E_global=8, E_local=8,
-                     H=256, I=128, block_m=16, routing="softmax_topk", seed=0)
-    elif index == 1:
-        s = MoEShape("ep8-decode-E48of384-k8-T512-H7168-I2048", T=512, k=8,
-                     E_global=384, E_local=48, H=7168, I=2048, seed=1)
-    elif index == 2:
-        s = MoEShape("ep8-prefill-E48of384-k8-T8192-H7168-I2048", T=8192, k=8,
-                     E_global=384, E_local=48, H=7168, I=2048, seed=2)
-    elif index == 3:
-        s = MoEShape("tp8-E384-k8-T2048-H7168-I256", T=2048, k=8,
-                     E_global=384, E_local=384, H=7168, I=256, seed=3)
-    elif index == 4:
-        s = MoEShape("skewed-zipf1.2-E48-k8-T128-H7168-I2048", T=128, k=8,
-                     E_global=48, E_local=48, H=7168, I=2048, routing="zipf",
-                     zipf_s=1.2, seed=4)
-    else:
-        raise ValueError(f"no workload {index}")
-    if T is not None:
+_WORKLOADS = {
+    "tiny": dict(name="tiny-E8-k2-T16-H256-I128", T=16, k=2, E_global=8, E_local=8,
+                 H=256, I=128, block_m=16, routing="softmax_topk", seed=0),
+    "ep8-decode": dict(name="ep8-decode-E48of384-k8-T512-H7168-I2048", T=512, k=8,
+                       E_global=384, E_local=48, H=7168, I=2048, seed=1),
+    "ep8-prefill": dict(name="ep8-prefill-E48of384-k8-T8192-H7168-I2048", T=8192, k=8,
+                        E_global=384, E_local=48, H=7168, I=2048, seed=2),
+    "tp8": dict(name="tp8-E384-k8-T2048-H7168-I256", T=2048, k=8,
+                E_global=384, E_local=384, H=7168, I=256, seed=3),
+    "skewed": dict(name="skewed-zipf1.2-E48-k8-T128-H7168-I2048", T=128, k=8,
+                   E_global=48, E_local=48, H=7168, I=2048, routing="zipf",
+                   zipf_s=1.2, seed=4),
+}
+WORKLOADS = tuple(_WORKLOADS)
+
+
+def workload(key: str, T: int | None = None) -> MoEShape:
+    """One of the workloads above by its short name (tiny, ep8-decode,
+    ep8-prefill, tp8, skewed), optionally with another token count T."""
+    if key not in _WORKLOADS:
+        raise ValueError(f"no workload {key!r} (known: {', '.join(WORKLOADS)})")
+    s = MoEShape(**_WORKLOADS[key])
+    if T is not None and int(T) != s.T:
+        if key != "tiny":
+            s.name = s.name.replace(f"-T{s.T}-", f"-T{int(T)}-")
         s.T = int(T)
-        s.name = s.name.replace(f"T{config(index).T}", f"T{T}") if index != 0 else s.name
     return s
 
 
