@@ -40,6 +40,8 @@ MUTATIONS = {
     "code_offset": 12,
     "route_tie_high": 13,
     "route_no_renorm": 14,
+    "pack_no_swizzle": 15,
+    "pack_tile_rows": 16,
 }
 
 
@@ -84,6 +86,8 @@ def _load():
         lib.oracle_moe_align.argtypes = [vp, i64, i64, i64, vp, i64, i64, vp, vp, vp, i64]
         lib.oracle_moe_align.restype = i32
         lib.oracle_route_topk.argtypes = [vp, i64, i64, i64, i32, vp, vp]
+        lib.oracle_prepack.argtypes = [i32, vp, vp, i64, i64, i64, vp]
+        lib.oracle_prepack.restype = i32
         lib.oracle_route_topk.restype = i32
         lib.oracle_expert_mlp.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, vp, vp, vp]
         lib.oracle_expert_mlp.restype = i32
@@ -194,6 +198,20 @@ def route_topk(logits, k, renormalize=True):
     if _load().oracle_route_topk(_p(lg), T, E, k, 1 if renormalize else 0, _p(ids), _p(w)) != 0:
         raise ValueError("oracle_route_topk: bad sizes")
     return ids, w
+
+
+def prepack(kind, w_q, w_s):
+    """Storage order of chord_w4a16_prepack (oracle.c, prepack): kind 1
+    (gate/up) or 2 (down), codes int32 [E, N, K/8] and scale bits uint16
+    [E, N, K/32] -> the packed bytes (uint8)."""
+    q = _c(w_q, np.int32)
+    sc = _c(w_s, np.uint16)
+    E, N, K8 = q.shape
+    K = K8 * 8
+    out = np.empty(256 + E * (N // 128) * (K // 256) * 18432, dtype=np.uint8)
+    if _load().oracle_prepack(int(kind), _p(q), _p(sc), E, N, K, _p(out)) != 0:
+        raise ValueError("oracle_prepack: bad kind or sizes")
+    return out
 
 
 def expert_mlp(w13_q, w13_s, w2_q, w2_s, e, x_rows):

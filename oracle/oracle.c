@@ -47,6 +47,10 @@
  *      the k largest logits, ties to the lower expert id, in descending order;
  *      weight of a selected expert = its softmax probability over all
  *      E_global experts, renormalised over the k selected when asked.
+ * Prepack (the storage order of chord_w4a16_prepack, stated in the library's
+ * header chord.h; an offline rearrangement that the pages' grouped kernels
+ * also make, "Kernel optimisation / grouped SM90 kernels"): no arithmetic,
+ * only where each code and scale goes, written out here loop by loop.
  *
  * Every function below is pinned by the CPU tests (closed forms, exhaustive
  * dequant against exact rational rounding, brute-force fp64 evaluation,
@@ -82,6 +86,8 @@ enum {
     MUT_CODE_OFFSET = 12,      /* reads the code of element c+1 */
     MUT_ROUTE_TIE_HIGH = 13,   /* R14 violated: equal logits go to the higher id */
     MUT_ROUTE_NO_RENORM = 14,  /* R14 violated: weights not renormalised */
+    MUT_PACK_NO_SWIZZLE = 15,  /* prepack: pieces stored unpermuted */
+    MUT_PACK_TILE_ROWS = 16,   /* prepack: gate/up tiles as 128 consecutive rows */
 };
 static int g_mutation = 0;
 void oracle_set_mutation(int m) { g_mutation = m; }
@@ -288,6 +294,72 @@ int oracle_route_topk(const float* logits, int64_t T, int64_t E, int64_t k, int 
             w[t * k + j] = (float)(exp((double)l[ids[t * k + j]] - m) / denom);
     }
     free(taken);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* prepack                                                                    */
+/* ------------------------------------------------------------------------- */
+/* weight row held at row r (0..127) of tile t */
+static int64_t pack_tile_row(int kind, int64_t N, int64_t t, int64_t r)
+{
+    if (kind == 1 && g_mutation != MUT_PACK_TILE_ROWS) /* gate/up: 64 gate rows, then 64 up */
+        return r < 64 ? 64 * t + r : N / 2 + 64 * t + (r - 64);
+    return 128 * t + r;
+}
+
+/* one bf16 scale is +-0 or of magnitude in [2^-86, 2^35): exponent field 41..161 */
+static int pack_scale_ok(uint16_t s)
+{
+    const unsigned mag = s & 0x7fffu;
+    const unsigned ex = mag >> 7;
+    return mag == 0 || (ex >= 41 && ex <= 161);
+}
+
+/*
+ * kind 1 (gate/up) or 2 (down); w_q int32 [E, N, K/8], w_s bf16 bits
+ * [E, N, K/32]; out has 256 + E*(N/128)*(K/256)*18432 bytes.  Header words:
+ * magic 0x4B504843, version 1, kind, E, N, K, 18432, flags (bit 0: a scale
+ * out of range), zeros.  Block (e, t, j), in that order: for tile row r and
+ * K half h, the row's four 16-byte pieces of codes 256j + 128h + 32c .. +31
+ * go to offset 8192h + 64r + 16(c ^ ((r >> 1) & 3)); the row's scales of
+ * groups 8j .. 8j+7 go to 16384 + 16r.  Returns -1 on bad sizes.
+ */
+int oracle_prepack(int kind, const int32_t* w_q, const uint16_t* w_s, int64_t E, int64_t N,
+                   int64_t K, uint8_t* out)
+{
+    if ((kind != 1 && kind != 2) || E < 1 || N % 128 != 0 || K % 256 != 0 || N < 128 || K < 256)
+        return -1;
+    const int64_t tiles = N / 128, kbs = K / 256;
+    uint32_t hdr[64];
+    memset(hdr, 0, sizeof hdr);
+    hdr[0] = 0x4B504843u;
+    hdr[1] = 1;
+    hdr[2] = (uint32_t)kind;
+    hdr[3] = (uint32_t)E;
+    hdr[4] = (uint32_t)N;
+    hdr[5] = (uint32_t)K;
+    hdr[6] = 18432;
+    uint8_t* blk = out + 256;
+    for (int64_t e = 0; e < E; ++e)
+        for (int64_t t = 0; t < tiles; ++t)
+            for (int64_t j = 0; j < kbs; ++j, blk += 18432)
+                for (int64_t r = 0; r < 128; ++r) {
+                    const int64_t row = e * N + pack_tile_row(kind, N, t, r);
+                    for (int64_t h = 0; h < 2; ++h)
+                        for (int64_t c = 0; c < 4; ++c) {
+                            const int64_t pos =
+                                g_mutation == MUT_PACK_NO_SWIZZLE ? c : (c ^ ((r >> 1) & 3));
+                            memcpy(blk + 8192 * h + 64 * r + 16 * pos,
+                                   w_q + row * (K / 8) + 32 * j + 16 * h + 4 * c, 16);
+                        }
+                    const uint16_t* sc = w_s + row * (K / 32) + 8 * j;
+                    memcpy(blk + 16384 + 16 * r, sc, 16);
+                    for (int g = 0; g < 8; ++g)
+                        if (!pack_scale_ok(sc[g]))
+                            hdr[7] |= 1u;
+                }
+    memcpy(out, hdr, sizeof hdr);
     return 0;
 }
 

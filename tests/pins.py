@@ -562,7 +562,107 @@ def pin_route_closed_forms():
     return True, "ok"
 
 
+def _unpack_codes(w_q):
+    """int32 words [..., K/8] -> codes [..., K] (element c = 8w+i in bits 4i..)."""
+    u = np.ascontiguousarray(w_q).view(np.uint32)
+    shifts = (4 * np.arange(8, dtype=np.uint32))
+    return ((u[..., None] >> shifts) & 0xF).reshape(*u.shape[:-1], u.shape[-1] * 8)
+
+
+def _pack_positions(kind, E, N, K):
+    """Byte position and nibble of every code (e, n, k), and byte position of
+    every scale (e, n, g), in the packed buffer, from the format statement
+    element by element (the oracle instead walks blocks and copies pieces)."""
+    e, n, k = np.meshgrid(np.arange(E), np.arange(N), np.arange(K), indexing="ij")
+    if kind == 1:
+        up = n >= N // 2
+        nn = np.where(up, n - N // 2, n)
+        t, r = nn // 64, nn % 64 + np.where(up, 64, 0)
+    else:
+        t, r = n // 128, n % 128
+    j, h, c, m = k // 256, (k % 256) // 128, (k % 128) // 32, k % 32
+    block = 256 + ((e * (N // 128) + t) * (K // 256) + j) * 18432
+    byte = block + h * 8192 + r * 64 + (c ^ ((r >> 1) & 3)) * 16 + (m // 8) * 4 + (m % 8) // 2
+    high = (m % 2) == 1
+    gs = np.arange(K // 32)
+    eg, ng, gg = np.meshgrid(np.arange(E), np.arange(N), gs, indexing="ij")
+    if kind == 1:
+        upg = ng >= N // 2
+        nng = np.where(upg, ng - N // 2, ng)
+        tg, rg = nng // 64, nng % 64 + np.where(upg, 64, 0)
+    else:
+        tg, rg = ng // 128, ng % 128
+    sblock = 256 + ((eg * (N // 128) + tg) * (K // 256) + gg // 8) * 18432
+    sbyte = sblock + 16384 + rg * 16 + (gg % 8) * 2
+    return byte, high, sbyte
+
+
+def pin_prepack_positions(seed=61):
+    """Every code and scale is where the packed format puts it, for both
+    kinds, with random codes and scales: read back through the per-element
+    position map, the packed buffer gives the input codes and scales exactly."""
+    rng = np.random.default_rng(seed)
+    for kind, (E, N, K) in [(1, (2, 256, 512)), (2, (3, 128, 768)), (1, (1, 384, 256))]:
+        w_q = rng.integers(0, 2**32, size=(E, N, K // 8), dtype=np.uint32).view(np.int32)
+        w_s = rng.integers(0, 2**16, size=(E, N, K // 32), dtype=np.uint16)
+        out = oracle.prepack(kind, w_q, w_s)
+        if out.size != 256 + E * (N // 128) * (K // 256) * 18432:
+            return False, f"size {out.size}"
+        byte, high, sbyte = _pack_positions(kind, E, N, K)
+        got = np.where(high, out[byte] >> 4, out[byte] & 0xF)
+        if not np.array_equal(got, _unpack_codes(w_q)):
+            return False, f"codes misplaced (kind {kind}, {E}x{N}x{K})"
+        sg = out[sbyte].astype(np.uint16) | (out[sbyte + 1].astype(np.uint16) << 8)
+        if not np.array_equal(sg, w_s):
+            return False, f"scales misplaced (kind {kind}, {E}x{N}x{K})"
+    return True, "ok"
+
+
+def pin_prepack_header_and_hand_cases():
+    """Header words; the range flag for scales just inside and outside
+    [2^-86, 2^35); and three code positions worked out by hand from the
+    format (down, E=1, N=128, K=256, every code 0 except one)."""
+    w_s = np.full((1, 128, 8), 0x3F80, np.uint16)  # 1.0
+    for code_at, want_byte, want_high in [
+        # (n=3, k=200): block 0, half 1, row 3, piece (200-128)//32 = 2 stored at
+        # 2 ^ ((3 >> 1) & 3) = 3, element 8 of the piece: word 1, low nibble
+        # -> 256 + 8192 + 3*64 + 3*16 + 4 = 8692
+        ((3, 200), 8692, False),
+        # (n=0, k=1): row 0, piece 0 at 0, element 1: byte 256, high nibble
+        ((0, 1), 256, True),
+        # (n=127, k=127): half 0, row 127, piece 3 stored at 3 ^ 3 = 0, element
+        # 31: word 3, byte 3, high nibble -> 256 + 127*64 + 0 + 12 + 3 = 8399
+        ((127, 127), 8399, True),
+    ]:
+        codes = np.zeros((1, 128, 256), np.uint32)
+        codes[0, code_at[0], code_at[1]] = 0xB
+        w_q = (codes.reshape(1, 128, 32, 8) << (4 * np.arange(8, dtype=np.uint32))).sum(
+            axis=-1, dtype=np.uint64).astype(np.uint32).view(np.int32)
+        out = oracle.prepack(2, w_q, w_s)
+        nz = np.nonzero(out[256:256 + 16384])[0]
+        if list(nz + 256) != [want_byte]:
+            return False, f"code at {code_at} landed at bytes {list(nz + 256)}"
+        v = out[want_byte]
+        if (v >> 4 if want_high else v & 0xF) != 0xB:
+            return False, f"code at {code_at}: wrong nibble of byte {want_byte}"
+    hd = out[:256].view(np.uint32)
+    if list(hd[:8]) != [0x4B504843, 1, 2, 1, 128, 256, 18432, 0] or hd[8:].any():
+        return False, f"header {list(hd[:8])}"
+    # exponent field 41 (2^-86) and 161 (2^34 * 1.x) are in range, 40 and 162 not;
+    # +-0 is in range
+    for bits, flag in [(41 << 7, 0), (161 << 7 | 0x7F, 0), (0x8000, 0), (40 << 7, 1), (162 << 7, 1),
+                       (0x7F80, 1)]:
+        s2 = w_s.copy()
+        s2[0, 5, 3] = bits
+        hd = oracle.prepack(2, w_q, s2)[:256].view(np.uint32)
+        if hd[7] != flag:
+            return False, f"scale bits {bits:#06x}: flag {hd[7]} != {flag}"
+    return True, "ok"
+
+
 ALL_PINS = {
+    "prepack_positions": pin_prepack_positions,
+    "prepack_header_and_hand_cases": pin_prepack_header_and_hand_cases,
     "route_brute_force": pin_route_brute_force,
     "route_closed_forms": pin_route_closed_forms,
     "silu": pin_silu,
