@@ -1,12 +1,14 @@
 """Benchmark of the W4A16 INT4 MoE layer (align + gate/up + SiLU + down + combine).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T]
-                    [--impl ours|reference] [--flags F]
+                    [--impl ours|reference] [--flags F] [--weights plain|packed]
 
 Prints ONE JSON line.  A step is one pass of the whole hot path (moe_align +
 the indexed layer) over one batch of synthetic inputs already resident in HBM,
 replayed from a CUDA graph; the weights (1.19 GB for the EP8 workloads) are
-far larger than L2, so every step streams them from HBM.  `value` is
+far larger than L2, so every step streams them from HBM.  By default they are
+packed once with chord_w4a16_prepack before anything is timed, as a server
+does when it loads them (--weights plain keeps the [E, N, K/8] layout).  `value` is
 microseconds per layer call (lower is better).
 
 --impl reference times the CPU oracle (test infrastructure, plain C) on the
@@ -46,6 +48,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", choices=synth.WORKLOADS, default="ep8-decode")
+    ap.add_argument("--weights", choices=("plain", "packed"), default="packed",
+                    help="plain [E,N,K/8] codes + scales, or chord_w4a16_prepack packs "
+                         "(packed once before timing, like loading the weights)")
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flags", type=int, default=0)
@@ -287,6 +292,9 @@ def run_ours(args, rank, world, dev_index):
     ws_l = torch.empty(chord.moe_workspace_size(s.T, s.k, s.E_global, s.E_local, s.H, s.I, bm,
                                                 cap, args.flags), dtype=torch.uint8, device=dev)
     w = (d["w13_q"], d["w13_s"], d["w2_q"], d["w2_s"])
+    if args.weights == "packed":
+        w = (chord.prepack_weights(*w), None, None, None)
+        torch.cuda.synchronize()
 
     def step(x=d["x"], ids=d["ids"], tw=d["tw"], o=out):
         chord.moe_align(ids, s.E_global, s.E_local, bm, expert_map=d["emap"], capacity=cap,
@@ -383,8 +391,9 @@ def run_ours(args, rank, world, dev_index):
         ach = gu["flops"] / gu_s / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tfl, "unit": "TFLOP/s",
                 "frac": round(ach / tfl, 4)}
-    roof["traffic"] = ncu_traffic("gate_up", s.name, src_hash)
-    roof["kernel"] = "w4a16_gemm_kernel (gate_up, fused SiLU*up)"
+    roof["traffic"] = ncu_traffic("gate_up" + (".packed" if args.weights == "packed" else ""),
+                                  s.name, src_hash)
+    roof["kernel"] = f"w4a16_gemm_kernel (gate_up, fused SiLU*up; {args.weights} weights)"
     roof["peak_source"] = f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else src
     roof["algorithmic_bytes_per_launch"] = int(gu_bytes)
     roof["launch_ms"] = round(stage[1], 5)
@@ -403,6 +412,7 @@ def run_ours(args, rank, world, dev_index):
                                                        args.flags),
                    "l2": "inputs larger than L2 (weights of the touched experts "
                          f"{work['layer']['bytes'] / 1e9:.2f} GB per step)",
+                   "weights": args.weights,
                    "timing": "CUDA events over K CUDA-graph replays on the launching stream",
                    "parallelism": f"replicas x{world}",
                    "value": "whole job: the slowest rank's step time / the N layer calls the "

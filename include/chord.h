@@ -65,7 +65,8 @@ typedef enum {
     CHORD_ERR_ROUTING = -7,           /* device found invalid routing data (validate / query) */
     CHORD_ERR_WORKSPACE = -8,         /* workspace missing, misaligned or too small */
     CHORD_ERR_NO_DEVICE = -9,         /* no sm_103a device is current */
-    CHORD_ERR_SCALE_RANGE = -10       /* a scale outside the supported range (validate / query) */
+    CHORD_ERR_SCALE_RANGE = -10,      /* a scale outside the supported range (validate / query) */
+    CHORD_ERR_PACKED = -11            /* packed weights that do not match the call (validate / query) */
 } chord_status;
 
 /* grouped layouts (page: "grouped SM90 kernels", Fig. 3) */
@@ -85,12 +86,16 @@ typedef enum {
                                          to show that an expired wait ends the kernel cleanly. */
 #define CHORD_FLAG_NO_SPLIT_K 8 /* keep every work unit whole: no K-split of the last, partly
                                    filled round of units (see chord_w4a16_moe_indexed) */
+#define CHORD_FLAG_PREPACKED 16 /* the layer calls' w13_q / w2_q are chord_w4a16_prepack
+                                   outputs (kinds CHORD_PACK_GATE_UP / CHORD_PACK_DOWN) and
+                                   w13_s / w2_s are NULL (the scales live in the packs) */
 
 /* bits of the device error word */
 #define CHORD_DEVERR_TIMEOUT 1
 #define CHORD_DEVERR_ROUTING 2
 #define CHORD_DEVERR_CAPACITY 4
 #define CHORD_DEVERR_SCALE_RANGE 8
+#define CHORD_DEVERR_PACKED 16
 
 /* Human-readable name of a status. */
 const char* chord_status_string(int status);
@@ -225,6 +230,49 @@ chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global,
                                    size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* offline weight prepack                                                     */
+/* ------------------------------------------------------------------------- */
+/*
+ * Rewrites one GEMM's codes and scales into the order the GEMM kernels hold
+ * them in shared memory, so that each K stage of a weight tile is one
+ * contiguous block read with plain bulk copies (page: "Kernel optimisation /
+ * grouped SM90 kernels": the grouped weights are prepacked offline into a
+ * kernel layout, and the packing mode is recorded in the prepared weight and
+ * checked when the kernel runs).  Done once per weight, like loading it.
+ *
+ * kind CHORD_PACK_GATE_UP: w_q [E, N = 2I, K/8], w_s [E, 2I, K/32]; tile t
+ *   (0 <= t < I/64) has rows 64t .. 64t+63 (gate) then I+64t .. I+64t+63 (up).
+ * kind CHORD_PACK_DOWN: w_q [E, N, K/8], w_s [E, N, K/32]; tile t has rows
+ *   128t .. 128t+127.
+ * Sizes: K % 256 == 0 and N % 128 == 0 (else CHORD_ERR_UNSUPPORTED_SHAPE).
+ *
+ * Format (version 1), little-endian:
+ *   bytes [0, 256): header of 64 uint32: [0] magic 0x4B504843 ("CHPK"),
+ *     [1] version 1, [2] kind, [3] E, [4] N, [5] K, [6] block bytes 18432,
+ *     [7] flags (bit 0: some scale outside the range of the header comment),
+ *     the rest 0.
+ *   then blocks of 18432 bytes, block b = (e * (N/128) + t) * (K/256) + j for
+ *   expert e, tile t and K block j (codes 256j .. 256j+255):
+ *     [0, 16384) codes: half h (codes 256j + 128h ..) at 8192 h; in it, tile
+ *       row r at 64 r; the row's four 16-byte pieces (32 codes each, one scale
+ *       group, in the word order of the source) with piece c stored at
+ *       position c ^ ((r >> 1) & 3);
+ *     [16384, 18432) scales: tile row r at 16 r, its 8 bf16 scales of groups
+ *       8j .. 8j+7.
+ * Total bytes: chord_w4a16_prepack_size() = 256 + E * (N/128) * (K/256) *
+ * 18432 (the same as codes + scales, plus the header).
+ *
+ *   w_q, w_s   device, as above (read only)
+ *   packed     device, >= packed_bytes, 16-byte aligned; written entirely
+ * Asynchronous on `stream`; two kernels; graph capturable.
+ */
+#define CHORD_PACK_GATE_UP 1
+#define CHORD_PACK_DOWN 2
+size_t chord_w4a16_prepack_size(int kind, int E, int N, int K);  /* 0 for bad arguments */
+chord_status chord_w4a16_prepack(int kind, const int32_t* w_q, const uint16_t* w_s, int E, int N,
+                                 int K, void* packed, size_t packed_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* the MoE layer on the indexed layout                                        */
 /* ------------------------------------------------------------------------- */
 /*
@@ -237,7 +285,15 @@ chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global,
  *   E_global     experts the router chose from; with T*k it gives the expected
  *                rows per local expert that steers the schedule (must match the
  *                value given to chord_w4a16_moe_workspace_size)
- *   w13_q, w13_s, w2_q, w2_s  device weights as in the header comment
+ *   w13_q, w13_s, w2_q, w2_s  device weights as in the header comment; with
+ *                CHORD_FLAG_PREPACKED, w13_q / w2_q are chord_w4a16_prepack
+ *                outputs (kinds GATE_UP with N = 2I, K = H, and DOWN with N = H,
+ *                K = I, E >= E_local) and w13_s / w2_s are NULL.  The call
+ *                checks both headers on the device before the GEMMs run; on a
+ *                mismatch the GEMMs compute nothing (no output is valid) and
+ *                CHORD_DEVERR_PACKED is set (CHORD_ERR_PACKED with
+ *                CHORD_FLAG_VALIDATE); a pack whose flags record an
+ *                out-of-range scale sets CHORD_DEVERR_SCALE_RANGE
  *   topk_weights device float [T, k]; weight of pair p = t*k+j is topk_weights[p]
  *   sorted_ids, expert_ids, num_tokens_padded  device, the chord_moe_align
  *                layout (any producer of the same layout works)
@@ -299,6 +355,8 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
  *                the same combine as the indexed layer.
  *   h_out        device bf16 [M, I] or NULL: the gate/up output of every row
  *                the call computes (as for the indexed call).
+ *   w13_q, w13_s, w2_q, w2_s  as for the indexed call, CHORD_FLAG_PREPACKED
+ *                included.
  * Limits as for the indexed call, plus max_m >= 1.
  */
 chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int H, int I,
@@ -316,8 +374,9 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
 /* ------------------------------------------------------------------------- */
 /* Synchronises `stream`, copies the error word of `workspace` (of a layer or
  * align call) to *error_bits, clears it when `clear` is non-zero, and returns
- * CHORD_ERR_TIMEOUT / CHORD_ERR_ROUTING / CHORD_ERR_CAPACITY for the first bit
- * set, else CHORD_OK.  Not capturable. */
+ * CHORD_ERR_TIMEOUT / CHORD_ERR_ROUTING / CHORD_ERR_CAPACITY /
+ * CHORD_ERR_SCALE_RANGE / CHORD_ERR_PACKED for the first bit set, else
+ * CHORD_OK.  Not capturable. */
 chord_status chord_get_device_error(void* workspace, int* error_bits, int clear, void* stream);
 
 /* ------------------------------------------------------------------------- */

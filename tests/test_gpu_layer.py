@@ -185,10 +185,10 @@ def test_poisoned_workspace_does_not_leak(chord):
 
 
 # ---------------------------------------------------------------- grouped
-def contiguous_layer_check(chord, inp, align, label, flags=0):
+def contiguous_layer_check(chord, inp, align, label, flags=0, weights=None):
     s = inp.shape
     a2, m_idx, r2p = synth.grouped_contiguous_layout(inp, align=align)
-    w = weights_to(inp, DEV)
+    w = weights or weights_to(inp, DEV)
     h = torch.empty((a2.shape[0], s.I), dtype=torch.bfloat16, device=DEV)
     rows, toks = chord.w4a16_moe_grouped("contiguous", dev_tensor(a2, DEV, True), *w,
                                          m_indices=dev_tensor(m_idx, DEV),

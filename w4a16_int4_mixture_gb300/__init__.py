@@ -17,6 +17,10 @@ from .ops import (  # noqa: F401
     moe_align_capacity,
     moe_route_align,
     moe_workspace_size,
+    PackedWeights,
+    prepack,
+    prepack_size,
+    prepack_weights,
     select_block_m,
     stage_timing_enable,
     stage_timing_read,
@@ -28,7 +32,8 @@ from . import synth  # noqa: F401
 
 __all__ = [
     "build", "ChordError", "describe_schedule", "get_device_error", "grouped_workspace_size",
-    "moe_align", "moe_align_capacity", "moe_route_align", "moe_workspace_size", "select_block_m",
+    "moe_align", "moe_align_capacity", "moe_route_align", "moe_workspace_size", "PackedWeights",
+    "prepack", "prepack_size", "prepack_weights", "select_block_m",
     "stage_timing_enable", "stage_timing_read", "w4a16_moe", "w4a16_moe_grouped",
     "w4a16_moe_indexed", "synth",
 ]

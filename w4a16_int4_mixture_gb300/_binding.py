@@ -24,6 +24,7 @@ STATUS = {
     -7: "invalid routing data", -8: "workspace missing, misaligned or too small",
     -9: "no sm_103a device current",
     -10: "scale outside the supported range",
+    -11: "packed weights do not match the call",
 }
 GROUPED_CONTIGUOUS = 0
 GROUPED_MASKED = 1
@@ -31,10 +32,14 @@ FLAG_VALIDATE = 1
 FLAG_DETERMINISTIC = 2
 FLAG_TEST_SKIP_ARRIVE = 4
 FLAG_NO_SPLIT_K = 8
+FLAG_PREPACKED = 16
+PACK_GATE_UP = 1
+PACK_DOWN = 2
 DEVERR_TIMEOUT = 1
 DEVERR_ROUTING = 2
 DEVERR_CAPACITY = 4
 DEVERR_SCALE_RANGE = 8
+DEVERR_PACKED = 16
 
 # every symbol include/chord.h declares, with (restype, argtypes)
 _i64, _int, _sz, _vp, _cp = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
@@ -52,6 +57,8 @@ SIGNATURES = {
                                _sz, _vp]),
     "chord_moe_align_noalloc": (_int, [_vp, _i64, _int, _int, _vp, _int, _int, _vp, _vp, _vp,
                                        _i64, _vp]),
+    "chord_w4a16_prepack_size": (_sz, [_int, _int, _int, _int]),
+    "chord_w4a16_prepack": (_int, [_int, _vp, _vp, _int, _int, _int, _vp, _sz, _vp]),
     "chord_moe_route_align": (_int, [_vp, _i64, _int, _int, _int, _vp, _int, _int, _vp, _vp, _vp,
                                      _vp, _vp, _i64, _vp, _sz, _vp]),
     "chord_w4a16_moe_indexed": (_int, [_vp, _i64, _int, _int, _int, _int, _int, _vp, _vp, _vp,

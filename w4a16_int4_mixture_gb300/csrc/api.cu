@@ -20,12 +20,22 @@ cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const CUtensorM
                                 cudaStream_t s);
 cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const CUtensorMap& smap,
                              const CUtensorMap& bmap, const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gemm_gate_up_packed(int cfg, const CUtensorMap& map, const CUtensorMap& smap,
+                                       const CUtensorMap& bmap, const GemmArgs& a, int grid,
+                                       cudaStream_t s);
+cudaError_t launch_gemm_down_packed(int cfg, const CUtensorMap& map, const CUtensorMap& smap,
+                                    const CUtensorMap& bmap, const GemmArgs& a, int grid,
+                                    cudaStream_t s);
 int gemm_cfg_smem_gate_up(int cfg);
 int gemm_cfg_smem_down(int cfg);
 
-cudaError_t launch_gemm(int cfg, bool gate_up, const CUtensorMap& map, const CUtensorMap& smap,
-                        const CUtensorMap& bmap, const GemmArgs& a, int grid, cudaStream_t s)
+cudaError_t launch_gemm(int cfg, bool gate_up, bool packed, const CUtensorMap& map,
+                        const CUtensorMap& smap, const CUtensorMap& bmap, const GemmArgs& a,
+                        int grid, cudaStream_t s)
 {
+    if (packed)
+        return gate_up ? launch_gemm_gate_up_packed(cfg, map, smap, bmap, a, grid, s)
+                       : launch_gemm_down_packed(cfg, map, smap, bmap, a, grid, s);
     return gate_up ? launch_gemm_gate_up(cfg, map, smap, bmap, a, grid, s)
                    : launch_gemm_down(cfg, map, smap, bmap, a, grid, s);
 }
@@ -82,9 +92,9 @@ struct MapKey {
     const void* ptr;
     int dtype;
     int rank;
-    uint64_t dims[3];
-    uint64_t strides[2];
-    uint32_t box[3];
+    uint64_t dims[4];
+    uint64_t strides[3];
+    uint32_t box[4];
     int swizzle;
     int device;
     bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
@@ -119,8 +129,8 @@ chord_status encode_map(MapKey key, CUtensorMap* out)
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     CUtensorMap m;
-    cuuint64_t dims[3], strides[2];
-    cuuint32_t box[3], es[3] = {1, 1, 1};
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4], es[4] = {1, 1, 1, 1};
     for (int i = 0; i < key.rank; ++i) {
         dims[i] = key.dims[i];
         box[i] = key.box[i];
@@ -158,33 +168,41 @@ MapKey blank_key(const void* ptr, int dtype, int rank, int swizzle, int device)
     return k;
 }
 
-// Packed codes of one GEMM: int32 words, rows of K/8.  gate_up (I > 0): a 3-D
-// map {K/8, E*N - I rows, 2 halves I rows apart}, box {bk/8, 64, 2}: gate rows
-// and the matching up rows in one box.  down: 2-D, box {bk/8, 128}.  128B
-// swizzle for bk 256, 64B for bk 128.
+// Packed codes of one GEMM: int32 words, rows of K/8, read in halves of 128
+// codes (16 words, 64 bytes, 64B swizzle) so that a stage of bk codes lands
+// as bk/128 halves of [128 tile rows][64 bytes], the layout the dequant reads
+// (and the one chord_w4a16_prepack stores).  gate_up (I > 0): a 4-D map
+// {16 words, E*N - I rows, 2 halves I rows apart, K/128 blocks}, box {16, 64,
+// 2, bk/128}: gate rows and the matching up rows in one box.  down: 3-D {16,
+// rows, K/128}, box {16, 128, bk/128}.
 chord_status codes_map(const int32_t* q, int64_t rows, int64_t K, int64_t I, int bk, int device,
                        CUtensorMap* out)
 {
-    const int sw = bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     const uint64_t row_bytes = static_cast<uint64_t>(K / 8) * 4;
     if (I > 0) {
-        MapKey k = blank_key(q, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, sw, device);
-        k.dims[0] = K / 8;
+        MapKey k = blank_key(q, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, CU_TENSOR_MAP_SWIZZLE_64B, device);
+        k.dims[0] = 16;
         k.dims[1] = rows - I;
         k.dims[2] = 2;
+        k.dims[3] = K / 128;
         k.strides[0] = row_bytes;
         k.strides[1] = row_bytes * I;
-        k.box[0] = bk / 8;
+        k.strides[2] = 64;
+        k.box[0] = 16;
         k.box[1] = 64;
         k.box[2] = 2;
+        k.box[3] = bk / 128;
         return encode_map(k, out);
     }
-    MapKey k = blank_key(q, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sw, device);
-    k.dims[0] = K / 8;
+    MapKey k = blank_key(q, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, CU_TENSOR_MAP_SWIZZLE_64B, device);
+    k.dims[0] = 16;
     k.dims[1] = rows;
+    k.dims[2] = K / 128;
     k.strides[0] = row_bytes;
-    k.box[0] = bk / 8;
+    k.strides[1] = 64;
+    k.box[0] = 16;
     k.box[1] = 128;
+    k.box[2] = bk / 128;
     return encode_map(k, out);
 }
 
@@ -463,7 +481,30 @@ chord_status read_error_word(void* ws, cudaStream_t s, int* bits, bool clear)
         return CHORD_ERR_CAPACITY;
     if (v & CHORD_DEVERR_SCALE_RANGE)
         return CHORD_ERR_SCALE_RANGE;
+    if (v & CHORD_DEVERR_PACKED)
+        return CHORD_ERR_PACKED;
     return CHORD_OK;
+}
+
+// The prep kernel checks the packs' headers against the call (gate/up: kind
+// GATE_UP, N = 2I, K = H; down: kind DOWN, N = H, K = I; E >= E_local).
+void set_pack_check(PrepArgs& pa, bool packed, const int32_t* w13_q, const int32_t* w2_q,
+                    int E_local, int H, int I)
+{
+    pa.pk_hdr[0] = packed ? reinterpret_cast<const uint32_t*>(w13_q) : nullptr;
+    pa.pk_hdr[1] = packed ? reinterpret_cast<const uint32_t*>(w2_q) : nullptr;
+    const uint32_t want[2][4] = {
+        {CHORD_PACK_GATE_UP, static_cast<uint32_t>(E_local), 2u * static_cast<uint32_t>(I),
+         static_cast<uint32_t>(H)},
+        {CHORD_PACK_DOWN, static_cast<uint32_t>(E_local), static_cast<uint32_t>(H),
+         static_cast<uint32_t>(I)}};
+    std::memcpy(pa.pk_want, want, sizeof want);
+}
+
+// Scales are separate arrays, or (prepacked) inside the packs and NULL here.
+bool scales_given(bool packed, const uint16_t* w13_s, const uint16_t* w2_s)
+{
+    return packed ? (w13_s == nullptr && w2_s == nullptr) : (w13_s != nullptr && w2_s != nullptr);
 }
 
 chord_status check_shape(int H, int I, int E_local, int k)
@@ -494,6 +535,7 @@ struct LayerIO {
     int flags;
     double tok_e;  // expected rows per local expert
     bool h_zero_unpaired;  // h rows without a pair are written as zeros (indexed layout)
+    bool packed;           // w13_q / w2_q are chord_w4a16_prepack outputs
 };
 
 // Weight tiles per unit of the down GEMM: with a one-stage K (I = BK) each
@@ -524,16 +566,23 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     const int bk13 = gemm_cfg_bk(sc.cfg_gate_up), bk2 = gemm_cfg_bk(sc.cfg_down);
     const int64_t rows13 = static_cast<int64_t>(io.E_local) * 2 * io.I;
     const int64_t rows2 = static_cast<int64_t>(io.E_local) * io.H;
-    chord_status st = codes_map(io.w13_q, rows13, io.H, io.I, bk13, dev.device, &map13);
-    if (st == CHORD_OK)
-        st = codes_map(io.w2_q, rows2, io.I, 0, bk2, dev.device, &map2);
-    // scales by TMA only for BK 256 stages; the kernel ignores the map otherwise
-    smap13 = map13;
-    smap2 = map2;
-    if (st == CHORD_OK && bk13 == 256)
-        st = scales_map(io.w13_s, rows13, io.H, io.I, dev.device, &smap13);
-    if (st == CHORD_OK && bk2 == 256)
-        st = scales_map(io.w2_s, rows2, io.I, 0, dev.device, &smap2);
+    chord_status st = CHORD_OK;
+    if (io.packed) {
+        // (prepacked weights are read with plain bulk copies: no weight maps)
+        std::memset(&map13, 0, sizeof map13);
+        map2 = smap13 = smap2 = map13;
+    } else {
+        st = codes_map(io.w13_q, rows13, io.H, io.I, bk13, dev.device, &map13);
+        if (st == CHORD_OK)
+            st = codes_map(io.w2_q, rows2, io.I, 0, bk2, dev.device, &map2);
+        // scales by TMA only for BK 256 stages; the kernel ignores the map otherwise
+        smap13 = map13;
+        smap2 = map2;
+        if (st == CHORD_OK && bk13 == 256)
+            st = scales_map(io.w13_s, rows13, io.H, io.I, dev.device, &smap13);
+        if (st == CHORD_OK && bk2 == 256)
+            st = scales_map(io.w2_s, rows2, io.I, 0, dev.device, &smap2);
+    }
     // (a call with no rows has no chunks, so no tile is ever read through these
     // maps; one row keeps the encoding valid)
     if (st == CHORD_OK)
@@ -555,6 +604,8 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.n_tiles = io.I / 64;
     g.tpu = 1;
     g.scales = io.w13_s;
+    if (io.packed)
+        g.pk = reinterpret_cast<const uint8_t*>(io.w13_q) + kPackHeaderBytes;
     g.chunks = reinterpret_cast<const Chunk*>(ws + w.off_chunks[0]);
     g.num_chunks = num_chunks;
     g.epi = 0;
@@ -580,7 +631,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.split_slots = slots_for(sc.cfg_gate_up);
     marks.mark(1);
     g.test_skip_arrive = (io.flags & CHORD_FLAG_TEST_SKIP_ARRIVE) ? 1 : 0;
-    if (launch_gemm(sc.cfg_gate_up, true, map13, smap13, bmap13, g, dev.sms, s) != cudaSuccess)
+    if (launch_gemm(sc.cfg_gate_up, true, io.packed, map13, smap13, bmap13, g, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(2);
 
@@ -592,6 +643,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     int cfg_down = sc.cfg_down;
     d.tpu = pick_tpu(&cfg_down, io.I, d.n_tiles, io.E_local, io.tok_e, dev.sms);
     d.scales = io.w2_s;
+    d.pk = io.packed ? reinterpret_cast<const uint8_t*>(io.w2_q) + kPackHeaderBytes : nullptr;
     d.chunks = reinterpret_cast<const Chunk*>(ws + w.off_chunks[1]);
     d.num_chunks = num_chunks + 1;
     d.epi = io.down_epi;
@@ -603,7 +655,7 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     d.split_cnt = split_cnt + kSplitSlots;
     d.split_part = g.split_part + static_cast<size_t>(kSplitSlots) * w.split_maxn * 128;
     d.split_slots = slots_for(sc.cfg_down);
-    if (launch_gemm(cfg_down, false, map2, smap2, bmap2, d, dev.sms, s) != cudaSuccess)
+    if (launch_gemm(cfg_down, false, io.packed, map2, smap2, bmap2, d, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(3);
     return CHORD_OK;
@@ -628,6 +680,7 @@ const char* chord_status_string(int status)
     case CHORD_ERR_TIMEOUT: return "device wait timed out";
     case CHORD_ERR_ROUTING: return "invalid routing data";
     case CHORD_ERR_SCALE_RANGE: return "scale outside the supported range";
+    case CHORD_ERR_PACKED: return "packed weights do not match the call";
     case CHORD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case CHORD_ERR_NO_DEVICE: return "no sm_103a device current";
     default: return "unknown status";
@@ -795,6 +848,33 @@ chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global,
     return from_cuda(launch_route_align(r, a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t chord_w4a16_prepack_size(int kind, int E, int N, int K)
+{
+    if ((kind != CHORD_PACK_GATE_UP && kind != CHORD_PACK_DOWN) || E < 1 || N < 128 || K < 256 ||
+        N % 128 != 0 || K % 256 != 0)
+        return 0;
+    return kPackHeaderBytes + static_cast<size_t>(E) * (N / 128) * (K / 256) * kPackBlockBytes;
+}
+
+chord_status chord_w4a16_prepack(int kind, const int32_t* w_q, const uint16_t* w_s, int E, int N,
+                                 int K, void* packed, size_t packed_bytes, void* stream)
+{
+    if ((kind != CHORD_PACK_GATE_UP && kind != CHORD_PACK_DOWN) || E < 1 || N < 1 || K < 1)
+        return CHORD_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 256 != 0)
+        return CHORD_ERR_UNSUPPORTED_SHAPE;
+    if (!w_q || !w_s || !packed || !aligned16(w_q) || !aligned16(w_s) || !aligned16(packed))
+        return CHORD_ERR_INVALID_ARG;
+    if (packed_bytes < chord_w4a16_prepack_size(kind, E, N, K))
+        return CHORD_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    chord_status st = device_info(&dev);
+    if (st != CHORD_OK)
+        return st;
+    PackArgs a{kind, w_q, w_s, E, N, K, static_cast<uint8_t*>(packed)};
+    return from_cuda(launch_prepack(a, dev.sms, static_cast<cudaStream_t>(stream)));
+}
+
 chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I, int E_global,
                                      int E_local, int k, const int32_t* w13_q,
                                      const uint16_t* w13_s, const int32_t* w2_q,
@@ -807,14 +887,15 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     chord_status st = check_shape(H, I, E_local, k);
     if (st != CHORD_OK)
         return st;
-    if (T < 0 || E_global < 1 || block_m < 1 || block_m > 256 || (flags & ~15))
+    if (T < 0 || E_global < 1 || block_m < 1 || block_m > 256 || (flags & ~31))
         return CHORD_ERR_INVALID_ARG;
+    const bool packed = (flags & CHORD_FLAG_PREPACKED) != 0;
     if (T * k >= (int64_t(1) << 31))
         return CHORD_ERR_UNSUPPORTED_SHAPE;
     if (T == 0)
         return CHORD_OK;
-    if (!x || !w13_q || !w13_s || !w2_q || !w2_s || !topk_weights || !sorted_ids || !expert_ids ||
-        !num_tokens_padded || !out)
+    if (!x || !w13_q || !w2_q || !topk_weights || !sorted_ids || !expert_ids ||
+        !num_tokens_padded || !out || !scales_given(packed, w13_s, w2_s))
         return CHORD_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w13_q) || !aligned16(w13_s) || !aligned16(w2_q) ||
         !aligned16(w2_s) || !aligned16(out) || (h_out && !aligned16(h_out)))
@@ -885,12 +966,14 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     pa.gx_pairs = T * k;
     pa.gx_H = H;
     pa.err = err;
+    set_pack_check(pa, packed, w13_q, w2_q, E_local, H, I);
     int work_blocks = zero_blocks_for(sc.reduce ? T * H : T * k, dev.sms);
     if (work_blocks < dev.sms)
         work_blocks = dev.sms;
     if (launch_prep(pa, work_blocks, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
-    if ((flags & CHORD_FLAG_VALIDATE) &&
+    // (prepacked weights: the pack recorded its scales' range; the GEMMs report it)
+    if ((flags & CHORD_FLAG_VALIDATE) && !packed &&
         launch_scale_check(w13_s, static_cast<int64_t>(E_local) * 2 * I * (H / 32), w2_s,
                            static_cast<int64_t>(E_local) * H * (I / 32), err, dev.sms, s) !=
             cudaSuccess)
@@ -915,6 +998,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     io.h_out = h_out;
     io.down_epi = sc.reduce ? kEpiReduceTok : kEpiStorePair;
     io.flags = flags;
+    io.packed = packed;
     io.tok_e = tok_e;
     io.h_zero_unpaired = true;
     if ((st = run_gemms(io, sc, w, ws, err, pair_row, acc, dev, s, marks)) != CHORD_OK)
@@ -950,8 +1034,9 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     chord_status st = check_shape(H, I, E_local, with_tokens ? k : 1);
     if (st != CHORD_OK)
         return st;
-    if (M < 0 || (flags & ~15))
+    if (M < 0 || (flags & ~31))
         return CHORD_ERR_INVALID_ARG;
+    const bool packed = (flags & CHORD_FLAG_PREPACKED) != 0;
     if (mode == CHORD_GROUPED_CONTIGUOUS) {
         if (masked_m != nullptr || (M > 0 && m_indices == nullptr))
             return CHORD_ERR_LAYOUT_MODE;
@@ -973,7 +1058,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     }
     if (M == 0 && !with_tokens)
         return CHORD_OK;
-    if (!a || !w13_q || !w13_s || !w2_q || !w2_s || !out_rows)
+    if (!a || !w13_q || !w2_q || !out_rows || !scales_given(packed, w13_s, w2_s))
         return CHORD_ERR_INVALID_ARG;
     if (!aligned16(a) || !aligned16(w13_q) || !aligned16(w13_s) || !aligned16(w2_q) ||
         !aligned16(w2_s) || !aligned16(out_rows) || (out_tokens && !aligned16(out_tokens)) ||
@@ -1032,12 +1117,14 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
         pa.mc_H = H;
     }
     pa.err = err;
+    set_pack_check(pa, packed, w13_q, w2_q, E_local, H, I);
     int work_blocks = zero_blocks_for(with_tokens ? T * H : 0, dev.sms);
     if ((with_tokens || compact) && work_blocks < dev.sms)
         work_blocks = dev.sms;  // the row records and the compacted rows come from the worker blocks
     if (launch_prep(pa, work_blocks, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
-    if ((flags & CHORD_FLAG_VALIDATE) &&
+    // (prepacked weights: the pack recorded its scales' range; the GEMMs report it)
+    if ((flags & CHORD_FLAG_VALIDATE) && !packed &&
         launch_scale_check(w13_s, static_cast<int64_t>(E_local) * 2 * I * (H / 32), w2_s,
                            static_cast<int64_t>(E_local) * H * (I / 32), err, dev.sms, s) !=
             cudaSuccess)
@@ -1063,6 +1150,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     io.rows_out = out_rows;
     io.down_epi = kEpiStoreRows | (with_tokens ? kEpiReduceTok : 0);
     io.flags = flags;
+    io.packed = packed;
     io.tok_e = tok_e;
     if ((st = run_gemms(io, sc, w, ws, err, nullptr, acc, dev, s, marks)) != CHORD_OK)
         return st;

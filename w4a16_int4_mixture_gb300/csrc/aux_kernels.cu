@@ -659,10 +659,26 @@ __device__ void build_chunk_lists(const PrepArgs& a)
     }
     __syncthreads();
     if (threadIdx.x == 0) {
+        // prepacked weights whose header does not describe this call: no GEMM
+        // unit may read them
+        bool pk_bad = false;
+        for (int g = 0; g < 2; ++g) {
+            const uint32_t* h = a.pk_hdr[g];
+            if (h == nullptr)
+                continue;
+            const uint32_t* w = a.pk_want[g];
+            if (h[0] != kPackMagic || h[1] != 1u || h[2] != w[0] || h[3] < w[1] || h[4] != w[2] ||
+                h[5] != w[3] || h[6] != static_cast<uint32_t>(kPackBlockBytes))
+                pk_bad = true;
+            else if (h[7] & 1u)
+                raise_error(a.err, CHORD_DEVERR_SCALE_RANGE);
+        }
+        if (pk_bad)
+            raise_error(a.err, CHORD_DEVERR_PACKED);
         // a malformed layout that overflows the list runs nothing rather than
         // reading entries this call did not write
-        a.num_chunks[0] = s_bad ? 0 : s_off[0];
-        a.num_chunks[1] = s_bad ? 0 : s_off[1];
+        a.num_chunks[0] = (s_bad || pk_bad) ? 0 : s_off[0];
+        a.num_chunks[1] = (s_bad || pk_bad) ? 0 : s_off[1];
     }
 }
 
@@ -864,6 +880,84 @@ cudaError_t launch_scale_check(const uint16_t* a, int64_t na, const uint16_t* b,
     if (na + nb <= 0)
         return cudaSuccess;
     return launch_pdl(scale_range_kernel, 4 * sms, 256, 0, s, a, na, b, nb, err);
+}
+
+// ---------------------------------------------------------------------------
+// offline prepack (format in chord.h)
+// ---------------------------------------------------------------------------
+__global__ void pack_header_kernel(PackArgs a)
+{
+    uint32_t* hd = reinterpret_cast<uint32_t*>(a.out);
+    const int i = threadIdx.x;  // 64 threads: the 64 header words
+    uint32_t v = 0;
+    if (i == 0)
+        v = kPackMagic;
+    else if (i == 1)
+        v = 1;
+    else if (i == 2)
+        v = static_cast<uint32_t>(a.kind);
+    else if (i == 3)
+        v = static_cast<uint32_t>(a.E);
+    else if (i == 4)
+        v = static_cast<uint32_t>(a.N);
+    else if (i == 5)
+        v = static_cast<uint32_t>(a.K);
+    else if (i == 6)
+        v = kPackBlockBytes;
+    hd[i] = v;  // word 7 (flags) starts at 0
+}
+
+// One thread per 16-byte piece of the output: pieces 0..1023 of a block are
+// codes (half h = j / 512, tile row r, stored position pos of the row's four
+// pieces, holding source piece pos ^ ((r >> 1) & 3)), 1024..1151 the rows'
+// scales.  Consecutive threads write consecutive pieces.
+__global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
+{
+    const int tiles = a.N / 128;
+    const int kbs = a.K / 256;
+    const int64_t words_per_row = a.K / 8;
+    const int64_t scales_per_row = a.K / 32;
+    const int64_t total = static_cast<int64_t>(a.E) * tiles * kbs * 1152;
+    uint8_t* blocks = a.out + kPackHeaderBytes;
+    uint32_t* flags = reinterpret_cast<uint32_t*>(a.out) + 7;
+    bool ok = true;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t b = i / 1152;
+        const int j = static_cast<int>(i - b * 1152);
+        const int kb = static_cast<int>(b % kbs);
+        const int t = static_cast<int>((b / kbs) % tiles);
+        const int64_t e = b / (static_cast<int64_t>(kbs) * tiles);
+        const int r = j < 1024 ? (j >> 2) & 127 : j - 1024;
+        const int row = a.kind == CHORD_PACK_GATE_UP ? (r < 64 ? 64 * t + r : a.N / 2 + 64 * t + r - 64)
+                                                     : 128 * t + r;
+        const int64_t grow = e * a.N + row;
+        uint4 v;
+        if (j < 1024) {
+            const int h = j >> 9;
+            const int c = (j & 3) ^ ((r >> 1) & 3);
+            v = *reinterpret_cast<const uint4*>(a.q + grow * words_per_row + kb * 32 + h * 16 + c * 4);
+        } else {
+            v = *reinterpret_cast<const uint4*>(a.sc + grow * scales_per_row + kb * 8);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                ok = ok && scale_in_range(w[q] & 0xFFFFu) && scale_in_range(w[q] >> 16);
+        }
+        *reinterpret_cast<uint4*>(blocks + b * kPackBlockBytes + static_cast<int64_t>(j) * 16) = v;
+    }
+    if (!ok)
+        atomicOr(flags, 1u);
+}
+
+cudaError_t launch_prepack(const PackArgs& a, int sms, cudaStream_t s)
+{
+    pack_header_kernel<<<1, 64, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    pack_kernel<<<8 * sms, 256, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_prep(const PrepArgs& a, int work_blocks, cudaStream_t s)

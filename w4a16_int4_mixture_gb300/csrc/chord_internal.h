@@ -35,6 +35,11 @@ struct GemmArgs {
     int n_tiles;              // output tiles per chunk
     int tpu;                  // tiles per work unit (n_tiles % tpu == 0; > 1 only when K is one stage)
     const uint16_t* scales;   // [E, N, K/32]
+    // prepacked weights (chord_w4a16_prepack; its header was checked by the
+    // prep kernel), or null: the codes and scales of K block j of tile t of
+    // expert e are block (e * n_tiles + t) * (K/256) + j of pk, in the
+    // shared-memory order of a code / scale stage
+    const uint8_t* pk;
     const Chunk* chunks;
     const int32_t* num_chunks;
     // epilogue
@@ -60,6 +65,12 @@ struct GemmArgs {
 constexpr int kSplitSlots = 160;
 // Fewest K stages in one piece of a split unit.
 constexpr int kSplitMinStages = 2;
+
+// prepacked weights (format in chord.h, chord_w4a16_prepack)
+constexpr uint32_t kPackMagic = 0x4B504843u;  // "CHPK"
+constexpr int kPackHeaderBytes = 256;
+constexpr int kPackCodeBytes = 16384;          // one 256-deep K block of a 128-row tile
+constexpr int kPackBlockBytes = kPackCodeBytes + 2048;
 
 constexpr int kGemmThreads = 512;  // 16 warps (the GEMM configurations may add a warp group)
 

@@ -6,15 +6,7 @@ namespace chord {
 cudaError_t launch_gemm_down(int cfg, const CUtensorMap& map, const CUtensorMap& smap, const CUtensorMap& bmap,
                              const GemmArgs& a, int grid, cudaStream_t s)
 {
-    switch (cfg) {
-    case kCfgD32: return launch_gemm_cfg<CfgD32<false>>(map, smap, bmap, a, grid, s);
-    case kCfgD64: return launch_gemm_cfg<CfgD64<false>>(map, smap, bmap, a, grid, s);
-    case kCfgD128: return launch_gemm_cfg<CfgD128<false>>(map, smap, bmap, a, grid, s);
-    case kCfgP192: return launch_gemm_cfg<CfgP192<false>>(map, smap, bmap, a, grid, s);
-    case kCfgS32: return launch_gemm_cfg<CfgS32>(map, smap, bmap, a, grid, s);
-    case kCfgS64: return launch_gemm_cfg<CfgS64>(map, smap, bmap, a, grid, s);
-    default: return cudaErrorInvalidValue;
-    }
+    return dispatch_down<false>(cfg, map, smap, bmap, a, grid, s);
 }
 
 int gemm_cfg_smem_down(int cfg)

@@ -6,13 +6,7 @@ namespace chord {
 cudaError_t launch_gemm_gate_up(int cfg, const CUtensorMap& map, const CUtensorMap& smap, const CUtensorMap& bmap,
                                 const GemmArgs& a, int grid, cudaStream_t s)
 {
-    switch (cfg) {
-    case kCfgD32: return launch_gemm_cfg<CfgD32<true>>(map, smap, bmap, a, grid, s);
-    case kCfgD64: return launch_gemm_cfg<CfgD64<true>>(map, smap, bmap, a, grid, s);
-    case kCfgD128: return launch_gemm_cfg<CfgD128<true>>(map, smap, bmap, a, grid, s);
-    case kCfgP192: return launch_gemm_cfg<CfgP192<true>>(map, smap, bmap, a, grid, s);
-    default: return cudaErrorInvalidValue;
-    }
+    return dispatch_gate_up<false>(cfg, map, smap, bmap, a, grid, s);
 }
 
 int gemm_cfg_smem_gate_up(int cfg)

@@ -9,10 +9,13 @@
 // optimisation / H200 and Blackwell indexed decode": dequantised weights take
 // the MMA-M operand), used here for every token count.
 //
-// Roles (16 warps, 20 for the down GEMM with token tiles <= 64):
+// Roles (16 warps; 20 for the down GEMM with token tiles <= 64 and for the
+// gate/up GEMM with three A stages):
 //   warp 0      code producer: packed INT4 codes of each K stage into a ring, one
-//               TMA box (gate and up halves as one 3-D box), L2 evict-first,
-//               and the group-32 scales (a TMA box, or cp.async for BK 128).
+//               TMA box (gate and up halves as one 4-D box), L2 evict-first,
+//               and the group-32 scales (a TMA box, or cp.async for BK 128);
+//               for prepacked weights one or two plain bulk copies of the
+//               stage's contiguous block instead.
 //   warp 1      token producer: the chunk's activation rows, contiguous in the
 //               B tensor map, as 128B-swizzled K-major TMA tiles (one 3-D box
 //               per stage for token tiles of up to 64 rows; the rows past the
@@ -25,7 +28,8 @@
 //               or bf16 row store.
 //   warps 16-19 (down GEMM with token tiles <= 64 only) a second epilogue
 //               group taking every other unit.
-//   warps 8-15  dequant, two warps per TMEM lane quadrant taking K stages in
+//   warps 8-15  dequant (8-19 for the gate/up GEMM with three A stages), two
+//               (three) warps per TMEM lane quadrant taking K stages in
 //               order from a shared counter: codes + scales from shared memory
 //               -> w = bf16((q - 8) * s), one rounding of the exact product as
 //               in the page's order (exact q - 8, then the scale multiply),
@@ -54,8 +58,8 @@ struct GemmCfg {
     static constexpr int TPU_MAX = ACCW / MAXN;
     static constexpr bool GATE_UP = GATE_UP_;
 
-    static constexpr int CODE_ROW = BK / 2;                 // bytes of codes per weight row
-    static constexpr int CODE_STAGE = 128 * CODE_ROW;
+    // codes of a stage: BK/128 halves of [128 tile rows][64 bytes], 64B swizzle
+    static constexpr int CODE_STAGE = 128 * (BK / 2);
     static constexpr int SCALE_ROW = BK / 16;               // bytes of scales per weight row
     static constexpr int SCALE_STAGE = 128 * SCALE_ROW;
     static constexpr int B_KBLK = BK / 64;                  // 128B swizzle atoms along K
@@ -74,7 +78,15 @@ struct GemmCfg {
     // a second group of four epilogue warps (warps 16-19) takes every other
     // unit, each group owning one accumulator buffer
     static constexpr int EPI_GROUPS = (!GATE_UP && MAXN <= 64) ? 2 : 1;
-    static constexpr int THREADS = 512 + 128 * (EPI_GROUPS - 1);
+    // dequant warps per TMEM lane quadrant.  Each holds one claimed K stage,
+    // so up to DQW stages are in dequant at once; their A slots (and code
+    // slots) must be distinct phases of the rings, hence DQW <= AS and KS.
+    // Three for the gate/up GEMM when it has three A stages: the dequant is
+    // the bound there (measured 145.6 -> 141.1 us for the EP8 decode gate/up);
+    // the down GEMM's 640 threads leave no registers for a fifth group.
+    static constexpr int DQW = (GATE_UP && AS >= 3) ? 3 : 2;
+    static constexpr int EPI1_WARP = 8 + 4 * DQW;  // first warp of the second epilogue group
+    static constexpr int THREADS = 32 * EPI1_WARP + 128 * (EPI_GROUPS - 1);
     // down: per epilogue warp a 16-column x 32-row fp32 tile to transpose the
     // accumulator so each lane owns four consecutive output rows of a column
     static constexpr int EPIT_BYTES = GATE_UP ? 0 : EPI_GROUPS * 4 * 16 * 32 * 4;
@@ -111,17 +123,20 @@ struct GemmCfg {
     static_assert(OFF_B % 1024 == 0 && B_REGION % 1024 == 0, "swizzle atoms need 1024B alignment");
     static_assert(MAXN % B_BOX_ROWS == 0 && (B_BOX_ROWS * 128) % 1024 == 0, "token boxes");
     static_assert(ACCB % EPI_GROUPS == 0, "each epilogue group owns whole accumulator buffers");
+    static_assert(DQW <= AS && DQW <= KS, "stages in dequant at once fit the A and code rings");
+    static_assert(THREADS <= 640, "register budget of one CTA per SM");
     static_assert(CODE_STAGE % 1024 == 0, "TMA destinations");
 };
 
-// 16-byte chunk c of row r of a TMA tile with 128B (BK=256) or 64B (BK=128) rows.
-template <int BK>
-__device__ __forceinline__ int code_chunk_swizzle(int c, int r)
+// Byte offset in a code stage of piece g (codes 32g .. 32g+31 of the stage,
+// one scale group, 16 bytes) of tile row r: halves of 128 codes, each 128
+// rows x 64 bytes with the 64-byte swizzle (piece c of a half at position
+// c ^ ((r >> 1) & 3)).  The TMA writes this layout and chord_w4a16_prepack
+// stores it.  The 32 rows a warp reads at once fall on distinct banks for
+// every 8 rows.
+__device__ __forceinline__ int code_piece_offset(int g, int r)
 {
-    if constexpr (BK == 256)
-        return c ^ (r & 7);
-    else
-        return c ^ ((r >> 1) & 3);
+    return (g >> 2) * 8192 + r * 64 + (((g & 3) ^ ((r >> 1) & 3)) << 4);
 }
 
 // bf16x2 helpers (single rounding each, round to nearest even)
@@ -199,7 +214,11 @@ struct WorkItem {
     int tail;   // split units: index of the unit among the split ones
 };
 
-template <class C>
+// PK: the weights are prepacked (chord_w4a16_prepack) and arrive by plain bulk
+// copies.  A template parameter, not a run-time switch: with both load paths
+// in one kernel the plain path ran 23 % slower (EP8 decode gate/up 139.5 ->
+// 171 us) although the branch was never taken.
+template <class C, bool PK>
 __global__ void __launch_bounds__(C::THREADS, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap codes_map,
                       const __grid_constant__ CUtensorMap scales_map,
@@ -260,7 +279,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             stage_ctr[qq] = 0;
         mbar_fence_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && !PK) {
         prefetch_tensormap(&codes_map);
         if constexpr (C::SCALES_TMA)
             prefetch_tensormap(&scales_map);
@@ -377,14 +396,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 const uint32_t dst = sbase + C::OFF_CODES + s * C::CODE_STAGE;
                 const uint32_t sdst = sbase + C::OFF_SCALES + s * C::SCALE_STAGE;
-                if (lane == 0) {
+                // prepacked: the stage's block (BK 256), or half h of it (BK 128)
+                const uint8_t* pblk = nullptr;
+                if constexpr (PK)
+                    pblk = args.pk + ((static_cast<int64_t>(e) * n_tiles + nt) * (args.K / 256) +
+                                      ks / (256 / C::BK)) *
+                                         kPackBlockBytes;
+                const int ph = C::BK == 256 ? 0 : (ks & 1);
+                if (PK && lane == 0) {
                     mbar_arrive_expect_tx(codes_full(s),
                                           C::CODE_STAGE + (C::SCALES_TMA ? C::SCALE_STAGE : 0));
-                    const int x = ks * (C::BK / 8);
+                    bulk_load(dst, pblk + ph * 8192, C::CODE_STAGE, codes_full(s), pol);
+                    if constexpr (C::SCALES_TMA)
+                        bulk_load(sdst, pblk + kPackCodeBytes, C::SCALE_STAGE, codes_full(s), pol);
+                } else if (!PK && lane == 0) {
+                    mbar_arrive_expect_tx(codes_full(s),
+                                          C::CODE_STAGE + (C::SCALES_TMA ? C::SCALE_STAGE : 0));
+                    const int kb = ks * (C::BK / 128);
                     if constexpr (C::GATE_UP)
-                        tma_load_3d(dst, &codes_map, x, row0, 0, codes_full(s), pol);
+                        tma_load_4d(dst, &codes_map, 0, row0, 0, kb, codes_full(s), pol);
                     else
-                        tma_load_2d(dst, &codes_map, x, row0, codes_full(s), pol);
+                        tma_load_3d(dst, &codes_map, 0, row0, kb, codes_full(s), pol);
                     if constexpr (C::SCALES_TMA) {
                         if constexpr (C::GATE_UP)
                             tma_load_3d(sdst, &scales_map, ks * (C::BK / 32), row0, 0, codes_full(s), pol);
@@ -397,8 +429,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     for (int rr = 0; rr < 4; ++rr) {
                         const int r = lane + 32 * rr;
                         const int grow = C::GATE_UP ? row0 + (r < 64 ? r : args.I + r - 64) : row0 + r;
-                        const uint16_t* src = args.scales + static_cast<int64_t>(grow) * (args.K / 32) +
-                                              ks * (C::BK / 32);
+                        const void* src =
+                            PK  ? static_cast<const void*>(pblk + kPackCodeBytes + r * 16 + ph * 8)
+                                : static_cast<const void*>(args.scales +
+                                                           static_cast<int64_t>(grow) * (args.K / 32) +
+                                                           ks * (C::BK / 32));
                         cp_async_8(sdst + r * C::SCALE_ROW, src);
                     }
                     cp_async_arrive_noinc(codes_full(s));
@@ -532,11 +567,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if ((warp >= 4 && warp < 8) || warp >= 16) {
+    } else if ((warp >= 4 && warp < 8) || warp >= C::EPI1_WARP) {
         // --------------------------------------------------------------- epilogue
         const int q = warp & 3;
-        const int egrp = warp >= 16 ? 1 : 0;  // epilogue group: units i with i % EPI_GROUPS == egrp
-        const int et = threadIdx.x - (egrp ? 512 : 128);  // 0..127 inside the epilogue group
+        const int egrp = warp >= C::EPI1_WARP ? 1 : 0;  // epilogue group: units i with i % EPI_GROUPS == egrp
+        const int et = threadIdx.x - (egrp ? 32 * C::EPI1_WARP : 128);  // 0..127 inside the epilogue group
         int esync = 0;
         const uint32_t epi_bar = epi_bar0 + 8u * egrp;
         // the four warps of the group meet here (bounded, unlike bar.sync)
@@ -779,9 +814,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
     } else if (warp >= 8) {
         // ---------------------------------------------------------------- dequant
-        // The two warps of each TMEM lane quadrant (warps q+8 and q+12) take K
-        // stages in order from a shared counter, each the next one not yet
-        // taken, so neither waits for the other's turn.
+        // The DQW warps of each TMEM lane quadrant (warps q+8, q+12 [, q+16])
+        // take K stages in order from a shared counter, each the next one not
+        // yet taken, so none waits for another's turn.
         const int q = warp & 3;
         int srow;
         if constexpr (C::GATE_UP)
@@ -808,7 +843,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     ok = false;
                     break;
                 }
-                const uint8_t* crow = smem + C::OFF_CODES + s * C::CODE_STAGE + srow * C::CODE_ROW;
+                const uint8_t* cstage = smem + C::OFF_CODES + s * C::CODE_STAGE;
                 uint32_t sc[C::BK / 64];  // two bf16 scales per 32-bit word
                 {
                     const uint8_t* sp = smem + C::OFF_SCALES + s * C::SCALE_STAGE + srow * C::SCALE_ROW;
@@ -836,8 +871,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // arithmetic of the next without running out of registers.
 #pragma unroll
                 for (int grp = 0; grp < C::BK / 32; ++grp) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(
-                        crow + (code_chunk_swizzle<C::BK>(grp, srow) << 4));
+                    const uint4 v = *reinterpret_cast<const uint4*>(cstage + code_piece_offset(grp, srow));
                     const ScalePair sp =
                         scale_pair(__byte_perm(sc[grp >> 1], 0, (grp & 1) ? 0x3232 : 0x1010));
                     uint32_t o[16];

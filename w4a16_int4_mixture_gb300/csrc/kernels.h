@@ -124,6 +124,11 @@ struct PrepArgs {
     int64_t zero_count;
     int32_t* fill_i32;  // set to -1
     int64_t fill_count;
+    // prepacked weights: the two packs' headers (gate/up, down) and what each
+    // must say {kind, experts at least, N, K}; on a mismatch both chunk lists
+    // are left empty (the GEMMs compute nothing) and CHORD_DEVERR_PACKED is set
+    const uint32_t* pk_hdr[2];
+    uint32_t pk_want[2][4];
     int* err;
 };
 
@@ -141,6 +146,16 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
 // Router, then align of its ids (a.topk_ids == r.ids): one CTA for both up to
 // 4096 pairs and 512 local experts, else a router kernel and launch_align.
 cudaError_t launch_route_align(const RouteArgs& r, const AlignArgs& a, cudaStream_t s);
+
+// chord_w4a16_prepack: header, then every 16-byte piece of every block.
+struct PackArgs {
+    int kind;               // CHORD_PACK_GATE_UP / CHORD_PACK_DOWN
+    const int32_t* q;       // [E, N, K/8]
+    const uint16_t* sc;     // [E, N, K/32]
+    int E, N, K;
+    uint8_t* out;           // header + E * (N/128) * (K/256) blocks
+};
+cudaError_t launch_prepack(const PackArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_prep(const PrepArgs& a, int work_blocks, cudaStream_t s);
 // Sets CHORD_DEVERR_SCALE_RANGE when a scale of a[0..na) or b[0..nb) (bf16
 // bits) is neither +-0 nor of magnitude in [2^-86, 2^35).

@@ -152,6 +152,62 @@ def moe_route_align(logits: torch.Tensor, k: int, E_local: int, block_m: int = 1
     return topk_ids, topk_weights, sorted_ids, expert_ids, ntp
 
 
+class PackedWeights:
+    """One layer's weights after chord_w4a16_prepack: w13 (kind GATE_UP) and
+    w2 (kind DOWN) as uint8 device buffers, with the sizes they were packed
+    for.  Pass it as w13_q (with w13_s, w2_q, w2_s None) to the layer calls."""
+
+    def __init__(self, w13: torch.Tensor, w2: torch.Tensor, E: int, H: int, I: int):
+        self.w13, self.w2, self.E, self.H, self.I = w13, w2, E, H, I
+
+
+def prepack_size(kind: int, E: int, N: int, K: int) -> int:
+    return int(lib().chord_w4a16_prepack_size(kind, E, N, K))
+
+
+def prepack(w_q: torch.Tensor, w_s: torch.Tensor, kind: int, out=None) -> torch.Tensor:
+    """One GEMM's codes [E, N, K/8] and scales [E, N, K/32] -> the packed
+    uint8 buffer (include/chord.h, chord_w4a16_prepack)."""
+    _req(w_q, "w_q", _I32, ndim=3)
+    dev = w_q.device
+    _req(w_s, "w_s", _BF16, dev, 3)
+    E, N, K8 = w_q.shape
+    K = K8 * 8
+    if tuple(w_s.shape) != (E, N, K // 32):
+        raise ValueError("scales must be [E, N, K/32]")
+    need = prepack_size(kind, E, N, K)
+    if need == 0:
+        B.check(-2, "chord_w4a16_prepack_size")
+    if out is None:
+        out = torch.empty(need, dtype=torch.uint8, device=dev)
+    else:
+        _req(out, "out", (torch.uint8,), dev, 1)
+    st = lib().chord_w4a16_prepack(kind, _p(w_q), _p(w_s), E, N, K, _p(out), out.numel(),
+                                   _stream(dev))
+    B.check(st, "chord_w4a16_prepack")
+    return out
+
+
+def prepack_weights(w13_q, w13_s, w2_q, w2_s) -> PackedWeights:
+    """Both GEMMs of a layer -> PackedWeights."""
+    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, w13_q.device)
+    return PackedWeights(prepack(w13_q, w13_s, B.PACK_GATE_UP), prepack(w2_q, w2_s, B.PACK_DOWN),
+                         E, H, I)
+
+
+def _weights(w13_q, w13_s, w2_q, w2_s, dev):
+    """-> (E, H, I, four pointers, extra flags) for plain or prepacked weights."""
+    if isinstance(w13_q, PackedWeights):
+        if w13_s is not None or w2_q is not None or w2_s is not None:
+            raise ValueError("with PackedWeights, w13_s, w2_q and w2_s must be None")
+        pw = w13_q
+        for n, t in (("packed w13", pw.w13), ("packed w2", pw.w2)):
+            _req(t, n, (torch.uint8,), dev, 1)
+        return pw.E, pw.H, pw.I, (_p(pw.w13), None, _p(pw.w2), None), B.FLAG_PREPACKED
+    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, dev)
+    return E, H, I, (_p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s)), 0
+
+
 def _check_weights(w13_q, w13_s, w2_q, w2_s, dev):
     _req(w13_q, "w13_q", _I32, dev, 3)
     _req(w13_s, "w13_s", _BF16, dev, 3)
@@ -178,7 +234,8 @@ def w4a16_moe_indexed(x, w13_q, w13_s, w2_q, w2_s, topk_weights, sorted_ids, exp
     h_out (bf16 [capacity, I]) optionally receives the gate/up output."""
     _req(x, "x", _BF16, ndim=2)
     dev = x.device
-    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, dev)
+    E, H, I, wp, wflag = _weights(w13_q, w13_s, w2_q, w2_s, dev)
+    flags |= wflag
     T = x.shape[0]
     if x.shape[1] != H:
         raise ValueError("x and weights disagree on H")
@@ -198,8 +255,8 @@ def w4a16_moe_indexed(x, w13_q, w13_s, w2_q, w2_s, topk_weights, sorted_ids, exp
             raise ValueError("h_out must be [capacity, I]")
     need = moe_workspace_size(T, k, E_global, E, H, I, block_m, capacity, flags)
     ws = workspace if workspace is not None else _pool.get(dev, need, "layer")
-    st = lib().chord_w4a16_moe_indexed(_p(x), T, H, I, E_global, E, k, _p(w13_q), _p(w13_s),
-                                       _p(w2_q), _p(w2_s), _p(topk_weights), _p(sorted_ids),
+    st = lib().chord_w4a16_moe_indexed(_p(x), T, H, I, E_global, E, k, *wp, _p(topk_weights),
+                                       _p(sorted_ids),
                                        _p(expert_ids), _p(num_tokens_padded), capacity, block_m,
                                        _p(ws), ws.numel(), _p(out), _p(h_out), flags,
                                        _stream(dev))
@@ -223,7 +280,8 @@ def w4a16_moe_grouped(mode: str, a, w13_q, w13_s, w2_q, w2_s, m_indices=None, ma
     Returns out_rows [M, H] (and out_tokens [T, H] when row_to_pair /
     topk_weights are given)."""
     dev = a.device
-    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, dev)
+    E, H, I, wp, wflag = _weights(w13_q, w13_s, w2_q, w2_s, dev)
+    flags |= wflag
     if mode == "contiguous":
         _req(a, "a", _BF16, dev, 2)
         _req(m_indices, "m_indices", _I32, dev, 1)
@@ -260,7 +318,7 @@ def w4a16_moe_grouped(mode: str, a, w13_q, w13_s, w2_q, w2_s, m_indices=None, ma
     need = grouped_workspace_size(mcode, M, H, I, E, T, k, with_tokens, exp_m)
     ws = workspace if workspace is not None else _pool.get(dev, need, "grouped")
     st = lib().chord_w4a16_moe_grouped(mcode, _p(a), M, H, I, E, _p(m_indices), _p(masked_m),
-                                       max_m, exp_m, _p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s),
+                                       max_m, exp_m, *wp,
                                        _p(row_to_pair), _p(topk_weights), T, k, _p(ws),
                                        ws.numel(), _p(out_rows), _p(out_tokens), _p(h_out),
                                        flags, _stream(dev))
@@ -271,7 +329,7 @@ def w4a16_moe_grouped(mode: str, a, w13_q, w13_s, w2_q, w2_s, m_indices=None, ma
 def w4a16_moe(x, topk_ids, topk_weights, w13_q, w13_s, w2_q, w2_s, E_global: int,
               expert_map=None, block_m: Optional[int] = None, flags: int = 0, out=None):
     """Align + indexed layer in one call (both graph-capturable)."""
-    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, x.device)
+    E, H, I, _, _ = _weights(w13_q, w13_s, w2_q, w2_s, x.device)
     T, k = topk_ids.shape
     bm = block_m or select_block_m(T, k, E_global, E, H, I)
     si, ei, ntp = moe_align(topk_ids, E_global, E, bm, expert_map=expert_map)
