@@ -114,3 +114,54 @@ def test_host_checks_reject_before_launch(lib):
 def test_status_strings(lib):
     for code in range(-9, 1):
         assert lib.chord_status_string(code)
+
+
+def test_prepack_size_and_host_checks(lib):
+    """chord_w4a16_prepack_size is the header plus one 18432-byte block per
+    (expert, 128-row tile, 256-deep K block); bad arguments are rejected on
+    the host before any device work."""
+    lib.chord_w4a16_prepack_size.restype = ctypes.c_size_t
+    assert lib.chord_w4a16_prepack_size(1, 48, 4096, 7168) == 256 + 48 * 32 * 28 * 18432
+    assert lib.chord_w4a16_prepack_size(2, 48, 7168, 2048) == 256 + 48 * 56 * 8 * 18432
+    for bad in [(3, 1, 128, 256), (1, 0, 128, 256), (1, 1, 64, 256), (2, 1, 128, 128),
+                (2, 1, 200, 256)]:
+        assert lib.chord_w4a16_prepack_size(*bad) == 0
+    vp = ctypes.c_void_p
+    fake = vp(4096)  # never dereferenced: the host checks come first
+    n = lib.chord_w4a16_prepack_size(2, 1, 128, 256)
+    assert lib.chord_w4a16_prepack(7, fake, fake, 1, 128, 256, fake, n, None) == -1
+    assert lib.chord_w4a16_prepack(2, fake, fake, 1, 100, 256, fake, n, None) == -2
+    assert lib.chord_w4a16_prepack(2, fake, fake, 1, 128, 300, fake, n, None) == -2
+    assert lib.chord_w4a16_prepack(2, None, fake, 1, 128, 256, fake, n, None) == -1
+    assert lib.chord_w4a16_prepack(2, fake, fake, 1, 128, 256, vp(4100), n, None) == -1
+    assert lib.chord_w4a16_prepack(2, fake, fake, 1, 128, 256, fake, n - 16, None) == -1
+
+
+def test_prepacked_flag_host_checks(lib):
+    """With CHORD_FLAG_PREPACKED the scale pointers must be NULL, without it
+    they must be given; unknown flag bits are rejected."""
+    vp = ctypes.c_void_p
+    f = vp(4096)
+    T, H, I, Eg, El, k, bm = 4, 256, 128, 8, 8, 2, 16
+    cap = lib.chord_moe_align_capacity(T, k, El, bm)
+
+    def call(w13_s, w2_s, flags):
+        return lib.chord_w4a16_moe_indexed(f, T, H, I, Eg, El, k, f, w13_s, f, w2_s, f, f, f, f,
+                                           cap, bm, f, 1 << 20, f, None, flags, None)
+
+    assert call(f, f, 16) == -1      # packed: scales must be NULL
+    assert call(None, None, 0) == -1  # plain: scales required
+    assert call(f, None, 16) == -1
+    assert call(None, None, 32) == -1  # unknown flag bit
+    g = lib.chord_w4a16_moe_grouped(0, f, 16, H, I, El, f, None, 0, 1, f, f, f, f, None, None,
+                                    0, 0, f, 1 << 20, f, None, None, 16, None)
+    assert g == -1
+
+
+def test_packed_weights_python_checks():
+    import w4a16_int4_mixture_gb300 as m
+    import torch
+    pw = m.PackedWeights(torch.empty(0, dtype=torch.uint8), torch.empty(0, dtype=torch.uint8),
+                         1, 256, 128)
+    with pytest.raises(ValueError):
+        m.ops._weights(pw, torch.empty(1), None, None, torch.device("cpu"))
