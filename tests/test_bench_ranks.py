@@ -72,3 +72,17 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "us/call" and d["value"] > 0
+
+
+def test_l2_flush_only_for_steps_that_fit_in_l2():
+    import bench
+    from w4a16_int4_mixture_gb300 import synth
+
+    def step_bytes(wl, T=None):
+        inp = synth.make_inputs(synth.workload(wl, T=T), weights=False)
+        return bench.workload_bytes_flops(inp)["layer"]["bytes"]
+
+    assert not bench.needs_l2_flush(step_bytes("ep8-decode"))  # ~1.2 GB of weights
+    assert not bench.needs_l2_flush(step_bytes("tp8", 128))    # ~1.1 GB
+    assert bench.needs_l2_flush(step_bytes("tp8", 1))          # 8 experts, ~25 MB
+    assert bench.needs_l2_flush(step_bytes("tiny"))
