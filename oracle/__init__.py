@@ -42,7 +42,11 @@ MUTATIONS = {
     "route_no_renorm": 14,
     "pack_no_swizzle": 15,
     "pack_tile_rows": 16,
+    "mx_scale_bias": 17,
+    "mx_no_subnormal": 18,
 }
+WEIGHT_FORMATS = {"int4": 0, "mxfp4": 1}
+_wfmt = 0
 
 
 def build(force: bool = False) -> str:
@@ -88,6 +92,12 @@ def _load():
         lib.oracle_route_topk.argtypes = [vp, i64, i64, i64, i32, vp, vp]
         lib.oracle_prepack.argtypes = [i32, vp, vp, i64, i64, i64, vp]
         lib.oracle_prepack.restype = i32
+        lib.oracle_set_weight_format.argtypes = [i32]
+        lib.oracle_get_weight_format.restype = i32
+        lib.oracle_e2m1.argtypes = [i32]
+        lib.oracle_e2m1.restype = ctypes.c_double
+        lib.oracle_e8m0.argtypes = [i32]
+        lib.oracle_e8m0.restype = ctypes.c_double
         lib.oracle_route_topk.restype = i32
         lib.oracle_expert_mlp.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, vp, vp, vp]
         lib.oracle_expert_mlp.restype = i32
@@ -130,6 +140,42 @@ class mutation:
         return False
 
 
+class weight_format:
+    """Context manager: the weight format the oracle reads.  "int4" (the
+    default): codes q with bf16 scales, w = (q - 8) * s.  "mxfp4": E2M1 codes
+    with one E8M0 scale byte per 32 input channels (uint8 [E, N, K/32] in
+    place of the bf16 scales), w = e2m1(q) * 2^(s - 127) (oracle.c, header)."""
+
+    def __init__(self, name: str):
+        self.code = WEIGHT_FORMATS[name]
+
+    def __enter__(self):
+        global _wfmt
+        self.prev = _wfmt
+        _wfmt = self.code
+        _load().oracle_set_weight_format(self.code)
+        return self
+
+    def __exit__(self, *exc):
+        global _wfmt
+        _wfmt = self.prev
+        _load().oracle_set_weight_format(self.prev)
+        return False
+
+
+def _s(a):
+    """Scales as the current weight format stores them."""
+    return _c(a, np.uint8 if _wfmt == 1 else np.uint16)
+
+
+def e2m1(q: int) -> float:
+    return float(_load().oracle_e2m1(int(q)))
+
+
+def e8m0(s: int) -> float:
+    return float(_load().oracle_e8m0(int(s)))
+
+
 def set_threads(n: int) -> None:
     _load().oracle_set_threads(int(n))
 
@@ -160,7 +206,7 @@ def code(wq: np.ndarray, K: int, n: int, c: int) -> int:
 def dequant(wq: np.ndarray, ws: np.ndarray, N: int, K: int) -> np.ndarray:
     """Dequantised [N, K] weight as float32 (every value a bf16 value)."""
     wq = _c(wq, np.int32)
-    ws = _c(ws, np.uint16)
+    ws = _s(ws)
     assert wq.size == N * K // 8 and ws.size == N * K // 32
     out = np.empty((N, K), dtype=np.float32)
     _load().oracle_dequant(_p(wq), _p(ws), N, K, _p(out))
@@ -204,6 +250,8 @@ def prepack(kind, w_q, w_s):
     """Storage order of chord_w4a16_prepack (oracle.c, prepack): kind 1
     (gate/up) or 2 (down), codes int32 [E, N, K/8] and scale bits uint16
     [E, N, K/32] -> the packed bytes (uint8)."""
+    if _wfmt != 0:
+        raise ValueError("prepack is defined for the INT4 format")
     q = _c(w_q, np.int32)
     sc = _c(w_s, np.uint16)
     E, N, K8 = q.shape
@@ -219,8 +267,8 @@ def expert_mlp(w13_q, w13_s, w2_q, w2_s, e, x_rows):
     x_rows = _c(x_rows, np.uint16)
     n, H = x_rows.shape
     I = w2_q.shape[2] * 8
-    w13_q, w13_s, w2_q, w2_s = (_c(w13_q, np.int32), _c(w13_s, np.uint16),
-                                _c(w2_q, np.int32), _c(w2_s, np.uint16))
+    w13_q, w13_s, w2_q, w2_s = (_c(w13_q, np.int32), _s(w13_s),
+                                _c(w2_q, np.int32), _s(w2_s))
     g = np.empty((n, I), np.float32)
     u = np.empty((n, I), np.float32)
     h = np.empty((n, I), np.uint16)
@@ -240,8 +288,8 @@ def moe_indexed(x, w13_q, w13_s, w2_q, w2_s, topk_weights, sorted_ids, expert_id
     T, H = x.shape
     E = w13_q.shape[0]
     I = w2_q.shape[2] * 8
-    w13_q, w13_s, w2_q, w2_s = (_c(w13_q, np.int32), _c(w13_s, np.uint16),
-                                _c(w2_q, np.int32), _c(w2_s, np.uint16))
+    w13_q, w13_s, w2_q, w2_s = (_c(w13_q, np.int32), _s(w13_s),
+                                _c(w2_q, np.int32), _s(w2_s))
     tw = _c(topk_weights, np.float32)
     sorted_ids = _c(sorted_ids, np.int32)
     expert_ids = _c(expert_ids, np.int32)
@@ -271,7 +319,7 @@ def moe_indexed_down(h_rows, w2_q, w2_s, topk_weights, sorted_ids, expert_ids, n
     h_rows = _c(h_rows, np.uint16)
     E, H = w2_q.shape[0], w2_q.shape[1]
     I = w2_q.shape[2] * 8
-    w2_q, w2_s = _c(w2_q, np.int32), _c(w2_s, np.uint16)
+    w2_q, w2_s = _c(w2_q, np.int32), _s(w2_s)
     tw = _c(topk_weights, np.float32)
     sorted_ids = _c(sorted_ids, np.int32)
     expert_ids = _c(expert_ids, np.int32)
@@ -292,7 +340,7 @@ def moe_grouped_down(mode, h_rows, w2_q, w2_s, m_indices=None, masked_m=None, ma
     h_rows = _c(h_rows, np.uint16)
     M, I = h_rows.shape
     E, H = w2_q.shape[0], w2_q.shape[1]
-    w2_q, w2_s = _c(w2_q, np.int32), _c(w2_s, np.uint16)
+    w2_q, w2_s = _c(w2_q, np.int32), _s(w2_s)
     mi, mm = _c(m_indices, np.int32), _c(masked_m, np.int32)
     r2p, tw = _c(row_to_pair, np.int32), _c(topk_weights, np.float32)
     out_rows = np.empty((M, H), np.uint16)
@@ -323,8 +371,8 @@ def moe_grouped(mode, a, w13_q, w13_s, w2_q, w2_s, m_indices=None, masked_m=None
     else:
         max_m = 0
     M, H = a.shape
-    w13_q, w13_s, w2_q, w2_s = (_c(w13_q, np.int32), _c(w13_s, np.uint16),
-                                _c(w2_q, np.int32), _c(w2_s, np.uint16))
+    w13_q, w13_s, w2_q, w2_s = (_c(w13_q, np.int32), _s(w13_s),
+                                _c(w2_q, np.int32), _s(w2_s))
     mi = _c(m_indices, np.int32)
     mm = _c(masked_m, np.int32)
     r2p = _c(row_to_pair, np.int32)

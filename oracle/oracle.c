@@ -47,6 +47,16 @@
  *      the k largest logits, ties to the lower expert id, in descending order;
  *      weight of a selected expert = its softmax probability over all
  *      E_global experts, renormalised over the k selected when asked.
+ * MXFP4 weights (the variant on the vLLM Kimi K3 page, "MXFP4 MoE"; the
+ * element and scale encodings are those of the OCP Microscaling formats the
+ * name refers to): with oracle_set_weight_format(1) every code is an FP4
+ * E2M1 number (bit 3 sign, bits 2..1 exponent with bias 1, bit 0 mantissa;
+ * exponent 0 is subnormal, m * 2^-1) and every group of 32 input channels
+ * shares one E8M0 scale byte s (2^(s - 127), s = 255 is NaN), stored uint8
+ * [E, N, K/32] in place of the bf16 scales.  W = RNE_bf16(e2m1(q) * 2^(s-127)),
+ * which is exact unless it overflows bf16.  The page names a "SiTU"
+ * activation for this variant without defining it; the MLP here keeps
+ * SiLU(gate) * up (R7).
  * Prepack (the storage order of chord_w4a16_prepack, stated in the library's
  * header chord.h; an offline rearrangement that the pages' grouped kernels
  * also make, "Kernel optimisation / grouped SM90 kernels"): no arithmetic,
@@ -88,6 +98,8 @@ enum {
     MUT_ROUTE_NO_RENORM = 14,  /* R14 violated: weights not renormalised */
     MUT_PACK_NO_SWIZZLE = 15,  /* prepack: pieces stored unpermuted */
     MUT_PACK_TILE_ROWS = 16,   /* prepack: gate/up tiles as 128 consecutive rows */
+    MUT_MX_SCALE_BIAS = 17,    /* MXFP4: scale 2^(s - 128) instead of 2^(s - 127) */
+    MUT_MX_NO_SUBNORMAL = 18,  /* MXFP4: exponent field 0 read as a normal number */
 };
 static int g_mutation = 0;
 void oracle_set_mutation(int m) { g_mutation = m; }
@@ -189,6 +201,40 @@ static void parallel_for(int64_t n, range_fn fn, void* ctx)
 /* ------------------------------------------------------------------------- */
 /* weights: unpack (R1) and dequantise (R2, R3, R4)                          */
 /* ------------------------------------------------------------------------- */
+/* 0: INT4 codes with bf16 scales; 1: MXFP4 (E2M1 codes, E8M0 scale bytes) */
+static int g_wfmt = 0;
+void oracle_set_weight_format(int f) { g_wfmt = f; }
+int oracle_get_weight_format(void) { return g_wfmt; }
+
+/* The scale array advanced by idx scales of the current format. */
+static const uint16_t* scales_at(const uint16_t* base, int64_t idx)
+{
+    if (g_wfmt == 1)
+        return (const uint16_t*)(const void*)((const uint8_t*)(const void*)base + idx);
+    return base + idx;
+}
+
+/* FP4 E2M1 value of a 4-bit code (exact in double). */
+double oracle_e2m1(int q)
+{
+    const int sign = (q >> 3) & 1;
+    const int ex = (q >> 1) & 3;
+    const int man = q & 1;
+    double v;
+    if (ex == 0 && g_mutation != MUT_MX_NO_SUBNORMAL)
+        v = 0.5 * man;                               /* subnormal: m * 2^(1 - bias) / 2 */
+    else
+        v = ldexp(1.0 + 0.5 * man, ex - 1);          /* (1 + m/2) * 2^(e - bias) */
+    return sign ? -v : v;
+}
+
+/* E8M0 scale byte -> 2^(s - 127); s = 255 is NaN. */
+double oracle_e8m0(int s)
+{
+    if (s == 255)
+        return NAN;
+    return ldexp(1.0, s - (g_mutation == MUT_MX_SCALE_BIAS ? 128 : 127));
+}
 
 /* 4-bit code of element (n, c) of a [N, K] weight stored as [N, K/8] words. */
 int oracle_code(const int32_t* wq, int64_t K, int64_t n, int64_t c)
@@ -202,19 +248,29 @@ int oracle_code(const int32_t* wq, int64_t K, int64_t n, int64_t c)
     return (int)((w >> (4 * i)) & 0xFu);
 }
 
-/* The scale of element (n, c): scales stored [N, K/32]. */
-static float scale_of(const uint16_t* ws, int64_t K, int64_t n, int64_t c)
+/* Index of the scale of element (n, c): scales stored [N, K/32]. */
+static int64_t scale_index(int64_t K, int64_t n, int64_t c)
 {
     int64_t g = c / 32;
     if (g_mutation == MUT_SCALE_GROUP)
         g = (g + 1) % (K / 32);
-    return oracle_bf16_to_f32(ws[n * (K / 32) + g]);
+    return n * (K / 32) + g;
 }
 
-/* W[n, c] = RNE_bf16( float(q - 8) * float(s) ): one rounding. */
+static float scale_of(const uint16_t* ws, int64_t K, int64_t n, int64_t c)
+{
+    return oracle_bf16_to_f32(ws[scale_index(K, n, c)]);
+}
+
+/* W[n, c] = RNE_bf16( float(q - 8) * float(s) ): one rounding.  (MXFP4:
+ * RNE_bf16( e2m1(q) * 2^(s - 127) ), the product formed in double.) */
 float oracle_dequant_one(const int32_t* wq, const uint16_t* ws, int64_t K, int64_t n, int64_t c)
 {
     int q = oracle_code(wq, K, n, c);
+    if (g_wfmt == 1) {
+        const uint8_t* sb = (const uint8_t*)(const void*)ws;
+        return rbf((float)(oracle_e2m1(q) * oracle_e8m0(sb[scale_index(K, n, c)])));
+    }
     float s = scale_of(ws, K, n, c);
     if (g_mutation == MUT_DEQUANT_FMA) /* magic-number form folded into one multiply-add */
         return rbf((float)(128 + q) * s - rbf(136.0f * s));
@@ -506,8 +562,9 @@ static int expert_mlp(const int32_t* w13_q, const uint16_t* w13_s, const int32_t
         free(W2);
         return -1;
     }
-    oracle_dequant(w13_q + e * (2 * I) * (H / 8), w13_s + e * (2 * I) * (H / 32), 2 * I, H, W13);
-    oracle_dequant(w2_q + e * H * (I / 8), w2_s + e * H * (I / 32), H, I, W2);
+    oracle_dequant(w13_q + e * (2 * I) * (H / 8), scales_at(w13_s, e * (2 * I) * (H / 32)), 2 * I, H,
+                   W13);
+    oracle_dequant(w2_q + e * H * (I / 8), scales_at(w2_s, e * H * (I / 32)), H, I, W2);
     mlp_ctx m = {W13, W2, H, I, nrows, xrows, g, u, h, y};
     parallel_for(I, mlp_gate_up, &m);
     parallel_for(H, mlp_down, &m);
@@ -687,7 +744,7 @@ int oracle_moe_indexed_down(const uint16_t* h_rows, int64_t T, int64_t H, int64_
         }
         if (n == 0)
             continue;
-        oracle_dequant(w2_q + e * H * (I / 8), w2_s + e * H * (I / 32), H, I, W2);
+        oracle_dequant(w2_q + e * H * (I / 8), scales_at(w2_s, e * H * (I / 32)), H, I, W2);
         mlp_ctx m = {NULL, W2, H, I, n, NULL, NULL, NULL, hbuf, y};
         parallel_for(H, mlp_down, &m);
         for (int64_t i = 0; i < n; ++i) {
@@ -741,7 +798,7 @@ int oracle_moe_grouped_down(int mode, const uint16_t* h_rows, int64_t M, int64_t
         }
         if (n == 0)
             continue;
-        oracle_dequant(w2_q + e * H * (I / 8), w2_s + e * H * (I / 32), H, I, W2);
+        oracle_dequant(w2_q + e * H * (I / 8), scales_at(w2_s, e * H * (I / 32)), H, I, W2);
         mlp_ctx m = {NULL, W2, H, I, n, NULL, NULL, NULL, hbuf, y};
         parallel_for(H, mlp_down, &m);
         for (int64_t i = 0; i < n; ++i) {

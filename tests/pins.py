@@ -71,6 +71,23 @@ def dequant_f64(wq: np.ndarray, ws: np.ndarray) -> np.ndarray:
     return rne_bf16((q - 8).astype(np.float64) * s_full)
 
 
+# FP4 E2M1 values of codes 0..7 as the OCP Microscaling formats list them;
+# codes 8..15 are the same magnitudes with the sign bit set
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def dequant_mx_f64(wq: np.ndarray, ws8: np.ndarray) -> np.ndarray:
+    """Reference MXFP4 dequant of one [N, K] weight: E2M1 code values from the
+    table above times 2^(s - 127) per 32 channels, float64 (exact for finite
+    values; bf16 rounding only changes values that overflow it)."""
+    q = decode_codes(wq)
+    mag = np.array(E2M1_VALUES)[q & 7]
+    v = np.where(q >= 8, -mag, mag)
+    K = q.shape[-1]
+    sc = np.repeat(ws8.astype(np.int64), 32, axis=-1)[..., :K]
+    return rne_bf16(np.ldexp(v, sc - 127))
+
+
 def silu64(v):
     v = np.asarray(v, dtype=np.float64)
     return v / (1.0 + np.exp(-v))
@@ -105,7 +122,7 @@ def tolerance_violation(out, ref) -> float:
 # --------------------------------------------------------------------------
 # brute force: one token at a time, fp64, straight from the definition
 # --------------------------------------------------------------------------
-def brute_force_token(inp: synth.MoEInputs, t: int, local_of_slot):
+def brute_force_token(inp: synth.MoEInputs, t: int, local_of_slot, deq=None):
     """fp64 output row of token t: sum over local slots j of
     w[t,j] * W2_e (bf16(silu(W13_e[:I] x) * (W13_e[I:] x))).  Also returns the
     per-slot pre-rounding (g, u) for finer checks."""
@@ -117,8 +134,8 @@ def brute_force_token(inp: synth.MoEInputs, t: int, local_of_slot):
         e = local_of_slot[t, j]
         if e < 0:
             continue
-        W13 = dequant_f64(inp.w13_q[e], inp.w13_s[e])
-        W2 = dequant_f64(inp.w2_q[e], inp.w2_s[e])
+        W13 = (deq or dequant_f64)(inp.w13_q[e], inp.w13_s[e])
+        W2 = (deq or dequant_f64)(inp.w2_q[e], inp.w2_s[e])
         g = W13[:s.I] @ x
         u = W13[s.I:] @ x
         h = rne_bf16(silu64(g) * u)
@@ -660,7 +677,63 @@ def pin_prepack_header_and_hand_cases():
     return True, "ok"
 
 
+def pin_mxfp4_dequant_exhaustive():
+    """MXFP4 dequant: all 16 E2M1 codes x all 256 E8M0 scale bytes against the
+    published value table and 2^(s - 127): finite products exact in bf16,
+    overflow to +-inf, s = 255 NaN."""
+    K = 256 * 32
+    codes = np.repeat(np.arange(16, dtype=np.uint32)[:, None], K, axis=1)
+    wq = (codes.reshape(16, K // 8, 8) << (4 * np.arange(8, dtype=np.uint32))).sum(
+        axis=-1, dtype=np.uint64).astype(np.uint32).view(np.int32)
+    ws = np.repeat(np.arange(256, dtype=np.uint8)[None, :], 16, axis=0)
+    with oracle.weight_format("mxfp4"):
+        got = oracle.dequant(wq, ws, 16, K).astype(np.float64)
+    sgn = np.where(np.arange(16) >= 8, -1.0, 1.0)[:, None]
+    mag = np.array(E2M1_VALUES)[np.arange(16) & 7][:, None]
+    ex = np.repeat(np.arange(256)[None, :], 32, axis=1)
+    want = np.ldexp(sgn * mag, ex - 127)
+    bf16_max = float(np.ldexp(2.0 - 2.0 ** -7, 127))
+    want = np.where(np.abs(want) > bf16_max, np.copysign(np.inf, want), want)
+    nan_cols = ex[0] == 255
+    if not np.all(np.isnan(got[:, nan_cols])):
+        return False, "scale byte 255 is not NaN"
+    ok = np.array_equal(got[:, ~nan_cols], want[:, ~nan_cols])
+    if not ok:
+        bad = np.argwhere(got[:, ~nan_cols] != want[:, ~nan_cols])[0]
+        return False, f"code {bad[0]} scale {bad[1] // 32}: {got[:, ~nan_cols][tuple(bad)]} != " \
+                      f"{want[:, ~nan_cols][tuple(bad)]}"
+    return True, "ok"
+
+
+def pin_mxfp4_brute_force(seed=31):
+    """A small layer with MXFP4 weights against the per-token fp64 brute force
+    on the table-based dequant (the same checks as the INT4 brute force)."""
+    inp = small_random_inputs(seed)
+    s = inp.shape
+    rng = np.random.default_rng(seed + 1)
+    inp.w13_s = synth.mx_scales(rng, s.E_local, 2 * s.I, s.H, center=124)
+    inp.w2_s = synth.mx_scales(rng, s.E_local, s.H, s.I, center=124)
+    lid = synth.local_ids(inp)
+    with oracle.weight_format("mxfp4"):
+        (sorted_ids, _, ntp), (out, h_rows, _) = oracle.run_workload(inp, want_h=True, want_y=True)
+    got = bf16_bits_to_f64(out)
+    worst = 0.0
+    ok = True
+    for t in range(s.T):
+        ref, parts = brute_force_token(inp, t, lid, deq=dequant_mx_f64)
+        for (j, e, g, u, h, y) in parts:
+            r = int(np.nonzero(sorted_ids[:ntp] == t * s.k + j)[0][0])
+            ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(h), 1e-30))[1] - 8)
+            if np.any(np.abs(bf16_bits_to_f64(h_rows[r]) - h) > ulp * 1.0001):
+                ok = False
+        worst = max(worst, rounding_ratio(got[t], ref))
+    ok = ok and worst <= 1.0
+    return ok, f"mxfp4 brute force worst ratio {worst:.3g}"
+
+
 ALL_PINS = {
+    "mxfp4_dequant_exhaustive": pin_mxfp4_dequant_exhaustive,
+    "mxfp4_brute_force": pin_mxfp4_brute_force,
     "prepack_positions": pin_prepack_positions,
     "prepack_header_and_hand_cases": pin_prepack_header_and_hand_cases,
     "route_brute_force": pin_route_brute_force,

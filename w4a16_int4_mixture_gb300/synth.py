@@ -108,6 +108,15 @@ def scales(rng: np.random.Generator, E: int, N: int, K: int, sigma: float = 0.02
     return _bf16_bits(s)
 
 
+def mx_scales(rng: np.random.Generator, E: int, N: int, K: int, center: int = 121) -> np.ndarray:
+    """MXFP4 block scales: one E8M0 byte per 32 input channels, uniform over
+    center-1 .. center+1 (2^-7 .. 2^-5 with the default, so that E2M1 codes
+    of magnitude up to 6 give weights of the INT4 draw's size).  uint8
+    [E, N, K/32]."""
+    assert K % 32 == 0
+    return rng.integers(center - 1, center + 2, size=(E, N, K // 32)).astype(np.uint8)
+
+
 def pack_codes(codes: np.ndarray) -> np.ndarray:
     """Pack explicit 4-bit codes [..., K] (values 0..15) into int32 words [..., K/8]
     in the storage order above.  Used to build structured test inputs."""
