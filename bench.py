@@ -255,6 +255,19 @@ def needs_l2_flush(step_bytes: int) -> bool:
     return step_bytes < 2 * L2_BYTES
 
 
+def replay_spread_us(ms_list):
+    """Median, 10th and 90th percentile of single-replay times (ms in, us out)."""
+    v = sorted(float(x) * 1e3 for x in ms_list)
+    if not v:
+        return None
+
+    def pct(q):
+        i = min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))
+        return round(v[i], 2)
+    return {"median": round(statistics.median(v), 2), "p10": pct(0.1), "p90": pct(0.9),
+            "replays": len(v)}
+
+
 def kernels_per_call(pairs: int, e_local: int) -> int:
     """Kernels of one align + indexed layer call: the align runs as one CTA up to
     4096 pairs and 512 local experts (aux_kernels.cu), else as three kernels;
@@ -371,6 +384,21 @@ def run_ours(args, rank, world, dev_index):
         local_ms = sum(a.elapsed_time(b) for a, b in pairs_ev) / args.steps
     ms = max_over_ranks(local_ms, world, dev)
 
+    # spread of single replays (after the timed region; not part of `value`):
+    # events around each of K more replays (L2 flushed before each when the
+    # step fits in it)
+    spread = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            spread[2 * i].record(stream)
+            graph.replay()
+            spread[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    replay_us = replay_spread_us([spread[2 * i].elapsed_time(spread[2 * i + 1])
+                                  for i in range(args.steps)])
+
     # per-stage times (eager launches with stage events on the same stream)
     chord.stage_timing_enable(True)
     with torch.cuda.stream(stream):
@@ -455,6 +483,7 @@ def run_ours(args, rank, world, dev_index):
                   "tensor_frac_sustained": round(layer_tflops / tfl_sus, 4),
                   "algorithmic_bytes": int(work["layer"]["bytes"]),
                   "algorithmic_flops": int(work["layer"]["flops"])},
+        "replay_us": replay_us,
         "stages_ms": {"prepare": round(stage[0], 5), "gate_up": round(stage[1], 5),
                       "down": round(stage[2], 5), "combine": round(stage[3], 5)},
         "roofline": roof,
@@ -488,18 +517,30 @@ def cpu_oracle_time(inp, max_tokens=None):
     return dt, T, oracle.num_threads()
 
 
-def cpu_baseline(inp):
+def cpu_baseline(inp, single_thread_tokens=16):
     """The oracle on the host cores, on the whole workload when it has at most
     1024 tokens, else on its first 512 tokens scaled by tokens (a bounded sample
-    of about 10-30 s)."""
+    of about 10-30 s); and on one thread over the first few tokens."""
+    import oracle
     s = inp.shape
     max_tok = s.T if s.T <= 1024 else 512
     dt, T, cores = cpu_oracle_time(inp, max_tok)
     per_call_us = dt * 1e6 * (s.T / T)
     sample = (f"CPU oracle (plain C, fp32) on {T} of {s.T} tokens of {s.name}: align + "
               f"gate/up + SiLU + down + combine, {dt:.2f} s wall; scaled by tokens to one call")
-    return {"value": round(per_call_us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": sample}
+    res = {"value": round(per_call_us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": sample}
+    oracle.set_threads(1)
+    try:
+        dt1, T1, _ = cpu_oracle_time(inp, single_thread_tokens)
+    finally:
+        oracle.set_threads(0)
+    res["single_thread"] = {
+        "value": round(dt1 * 1e6 * (s.T / T1), 1), "unit": UNIT, "cores": 1,
+        "sample": f"the first {T1} tokens on one thread, {dt1:.2f} s wall; scaled by tokens "
+                  f"(each touched expert is dequantised once per call, so a short sample "
+                  f"overstates the per-token cost)"}
+    return res
 
 
 def run_reference(args):

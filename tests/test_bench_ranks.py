@@ -86,3 +86,17 @@ def test_l2_flush_only_for_steps_that_fit_in_l2():
     assert not bench.needs_l2_flush(step_bytes("tp8", 128))    # ~1.1 GB
     assert bench.needs_l2_flush(step_bytes("tp8", 1))          # 8 experts, ~25 MB
     assert bench.needs_l2_flush(step_bytes("tiny"))
+
+
+def test_cpu_baseline_and_replay_spread():
+    import bench
+    import oracle
+    from w4a16_int4_mixture_gb300 import synth
+    oracle.build()
+    cb = bench.cpu_baseline(synth.make_inputs(synth.workload("tiny")), single_thread_tokens=4)
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+    assert oracle.num_threads() == cb["cores"]  # restored after the one-thread run
+    sp = bench.replay_spread_us([0.2, 0.1, 0.3, 0.25, 0.15])
+    assert sp == {"median": 200.0, "p10": 100.0, "p90": 300.0, "replays": 5}
+    assert bench.replay_spread_us([]) is None
