@@ -165,3 +165,16 @@ def test_packed_weights_python_checks():
                          1, 256, 128)
     with pytest.raises(ValueError):
         m.ops._weights(pw, torch.empty(1), None, None, torch.device("cpu"))
+
+
+def test_empty_calls_are_no_ops(lib):
+    """T = 0 (indexed) and M = 0 without a token combine (grouped) launch
+    nothing and succeed before any pointer or device is looked at."""
+    assert lib.chord_w4a16_moe_indexed(None, 0, 256, 128, 8, 8, 2, None, None, None, None, None,
+                                       None, None, None, 0, 16, None, 0, None, None, 0, None) == 0
+    assert lib.chord_w4a16_moe_grouped(0, None, 0, 256, 128, 8, None, None, 0, 1, None, None,
+                                       None, None, None, None, 0, 0, None, 0, None, None, None, 0,
+                                       None) == 0
+    # and shape checks still come first
+    assert lib.chord_w4a16_moe_indexed(None, 0, 100, 128, 8, 8, 2, None, None, None, None, None,
+                                       None, None, None, 0, 16, None, 0, None, None, 0, None) == -2
