@@ -384,7 +384,21 @@ def pin_token_permutation(seed=31):
 def pin_cross_layout(seed=41):
     """Indexed, grouped-contiguous and grouped-masked layers agree bit-exactly on
     the same draw (per-row outputs and token outputs)."""
+    return _cross_layout(small_random_inputs(seed))
+
+
+def pin_cross_layout_mxfp4(seed=43):
+    """The same agreement with MXFP4 weights."""
     inp = small_random_inputs(seed)
+    s = inp.shape
+    rng = np.random.default_rng(seed + 1)
+    inp.w13_s = synth.mx_scales(rng, s.E_local, 2 * s.I, s.H, center=124)
+    inp.w2_s = synth.mx_scales(rng, s.E_local, s.H, s.I, center=124)
+    with oracle.weight_format("mxfp4"):
+        return _cross_layout(inp)
+
+
+def _cross_layout(inp):
     s = inp.shape
     _, (out, h_rows, y_pairs) = oracle.run_workload(inp, want_h=True, want_y=True)
     a2, m_idx, r2p = synth.grouped_contiguous_layout(inp, align=8)
@@ -400,7 +414,7 @@ def pin_cross_layout(seed=41):
     ok &= np.array_equal(rows_c[valid], f64_to_bf16_bits(rne_bf16(y_pairs[r2p[valid]])))
     v3 = r2p3 >= 0
     ok &= np.array_equal(rows_m[v3], f64_to_bf16_bits(rne_bf16(y_pairs[r2p3[v3]])))
-    return bool(ok), "layouts disagree"
+    return bool(ok), "ok" if ok else "layouts disagree"
 
 
 def check_align(topk_ids, E_global, expert_map, E_local, bm, sorted_ids, expert_ids, ntp):
@@ -734,6 +748,7 @@ def pin_mxfp4_brute_force(seed=31):
 ALL_PINS = {
     "mxfp4_dequant_exhaustive": pin_mxfp4_dequant_exhaustive,
     "mxfp4_brute_force": pin_mxfp4_brute_force,
+    "cross_layout_mxfp4": pin_cross_layout_mxfp4,
     "prepack_positions": pin_prepack_positions,
     "prepack_header_and_hand_cases": pin_prepack_header_and_hand_cases,
     "route_brute_force": pin_route_brute_force,

@@ -198,15 +198,21 @@ class MoEInputs:
     expert_map: np.ndarray | None
 
 
-def make_inputs(s: MoEShape, seed: int | None = None, weights: bool = True) -> MoEInputs:
-    """Draw every input of one workload from numpy.random.default_rng(seed)."""
+def make_inputs(s: MoEShape, seed: int | None = None, weights: bool = True,
+                weight_format: str = "int4") -> MoEInputs:
+    """Draw every input of one workload from numpy.random.default_rng(seed).
+    weight_format "mxfp4" draws E8M0 scale bytes (mx_scales) instead of bf16
+    scales; the codes are uniform 4-bit values either way."""
     rng = np.random.default_rng(s.seed if seed is None else seed)
     E, H, I = s.E_local, s.H, s.I
+    if weight_format not in ("int4", "mxfp4"):
+        raise ValueError(f"unknown weight format {weight_format!r}")
+    draw_scales = scales if weight_format == "int4" else mx_scales
     if weights:
         w13_q = codes_words(rng, E, 2 * I, H)
-        w13_s = scales(rng, E, 2 * I, H)
+        w13_s = draw_scales(rng, E, 2 * I, H)
         w2_q = codes_words(rng, E, H, I)
-        w2_s = scales(rng, E, H, I)
+        w2_s = draw_scales(rng, E, H, I)
     else:
         w13_q = w13_s = w2_q = w2_s = None
     x = activations(rng, s.T, H)
