@@ -263,7 +263,9 @@ chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global,
  * 18432 (the same as codes + scales, plus the header).
  *
  *   w_q, w_s   device, as above (read only)
- *   packed     device, >= packed_bytes, 16-byte aligned; written entirely
+ *   packed     device, >= packed_bytes, 16-byte aligned; written entirely.
+ *              The layer calls read a pack through its header alone: it must
+ *              stay whole (chord_w4a16_prepack_size bytes) while in use.
  * Asynchronous on `stream`; two kernels; graph capturable.
  */
 #define CHORD_PACK_GATE_UP 1

@@ -105,17 +105,28 @@ def _status(chord, fn):
 def test_mismatched_pack_is_reported(chord):
     inp = small(20, 2, 4, 4, 256, 256, 75, emap=False)
     pw, w = _packed(chord, inp)
-    # the gate/up pack given as the down pack (and the reverse): kinds differ
-    swapped = chord.PackedWeights(pw.w2, pw.w13, pw.E, pw.H, pw.I)
+    # the gate/up pack given as the down pack (and the reverse): kinds differ.
+    # Each goes into a buffer of the size its slot needs, so the host's size
+    # check passes and the device's header check decides.
+    a = torch.zeros(pw.w13.numel(), dtype=torch.uint8, device=DEV)
+    a[:pw.w2.numel()] = pw.w2
+    b = pw.w13[:pw.w2.numel()].clone()
+    swapped = chord.PackedWeights(a, b, pw.E, pw.H, pw.I)
     st = _status(chord, lambda: run_indexed_full(chord, inp, weights=(swapped, None, None, None)))
     assert st == ERR_PACKED
-    # a pack of fewer experts than the call reads
+    # a pack of fewer experts than the call reads, in a buffer of the full size
+    # (so that only the header tells)
     inp2 = small(20, 2, 4, 4, 256, 256, 76, emap=False)
     w2 = weights_to(inp2, DEV)
-    short = chord.PackedWeights(chord.prepack(w2[0][:2].contiguous(), w2[1][:2].contiguous(), 1),
-                                pw.w2, pw.E, pw.H, pw.I)
+    full = torch.empty_like(pw.w13)
+    chord.prepack(w2[0][:2].contiguous(), w2[1][:2].contiguous(), 1, out=full)
+    short = chord.PackedWeights(full, pw.w2, pw.E, pw.H, pw.I)
     st = _status(chord, lambda: run_indexed_full(chord, inp, weights=(short, None, None, None)))
     assert st == ERR_PACKED
+    # a buffer shorter than a pack of the call's sizes is refused on the host
+    cut = chord.PackedWeights(pw.w13[:-16], pw.w2, pw.E, pw.H, pw.I)
+    with pytest.raises(ValueError):
+        run_indexed_full(chord, inp, weights=(cut, None, None, None))
     # the context is fine afterwards
     verify_indexed(inp, run_indexed_full(chord, inp, weights=(pw, None, None, None)),
                    label="after a mismatched pack")

@@ -201,8 +201,13 @@ def _weights(w13_q, w13_s, w2_q, w2_s, dev):
         if w13_s is not None or w2_q is not None or w2_s is not None:
             raise ValueError("with PackedWeights, w13_s, w2_q and w2_s must be None")
         pw = w13_q
-        for n, t in (("packed w13", pw.w13), ("packed w2", pw.w2)):
+        need = (prepack_size(B.PACK_GATE_UP, pw.E, 2 * pw.I, pw.H),
+                prepack_size(B.PACK_DOWN, pw.E, pw.H, pw.I))
+        for n, t, nb in (("packed w13", pw.w13, need[0]), ("packed w2", pw.w2, need[1])):
             _req(t, n, (torch.uint8,), dev, 1)
+            # (the device checks the header; a short buffer would be read past its end)
+            if t.numel() < nb:
+                raise ValueError(f"{n}: {t.numel()} bytes, a pack of these sizes has {nb}")
         return pw.E, pw.H, pw.I, (_p(pw.w13), None, _p(pw.w2), None), B.FLAG_PREPACKED
     E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, dev)
     return E, H, I, (_p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s)), 0
