@@ -77,7 +77,13 @@ typedef enum {
 #define CHORD_FLAG_VALIDATE 1      /* synchronise the stream after the call and turn the
                                       device error word into the status (not capturable) */
 #define CHORD_FLAG_DETERMINISTIC 2 /* per-pair fp32 down outputs + ordered combine instead of
-                                      fp32 reductions into the token rows */
+                                      fp32 reductions into the token rows.  Without it the
+                                      indexed call (for outputs of up to 96 MB of fp32 token
+                                      rows) and the grouped call's token output add the pairs
+                                      of a token in the order their reductions reach memory,
+                                      which changes from run to run: the result is within
+                                      the tolerance but not bit-reproducible.  With it the
+                                      indexed output is bit-identical run to run. */
 
 #define CHORD_FLAG_TEST_SKIP_ARRIVE 4 /* test hook: the gate/up GEMM drops one mbarrier arrival
                                          (first K stage, CTA 0), so that a bounded device wait
@@ -185,9 +191,11 @@ chord_status chord_moe_align(const int32_t* topk_ids, int64_t T, int k, int E_gl
  * loads it until the process exits.  Limit: ceil(T*k/256) * E_local must not
  * exceed 1048512 (T*k up to 261888 pairs at the largest E_local of 1024, or
  * up to about 5.5 million pairs at 48 local experts); larger problems return
- * CHORD_ERR_UNSUPPORTED_SHAPE.  The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress), so make
- * that first call before capturing a stream on that device.  All calls share
+ * CHORD_ERR_UNSUPPORTED_SHAPE (checked before any pointer is looked at).  The
+ * first call in a CUDA context of a device looks up the array's device address
+ * (cudaGetSymbolAddress), and does so again when the device's current context
+ * has changed since (a symbol address belongs to one context), so make the
+ * first call after a context is created before capturing a stream in it.  All calls share
  * the array: calls whose work overlaps on the GPU (different streams, or
  * different host threads) race and must not be issued; each call rewrites all
  * the scratch it reads.  Routing errors are recorded in the array and are not
@@ -307,7 +315,8 @@ chord_status chord_w4a16_prepack(int kind, const int32_t* w_q, const uint16_t* w
  *                < num_tokens_padded; sentinel rows get 0) instead of into the
  *                workspace, so a caller can inspect or reuse it
  *   flags        CHORD_FLAG_* ; CHORD_FLAG_DETERMINISTIC gives run-to-run
- *                bit-identical outputs (slots summed in a fixed order)
+ *                bit-identical outputs (slots summed in a fixed order); the
+ *                default fp32 reductions are not bit-reproducible run to run
  * Limits (CHORD_ERR_UNSUPPORTED_SHAPE otherwise): H % 256 == 0, I % 128 == 0,
  *   1 <= k <= 32, E_local >= 1, T*k < 2^31, block_m in [1, 256].
  * Work schedule of both GEMMs: one CTA per SM takes (chunk of rows, weight

@@ -45,22 +45,13 @@ int gemm_cfg_smem(int cfg, bool gate_up)
     return gate_up ? gemm_cfg_smem_gate_up(cfg) : gemm_cfg_smem_down(cfg);
 }
 
-namespace {
-
-constexpr size_t kAlign = 256;
-inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
 // ---------------------------------------------------------------------------
 // device properties
 // ---------------------------------------------------------------------------
-struct DeviceInfo {
-    int device = -1;
-    int sms = 0;
-    bool ok = false;
-};
-
+namespace {
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
+}  // namespace
 
 chord_status device_info(DeviceInfo* out)
 {
@@ -82,6 +73,13 @@ chord_status device_info(DeviceInfo* out)
     *out = d;
     return d.ok ? CHORD_OK : CHORD_ERR_NO_DEVICE;
 }
+
+chord_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CHORD_OK : CHORD_ERR_CUDA; }
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ---------------------------------------------------------------------------
 // tensor maps, memoised by everything that goes into the encoding
@@ -438,8 +436,6 @@ struct StageMarks {
         g_prof.push_back(call);
     }
 };
-
-chord_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CHORD_OK : CHORD_ERR_CUDA; }
 
 chord_status check_ws(void* ws, size_t bytes, size_t need)
 {

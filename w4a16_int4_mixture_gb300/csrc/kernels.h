@@ -41,6 +41,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// The current device: its index and SM count; CHORD_ERR_NO_DEVICE unless it is
+// an sm_103 GPU (api.cu; the attributes are read once per device).
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    bool ok = false;
+};
+chord_status device_info(DeviceInfo* out);
+// CHORD_OK for cudaSuccess, else CHORD_ERR_CUDA.
+chord_status from_cuda(cudaError_t e);
+
 struct AlignArgs {
     const int32_t* topk_ids;
     int64_t num_pairs;  // T*k, also the sentinel

@@ -8,9 +8,12 @@
 // error word) in a fixed, file-scope device array instead of a workspace.
 //
 // The array is kScratchInts int32 (4 MiB) and lives on every GPU that loads the
-// library until the process exits.  Its device address is looked up once per
-// device with cudaGetSymbolAddress (the host-side name of a __device__ array is
-// only a stand-in, never a device pointer).
+// library until the process exits.  Its device address is looked up with
+// cudaGetSymbolAddress (the host-side name of a __device__ array is only a
+// stand-in, never a device pointer) on the first call in each CUDA context of
+// a device, and looked up again when the device's current context changes (a
+// symbol address belongs to the context that loaded the module).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -26,24 +29,43 @@ constexpr int64_t kErrInts = 64;           // first 256 bytes: the error word
 
 static __device__ __align__(256) int32_t g_align_scratch[kScratchInts];
 
-std::mutex g_scratch_mu;
-int32_t* g_scratch_ptr[64] = {nullptr};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
-// Device address of the scratch array on the current device (set-up on the
-// first call per device).
-chord_status scratch_on_current_device(int32_t** out)
+std::mutex g_scratch_mu;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+struct ScratchAddr {
+    CUcontext ctx;
+    int32_t* ptr;
+};
+ScratchAddr g_scratch[64] = {};
+
+// Device address of the scratch array in the current context of the current
+// device (looked up on the first call in that context).
+chord_status scratch_on_current_device(int dev, int32_t** out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return CHORD_ERR_NO_DEVICE;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_align_scratch) != cudaSuccess || p == nullptr)
+    if (!g_ctx_get_current) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
             return CHORD_ERR_CUDA;
-        g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+        g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
     }
-    *out = g_scratch_ptr[dev];
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+        return CHORD_ERR_CUDA;
+    ScratchAddr& a = g_scratch[dev];
+    if (a.ptr == nullptr || a.ctx != ctx) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_align_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return CHORD_ERR_CUDA;
+        a.ctx = ctx;
+        a.ptr = static_cast<int32_t*>(p);
+    }
+    *out = a.ptr;
     return CHORD_OK;
 }
 
@@ -61,20 +83,25 @@ extern "C" chord_status chord_moe_align_noalloc(const int32_t* topk_ids, int64_t
     if (T < 0 || k < 1 || k > 32 || E_global < 1 || E_local < 1 || E_local > 1024 || block_m < 1 ||
         block_m > 256)
         return CHORD_ERR_INVALID_ARG;
-    if (!expert_map && E_local != E_global)
-        return CHORD_ERR_INVALID_ARG;
     if (T * k >= (int64_t(1) << 31))
         return CHORD_ERR_UNSUPPORTED_SHAPE;
+    // sizes first: a problem beyond the fixed scratch array is refused before
+    // any pointer is looked at
+    const int64_t tiles = (T * k + 255) / 256;
+    if ((tiles > 0 ? tiles : 1) * E_local > kScratchInts - kErrInts)
+        return CHORD_ERR_UNSUPPORTED_SHAPE;
+    if (!expert_map && E_local != E_global)
+        return CHORD_ERR_INVALID_ARG;
     if (!sorted_ids || !expert_ids || !num_tokens_padded || (T > 0 && !topk_ids))
         return CHORD_ERR_INVALID_ARG;
     if (capacity < chord_moe_align_capacity(T, k, E_local, block_m) || capacity % block_m != 0)
         return CHORD_ERR_CAPACITY;
-    const int64_t tiles = (T * k + 255) / 256;
-    if ((tiles > 0 ? tiles : 1) * E_local > kScratchInts - kErrInts)
-        return CHORD_ERR_UNSUPPORTED_SHAPE;  // beyond the fixed scratch array
-    int32_t* scratch = nullptr;
-    chord_status st = scratch_on_current_device(&scratch);
+    DeviceInfo dev;
+    chord_status st = device_info(&dev);
     if (st != CHORD_OK)
+        return st;
+    int32_t* scratch = nullptr;
+    if ((st = scratch_on_current_device(dev.device, &scratch)) != CHORD_OK)
         return st;
     AlignArgs a{};
     a.topk_ids = topk_ids;
@@ -93,6 +120,5 @@ extern "C" chord_status chord_moe_align_noalloc(const int32_t* topk_ids, int64_t
     a.n_tiles = static_cast<int>(tiles);
     a.err = scratch;
     PdlScope pdl(T * k <= kPdlMaxRows);
-    return launch_align(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CHORD_OK
-                                                                              : CHORD_ERR_CUDA;
+    return from_cuda(launch_align(a, static_cast<cudaStream_t>(stream)));
 }

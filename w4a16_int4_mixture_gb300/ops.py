@@ -333,11 +333,20 @@ def w4a16_moe_grouped(mode: str, a, w13_q, w13_s, w2_q, w2_s, m_indices=None, ma
 
 def w4a16_moe(x, topk_ids, topk_weights, w13_q, w13_s, w2_q, w2_s, E_global: int,
               expert_map=None, block_m: Optional[int] = None, flags: int = 0, out=None):
-    """Align + indexed layer in one call (both graph-capturable)."""
+    """Align + indexed layer in one call (both graph-capturable).  The routing
+    layout goes into per-device buffers reused from call to call (like the
+    workspaces), so a call allocates nothing once the buffers are large
+    enough; calls on different streams of one device share them and must not
+    overlap."""
     E, H, I, _, _ = _weights(w13_q, w13_s, w2_q, w2_s, x.device)
     T, k = topk_ids.shape
     bm = block_m or select_block_m(T, k, E_global, E, H, I)
-    si, ei, ntp = moe_align(topk_ids, E_global, E, bm, expert_map=expert_map)
+    cap = moe_align_capacity(T, k, E, bm)
+    nblk = cap // bm
+    nb = 4 * (cap + nblk + 1)
+    buf = _pool.get(x.device, nb, "routing")[:nb].view(torch.int32)
+    si, ei, ntp = buf[:cap], buf[cap:cap + nblk], buf[cap + nblk:cap + nblk + 1]
+    moe_align(topk_ids, E_global, E, bm, expert_map=expert_map, capacity=cap, out=(si, ei, ntp))
     return w4a16_moe_indexed(x, w13_q, w13_s, w2_q, w2_s, topk_weights, si, ei, ntp, bm,
                              E_global, out=out, flags=flags)
 
