@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only the headline configuration (default: also every other "
+                         "configuration, under the `configs` key)")
     return ap.parse_args()
 
 
@@ -78,8 +81,11 @@ def workload_bytes_flops(inp):
     touched = np.unique(lid[lid >= 0])
     pairs = int(np.count_nonzero(lid >= 0))
     tokens = int(np.count_nonzero((lid >= 0).any(axis=1)))
-    w13 = 2 * s.I * s.H // 2 + 2 * s.I * (s.H // 32) * 2
-    w2 = s.H * s.I // 2 + s.H * (s.I // 32) * 2
+    # scale bytes per group of 32: bf16 (INT4) or one E8M0 byte (MXFP4; its pack
+    # holds them widened to bf16, but the format's own traffic is counted)
+    sb = 1 if getattr(inp.w13_s, "dtype", None) == np.uint8 else 2
+    w13 = 2 * s.I * s.H // 2 + 2 * s.I * (s.H // 32) * sb
+    w2 = s.H * s.I // 2 + s.H * (s.I // 32) * sb
     n = len(touched)
     gate_up = {"weights": n * w13, "x": tokens * s.H * 2, "h": pairs * s.I * 2,
                "flops": 2 * pairs * 2 * s.I * s.H}
@@ -233,14 +239,15 @@ class Clocks:
                 "power_w_max": max(pw) if pw else None, "sampler": self.source}
 
 
-def device_inputs(inp, torch, dev):
+def device_inputs(inp, torch, dev, weights=True):
     def t(a, bf16=False):
         a = np.ascontiguousarray(a)
         x = torch.from_numpy(a.view(np.int16) if bf16 else a)
         return (x.view(torch.bfloat16) if bf16 else x).to(dev)
-    d = {"x": t(inp.x, True), "w13_q": t(inp.w13_q), "w13_s": t(inp.w13_s, True),
-         "w2_q": t(inp.w2_q), "w2_s": t(inp.w2_s, True), "ids": t(inp.topk_ids),
-         "tw": t(inp.topk_weights)}
+    d = {"x": t(inp.x, True), "ids": t(inp.topk_ids), "tw": t(inp.topk_weights)}
+    if weights:
+        d.update({"w13_q": t(inp.w13_q), "w13_s": t(inp.w13_s, True), "w2_q": t(inp.w2_q),
+                  "w2_s": t(inp.w2_s, True)})
     d["emap"] = None if inp.expert_map is None else t(inp.expert_map)
     return d
 
@@ -292,6 +299,309 @@ def whole_job_us_per_call(max_ms: float, world: int) -> float:
     return round(max_ms * 1e3 / max(world, 1), 2)
 
 
+def layer_weights(chord, d, packed: bool):
+    """The four weight arguments of the layer calls: plain device tensors, or
+    packed once with chord_w4a16_prepack (before anything is timed, like
+    loading the weights)."""
+    import torch
+    w = (d["w13_q"], d["w13_s"], d["w2_q"], d["w2_s"])
+    if packed:
+        w = (chord.prepack_weights(*w), None, None, None)
+        torch.cuda.synchronize()
+    return w
+
+
+def capture(step, stream):
+    """Three eager calls, then one CUDA graph of `step` on `stream`."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    torch.cuda.synchronize()
+    return graph
+
+
+def time_graph(graph, stream, steps, warmup, flush, barrier=None):
+    """Mean ms of one replay over `steps` timed replays after `warmup` untimed
+    ones: CUDA events around the whole run, or (flush given: a step that could
+    stay in L2) around each replay with the flush buffer written in between,
+    outside the events."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        if flush is None:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            e1.record(stream)
+        else:
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(steps)]
+            for a, b in pairs:
+                flush.zero_()
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    if flush is None:
+        return e0.elapsed_time(e1) / steps
+    return sum(a.elapsed_time(b) for a, b in pairs) / steps
+
+
+def replay_spread(graph, stream, steps, flush):
+    """Single-replay times (after the timed region; not part of `value`)."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            if flush is not None:
+                flush.zero_()
+            ev[2 * i].record(stream)
+            graph.replay()
+            ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    return replay_spread_us([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)])
+
+
+def stage_times(chord, step, stream, calls):
+    """Per-stage ms (prepare, gate_up, down, combine) of eager calls, from the
+    library's stage events on the same stream."""
+    import torch
+    chord.stage_timing_enable(True)
+    with torch.cuda.stream(stream):
+        for _ in range(calls):
+            step()
+    stage_ms, n = chord.stage_timing_read()
+    chord.stage_timing_enable(False)
+    return [v / max(n, 1) for v in stage_ms]
+
+
+def roofline(work, stage, layer_ms, decode, label):
+    """The dominant kernel's roofline (the gate/up GEMM: HBM-bound for decode
+    shapes, tensor-bound for prefill) and the layer's achieved fractions."""
+    hbm, tfl, tfl_sus, src = peaks()
+    gu = work["gate_up"]
+    gu_bytes = gu["weights"] + gu["x"] + gu["h"]
+    gu_s = stage[1] / 1e3
+    if decode:
+        ach = gu_bytes / gu_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4)}
+    else:
+        ach = gu["flops"] / gu_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tfl, "unit": "TFLOP/s",
+                "frac": round(ach / tfl, 4)}
+    roof["kernel"] = f"w4a16_gemm_kernel (gate_up, fused SiLU*up; {label})"
+    roof["peak_source"] = (f"{src} (MEASURED_PEAKS.json burst; 'of measured')" if src == "measured"
+                           else "fallback (6.8 TB/s, 1.9 PFLOP/s)")
+    roof["algorithmic_bytes_per_launch"] = int(gu_bytes)
+    roof["algorithmic_flops_per_launch"] = int(gu["flops"])
+    roof["launch_ms"] = round(stage[1], 5)
+    layer_s = layer_ms / 1e3
+    layer_tbs = work["layer"]["bytes"] / layer_s / 1e12
+    layer_tflops = work["layer"]["flops"] / layer_s / 1e12
+    layer = {"hbm_tbs": round(layer_tbs, 3), "hbm_frac": round(layer_tbs * 1e3 / hbm, 4),
+             "tflops": round(layer_tflops, 2), "tensor_frac": round(layer_tflops / tfl, 4),
+             "tensor_frac_sustained": round(layer_tflops / tfl_sus, 4),
+             "algorithmic_bytes": int(work["layer"]["bytes"]),
+             "algorithmic_flops": int(work["layer"]["flops"])}
+    return roof, layer
+
+
+def is_decode(work):
+    """HBM-bound (weight streaming) below 80 routed rows per touched expert."""
+    return work["pairs"] / max(work["touched"], 1) < 80
+
+
+class IndexedCase:
+    """Device state of one align + indexed-layer step: routing buffers and
+    workspaces sized for `cap_T` tokens (over-allocated, like a server that
+    serves every batch size from one set), reused for any T <= cap_T."""
+
+    def __init__(self, chord, torch, dev, s, cap_T, flags):
+        self.chord, self.s, self.flags = chord, s, flags
+        self.bm = chord.select_block_m(cap_T, s.k, s.E_global, s.E_local, s.H, s.I)
+        self.cap = chord.moe_align_capacity(cap_T, s.k, s.E_local, self.bm)
+        self.si = torch.empty(self.cap, dtype=torch.int32, device=dev)
+        self.ei = torch.empty(self.cap // self.bm, dtype=torch.int32, device=dev)
+        self.ntp = torch.empty(1, dtype=torch.int32, device=dev)
+        self.out = torch.empty((cap_T, s.H), dtype=torch.bfloat16, device=dev)
+        self.ws_a = torch.empty(chord.ops.align_workspace_size(cap_T, s.k, s.E_local),
+                                dtype=torch.uint8, device=dev)
+        self.ws_l = torch.empty(chord.moe_workspace_size(cap_T, s.k, s.E_global, s.E_local, s.H,
+                                                         s.I, self.bm, self.cap, flags),
+                                dtype=torch.uint8, device=dev)
+
+    def step_fn(self, d, w, T):
+        chord, s = self.chord, self.s
+        x, ids, tw, out = d["x"][:T], d["ids"][:T], d["tw"][:T], self.out[:T]
+
+        def step():
+            chord.moe_align(ids, s.E_global, s.E_local, self.bm, expert_map=d["emap"],
+                            capacity=self.cap, workspace=self.ws_a, out=(self.si, self.ei, self.ntp))
+            chord.w4a16_moe_indexed(x, *w, tw, self.si, self.ei, self.ntp, self.bm, s.E_global,
+                                    out=out, workspace=self.ws_l, flags=self.flags)
+        return step
+
+
+def config_record(chord, torch, dev, stream, step, graph, work, steps, warmup, label, extra,
+                  dev_index, uuid):
+    """Timing record of one extra configuration (same rules as the headline)."""
+    flush = None
+    if needs_l2_flush(work["layer"]["bytes"]):
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    with Clocks(dev_index, uuid) as clk:
+        ms = time_graph(graph, stream, steps, warmup, flush)
+    stage = stage_times(chord, step, stream, max(3, min(steps, 10)))
+    roof, layer = roofline(work, stage, ms, is_decode(work), label)
+    rec = {"value": round(ms * 1e3, 2), "unit": UNIT, "ms_per_step": round(ms, 5),
+           "steps": steps, "warmup": warmup,
+           "timing": ("CUDA events over K CUDA-graph replays" if flush is None else
+                      "CUDA events around each of K CUDA-graph replays, L2 flushed between them "
+                      "outside the events"),
+           "routed_pairs": work["pairs"], "touched_experts": work["touched"],
+           "roofline": roof, "layer": layer,
+           "stages_ms": {"prepare": round(stage[0], 5), "gate_up": round(stage[1], 5),
+                         "down": round(stage[2], 5), "combine": round(stage[3], 5)},
+           "clocks": clk.summary()}
+    rec.update(extra)
+    return rec
+
+
+def run_configs(args, chord, torch, dev, stream, ep8_inp, ep8_dev, dev_index, uuid):
+    """Every other configuration of the benchmark, each timed like the headline
+    one: the tiny case, EP8 decode with MXFP4 weights, EP8 prefill (the EP8
+    weights), TP8 at T = 1, 16, 128 and 2048 from one weight set and one set of
+    routing buffers and workspaces sized for 2048 tokens, and the skewed
+    decode on the indexed and the masked layouts (the EP8 weights)."""
+    from w4a16_int4_mixture_gb300 import synth
+    steps = max(5, min(args.steps, 50))
+    warmup = max(3, args.warmup)
+    packed = args.weights == "packed"
+    recs = {}
+
+    def indexed(s, inp, d, w, label, cap_T=None, T=None):
+        case = IndexedCase(chord, torch, dev, s, cap_T or s.T, args.flags)
+        T = s.T if T is None else T
+        step = case.step_fn(d, w, T)
+        graph = capture(step, stream)
+        work = workload_bytes_flops(inp)
+        extra = {"T": T, "k": s.k, "E_global": s.E_global, "E_local": s.E_local, "H": s.H,
+                 "I": s.I, "weights": label,
+                 "schedule": chord.describe_schedule(T, s.k, s.E_global, s.E_local, s.H, s.I,
+                                                     args.flags),
+                 "gpu_launches_per_step": kernels_per_call(T * s.k, s.E_local)}
+        if cap_T:
+            extra["buffers"] = f"routing buffers and workspaces sized for {cap_T} tokens"
+        return config_record(chord, torch, dev, stream, step, graph, work, steps, warmup, label,
+                             extra, dev_index, uuid)
+
+    # tiny: K = 128 of its down GEMM is below the prepack's 256-deep blocks
+    s = synth.workload("tiny")
+    inp = synth.make_inputs(s)
+    d = device_inputs(inp, torch, dev)
+    recs[s.name] = indexed(s, inp, d, layer_weights(chord, d, False),
+                           "plain weights (the prepack needs K % 256 == 0)")
+
+    # EP8 decode with MXFP4 weights: the EP8 codes read as E2M1 numbers, one
+    # E8M0 scale byte per 32 inputs (synth.mx_scales), packed once
+    s = synth.workload("ep8-decode")
+    rng = np.random.default_rng(101)
+    mx13 = synth.mx_scales(rng, s.E_local, 2 * s.I, s.H)
+    mx2 = synth.mx_scales(rng, s.E_local, s.H, s.I)
+    w_mx = (chord.prepack_weights(ep8_dev["w13_q"], torch.from_numpy(mx13).to(dev),
+                                  ep8_dev["w2_q"], torch.from_numpy(mx2).to(dev)),
+            None, None, None)
+    torch.cuda.synchronize()
+    inp = synth.MoEInputs(s, ep8_inp.x, ep8_inp.w13_q, mx13, ep8_inp.w2_q, mx2,
+                          ep8_inp.topk_ids, ep8_inp.topk_weights, ep8_inp.expert_map)
+    recs[s.name + "-mxfp4"] = indexed(s, inp, ep8_dev, w_mx, "MXFP4 packs (chord_mxfp4_prepack)")
+    del w_mx
+
+    # EP8 prefill and skewed decode on the EP8 weights
+    w_ep8 = layer_weights(chord, ep8_dev, packed)
+    label = f"{args.weights} weights"
+    for wl in ("ep8-prefill", "skewed"):
+        s = synth.workload(wl)
+        inp = synth.make_inputs(s, weights=False)
+        inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s = (ep8_inp.w13_q, ep8_inp.w13_s, ep8_inp.w2_q,
+                                                    ep8_inp.w2_s)
+        d = device_inputs(inp, torch, dev, weights=False)
+        recs[s.name + ("-indexed" if wl == "skewed" else "")] = indexed(s, inp, d, w_ep8, label)
+        if wl == "skewed":
+            recs[s.name + "-masked"] = masked(args, chord, torch, dev, stream, s, inp, w_ep8,
+                                              label, steps, warmup, dev_index, uuid)
+    del w_ep8
+
+    # TP8: one weight set, buffers for 2048 tokens, T = 1, 16, 128, 2048
+    s = synth.workload("tp8", T=2048)
+    inp = synth.make_inputs(s)
+    d = device_inputs(inp, torch, dev)
+    w = layer_weights(chord, d, packed)
+    for k in ("w13_q", "w13_s", "w2_q", "w2_s"):
+        d[k] = None
+    for T in (1, 16, 128, 2048):
+        sT = synth.workload("tp8", T=T)
+        sub = synth.MoEInputs(sT, inp.x[:T], inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s,
+                              inp.topk_ids[:T], inp.topk_weights[:T], inp.expert_map)
+        recs[sT.name] = indexed(sT, sub, d, w, label, cap_T=2048, T=T)
+    return recs
+
+
+def masked(args, chord, torch, dev, stream, s, inp, w, label, steps, warmup, dev_index, uuid):
+    """The grouped masked layout of a draw ([E, max_m, H], max_m = T): the
+    layer with the token combine, timed like the indexed step."""
+    from w4a16_int4_mixture_gb300 import synth
+    a3, mm, r2p = synth.grouped_masked_layout(inp)
+
+    def t(a, bf16=False):
+        a = np.ascontiguousarray(a)
+        x = torch.from_numpy(a.view(np.int16) if bf16 else a)
+        return (x.view(torch.bfloat16) if bf16 else x).to(dev)
+    da3, dmm, dr2p, dtw = t(a3, True), t(mm), t(r2p), t(inp.topk_weights)
+    exp_m = int(np.ceil(mm.sum() / s.E_local))
+    M = a3.shape[0] * a3.shape[1]
+    out_rows = torch.empty((M, s.H), dtype=torch.bfloat16, device=dev)
+    out_tok = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(chord.ops.grouped_workspace_size(1, M, s.H, s.I, s.E_local, s.T, s.k, True,
+                                                      exp_m), dtype=torch.uint8, device=dev)
+
+    def step():
+        chord.w4a16_moe_grouped("masked", da3, *w, masked_m=dmm, expected_m=exp_m,
+                                row_to_pair=dr2p, topk_weights=dtw, out_rows=out_rows,
+                                out_tokens=out_tok, workspace=ws, flags=args.flags)
+    graph = capture(step, stream)
+    work = workload_bytes_flops(inp)
+    rows = int(mm.sum())
+    # the masked call reads each valid row of a3 and writes its bf16 row output
+    # as well as the token rows
+    work["layer"]["bytes"] += rows * s.H * 2 * 2 - work["tokens"] * s.H * 2
+    work["gate_up"]["x"] = rows * s.H * 2
+    extra = {"T": s.T, "k": s.k, "E_local": s.E_local, "H": s.H, "I": s.I, "weights": label,
+             "layout": f"grouped masked [{s.E_local}, {a3.shape[1]}, {s.H}], expected_m={exp_m}",
+             "algorithmic_bytes_note": "valid rows of a3 read once, their bf16 row outputs and "
+                                       "the token outputs written once, plus the touched "
+                                       "experts' weights",
+             "gpu_launches_per_step": 4}
+    return config_record(chord, torch, dev, stream, step, graph, work, steps, warmup, label,
+                         extra, dev_index, uuid)
+
+
 def run_ours(args, rank, world, dev_index):
     import torch
     import w4a16_int4_mixture_gb300 as chord
@@ -304,37 +614,13 @@ def run_ours(args, rank, world, dev_index):
     inp = synth.make_inputs(s)
     work = workload_bytes_flops(inp)
     d = device_inputs(inp, torch, dev)
-    bm = chord.select_block_m(s.T, s.k, s.E_global, s.E_local, s.H, s.I)
-    cap = chord.moe_align_capacity(s.T, s.k, s.E_local, bm)
-    si = torch.empty(cap, dtype=torch.int32, device=dev)
-    ei = torch.empty(cap // bm, dtype=torch.int32, device=dev)
-    ntp = torch.empty(1, dtype=torch.int32, device=dev)
-    out = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=dev)
-    ws_a = torch.empty(chord.ops.align_workspace_size(s.T, s.k, s.E_local), dtype=torch.uint8,
-                       device=dev)
-    ws_l = torch.empty(chord.moe_workspace_size(s.T, s.k, s.E_global, s.E_local, s.H, s.I, bm,
-                                                cap, args.flags), dtype=torch.uint8, device=dev)
-    w = (d["w13_q"], d["w13_s"], d["w2_q"], d["w2_s"])
-    if args.weights == "packed":
-        w = (chord.prepack_weights(*w), None, None, None)
-        torch.cuda.synchronize()
-
-    def step(x=d["x"], ids=d["ids"], tw=d["tw"], o=out):
-        chord.moe_align(ids, s.E_global, s.E_local, bm, expert_map=d["emap"], capacity=cap,
-                        workspace=ws_a, out=(si, ei, ntp))
-        chord.w4a16_moe_indexed(x, *w, tw, si, ei, ntp, bm, s.E_global, out=o, workspace=ws_l,
-                                flags=args.flags)
-
+    packed = args.weights == "packed"
+    w = layer_weights(chord, d, packed)
+    case = IndexedCase(chord, torch, dev, s, s.T, args.flags)
+    bm, cap = case.bm, case.cap
+    step = case.step_fn(d, w, s.T)
     stream = torch.cuda.Stream(device=dev)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            step()
-    torch.cuda.synchronize()
+    graph = capture(step, stream)
     launches_per_step = kernels_per_call(s.T * s.k, s.E_local)
     if s.T * s.k == 0:
         launches_per_step = 1
@@ -343,15 +629,6 @@ def run_ours(args, rank, world, dev_index):
         if world > 1:
             torch.distributed.barrier()
 
-    # warm-up, then the timed region: K graph replays on `stream`
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            graph.replay()
-    torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
     try:
         uuid = str(torch.cuda.get_device_properties(dev_index).uuid)
     except Exception:
@@ -361,54 +638,14 @@ def run_ours(args, rank, world, dev_index):
     flush = None
     if needs_l2_flush(work["layer"]["bytes"]):
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    pairs_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps if flush is not None else 0)]
     with Clocks(dev_index, uuid) as clk:
-        with torch.cuda.stream(stream):
-            if flush is None:
-                ev0.record(stream)
-                for _ in range(args.steps):
-                    graph.replay()
-                ev1.record(stream)
-            else:
-                for a, b in pairs_ev:
-                    flush.zero_()
-                    a.record(stream)
-                    graph.replay()
-                    b.record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    if flush is None:
-        local_ms = ev0.elapsed_time(ev1) / args.steps
-    else:
-        local_ms = sum(a.elapsed_time(b) for a, b in pairs_ev) / args.steps
+        local_ms = time_graph(graph, stream, args.steps, args.warmup, flush, barrier)
     ms = max_over_ranks(local_ms, world, dev)
-
-    # spread of single replays (after the timed region; not part of `value`):
-    # events around each of K more replays (L2 flushed before each when the
-    # step fits in it)
-    spread = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            if flush is not None:
-                flush.zero_()
-            spread[2 * i].record(stream)
-            graph.replay()
-            spread[2 * i + 1].record(stream)
-    torch.cuda.synchronize()
-    replay_us = replay_spread_us([spread[2 * i].elapsed_time(spread[2 * i + 1])
-                                  for i in range(args.steps)])
-
-    # per-stage times (eager launches with stage events on the same stream)
-    chord.stage_timing_enable(True)
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            step()
-    stage_ms, calls = chord.stage_timing_read()
-    chord.stage_timing_enable(False)
-    stage = [v / max(calls, 1) for v in stage_ms]
+    replay_us = replay_spread(graph, stream, args.steps, flush)
+    stage = stage_times(chord, step, stream, args.steps)
 
     # end to end through the public API with host buffers
+    out = case.out
     hx = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).view(torch.bfloat16).pin_memory()
     hids = torch.from_numpy(inp.topk_ids).pin_memory()
     htw = torch.from_numpy(inp.topk_weights).pin_memory()
@@ -432,29 +669,9 @@ def run_ours(args, rank, world, dev_index):
     h2d = hx.numel() * 2 + hids.numel() * 4 + htw.numel() * 4
     d2h = hout.numel() * 2
 
-    hbm, tfl, tfl_sus, src = peaks()
-    gu = work["gate_up"]
-    gu_bytes = gu["weights"] + gu["x"] + gu["h"]
-    gu_s = stage[1] / 1e3
-    layer_s = ms / 1e3
-    decode = work["pairs"] / max(work["touched"], 1) < 80
     src_hash = kernel_source_hash()
-    if decode:
-        ach = gu_bytes / gu_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(ach / hbm, 4)}
-    else:
-        ach = gu["flops"] / gu_s / 1e12
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tfl, "unit": "TFLOP/s",
-                "frac": round(ach / tfl, 4)}
-    roof["traffic"] = ncu_traffic("gate_up" + (".packed" if args.weights == "packed" else ""),
-                                  s.name, src_hash)
-    roof["kernel"] = f"w4a16_gemm_kernel (gate_up, fused SiLU*up; {args.weights} weights)"
-    roof["peak_source"] = f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else src
-    roof["algorithmic_bytes_per_launch"] = int(gu_bytes)
-    roof["launch_ms"] = round(stage[1], 5)
-    layer_tbs = work["layer"]["bytes"] / layer_s / 1e12
-    layer_tflops = work["layer"]["flops"] / layer_s / 1e12
+    roof, layer = roofline(work, stage, ms, is_decode(work), f"{args.weights} weights")
+    roof["traffic"] = ncu_traffic("gate_up" + (".packed" if packed else ""), s.name, src_hash)
     res = {
         "metric": METRIC, "value": whole_job_us_per_call(ms, world), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -478,11 +695,7 @@ def run_ours(args, rank, world, dev_index):
                    "parallelism": f"replicas x{world}",
                    "value": "whole job: the slowest rank's step time / the N layer calls the "
                             "N replicas complete per step"},
-        "layer": {"hbm_tbs": round(layer_tbs, 3), "hbm_frac": round(layer_tbs * 1e3 / hbm, 4),
-                  "tflops": round(layer_tflops, 2), "tensor_frac": round(layer_tflops / tfl, 4),
-                  "tensor_frac_sustained": round(layer_tflops / tfl_sus, 4),
-                  "algorithmic_bytes": int(work["layer"]["bytes"]),
-                  "algorithmic_flops": int(work["layer"]["flops"])},
+        "layer": layer,
         "replay_us": replay_us,
         "stages_ms": {"prepare": round(stage[0], 5), "gate_up": round(stage[1], 5),
                       "down": round(stage[2], 5), "combine": round(stage[3], 5)},
@@ -493,6 +706,12 @@ def run_ours(args, rank, world, dev_index):
         "clocks": clk.summary(),
         "kernel_source": src_hash,
     }
+    if rank == 0 and not args.no_configs and args.workload == "ep8-decode" and args.T is None:
+        del graph, case
+        res["configs"] = run_configs(args, chord, torch, dev, stream, inp, d, dev_index, uuid)
+        res["configs_note"] = ("the other configurations, timed in the same process after the "
+                               "headline one, each with its own roofline and clock record; "
+                               "`value` is the headline configuration's")
     return res, inp
 
 

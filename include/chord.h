@@ -95,6 +95,8 @@ typedef enum {
 #define CHORD_FLAG_PREPACKED 16 /* the layer calls' w13_q / w2_q are chord_w4a16_prepack
                                    outputs (kinds CHORD_PACK_GATE_UP / CHORD_PACK_DOWN) and
                                    w13_s / w2_s are NULL (the scales live in the packs) */
+#define CHORD_FLAG_MXFP4 32     /* with CHORD_FLAG_PREPACKED: the packs are chord_mxfp4_prepack
+                                   outputs (MXFP4 weights); without it CHORD_ERR_INVALID_ARG */
 
 /* bits of the device error word */
 #define CHORD_DEVERR_TIMEOUT 1
@@ -258,7 +260,7 @@ chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global,
  *   bytes [0, 256): header of 64 uint32: [0] magic 0x4B504843 ("CHPK"),
  *     [1] version 1, [2] kind, [3] E, [4] N, [5] K, [6] block bytes 18432,
  *     [7] flags (bit 0: some scale outside the range of the header comment),
- *     the rest 0.
+ *     [8] weight format (0 INT4; 1 MXFP4, chord_mxfp4_prepack), the rest 0.
  *   then blocks of 18432 bytes, block b = (e * (N/128) + t) * (K/256) + j for
  *   expert e, tile t and K block j (codes 256j .. 256j+255):
  *     [0, 16384) codes: half h (codes 256j + 128h ..) at 8192 h; in it, tile
@@ -280,6 +282,30 @@ chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global,
 #define CHORD_PACK_DOWN 2
 size_t chord_w4a16_prepack_size(int kind, int E, int N, int K);  /* 0 for bad arguments */
 chord_status chord_w4a16_prepack(int kind, const int32_t* w_q, const uint16_t* w_s, int E, int N,
+                                 int K, void* packed, size_t packed_bytes, void* stream);
+
+/*
+ * MXFP4 weights (page: vLLM Kimi K3 production support, news.ainew.jp, "MXFP4
+ * MoE": MoE weights in MXFP4; the OCP Microscaling FP4 format that name
+ * refers to): each 4-bit code is an FP4 E2M1 number (bit 3 sign, bits 2-1 an
+ * exponent with bias 1, bit 0 a mantissa bit; exponent 0 is subnormal, so the
+ * sixteen codes are +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}), and each group of 32
+ * input channels shares one E8M0 scale byte e meaning 2^(e - 127) (e = 255:
+ * NaN).  The weight is w = bf16(e2m1(q) * 2^(e - 127)): exact for every code
+ * and byte unless it overflows bf16 (then +-inf, as bf16 rounding gives).  The
+ * activation (SiLU(gate) * up), the combine and everything else are those of
+ * the INT4 layer.
+ *
+ * chord_mxfp4_prepack packs such weights for the layer calls: the codes are
+ * stored like INT4 codes (8 per int32 word, low nibble first, [E, N, K/8]),
+ * w_e8m0 holds the scale bytes [E, N, K/32] (device, 16-byte aligned), and the
+ * output is a pack of the chord_w4a16_prepack format and size whose scale rows
+ * hold each byte widened to the bf16 value 2^(e - 127) (0x0040 for e = 0, NaN
+ * 0x7FC0 for e = 255), with header word 8 (weight format) = 1 (INT4 packs: 0).
+ * The layer calls take MXFP4 packs with CHORD_FLAG_PREPACKED | CHORD_FLAG_MXFP4
+ * and check the format word with the rest of the header.
+ */
+chord_status chord_mxfp4_prepack(int kind, const int32_t* w_q, const uint8_t* w_e8m0, int E, int N,
                                  int K, void* packed, size_t packed_bytes, void* stream);
 
 /* ------------------------------------------------------------------------- */

@@ -6,6 +6,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+import fp64_ref
 import oracle
 import pins
 
@@ -45,8 +46,61 @@ def assert_close_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "o
 # move an output by more than 1e-3*rms.  So the layer is checked at that
 # decision point: h against the oracle's h (same tolerance family, bounded flip
 # fraction), then the output against the oracle's down GEMM + combine applied
-# to the GPU's own h, with the full tolerance.
-MAX_H_FLIP_FRACTION = 0.03
+# to the GPU's own h, with the full tolerance.  Measured on the Kimi-shaped
+# workloads (K = 7168) the GPU's and the oracle's h differ in 0.15-0.5 % of
+# the elements; a defect that flips a whole tile of one row, or a scale group
+# across rows, exceeds the ceiling.
+MAX_H_FLIP_FRACTION = 0.008
+
+# Both implementations are also measured against the definition itself
+# (fp64_ref: fp64 accumulation, correctly rounded h, unrounded output).  The
+# reading of the element-wise tolerance asserted there: the GPU's h rounding
+# decisions differ from the exact ones at most C_FLIP times as often as the
+# sequential-fp32 oracle's (plus FLIP_SLACK elements of counting noise on
+# small draws), and its worst output element, in units of 1e-2*|ref| +
+# 1e-3*rms(ref) against the exact output, is at most C_E2E times the oracle's
+# worst (or C_E2E when the oracle's is below 1).  Measured: the GPU flips at
+# 0.9-2x the oracle's rate with the decode tiles (accumulation chains of
+# 1024-1792 inputs) and 3-4.4x with the prefill tile (chains of up to 3584
+# inputs: it has no spare tensor memory for a third accumulator, so shorter
+# chains would stall its tensor pipe on every merge), and no fp32
+# implementation stays below 1 everywhere: the oracle's own worst element
+# reaches ~2x at K = 7168.
+C_FLIP = 5.0
+FLIP_SLACK = 8
+C_E2E = 4.0
+
+
+def check_fp64_anchor(inp, tokens, h_gpu: dict, out_gpu_bits, h_orc: dict, out_orc_bits,
+                      what="layer"):
+    """The GPU's and the oracle's h (dicts (t, j) -> bf16 bits [I]) and
+    outputs (bf16 bits, rows of `tokens`) against the fp64 evaluation of the
+    definition on the same tokens.  Returns (gpu flips, oracle flips, gpu
+    worst, oracle worst)."""
+    ref = fp64_ref.Fp64Layer(inp, tokens)
+    fg, _, n = fp64_ref.h_flip_stats(h_gpu, ref.h64)
+    fo, _, n_o = fp64_ref.h_flip_stats(h_orc, ref.h64)
+    assert n == n_o == sum(v.size for v in ref.h64.values()), f"{what}: pairs missing"
+    assert fg * n <= C_FLIP * fo * n + FLIP_SLACK, \
+        f"{what}: h flips against fp64 {100 * fg:.3f}% vs the oracle's {100 * fo:.3f}%"
+    rg = fp64_ref.out_ratio(out_gpu_bits, ref.out64)
+    ro = fp64_ref.out_ratio(out_orc_bits, ref.out64)
+    assert rg <= C_E2E * max(ro, 1.0), \
+        f"{what}: worst element against fp64 {rg:.2f}x vs the oracle's {ro:.2f}x"
+    return fg, fo, rg, ro
+
+
+def h_by_pair(h_rows, pair_of_row, k, tokens=None, num_pairs=None):
+    """{(t, j): h row} for the rows whose pair id is valid (0 <= p < num_pairs);
+    t is tokens[p // k] when a token list maps a sub-batch back."""
+    d = {}
+    for r, p in enumerate(np.asarray(pair_of_row)):
+        p = int(p)
+        if p < 0 or (num_pairs is not None and p >= num_pairs):
+            continue
+        t, j = divmod(p, k)
+        d[(int(tokens[t]) if tokens is not None else t, j)] = h_rows[r]
+    return d
 
 
 def check_h(h_gpu_bits, h_ref_bits, what="h"):

@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close_bf16, bf16_to_np, check_h, dev_tensor, e2e_ratio, weights_to
+from gpu_util import (assert_close_bf16, bf16_to_np, check_fp64_anchor, check_h, dev_tensor,
+                      e2e_ratio, h_by_pair, weights_to)
 from w4a16_int4_mixture_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -66,8 +67,9 @@ def sub_batch(inp, tokens):
 
 def verify_indexed(inp, run, tokens=None, label=""):
     """Split check of an indexed layer run (see gpu_util): rows of `tokens`
-    (all tokens when None) against the oracle on the same tokens.  Returns the
-    end-to-end ratio (reported, not asserted)."""
+    (all tokens when None) against the oracle on the same tokens, and both
+    against the fp64 evaluation of the definition (gpu_util.check_fp64_anchor).
+    Returns the end-to-end ratio against the oracle (reported, not asserted)."""
     s = inp.shape
     if tokens is None:
         tokens = np.arange(s.T)
@@ -95,7 +97,13 @@ def verify_indexed(inp, run, tokens=None, label=""):
     got = run.out[tokens]
     assert_close_bf16(got, down_ref, f"{label} output given h")
     ratio = e2e_ratio(got, ref_out)
-    print(f"[{label}] h flips {100 * flips:.4f}%  end-to-end worst {ratio:.3f}x tolerance")
+    fg, fo, rg, ro = check_fp64_anchor(
+        inp, tokens, h_by_pair(h_sub[valid], rsi[valid], s.k, tokens),
+        got, h_by_pair(ref_h[valid], rsi[valid], s.k, tokens), ref_out,
+        f"{label} against fp64")
+    print(f"[{label}] h flips vs oracle {100 * flips:.4f}%  end-to-end worst {ratio:.3f}x | "
+          f"vs fp64: h flips gpu {100 * fg:.3f}% oracle {100 * fo:.3f}%, worst gpu {rg:.2f}x "
+          f"oracle {ro:.2f}x")
     return ratio
 
 
@@ -209,7 +217,12 @@ def contiguous_layer_check(chord, inp, align, label, flags=0, weights=None):
                                             topk_weights=inp.topk_weights, T=s.T, k=s.k)
     assert_close_bf16(bf16_to_np(rows)[valid], d_rows[valid], f"{label} rows given h")
     assert_close_bf16(bf16_to_np(toks), d_tok, f"{label} tokens given h")
-    print(f"[{label}] end-to-end tokens {e2e_ratio(bf16_to_np(toks), ref_tok):.3f}x")
+    fg, fo, rg, ro = check_fp64_anchor(inp, np.arange(s.T), h_by_pair(hg, r2p, s.k),
+                                       bf16_to_np(toks), h_by_pair(ref_h, r2p, s.k), ref_tok,
+                                       f"{label} against fp64")
+    print(f"[{label}] end-to-end tokens {e2e_ratio(bf16_to_np(toks), ref_tok):.3f}x | vs fp64: "
+          f"h flips gpu {100 * fg:.3f}% oracle {100 * fo:.3f}%, worst gpu {rg:.2f}x oracle "
+          f"{ro:.2f}x")
     return bf16_to_np(rows)[valid], bf16_to_np(toks)
 
 
@@ -243,8 +256,12 @@ def masked_layer_check(chord, inp, a3, mm, r2p, w, label):
                                             topk_weights=inp.topk_weights, T=s.T, k=s.k)
     assert_close_bf16(bf16_to_np(rows)[valid], d_rows[valid], f"{label} rows given h")
     assert_close_bf16(bf16_to_np(toks), d_tok, f"{label} tokens given h")
+    fg, fo, rg, ro = check_fp64_anchor(inp, np.arange(s.T), h_by_pair(hg, r2p, s.k),
+                                       bf16_to_np(toks), h_by_pair(ref_h, r2p, s.k), ref_tok,
+                                       f"{label} against fp64")
     print(f"[{label}] h flips {100 * flips:.4f}%  end-to-end tokens "
-          f"{e2e_ratio(bf16_to_np(toks), ref_tok):.3f}x")
+          f"{e2e_ratio(bf16_to_np(toks), ref_tok):.3f}x | vs fp64: h flips gpu {100 * fg:.3f}% "
+          f"oracle {100 * fo:.3f}%, worst gpu {rg:.2f}x oracle {ro:.2f}x")
     return bf16_to_np(toks)
 
 
@@ -310,6 +327,66 @@ def test_graph_capture_token_sweep(chord):
         sub = sub_batch(base, np.arange(T))
         run = Run(replay, bf16_to_np(h), si.cpu().numpy(), ei.cpu().numpy(), int(ntp.item()), 16)
         verify_indexed(sub, run, label=f"graph T={T}")
+
+
+def test_tp8_graph_capture_over_allocated(chord):
+    """The TP8 configuration as a server runs it: one packed weight set (384
+    experts, hidden 7168, intermediate 256), one set of routing buffers and one
+    workspace sized once for 2048 tokens, and one CUDA graph captured per token
+    count T in {1, 16, 128, 2048} on those same buffers (page: "vLLM
+    integration": over-allocated moe_align buffers consumed without host
+    readback).  Each replay equals the eager call bit for bit (ordered
+    combine) and is checked against the oracle and the fp64 evaluation
+    (sampled tokens at 2048)."""
+    Tmax = 2048
+    base = synth.make_inputs(synth.workload("tp8", T=Tmax))
+    s0 = base.shape
+    pw = chord.prepack_weights(*weights_to(base, DEV))
+    w = (pw, None, None, None)
+    cap = chord.moe_align_capacity(Tmax, s0.k, s0.E_local, 16)
+    si = torch.empty(cap, dtype=torch.int32, device=DEV)
+    ei = torch.empty(cap // 16, dtype=torch.int32, device=DEV)
+    ntp = torch.empty(1, dtype=torch.int32, device=DEV)
+    h = torch.empty((cap, s0.I), dtype=torch.bfloat16, device=DEV)
+    out_all = torch.empty((Tmax, s0.H), dtype=torch.bfloat16, device=DEV)
+    ws_a = torch.empty(chord.ops.align_workspace_size(Tmax, s0.k, s0.E_local), dtype=torch.uint8,
+                       device=DEV)
+    ws_l = torch.empty(chord.moe_workspace_size(Tmax, s0.k, s0.E_global, s0.E_local, s0.H, s0.I,
+                                                16, cap, 2), dtype=torch.uint8, device=DEV)
+    x_all = dev_tensor(base.x, DEV, True)
+    ids_all = dev_tensor(base.topk_ids, DEV)
+    tw_all = dev_tensor(base.topk_weights, DEV)
+    for T in (1, 16, 128, 2048):
+        x, ids, tw, out = x_all[:T], ids_all[:T], tw_all[:T], out_all[:T]
+        assert chord.moe_workspace_size(T, s0.k, s0.E_global, s0.E_local, s0.H, s0.I, 16, cap,
+                                        2) <= ws_l.numel()
+
+        def step():
+            chord.moe_align(ids, s0.E_global, s0.E_local, 16, capacity=cap, workspace=ws_a,
+                            out=(si, ei, ntp))
+            chord.w4a16_moe_indexed(x, *w, tw, si, ei, ntp, 16, s0.E_global, out=out,
+                                    workspace=ws_l, h_out=h, flags=2)
+
+        step()
+        torch.cuda.synchronize()
+        eager = bf16_to_np(out).copy()
+        g = torch.cuda.CUDAGraph()
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(g, stream=st):
+                step()
+        torch.cuda.current_stream().wait_stream(st)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        replay = bf16_to_np(out)
+        assert np.array_equal(replay, eager), f"graph replay differs from eager T={T}"
+        sub = sub_batch(base, np.arange(T))
+        run = Run(replay, bf16_to_np(h), si.cpu().numpy(), ei.cpu().numpy(), int(ntp.item()), 16)
+        tokens = None if T <= 128 else np.random.default_rng(9).choice(T, 48, replace=False)
+        verify_indexed(sub, run, tokens, label=f"TP8 graph T={T}, buffers for {Tmax}")
+        del g
 
 
 # ---------------------------------------------------------------- full workloads

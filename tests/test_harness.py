@@ -1,7 +1,9 @@
 """The split parity check the GPU tests use, exercised on the CPU with an
 oracle-made run standing in for the GPU (it must accept it with zero flips),
 and with planted errors in the output or the intermediate (it must reject
-those)."""
+those): a large change of one element, a tile of one row far off, and
+one-ulp rounding flips in 1.5 % of h (each within the element-wise
+tolerance, caught by the flip ceiling and the fp64 anchor)."""
 
 import numpy as np
 import pytest
@@ -36,4 +38,18 @@ def test_split_check_rejects_a_wrong_intermediate():
     rows = np.nonzero(run.si[:run.ntp] < inp.shape.T * inp.shape.k)[0]
     bad[rows[0], :64] ^= 0x0100  # one tile of one row far off
     with pytest.raises(AssertionError):
+        L.verify_indexed(inp, L.Run(run.out, bad, run.si, run.ei, run.ntp, run.bm))
+
+
+def test_split_check_rejects_many_one_ulp_flips():
+    inp, run = _self_run()
+    bad = run.h.copy()
+    rows = np.nonzero(run.si[:run.ntp] < inp.shape.T * inp.shape.k)[0]
+    body = bad[rows]
+    rng = np.random.default_rng(0)
+    flip = rng.random(body.shape) < 0.015
+    flip &= (body & 0x7F80) != 0  # normal numbers: +-1 in the last place stays close
+    body[flip] ^= 0x0001
+    bad[rows] = body
+    with pytest.raises(AssertionError, match="differ|flips"):
         L.verify_indexed(inp, L.Run(run.out, bad, run.si, run.ei, run.ntp, run.bm))

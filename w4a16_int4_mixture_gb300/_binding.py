@@ -33,6 +33,7 @@ FLAG_DETERMINISTIC = 2
 FLAG_TEST_SKIP_ARRIVE = 4
 FLAG_NO_SPLIT_K = 8
 FLAG_PREPACKED = 16
+FLAG_MXFP4 = 32
 PACK_GATE_UP = 1
 PACK_DOWN = 2
 DEVERR_TIMEOUT = 1
@@ -59,6 +60,7 @@ SIGNATURES = {
                                        _i64, _vp]),
     "chord_w4a16_prepack_size": (_sz, [_int, _int, _int, _int]),
     "chord_w4a16_prepack": (_int, [_int, _vp, _vp, _int, _int, _int, _vp, _sz, _vp]),
+    "chord_mxfp4_prepack": (_int, [_int, _vp, _vp, _int, _int, _int, _vp, _sz, _vp]),
     "chord_moe_route_align": (_int, [_vp, _i64, _int, _int, _int, _vp, _int, _int, _vp, _vp, _vp,
                                      _vp, _vp, _i64, _vp, _sz, _vp]),
     "chord_w4a16_moe_indexed": (_int, [_vp, _i64, _int, _int, _int, _int, _int, _vp, _vp, _vp,

@@ -19,6 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libchord_w4a16.so")
 SOURCES = ["api.cu", "aux_kernels.cu", "gemm_gate_up.cu", "gemm_down.cu", "gemm_packed.cu",
+           "gemm_mxfp4.cu",
            "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -26,13 +26,22 @@ cudaError_t launch_gemm_gate_up_packed(int cfg, const CUtensorMap& map, const CU
 cudaError_t launch_gemm_down_packed(int cfg, const CUtensorMap& map, const CUtensorMap& smap,
                                     const CUtensorMap& bmap, const GemmArgs& a, int grid,
                                     cudaStream_t s);
+cudaError_t launch_gemm_gate_up_mx(int cfg, const CUtensorMap& map, const CUtensorMap& smap,
+                                   const CUtensorMap& bmap, const GemmArgs& a, int grid,
+                                   cudaStream_t s);
+cudaError_t launch_gemm_down_mx(int cfg, const CUtensorMap& map, const CUtensorMap& smap,
+                                const CUtensorMap& bmap, const GemmArgs& a, int grid, cudaStream_t s);
 int gemm_cfg_smem_gate_up(int cfg);
 int gemm_cfg_smem_down(int cfg);
 
-cudaError_t launch_gemm(int cfg, bool gate_up, bool packed, const CUtensorMap& map,
+// packed: prepacked weights; mx: MXFP4 packs (always prepacked)
+cudaError_t launch_gemm(int cfg, bool gate_up, bool packed, bool mx, const CUtensorMap& map,
                         const CUtensorMap& smap, const CUtensorMap& bmap, const GemmArgs& a,
                         int grid, cudaStream_t s)
 {
+    if (mx)
+        return gate_up ? launch_gemm_gate_up_mx(cfg, map, smap, bmap, a, grid, s)
+                       : launch_gemm_down_mx(cfg, map, smap, bmap, a, grid, s);
     if (packed)
         return gate_up ? launch_gemm_gate_up_packed(cfg, map, smap, bmap, a, grid, s)
                        : launch_gemm_down_packed(cfg, map, smap, bmap, a, grid, s);
@@ -484,16 +493,17 @@ chord_status read_error_word(void* ws, cudaStream_t s, int* bits, bool clear)
 
 // The prep kernel checks the packs' headers against the call (gate/up: kind
 // GATE_UP, N = 2I, K = H; down: kind DOWN, N = H, K = I; E >= E_local).
-void set_pack_check(PrepArgs& pa, bool packed, const int32_t* w13_q, const int32_t* w2_q,
+void set_pack_check(PrepArgs& pa, bool packed, bool mx, const int32_t* w13_q, const int32_t* w2_q,
                     int E_local, int H, int I)
 {
     pa.pk_hdr[0] = packed ? reinterpret_cast<const uint32_t*>(w13_q) : nullptr;
     pa.pk_hdr[1] = packed ? reinterpret_cast<const uint32_t*>(w2_q) : nullptr;
-    const uint32_t want[2][4] = {
+    const uint32_t fmt = mx ? kPackFmtMxfp4 : kPackFmtInt4;
+    const uint32_t want[2][5] = {
         {CHORD_PACK_GATE_UP, static_cast<uint32_t>(E_local), 2u * static_cast<uint32_t>(I),
-         static_cast<uint32_t>(H)},
+         static_cast<uint32_t>(H), fmt},
         {CHORD_PACK_DOWN, static_cast<uint32_t>(E_local), static_cast<uint32_t>(H),
-         static_cast<uint32_t>(I)}};
+         static_cast<uint32_t>(I), fmt}};
     std::memcpy(pa.pk_want, want, sizeof want);
 }
 
@@ -531,26 +541,33 @@ struct LayerIO {
     int flags;
     double tok_e;  // expected rows per local expert
     bool h_zero_unpaired;  // h rows without a pair are written as zeros (indexed layout)
-    bool packed;           // w13_q / w2_q are chord_w4a16_prepack outputs
+    bool packed;           // w13_q / w2_q are chord_w4a16_prepack / chord_mxfp4_prepack outputs
+    bool mx;               // MXFP4 packs
 };
 
 // Weight tiles per unit of the down GEMM: with a one-stage K (I = BK) each
 // unit is short, and its fixed costs (waits, commits, the token tile) are
-// shared by several tiles of a short-K configuration, as long as the units
-// still give every SM several.  Returns the tiles per unit and sets *cfg to
-// the configuration that runs them.
+// shared by a run of tiles of one chunk in a token-stationary configuration,
+// which loads the chunk's token tile once per run.  The run is the longest
+// (of 14, 8, 7, 4, 2 tiles, dividing the tile count) that still deals every
+// SM twelve units or more (the units are dealt with a stride of the grid, so
+// fewer, longer units leave more of the last round idle).  Returns the tiles
+// per unit and sets *cfg to the configuration that runs them.
 int pick_tpu(int* cfg, int K, int n_tiles, int E_local, double tok_e, int sms)
 {
     const int s_cfg = *cfg == kCfgD32 ? kCfgS32 : *cfg == kCfgD64 ? kCfgS64 : -1;
     if (s_cfg < 0 || K != gemm_cfg_bk(s_cfg))
         return 1;
     const double chunks = E_local * (1.0 - std::exp(-(tok_e > 0 ? tok_e : 0.0)));
-    int tpu = gemm_cfg_tpu_max_down(s_cfg);
-    while (tpu > 1 && (n_tiles % tpu != 0 || chunks * n_tiles / tpu < 4.0 * sms))
-        tpu /= 2;
-    if (tpu > 1)
-        *cfg = s_cfg;
-    return tpu;
+    static const int runs[] = {14, 8, 7, 4, 2};
+    for (int r : runs)
+        if (r <= gemm_cfg_tpu_max_down(s_cfg) && n_tiles % r == 0 &&
+            chunks * n_tiles / r >= 12.0 * sms) {
+            *cfg = s_cfg;
+            return r;
+        }
+    *cfg = s_cfg;  // one tile per unit, still with the deeper accumulator ring
+    return 1;
 }
 
 chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w, uint8_t* ws,
@@ -627,7 +644,8 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     g.split_slots = slots_for(sc.cfg_gate_up);
     marks.mark(1);
     g.test_skip_arrive = (io.flags & CHORD_FLAG_TEST_SKIP_ARRIVE) ? 1 : 0;
-    if (launch_gemm(sc.cfg_gate_up, true, io.packed, map13, smap13, bmap13, g, dev.sms, s) != cudaSuccess)
+    if (launch_gemm(sc.cfg_gate_up, true, io.packed, io.mx, map13, smap13, bmap13, g, dev.sms, s) !=
+        cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(2);
 
@@ -651,10 +669,40 @@ chord_status run_gemms(const LayerIO& io, const Schedule& sc, const Workspace& w
     d.split_cnt = split_cnt + kSplitSlots;
     d.split_part = g.split_part + static_cast<size_t>(kSplitSlots) * w.split_maxn * 128;
     d.split_slots = slots_for(sc.cfg_down);
-    if (launch_gemm(cfg_down, false, io.packed, map2, smap2, bmap2, d, dev.sms, s) != cudaSuccess)
+    if (launch_gemm(cfg_down, false, io.packed, io.mx, map2, smap2, bmap2, d, dev.sms, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     marks.mark(3);
     return CHORD_OK;
+}
+
+chord_status prepack_common(int kind, const int32_t* w_q, const void* w_s, int fmt, int E, int N,
+                            int K, void* packed, size_t packed_bytes, void* stream)
+{
+    if ((kind != CHORD_PACK_GATE_UP && kind != CHORD_PACK_DOWN) || E < 1 || N < 1 || K < 1)
+        return CHORD_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 256 != 0)
+        return CHORD_ERR_UNSUPPORTED_SHAPE;
+    if (!w_q || !w_s || !packed || !aligned16(w_q) || !aligned16(w_s) || !aligned16(packed))
+        return CHORD_ERR_INVALID_ARG;
+    if (packed_bytes < chord_w4a16_prepack_size(kind, E, N, K))
+        return CHORD_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    chord_status st = device_info(&dev);
+    if (st != CHORD_OK)
+        return st;
+    PackArgs a{};
+    a.kind = kind;
+    a.q = w_q;
+    a.E = E;
+    a.N = N;
+    a.K = K;
+    a.out = static_cast<uint8_t*>(packed);
+    a.fmt = fmt;
+    if (fmt == static_cast<int>(kPackFmtMxfp4))
+        a.sc8 = static_cast<const uint8_t*>(w_s);
+    else
+        a.sc = static_cast<const uint16_t*>(w_s);
+    return from_cuda(launch_prepack(a, dev.sms, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -852,23 +900,19 @@ size_t chord_w4a16_prepack_size(int kind, int E, int N, int K)
     return kPackHeaderBytes + static_cast<size_t>(E) * (N / 128) * (K / 256) * kPackBlockBytes;
 }
 
+
+chord_status chord_mxfp4_prepack(int kind, const int32_t* w_q, const uint8_t* w_e8m0, int E, int N,
+                                 int K, void* packed, size_t packed_bytes, void* stream)
+{
+    return prepack_common(kind, w_q, w_e8m0, static_cast<int>(kPackFmtMxfp4), E, N, K, packed,
+                          packed_bytes, stream);
+}
+
 chord_status chord_w4a16_prepack(int kind, const int32_t* w_q, const uint16_t* w_s, int E, int N,
                                  int K, void* packed, size_t packed_bytes, void* stream)
 {
-    if ((kind != CHORD_PACK_GATE_UP && kind != CHORD_PACK_DOWN) || E < 1 || N < 1 || K < 1)
-        return CHORD_ERR_INVALID_ARG;
-    if (N % 128 != 0 || K % 256 != 0)
-        return CHORD_ERR_UNSUPPORTED_SHAPE;
-    if (!w_q || !w_s || !packed || !aligned16(w_q) || !aligned16(w_s) || !aligned16(packed))
-        return CHORD_ERR_INVALID_ARG;
-    if (packed_bytes < chord_w4a16_prepack_size(kind, E, N, K))
-        return CHORD_ERR_INVALID_ARG;
-    DeviceInfo dev;
-    chord_status st = device_info(&dev);
-    if (st != CHORD_OK)
-        return st;
-    PackArgs a{kind, w_q, w_s, E, N, K, static_cast<uint8_t*>(packed)};
-    return from_cuda(launch_prepack(a, dev.sms, static_cast<cudaStream_t>(stream)));
+    return prepack_common(kind, w_q, w_s, static_cast<int>(kPackFmtInt4), E, N, K, packed,
+                          packed_bytes, stream);
 }
 
 chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I, int E_global,
@@ -883,9 +927,12 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     chord_status st = check_shape(H, I, E_local, k);
     if (st != CHORD_OK)
         return st;
-    if (T < 0 || E_global < 1 || block_m < 1 || block_m > 256 || (flags & ~31))
+    if (T < 0 || E_global < 1 || block_m < 1 || block_m > 256 || (flags & ~63))
         return CHORD_ERR_INVALID_ARG;
     const bool packed = (flags & CHORD_FLAG_PREPACKED) != 0;
+    const bool mx = (flags & CHORD_FLAG_MXFP4) != 0;
+    if (mx && !packed)
+        return CHORD_ERR_INVALID_ARG;
     if (T * k >= (int64_t(1) << 31))
         return CHORD_ERR_UNSUPPORTED_SHAPE;
     if (T == 0)
@@ -962,7 +1009,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     pa.gx_pairs = T * k;
     pa.gx_H = H;
     pa.err = err;
-    set_pack_check(pa, packed, w13_q, w2_q, E_local, H, I);
+    set_pack_check(pa, packed, mx, w13_q, w2_q, E_local, H, I);
     int work_blocks = zero_blocks_for(sc.reduce ? T * H : T * k, dev.sms);
     if (work_blocks < dev.sms)
         work_blocks = dev.sms;
@@ -995,6 +1042,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     io.down_epi = sc.reduce ? kEpiReduceTok : kEpiStorePair;
     io.flags = flags;
     io.packed = packed;
+    io.mx = mx;
     io.tok_e = tok_e;
     io.h_zero_unpaired = true;
     if ((st = run_gemms(io, sc, w, ws, err, pair_row, acc, dev, s, marks)) != CHORD_OK)
@@ -1030,9 +1078,12 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     chord_status st = check_shape(H, I, E_local, with_tokens ? k : 1);
     if (st != CHORD_OK)
         return st;
-    if (M < 0 || (flags & ~31))
+    if (M < 0 || (flags & ~63))
         return CHORD_ERR_INVALID_ARG;
     const bool packed = (flags & CHORD_FLAG_PREPACKED) != 0;
+    const bool mx = (flags & CHORD_FLAG_MXFP4) != 0;
+    if (mx && !packed)
+        return CHORD_ERR_INVALID_ARG;
     if (mode == CHORD_GROUPED_CONTIGUOUS) {
         if (masked_m != nullptr || (M > 0 && m_indices == nullptr))
             return CHORD_ERR_LAYOUT_MODE;
@@ -1113,7 +1164,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
         pa.mc_H = H;
     }
     pa.err = err;
-    set_pack_check(pa, packed, w13_q, w2_q, E_local, H, I);
+    set_pack_check(pa, packed, mx, w13_q, w2_q, E_local, H, I);
     int work_blocks = zero_blocks_for(with_tokens ? T * H : 0, dev.sms);
     if ((with_tokens || compact) && work_blocks < dev.sms)
         work_blocks = dev.sms;  // the row records and the compacted rows come from the worker blocks
@@ -1147,6 +1198,7 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     io.down_epi = kEpiStoreRows | (with_tokens ? kEpiReduceTok : 0);
     io.flags = flags;
     io.packed = packed;
+    io.mx = mx;
     io.tok_e = tok_e;
     if ((st = run_gemms(io, sc, w, ws, err, nullptr, acc, dev, s, marks)) != CHORD_OK)
         return st;

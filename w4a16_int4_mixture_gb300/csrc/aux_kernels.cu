@@ -668,7 +668,8 @@ __device__ void build_chunk_lists(const PrepArgs& a)
                 continue;
             const uint32_t* w = a.pk_want[g];
             if (h[0] != kPackMagic || h[1] != 1u || h[2] != w[0] || h[3] < w[1] || h[4] != w[2] ||
-                h[5] != w[3] || h[6] != static_cast<uint32_t>(kPackBlockBytes))
+                h[5] != w[3] || h[6] != static_cast<uint32_t>(kPackBlockBytes) ||
+                h[kPackFormatWord] != w[4])
                 pk_bad = true;
             else if (h[7] & 1u)
                 raise_error(a.err, CHORD_DEVERR_SCALE_RANGE);
@@ -904,6 +905,8 @@ __global__ void pack_header_kernel(PackArgs a)
         v = static_cast<uint32_t>(a.K);
     else if (i == 6)
         v = kPackBlockBytes;
+    else if (i == kPackFormatWord)
+        v = static_cast<uint32_t>(a.fmt);
     hd[i] = v;  // word 7 (flags) starts at 0
 }
 
@@ -937,6 +940,23 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
             const int h = j >> 9;
             const int c = (j & 3) ^ ((r >> 1) & 3);
             v = *reinterpret_cast<const uint4*>(a.q + grow * words_per_row + kb * 32 + h * 16 + c * 4);
+        } else if (a.fmt == static_cast<int>(kPackFmtMxfp4)) {
+            // E8M0 byte e -> the bf16 value 2^(e - 127): exponent field e for
+            // 1 <= e <= 254, the subnormal 0x0040 for e = 0, NaN for e = 255
+            const uint2 b8 = *reinterpret_cast<const uint2*>(a.sc8 + grow * scales_per_row + kb * 8);
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t src = q < 2 ? b8.x : b8.y;
+                uint32_t h[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t e = (src >> (16 * (q & 1) + 8 * u)) & 0xFFu;
+                    h[u] = e == 0u ? 0x0040u : (e == 255u ? 0x7FC0u : e << 7);
+                }
+                o[q] = h[0] | (h[1] << 16);
+            }
+            v = make_uint4(o[0], o[1], o[2], o[3]);
         } else {
             v = *reinterpret_cast<const uint4*>(a.sc + grow * scales_per_row + kb * 8);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};

@@ -71,6 +71,9 @@ constexpr uint32_t kPackMagic = 0x4B504843u;  // "CHPK"
 constexpr int kPackHeaderBytes = 256;
 constexpr int kPackCodeBytes = 16384;          // one 256-deep K block of a 128-row tile
 constexpr int kPackBlockBytes = kPackCodeBytes + 2048;
+constexpr int kPackFormatWord = 8;             // header word: weight format of the pack
+constexpr uint32_t kPackFmtInt4 = 0;           // chord_w4a16_prepack
+constexpr uint32_t kPackFmtMxfp4 = 1;          // chord_mxfp4_prepack
 
 constexpr int kGemmThreads = 512;  // 16 warps (the GEMM configurations may add a warp group)
 

@@ -1,7 +1,8 @@
 // gemm_kernel.cuh -- the W4A16 expert GEMM for sm_103a (tcgen05 + TMEM + TMA).
 //
-// One persistent CTA per SM walks a contiguous range of work units (chunk of
-// padded rows that share an expert) x (128-row tile of that expert's weight).  Per unit it computes
+// One persistent CTA per SM takes work units (chunk of padded rows that share an
+// expert) x (128-row tile of that expert's weight), dealt to the CTAs with a
+// stride of the grid.  Per unit it computes
 //   D[128 weight rows, ntok tokens] = W_tile[128, K] * X_rows[ntok, K]^T
 // with the dequantised weights as the MMA's M operand (held in tensor memory)
 // and the routed tokens as its N operand (in shared memory).  This is the
@@ -44,7 +45,8 @@
 
 namespace chord {
 
-template <int BK_, int KS_, int BS_, int AS_, int MAXN_, int ACCB_, bool GATE_UP_, int ACCW_ = MAXN_>
+template <int BK_, int KS_, int BS_, int AS_, int MAXN_, int ACCB_, bool GATE_UP_, int ACCW_ = MAXN_,
+          int PS_ = 0, bool TS_ = false>
 struct GemmCfg {
     static constexpr int BK = BK_;        // K elements per stage
     static constexpr int KS = KS_;        // code/scale stages in shared memory
@@ -55,8 +57,22 @@ struct GemmCfg {
     // columns of one accumulator buffer: ACCW / MAXN weight tiles of a unit
     // (one-stage K: several tiles share the unit's token tile)
     static constexpr int ACCW = ACCW_;
-    static constexpr int TPU_MAX = ACCW / MAXN;
+    // token-stationary units (down GEMM, one K stage): a unit is one chunk and
+    // a run of weight tiles; its token tile is loaded once, and each tile is
+    // accumulated in the next of the ACCB buffers and drained on its own
+    static constexpr bool TS = TS_;
+    static constexpr int TPU_MAX = TS ? 64 : ACCW / MAXN;
     static constexpr bool GATE_UP = GATE_UP_;
+    // K stages per accumulation chain (0: a unit's whole K range in one chain).
+    // The tensor core's fp32 accumulation loses accuracy as one chain grows
+    // (measured against an fp64 evaluation: over K = 7168 in one chain the
+    // gate/up output's bf16 rounding differs from the exact one about 7x as
+    // often as for a sequential fp32 sum).  With PS > 0 the MMA starts a fresh
+    // accumulator every PS stages, alternating between the accumulator
+    // buffers, and the epilogue adds each finished partial into the next one
+    // (fp32, round to nearest, in order) before the unit's epilogue runs on
+    // the last.
+    static constexpr int PS = PS_;
 
     // codes of a stage: BK/128 halves of [128 tile rows][64 bytes], 64B swizzle
     static constexpr int CODE_STAGE = 128 * (BK / 2);
@@ -118,6 +134,7 @@ struct GemmCfg {
     static_assert(MAXN % 16 == 0 && MAXN >= 16 && MAXN <= 256, "token tile");
     static_assert(D_COL0 + ACCB * ACCW <= TMEM_COLS, "tensor memory budget");
     static_assert(ACCW % MAXN == 0 && (TPU_MAX == 1 || (!GATE_UP && BK == 256)), "tiles per unit");
+    static_assert(!TS || (ACCW == MAXN && PS == 0), "token-stationary: one tile per accumulator buffer");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM keeps the 512-column TMEM alloc safe");
     static_assert(OFF_B % 1024 == 0 && B_REGION % 1024 == 0, "swizzle atoms need 1024B alignment");
@@ -125,6 +142,8 @@ struct GemmCfg {
     static_assert(ACCB % EPI_GROUPS == 0, "each epilogue group owns whole accumulator buffers");
     static_assert(DQW <= AS && DQW <= KS, "stages in dequant at once fit the A and code rings");
     static_assert(THREADS <= 640, "register budget of one CTA per SM");
+    static_assert(PS == 0 || (EPI_GROUPS == 1 && TPU_MAX == 1 && ACCB >= 2),
+                  "partial accumulation: one epilogue group walks every partial of a unit");
     static_assert(CODE_STAGE % 1024 == 0, "TMA destinations");
 };
 
@@ -205,6 +224,58 @@ __device__ __forceinline__ void dequant_word(uint32_t w, ScalePair sp, uint32_t*
     }
 }
 
+// Weight formats of the kernel (a template parameter: see PK below for why not
+// a run-time switch).
+constexpr int kFmtInt4 = 0;   // unsigned codes q, bf16 scales s: w = bf16((q - 8) * s)
+constexpr int kFmtMxfp4 = 1;  // FP4 E2M1 codes, one E8M0 scale byte per 32 inputs:
+                              // w = bf16(e2m1(q) * 2^(e - 127)); the pack holds the
+                              // scale widened to the bf16 value 2^(e - 127)
+
+// MXFP4 (vLLM Kimi K3 production support page, "MXFP4 MoE"; OCP Microscaling
+// FP4): a code is sign (bit 3), two exponent bits with bias 1 (bits 2-1) and one
+// mantissa bit (bit 0); exponent 0 is subnormal (m * 0.5).  Placing the three
+// magnitude bits at bf16 bits 8-6 (the exponent's two low bits and the
+// mantissa's top bit) and the sign at bit 15 gives the bf16 number
+// e2m1(q) * 2^-126 exactly: a bf16 exponent field 1..3 reads (1 + m/2) *
+// 2^(e - 127), and field 0 is a bf16 subnormal m/2 * 2^-126, which continues
+// the spacing the same way E2M1's subnormal does.
+//   lo / hi: w & 0x0F0F0F0F / (w >> 4) & 0x0F0F0F0F, byte j holding code 2j /
+//            code 2j+1;
+//   prmt:    x = code 2j in bits 0-3 and code 2j+1 in bits 16-19 (the other
+//            bytes zero: sign replication of a byte below 0x80);
+//   place:   x * 0x1040 = (x << 6) + (x << 12): the two copies of each code
+//            do not overlap (bits 6-9 and 12-15 of each half), and the mask
+//            keeps the first copy's magnitude (bits 6-8 / 22-24) and the
+//            second copy's sign (bit 15 / 31).
+__device__ __forceinline__ uint32_t mx_place_pair(uint32_t lo, uint32_t hi, int j)
+{
+    const uint32_t sel = static_cast<uint32_t>(j | (8 << 4) | ((4 + j) << 8) | (8 << 12));
+    return (prmt(lo, hi, sel) * 0x1040u) & 0x81C081C0u;
+}
+// Every scale byte e <= 128: one exact product with m = (2^(e-1), 2^(e-1)),
+// e2m1(q) * 2^-126 * 2^(e-1) = e2m1(q) * 2^(e-127) (two significant bits, so
+// the one rounding is exact unless the value overflows bf16, as in the
+// definition's rounding).
+__device__ __forceinline__ void dequant_word_mx(uint32_t w, uint32_t m, uint32_t* o)
+{
+    const uint32_t lo = w & 0x0F0F0F0Fu;
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        o[j] = bf16x2_mul(mx_place_pair(lo, hi, j), m);
+}
+// Any scale byte: 2^(e-1) leaves bf16 above e = 128, so the factor is split:
+// e2m1(q) * 2^-126 * 2^127 = 2 e2m1(q) (exact), then * 2^(e-128) (m2, also a
+// bf16 value for every e): the same single effective rounding.
+__device__ __forceinline__ void dequant_word_mx2(uint32_t w, uint32_t m2, uint32_t* o)
+{
+    const uint32_t lo = w & 0x0F0F0F0Fu;
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        o[j] = bf16x2_mul(bf16x2_mul(mx_place_pair(lo, hi, j), 0x7F007F00u /* 2^127 */), m2);
+}
+
 // One work item of a GEMM CTA: a whole unit, or one K piece of a split unit.
 struct WorkItem {
     int unit;   // chunk * units_per_chunk + tile group
@@ -218,12 +289,17 @@ struct WorkItem {
 // copies.  A template parameter, not a run-time switch: with both load paths
 // in one kernel the plain path ran 23 % slower (EP8 decode gate/up 139.5 ->
 // 171 us) although the branch was never taken.
-template <class C, bool PK>
+// FMT: the weight format (kFmtInt4 / kFmtMxfp4; MXFP4 weights come prepacked).
+template <class C, bool PK, int FMT>
 __global__ void __launch_bounds__(C::THREADS, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap codes_map,
                       const __grid_constant__ CUtensorMap scales_map,
                       const __grid_constant__ CUtensorMap b_map, const GemmArgs args)
 {
+    static_assert(FMT == kFmtInt4 || (FMT == kFmtMxfp4 && PK), "MXFP4 weights are read from packs");
+    // the INT4 dequant forms w * 2^-40 (undone here on the fp32 accumulators);
+    // the MXFP4 dequant forms w itself
+    constexpr float kRescale = FMT == kFmtInt4 ? kWeightRescale : 1.0f;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -493,30 +569,63 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // and elect.sync picks the lane that issues each MMA and commit.
         int ga = 0;  // A stages (one per K stage and tile)
         int gb = 0;  // token stages (one per K stage)
+        int pc = 0;  // accumulation chains (one per unit, or one per PS stages)
         int issued = 0;
         bool ok = true;
-        int i = 0;
         Chunk next = chunk_of_item(blockIdx.x);
         Chunk next2 = chunk_of_item(blockIdx.x + gridDim.x);
-        for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x, ++i) {
+        for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x) {
             const WorkItem it = item_of(v);
             const Chunk ch = next;
             next = next2;
             next2 = chunk_of_item(v + 2 * gridDim.x);
             const int ntok16 = (ch.nrows + 15) & ~15;
             const uint32_t idesc = idesc_bf16_f32(128, ntok16);
-            const int acc = i % C::ACCB;
+            if constexpr (C::TS) {
+                // one K stage (the host picks these configurations only for K =
+                // BK): the unit's token stage, then each tile into the next buffer
+                const int sb = gb % C::BS;
+                if (!__all_sync(0xffffffffu, mbar_wait(b_full(sb), (gb / C::BS) & 1, abort_flag, err))) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t bdesc = smem_desc_sw128(sbase + C::OFF_B + sb * C::B_STAGE);
+                for (int t = 0; t < tpu; ++t, ++ga, ++pc) {
+                    const int acc = pc % C::ACCB;
+                    const int sa = ga % C::AS;
+                    const bool got = mbar_wait(d_empty(acc), ((pc / C::ACCB) & 1) ^ 1, abort_flag, err) &&
+                                     mbar_wait(a_full(sa), (ga / C::AS) & 1, abort_flag, err);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_stage16<C::B_REGION / 16>(tmem + C::D_COL0 + acc * C::ACCW, tmem + sa * C::A_COLS,
+                                                  bdesc, idesc, 0u);
+                    issued = 1;
+                    mma_commit_elect(a_empty(sa));
+                    mma_commit_elect(d_full(acc));
+                }
+                if (!ok)
+                    break;
+                mma_commit_elect(b_empty(sb));
+                ++gb;
+                continue;
+            }
+          for (int g0 = it.k0, g1; g0 < it.k1 && ok; g0 = g1, ++pc) {
+            g1 = (C::PS > 0 && g0 + C::PS < it.k1) ? g0 + C::PS : it.k1;
+            const int acc = pc % C::ACCB;
             if (!__all_sync(0xffffffffu,
-                            mbar_wait(d_empty(acc), ((i / C::ACCB) & 1) ^ 1, abort_flag, err))) {
+                            mbar_wait(d_empty(acc), ((pc / C::ACCB) & 1) ^ 1, abort_flag, err))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem + C::D_COL0 + acc * C::ACCW;
-            for (int ks = it.k0; ks < it.k1 && ok; ++ks, ++gb) {
+            for (int ks = g0; ks < g1 && ok; ++ks, ++gb) {
                 const int sb = gb % C::BS;
                 const uint64_t bdesc = smem_desc_sw128(sbase + C::OFF_B + sb * C::B_STAGE);
-                const uint32_t accum = ks != it.k0 ? 1u : 0u;
+                const uint32_t accum = ks != g0 ? 1u : 0u;
                 if constexpr (C::TPU_MAX == 1) {
                     const int sa = ga % C::AS;
                     const bool got = mbar_wait(a_full(sa), (ga / C::AS) & 1, abort_flag, err) &&
@@ -558,6 +667,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (!ok)
                 break;
             mma_commit_elect(d_full(acc));
+          }
         }
         if (!ok && issued) {
             // drain tensor-core work in flight before TMEM is released
@@ -601,12 +711,107 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
         };
         constexpr int EG = C::EPI_GROUPS;
-        int i = egrp;
-        Chunk c_cur = chunk_of_item(blockIdx.x + egrp * gridDim.x);
-        Chunk c_nxt = chunk_of_item(blockIdx.x + (egrp + EG) * gridDim.x);
+        // the epilogue groups take every EG-th unit, or (token-stationary
+        // units) every unit and in it every EG-th tile
+        constexpr int US = C::TS ? 1 : EG;
+        const int ev0 = C::TS ? 0 : egrp;
+        // accumulation chains taken (PS > 0: several per unit; TS: one per tile,
+        // counted over both groups)
+        int i = ev0;
+        Chunk c_cur = chunk_of_item(blockIdx.x + ev0 * gridDim.x);
+        Chunk c_nxt = chunk_of_item(blockIdx.x + (ev0 + US) * gridDim.x);
         load_meta(c_cur, meta_next);
         constexpr int kSlotFloats = 128 * C::MAXN;
-        for (int v = blockIdx.x + egrp * gridDim.x; v < total_items; v += EG * gridDim.x, i += EG) {
+        // down: the epilogue of one accumulator buffer holding weight tiles
+        // nt0u .. nt0u + tpuu - 1 of chunk ch (tpuu > 1: consecutive column
+        // ranges of the buffer); it goes back to the MMA after its last read
+        auto down_blocks = [&](const Chunk& ch, int nt0u, int tpuu, uint32_t dbase, int acc,
+                               const int4* meta_cur) {
+            const int ntok = ch.nrows;
+            const int ntok16 = (ntok + 15) & ~15;
+            // Each 32-row x 16-column block goes through a shared tile so that
+            // lane l owns rows 4 (l % 8) .. +3 of columns l / 8 + {0, 4, 8, 12}:
+            // 16-byte stores and vector reductions instead of one 4-byte
+            // access per lane and column.
+            const int N = args.N;
+            float* tile = reinterpret_cast<float*>(smem + C::OFF_EPIT) + (egrp * 4 + q) * 16 * 32;
+            const int m4 = (lane & 7) * 4;
+            const int cg = lane >> 3;
+            // one 16-column block of tile t: accumulator columns -> shared tile
+            // -> per-pair stores / token reductions / row stores
+            auto block = [&](int t, int c0, int4 mrec) {
+                const int nq = (nt0u + t) * 128 + q * 32;
+                uint32_t v[16];
+                tmem_ld_x16(dbase + t * C::MAXN + c0, v);
+                tmem_wait_ld();
+                if (t == tpuu - 1 && c0 + 16 >= ntok16) {
+                    // last block read: the accumulator goes back to the MMA
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(d_empty(acc));
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    tile[j * 32 + lane] = __uint_as_float(v[j]) * kRescale;
+                __syncwarp();
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) {
+                    const int j = cg + 4 * ii;
+                    const int c = c0 + j;
+                    const int src = c & 31;
+                    const int p = __shfl_sync(0xffffffffu, mrec.x, src);
+                    const int tok = __shfl_sync(0xffffffffu, mrec.y, src);
+                    const float w = __int_as_float(__shfl_sync(0xffffffffu, mrec.z, src));
+                    if (c >= ntok)
+                        continue;
+                    const float4 y = *reinterpret_cast<const float4*>(tile + j * 32 + m4);
+                    if (args.epi & kEpiStoreRows) {
+                        uint2 o;
+                        o.x = bf16x2_pack_rn(y.x, y.y);
+                        o.y = bf16x2_pack_rn(y.z, y.w);
+                        *reinterpret_cast<uint2*>(args.rows_out + static_cast<int64_t>(ch.row0 + c) * N + nq +
+                                                  m4) = o;
+                    }
+                    if (per_pair && p >= 0) {
+                        if (args.epi & kEpiStorePair)
+                            *reinterpret_cast<float4*>(args.y_pairs + static_cast<int64_t>(p) * N + nq + m4) = y;
+                        if (args.epi & kEpiReduceTok)
+                            red_add_v4_f32(args.out_acc + static_cast<int64_t>(tok) * N + nq + m4, w * y.x,
+                                           w * y.y, w * y.z, w * y.w);
+                    }
+                }
+                __syncwarp();  // the tile is rewritten by the next block
+            };
+            if constexpr (C::COLD_WAITS) {
+                // (rolled loops for the BK 256 tiles: their epilogue runs once
+                // per short unit, and its code competes for the instruction
+                // cache with every other role's)
+#pragma unroll 1
+                for (int t = 0; t < tpuu; ++t) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < ntok16; c0 += 16) {
+                        // columns c0 .. c0 + 15 sit in one lane group: records meta_cur[c0 / 32]
+                        int4 mrec = meta_cur[0];
+#pragma unroll
+                        for (int k = 1; k < MPT; ++k)
+                            if (c0 >= 32 * k)
+                                mrec = meta_cur[k];
+                        block(t, c0, mrec);
+                    }
+                }
+            } else {
+                // (the prefill tile's long units: unrolled over the token tile)
+#pragma unroll
+                for (int c0 = 0; c0 < C::MAXN; c0 += 16) {
+                    if (c0 >= ntok16)
+                        break;
+                    block(0, c0, meta_cur[c0 / 32]);
+                }
+            }
+        };
+        for (int v = blockIdx.x + ev0 * gridDim.x; v < total_items;
+             v += US * gridDim.x, i += C::TS ? 0 : EG) {
             const WorkItem it = item_of(v);
             const Chunk ch = c_cur;
             int4 meta_cur[MPT];
@@ -614,16 +819,89 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int k = 0; k < MPT; ++k)
                 meta_cur[k] = meta_next[k];
             load_meta(c_nxt, meta_next);
-            const Chunk c_nn = chunk_of_item(v + 2 * EG * gridDim.x);
+            const Chunk c_nn = chunk_of_item(v + 2 * US * gridDim.x);
             const int nt0 = (it.unit % units_per_chunk) * tpu;
             const int ntok = ch.nrows;
             const int ntok16 = (ntok + 15) & ~15;
-            const int acc = i % C::ACCB;
             c_cur = c_nxt;
             c_nxt = c_nn;
+            if constexpr (C::TS) {
+                // one K stage; tile t of the unit is accumulation chain i, in
+                // buffer i % ACCB, drained by group i % EG
+                bool okt = true;
+                for (int t = 0; t < tpu; ++t, ++i) {
+                    if (i % EG != egrp)
+                        continue;
+                    const int acct = i % C::ACCB;
+                    if (!wait_side(d_full(acct), (i / C::ACCB) & 1)) {
+                        okt = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    down_blocks(ch, nt0 + t, 1,
+                                tmem + (static_cast<uint32_t>(q * 32) << 16) + C::D_COL0 + acct * C::ACCW,
+                                acct, meta_cur);
+                }
+                if (!okt)
+                    break;
+                continue;
+            }
+            int acc = i % C::ACCB;
             if (!wait_side(d_full(acc), (i / C::ACCB) & 1))
                 break;
             tc_fence_after();
+            if constexpr (C::PS > 0) {
+                // add each finished partial into the next one; the last holds the sum
+                bool okp = true;
+                for (int g0 = it.k0 + C::PS; g0 < it.k1; g0 += C::PS) {
+                    const int nacc = (i + 1) % C::ACCB;
+                    if (!wait_side(d_full(nacc), ((i + 1) / C::ACCB) & 1)) {
+                        okp = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::D_COL0;
+                    const uint32_t src = lane_base + acc * C::ACCW;
+                    const uint32_t dst = lane_base + nacc * C::ACCW;
+                    // 32 columns per load wait, then a 16-column tail
+                    int c0 = 0;
+                    for (; c0 + 32 <= ntok16; c0 += 32) {
+                        uint32_t a0[16], b0[16], a1[16], b1[16];
+                        tmem_ld_x16(src + c0, a0);
+                        tmem_ld_x16(dst + c0, b0);
+                        tmem_ld_x16(src + c0 + 16, a1);
+                        tmem_ld_x16(dst + c0 + 16, b1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            b0[jj] = __float_as_uint(__uint_as_float(a0[jj]) + __uint_as_float(b0[jj]));
+                            b1[jj] = __float_as_uint(__uint_as_float(a1[jj]) + __uint_as_float(b1[jj]));
+                        }
+                        tmem_st_x16(dst + c0, b0);
+                        tmem_st_x16(dst + c0 + 16, b1);
+                    }
+                    if (c0 < ntok16) {
+                        uint32_t a0[16], b0[16];
+                        tmem_ld_x16(src + c0, a0);
+                        tmem_ld_x16(dst + c0, b0);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            b0[jj] = __float_as_uint(__uint_as_float(a0[jj]) + __uint_as_float(b0[jj]));
+                        tmem_st_x16(dst + c0, b0);
+                    }
+                    tmem_wait_st();
+                    // the earlier partial's buffer goes back to the MMA
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(d_empty(acc));
+                    ++i;
+                    acc = nacc;
+                }
+                if (!okp)
+                    break;
+            }
             const uint32_t dbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + C::D_COL0 + acc * C::ACCW;
             // A piece of a split unit: the accumulator goes to the piece's slot
@@ -690,7 +968,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tmem_wait_ld();
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const float mine = __uint_as_float(v[jj]) * kWeightRescale;
+                        const float mine = __uint_as_float(v[jj]) * kRescale;
                         const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
                         if (is_gate) {
                             // fast exp / divide: a few fp32 ulp, far below the bf16 rounding of h
@@ -730,86 +1008,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (!epi_sync())
                     break;
             } else {
-                // Each 32-row x 16-column block goes through a shared tile so that
-                // lane l owns rows 4 (l % 8) .. +3 of columns l / 8 + {0, 4, 8, 12}:
-                // 16-byte stores and vector reductions instead of one 4-byte
-                // access per lane and column.
-                const int N = args.N;
-                float* tile = reinterpret_cast<float*>(smem + C::OFF_EPIT) + (egrp * 4 + q) * 16 * 32;
-                const int m4 = (lane & 7) * 4;
-                const int cg = lane >> 3;
-                // one 16-column block of tile t: accumulator columns -> shared tile
-                // -> per-pair stores / token reductions / row stores
-                auto block = [&](int t, int c0, int4 mrec) {
-                    const int nq = (nt0 + t) * 128 + q * 32;
-                    uint32_t v[16];
-                    tmem_ld_x16(dbase + t * C::MAXN + c0, v);
-                    tmem_wait_ld();
-                    if (t == tpu - 1 && c0 + 16 >= ntok16) {
-                        // last block read: the accumulator goes back to the MMA
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(d_empty(acc));
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        tile[j * 32 + lane] = __uint_as_float(v[j]) * kWeightRescale;
-                    __syncwarp();
-#pragma unroll
-                    for (int ii = 0; ii < 4; ++ii) {
-                        const int j = cg + 4 * ii;
-                        const int c = c0 + j;
-                        const int src = c & 31;
-                        const int p = __shfl_sync(0xffffffffu, mrec.x, src);
-                        const int tok = __shfl_sync(0xffffffffu, mrec.y, src);
-                        const float w = __int_as_float(__shfl_sync(0xffffffffu, mrec.z, src));
-                        if (c >= ntok)
-                            continue;
-                        const float4 y = *reinterpret_cast<const float4*>(tile + j * 32 + m4);
-                        if (args.epi & kEpiStoreRows) {
-                            uint2 o;
-                            o.x = bf16x2_pack_rn(y.x, y.y);
-                            o.y = bf16x2_pack_rn(y.z, y.w);
-                            *reinterpret_cast<uint2*>(args.rows_out + static_cast<int64_t>(ch.row0 + c) * N + nq +
-                                                      m4) = o;
-                        }
-                        if (per_pair && p >= 0) {
-                            if (args.epi & kEpiStorePair)
-                                *reinterpret_cast<float4*>(args.y_pairs + static_cast<int64_t>(p) * N + nq + m4) = y;
-                            if (args.epi & kEpiReduceTok)
-                                red_add_v4_f32(args.out_acc + static_cast<int64_t>(tok) * N + nq + m4, w * y.x,
-                                               w * y.y, w * y.z, w * y.w);
-                        }
-                    }
-                    __syncwarp();  // the tile is rewritten by the next block
-                };
-                if constexpr (C::COLD_WAITS) {
-                    // (rolled loops for the BK 256 tiles: their epilogue runs once
-                    // per short unit, and its code competes for the instruction
-                    // cache with every other role's)
-#pragma unroll 1
-                    for (int t = 0; t < tpu; ++t) {
-#pragma unroll 1
-                        for (int c0 = 0; c0 < ntok16; c0 += 16) {
-                            // columns c0 .. c0 + 15 sit in one lane group: records meta_cur[c0 / 32]
-                            int4 mrec = meta_cur[0];
-#pragma unroll
-                            for (int k = 1; k < MPT; ++k)
-                                if (c0 >= 32 * k)
-                                    mrec = meta_cur[k];
-                            block(t, c0, mrec);
-                        }
-                    }
-                } else {
-                    // (the prefill tile's long units: unrolled over the token tile)
-#pragma unroll
-                    for (int c0 = 0; c0 < C::MAXN; c0 += 16) {
-                        if (c0 >= ntok16)
-                            break;
-                        block(0, c0, meta_cur[c0 / 32]);
-                    }
-                }
+                down_blocks(ch, nt0, tpu, dbase, acc, meta_cur);
             }
         }
     } else if (warp >= 8) {
@@ -869,17 +1068,55 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // 16 TMEM columns.  Codes are read from shared memory group by group
                 // (not all up front) so the stores of one group overlap the
                 // arithmetic of the next without running out of registers.
+                if constexpr (FMT == kFmtInt4) {
 #pragma unroll
-                for (int grp = 0; grp < C::BK / 32; ++grp) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(cstage + code_piece_offset(grp, srow));
-                    const ScalePair sp =
-                        scale_pair(__byte_perm(sc[grp >> 1], 0, (grp & 1) ? 0x3232 : 0x1010));
-                    uint32_t o[16];
-                    dequant_word(v.x, sp, &o[0]);
-                    dequant_word(v.y, sp, &o[4]);
-                    dequant_word(v.z, sp, &o[8]);
-                    dequant_word(v.w, sp, &o[12]);
-                    tmem_st_x16(tmem + tlane + sa * C::A_COLS + grp * 16, o);
+                    for (int grp = 0; grp < C::BK / 32; ++grp) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(cstage + code_piece_offset(grp, srow));
+                        const ScalePair sp =
+                            scale_pair(__byte_perm(sc[grp >> 1], 0, (grp & 1) ? 0x3232 : 0x1010));
+                        uint32_t o[16];
+                        dequant_word(v.x, sp, &o[0]);
+                        dequant_word(v.y, sp, &o[4]);
+                        dequant_word(v.z, sp, &o[8]);
+                        dequant_word(v.w, sp, &o[12]);
+                        tmem_st_x16(tmem + tlane + sa * C::A_COLS + grp * 16, o);
+                    }
+                } else {
+                    // the widened scales are 2^(e-127) (or NaN for e = 255): a scale
+                    // byte above 128 is a bf16 value above 2 (bits above 0x4000)
+                    bool big = false;
+#pragma unroll
+                    for (int i = 0; i < C::BK / 64; ++i)
+                        big = big || (sc[i] & 0x7FFFu) > 0x4000u || ((sc[i] >> 16) & 0x7FFFu) > 0x4000u;
+                    if (!__any_sync(0xffffffffu, big)) {
+#pragma unroll
+                        for (int grp = 0; grp < C::BK / 32; ++grp) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(cstage + code_piece_offset(grp, srow));
+                            // (2^(e-127), 2^(e-127)) * 2^126 = 2^(e-1), exact
+                            const uint32_t m = bf16x2_mul(
+                                __byte_perm(sc[grp >> 1], 0, (grp & 1) ? 0x3232 : 0x1010), 0x7E807E80u);
+                            uint32_t o[16];
+                            dequant_word_mx(v.x, m, &o[0]);
+                            dequant_word_mx(v.y, m, &o[4]);
+                            dequant_word_mx(v.z, m, &o[8]);
+                            dequant_word_mx(v.w, m, &o[12]);
+                            tmem_st_x16(tmem + tlane + sa * C::A_COLS + grp * 16, o);
+                        }
+                    } else {
+#pragma unroll
+                        for (int grp = 0; grp < C::BK / 32; ++grp) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(cstage + code_piece_offset(grp, srow));
+                            // 2^(e-127) * 2^-1 = 2^(e-128), exact (a subnormal for e = 0)
+                            const uint32_t m2 = bf16x2_mul(
+                                __byte_perm(sc[grp >> 1], 0, (grp & 1) ? 0x3232 : 0x1010), 0x3F003F00u);
+                            uint32_t o[16];
+                            dequant_word_mx2(v.x, m2, &o[0]);
+                            dequant_word_mx2(v.y, m2, &o[4]);
+                            dequant_word_mx2(v.z, m2, &o[8]);
+                            dequant_word_mx2(v.w, m2, &o[12]);
+                            tmem_st_x16(tmem + tlane + sa * C::A_COLS + grp * 16, o);
+                        }
+                    }
                 }
                 // The next TMA into this code stage writes through the async proxy;
                 // order these generic-proxy reads before it (without the fence a

@@ -136,10 +136,10 @@ struct PrepArgs {
     int32_t* fill_i32;  // set to -1
     int64_t fill_count;
     // prepacked weights: the two packs' headers (gate/up, down) and what each
-    // must say {kind, experts at least, N, K}; on a mismatch both chunk lists
+    // must say; on a mismatch both chunk lists
     // are left empty (the GEMMs compute nothing) and CHORD_DEVERR_PACKED is set
     const uint32_t* pk_hdr[2];
-    uint32_t pk_want[2][4];
+    uint32_t pk_want[2][5];  // {kind, experts at least, N, K, weight format}
     int* err;
 };
 
@@ -162,9 +162,11 @@ cudaError_t launch_route_align(const RouteArgs& r, const AlignArgs& a, cudaStrea
 struct PackArgs {
     int kind;               // CHORD_PACK_GATE_UP / CHORD_PACK_DOWN
     const int32_t* q;       // [E, N, K/8]
-    const uint16_t* sc;     // [E, N, K/32]
+    const uint16_t* sc;     // INT4: bf16 scales [E, N, K/32]
     int E, N, K;
     uint8_t* out;           // header + E * (N/128) * (K/256) blocks
+    int fmt;                // kPackFmtInt4 / kPackFmtMxfp4 (header word kPackFormatWord)
+    const uint8_t* sc8;     // MXFP4: E8M0 scale bytes [E, N, K/32], widened to bf16 2^(e-127)
 };
 cudaError_t launch_prepack(const PackArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_prep(const PrepArgs& a, int work_blocks, cudaStream_t s);

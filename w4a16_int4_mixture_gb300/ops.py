@@ -153,12 +153,16 @@ def moe_route_align(logits: torch.Tensor, k: int, E_local: int, block_m: int = 1
 
 
 class PackedWeights:
-    """One layer's weights after chord_w4a16_prepack: w13 (kind GATE_UP) and
-    w2 (kind DOWN) as uint8 device buffers, with the sizes they were packed
-    for.  Pass it as w13_q (with w13_s, w2_q, w2_s None) to the layer calls."""
+    """One layer's weights after chord_w4a16_prepack (fmt "int4") or
+    chord_mxfp4_prepack (fmt "mxfp4"): w13 (kind GATE_UP) and w2 (kind DOWN)
+    as uint8 device buffers, with the sizes they were packed for.  Pass it as
+    w13_q (with w13_s, w2_q, w2_s None) to the layer calls."""
 
-    def __init__(self, w13: torch.Tensor, w2: torch.Tensor, E: int, H: int, I: int):
-        self.w13, self.w2, self.E, self.H, self.I = w13, w2, E, H, I
+    def __init__(self, w13: torch.Tensor, w2: torch.Tensor, E: int, H: int, I: int,
+                 fmt: str = "int4"):
+        if fmt not in ("int4", "mxfp4"):
+            raise ValueError(f"unknown weight format {fmt!r}")
+        self.w13, self.w2, self.E, self.H, self.I, self.fmt = w13, w2, E, H, I, fmt
 
 
 def prepack_size(kind: int, E: int, N: int, K: int) -> int:
@@ -167,10 +171,13 @@ def prepack_size(kind: int, E: int, N: int, K: int) -> int:
 
 def prepack(w_q: torch.Tensor, w_s: torch.Tensor, kind: int, out=None) -> torch.Tensor:
     """One GEMM's codes [E, N, K/8] and scales [E, N, K/32] -> the packed
-    uint8 buffer (include/chord.h, chord_w4a16_prepack)."""
+    uint8 buffer (include/chord.h): bf16 scales give an INT4 pack
+    (chord_w4a16_prepack), uint8 E8M0 scale bytes an MXFP4 pack
+    (chord_mxfp4_prepack)."""
     _req(w_q, "w_q", _I32, ndim=3)
     dev = w_q.device
-    _req(w_s, "w_s", _BF16, dev, 3)
+    _req(w_s, "w_s", _BF16 + (torch.uint8,), dev, 3)
+    mx = w_s.dtype == torch.uint8
     E, N, K8 = w_q.shape
     K = K8 * 8
     if tuple(w_s.shape) != (E, N, K // 32):
@@ -182,17 +189,19 @@ def prepack(w_q: torch.Tensor, w_s: torch.Tensor, kind: int, out=None) -> torch.
         out = torch.empty(need, dtype=torch.uint8, device=dev)
     else:
         _req(out, "out", (torch.uint8,), dev, 1)
-    st = lib().chord_w4a16_prepack(kind, _p(w_q), _p(w_s), E, N, K, _p(out), out.numel(),
-                                   _stream(dev))
-    B.check(st, "chord_w4a16_prepack")
+    fn = lib().chord_mxfp4_prepack if mx else lib().chord_w4a16_prepack
+    st = fn(kind, _p(w_q), _p(w_s), E, N, K, _p(out), out.numel(), _stream(dev))
+    B.check(st, "chord_mxfp4_prepack" if mx else "chord_w4a16_prepack")
     return out
 
 
 def prepack_weights(w13_q, w13_s, w2_q, w2_s) -> PackedWeights:
-    """Both GEMMs of a layer -> PackedWeights."""
-    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, w13_q.device)
+    """Both GEMMs of a layer -> PackedWeights.  bf16 scales: INT4 weights;
+    uint8 scales (E8M0 bytes): MXFP4 weights, whose codes are E2M1 numbers."""
+    mx = w13_s.dtype == torch.uint8
+    E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, w13_q.device, mx)
     return PackedWeights(prepack(w13_q, w13_s, B.PACK_GATE_UP), prepack(w2_q, w2_s, B.PACK_DOWN),
-                         E, H, I)
+                         E, H, I, "mxfp4" if mx else "int4")
 
 
 def _weights(w13_q, w13_s, w2_q, w2_s, dev):
@@ -208,16 +217,20 @@ def _weights(w13_q, w13_s, w2_q, w2_s, dev):
             # (the device checks the header; a short buffer would be read past its end)
             if t.numel() < nb:
                 raise ValueError(f"{n}: {t.numel()} bytes, a pack of these sizes has {nb}")
-        return pw.E, pw.H, pw.I, (_p(pw.w13), None, _p(pw.w2), None), B.FLAG_PREPACKED
+        flags = B.FLAG_PREPACKED | (B.FLAG_MXFP4 if pw.fmt == "mxfp4" else 0)
+        return pw.E, pw.H, pw.I, (_p(pw.w13), None, _p(pw.w2), None), flags
+    if w13_s is not None and w13_s.dtype == torch.uint8:
+        raise ValueError("MXFP4 weights are used through their packs: prepack_weights() first")
     E, H, I = _check_weights(w13_q, w13_s, w2_q, w2_s, dev)
     return E, H, I, (_p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s)), 0
 
 
-def _check_weights(w13_q, w13_s, w2_q, w2_s, dev):
+def _check_weights(w13_q, w13_s, w2_q, w2_s, dev, mx=False):
+    sdt = (torch.uint8,) if mx else _BF16
     _req(w13_q, "w13_q", _I32, dev, 3)
-    _req(w13_s, "w13_s", _BF16, dev, 3)
+    _req(w13_s, "w13_s", sdt, dev, 3)
     _req(w2_q, "w2_q", _I32, dev, 3)
-    _req(w2_s, "w2_s", _BF16, dev, 3)
+    _req(w2_s, "w2_s", sdt, dev, 3)
     E, N13, H8 = w13_q.shape
     H = H8 * 8
     I = N13 // 2
