@@ -90,22 +90,30 @@ struct GemmCfg {
     static constexpr int B_STAGE = B_KBLK * B_REGION;
     static constexpr int HS_BYTES = GATE_UP ? MAXN * 128 : 0;  // 64 channels of bf16 per row
     static constexpr int META_BYTES = 0;  // (column records live in registers)
-    // down with token tiles of at most 64 rows (short units when K is small):
-    // a second group of four epilogue warps (warps 16-19) takes every other
-    // unit, each group owning one accumulator buffer
-    static constexpr int EPI_GROUPS = (!GATE_UP && MAXN <= 64) ? 2 : 1;
+    // token-stationary down units (a one-stage K, where every tile's
+    // epilogue is short and the epilogue is the critical role): a second group
+    // of four epilogue warps (warps 16-19) takes every other tile, each group
+    // owning every other accumulator buffer
+    static constexpr int EPI_GROUPS = (!GATE_UP && MAXN <= 64 && TS) ? 2 : 1;
     // dequant warps per TMEM lane quadrant.  Each holds one claimed K stage,
     // so up to DQW stages are in dequant at once; their A slots (and code
     // slots) must be distinct phases of the rings, hence DQW <= AS and KS.
-    // Three for the gate/up GEMM when it has three A stages: the dequant is
-    // the bound there (measured 145.6 -> 141.1 us for the EP8 decode gate/up);
-    // the down GEMM's 640 threads leave no registers for a fifth group.
-    static constexpr int DQW = (GATE_UP && AS >= 3) ? 3 : 2;
+    // Three when there are three A stages and one epilogue group: the dequant
+    // is the bound of the weight-streaming tiles (measured 145.6 -> 141.1 us
+    // for the EP8 decode gate/up); a CTA of 640 threads has no registers for
+    // a sixth warp group.
+    static constexpr int DQW = (AS >= 3 && EPI_GROUPS == 1) ? 3 : 2;
     static constexpr int EPI1_WARP = 8 + 4 * DQW;  // first warp of the second epilogue group
     static constexpr int THREADS = 32 * EPI1_WARP + 128 * (EPI_GROUPS - 1);
     // down: per epilogue warp a 16-column x 32-row fp32 tile to transpose the
     // accumulator so each lane owns four consecutive output rows of a column
+    // (a direct epilogue without the tile, lane l reducing output channel l of
+    // its quadrant one token column at a time, took the TP8 2048-token down
+    // GEMM from 182 to 401 us: four times the reductions, each coalesced)
     static constexpr int EPIT_BYTES = GATE_UP ? 0 : EPI_GROUPS * 4 * 16 * 32 * 4;
+    // (bulk reductions of the tile's token columns through the copy engine,
+    // 128 bytes each, took the same GEMM to 281 us: vector reductions by every
+    // lane are the fastest of the three forms measured)
 
     static constexpr int OFF_CODES = 0;
     static constexpr int OFF_B = OFF_CODES + KS * CODE_STAGE;
