@@ -103,6 +103,9 @@ struct GemmCfg {
     // for the EP8 decode gate/up); a CTA of 640 threads has no registers for
     // a sixth warp group.
     static constexpr int DQW = (AS >= 3 && EPI_GROUPS == 1) ? 3 : 2;
+    // (a split dequant, every warp of a quadrant taking every stage and in it
+    // every DQW-th scale group, cut one stage's latency but ran the EP8 decode
+    // gate/up at 188 us against 145: whole stages per warp, in turn, it is)
     static constexpr int EPI1_WARP = 8 + 4 * DQW;  // first warp of the second epilogue group
     static constexpr int THREADS = 32 * EPI1_WARP + 128 * (EPI_GROUPS - 1);
     // down: per epilogue warp a 16-column x 32-row fp32 tile to transpose the
