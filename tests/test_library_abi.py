@@ -66,44 +66,67 @@ def test_workspace_sizes_are_positive_and_monotone(lib):
     assert lib.chord_moe_align_workspace_size(512, 8, 48) >= 256 + 16 * 48 * 4
 
 
+def _gpu_visible():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:  # pragma: no cover
+        return False
+
+
+# Checks that need a non-NULL pointer to reach them (a misaligned address, a
+# layout pointer that must be absent) pass a placeholder address the library
+# never dereferences: the host checks return first.  They run only where no GPU
+# is visible, so a regression in the order of the checks can never launch a
+# kernel on a placeholder address.
+placeholder_pointers = pytest.mark.skipif(
+    _gpu_visible(), reason="passes placeholder device addresses; host-side checks only")
+
+
 def test_host_checks_reject_before_launch(lib):
-    vp = ctypes.c_void_p
-    fake = vp(0x1000)
+    """Size, capacity and flag checks come before any pointer is looked at,
+    so every call here passes NULL for every device pointer."""
     # unsupported hidden size (not a multiple of 256)
-    st = lib.chord_w4a16_moe_indexed(fake, 4, 200, 128, 8, 8, 2, fake, fake, fake, fake, fake,
-                                     fake, fake, fake, 1024, 16, fake, 1 << 20, fake, None, 0, None)
+    st = lib.chord_w4a16_moe_indexed(None, 4, 200, 128, 8, 8, 2, None, None, None, None, None,
+                                     None, None, None, 1024, 16, None, 1 << 20, None, None, 0, None)
     assert st == -2
     # k too large
-    st = lib.chord_w4a16_moe_indexed(fake, 4, 256, 128, 8, 8, 33, fake, fake, fake, fake, fake,
-                                     fake, fake, fake, 1024, 16, fake, 1 << 20, fake, None, 0, None)
+    st = lib.chord_w4a16_moe_indexed(None, 4, 256, 128, 8, 8, 33, None, None, None, None, None,
+                                     None, None, None, 1024, 16, None, 1 << 20, None, None, 0, None)
     assert st == -2
     # capacity too small
-    st = lib.chord_w4a16_moe_indexed(fake, 4, 256, 128, 8, 8, 2, fake, fake, fake, fake, fake,
-                                     fake, fake, fake, 16, 16, fake, 1 << 20, fake, None, 0, None)
+    st = lib.chord_w4a16_moe_indexed(None, 4, 256, 128, 8, 8, 2, None, None, None, None, None,
+                                     None, None, None, 16, 16, None, 1 << 20, None, None, 0, None)
     assert st == -3
-    # null pointer
-    st = lib.chord_w4a16_moe_indexed(None, 4, 256, 128, 8, 8, 2, fake, fake, fake, fake, fake,
-                                     fake, fake, fake, 1024, 16, fake, 1 << 20, fake, None, 0, None)
+    # every size right: the NULL pointers are refused
+    st = lib.chord_w4a16_moe_indexed(None, 4, 256, 128, 8, 8, 2, None, None, None, None, None,
+                                     None, None, None, 1024, 16, None, 1 << 20, None, None, 0, None)
     assert st == -1
     # T = 0 is a no-op
     st = lib.chord_w4a16_moe_indexed(None, 0, 256, 128, 8, 8, 2, None, None, None, None, None,
                                      None, None, None, 0, 16, None, 0, None, None, 0, None)
     assert st == 0
     # align: capacity not enough / bad block_m / map missing with E_local != E_global
-    assert lib.chord_moe_align(fake, 10, 2, 8, None, 8, 16, fake, fake, fake, 16, fake, 4096,
+    assert lib.chord_moe_align(None, 10, 2, 8, None, 8, 16, None, None, None, 16, None, 4096,
                                None) == -3
-    assert lib.chord_moe_align(fake, 10, 2, 8, None, 8, 0, fake, fake, fake, 512, fake, 4096,
+    assert lib.chord_moe_align(None, 10, 2, 8, None, 8, 0, None, None, None, 512, None, 4096,
                                None) == -1
-    assert lib.chord_moe_align(fake, 10, 2, 16, None, 8, 16, fake, fake, fake, 512, fake, 4096,
+    assert lib.chord_moe_align(None, 10, 2, 16, None, 8, 16, None, None, None, 512, None, 4096,
                                None) == -1
+    # grouped: an unknown mode
+    assert lib.chord_w4a16_moe_grouped(7, None, 32, 256, 128, 4, None, None, 8, 1, None, None,
+                                       None, None, None, None, 0, 0, None, 1 << 20, None, None,
+                                       None, 0, None) == -4
+
+
+@placeholder_pointers
+def test_host_checks_that_need_a_pointer(lib):
+    fake = ctypes.c_void_p(0x1000)
     # grouped: wrong layout combinations fail loudly
     assert lib.chord_w4a16_moe_grouped(0, fake, 32, 256, 128, 4, None, None, 0, 1, fake, fake,
                                        fake, fake, None, None, 0, 0, fake, 1 << 20, fake, None,
                                        None, 0, None) == -4
     assert lib.chord_w4a16_moe_grouped(1, fake, 32, 256, 128, 4, fake, fake, 8, 1, fake, fake,
-                                       fake, fake, None, None, 0, 0, fake, 1 << 20, fake, None,
-                                       None, 0, None) == -4
-    assert lib.chord_w4a16_moe_grouped(7, fake, 32, 256, 128, 4, None, fake, 8, 1, fake, fake,
                                        fake, fake, None, None, 0, 0, fake, 1 << 20, fake, None,
                                        None, 0, None) == -4
     assert lib.chord_w4a16_moe_grouped(0, fake, 30, 256, 128, 4, fake, None, 0, 1, fake, fake,
@@ -126,17 +149,27 @@ def test_prepack_size_and_host_checks(lib):
     for bad in [(3, 1, 128, 256), (1, 0, 128, 256), (1, 1, 64, 256), (2, 1, 128, 128),
                 (2, 1, 200, 256)]:
         assert lib.chord_w4a16_prepack_size(*bad) == 0
-    vp = ctypes.c_void_p
-    fake = vp(4096)  # never dereferenced: the host checks come first
     n = lib.chord_w4a16_prepack_size(2, 1, 128, 256)
-    assert lib.chord_w4a16_prepack(7, fake, fake, 1, 128, 256, fake, n, None) == -1
-    assert lib.chord_w4a16_prepack(2, fake, fake, 1, 100, 256, fake, n, None) == -2
-    assert lib.chord_w4a16_prepack(2, fake, fake, 1, 128, 300, fake, n, None) == -2
+    assert lib.chord_w4a16_prepack(7, None, None, 1, 128, 256, None, n, None) == -1
+    assert lib.chord_w4a16_prepack(2, None, None, 1, 100, 256, None, n, None) == -2
+    assert lib.chord_w4a16_prepack(2, None, None, 1, 128, 300, None, n, None) == -2
+    assert lib.chord_w4a16_prepack(2, None, None, 1, 128, 256, None, n, None) == -1
+    assert lib.chord_mxfp4_prepack(2, None, None, 1, 128, 300, None, n, None) == -2
+
+
+@placeholder_pointers
+def test_prepack_pointer_checks(lib):
+    lib.chord_w4a16_prepack_size.restype = ctypes.c_size_t
+    vp = ctypes.c_void_p
+    fake = vp(4096)
+    n = lib.chord_w4a16_prepack_size(2, 1, 128, 256)
     assert lib.chord_w4a16_prepack(2, None, fake, 1, 128, 256, fake, n, None) == -1
     assert lib.chord_w4a16_prepack(2, fake, fake, 1, 128, 256, vp(4100), n, None) == -1
     assert lib.chord_w4a16_prepack(2, fake, fake, 1, 128, 256, fake, n - 16, None) == -1
+    assert lib.chord_mxfp4_prepack(2, fake, fake, 1, 128, 256, fake, n - 16, None) == -1
 
 
+@placeholder_pointers
 def test_prepacked_flag_host_checks(lib):
     """With CHORD_FLAG_PREPACKED the scale pointers must be NULL, without it
     they must be given; unknown flag bits are rejected."""
@@ -152,7 +185,8 @@ def test_prepacked_flag_host_checks(lib):
     assert call(f, f, 16) == -1      # packed: scales must be NULL
     assert call(None, None, 0) == -1  # plain: scales required
     assert call(f, None, 16) == -1
-    assert call(None, None, 32) == -1  # unknown flag bit
+    assert call(None, None, 64) == -1  # unknown flag bit
+    assert call(None, None, 32) == -1  # MXFP4 without the prepacked flag
     g = lib.chord_w4a16_moe_grouped(0, f, 16, H, I, El, f, None, 0, 1, f, f, f, f, None, None,
                                     0, 0, f, 1 << 20, f, None, None, 16, None)
     assert g == -1

@@ -807,10 +807,10 @@ chord_status chord_moe_align(const int32_t* topk_ids, int64_t T, int k, int E_gl
         return CHORD_ERR_INVALID_ARG;
     if (T * k >= (int64_t(1) << 31))
         return CHORD_ERR_UNSUPPORTED_SHAPE;
-    if (!sorted_ids || !expert_ids || !num_tokens_padded || (T > 0 && !topk_ids))
-        return CHORD_ERR_INVALID_ARG;
     if (capacity < chord_moe_align_capacity(T, k, E_local, block_m) || capacity % block_m != 0)
         return CHORD_ERR_CAPACITY;
+    if (!sorted_ids || !expert_ids || !num_tokens_padded || (T > 0 && !topk_ids))
+        return CHORD_ERR_INVALID_ARG;
     chord_status st =
         check_ws(workspace, workspace_bytes, chord_moe_align_workspace_size(T, k, E_local));
     if (st != CHORD_OK)
@@ -937,14 +937,15 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
         return CHORD_ERR_UNSUPPORTED_SHAPE;
     if (T == 0)
         return CHORD_OK;
+    // (every size check comes before the pointers are looked at)
+    if (capacity < chord_moe_align_capacity(T, k, E_local, block_m) || capacity % block_m != 0)
+        return CHORD_ERR_CAPACITY;
     if (!x || !w13_q || !w2_q || !topk_weights || !sorted_ids || !expert_ids ||
         !num_tokens_padded || !out || !scales_given(packed, w13_s, w2_s))
         return CHORD_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w13_q) || !aligned16(w13_s) || !aligned16(w2_q) ||
         !aligned16(w2_s) || !aligned16(out) || (h_out && !aligned16(h_out)))
         return CHORD_ERR_INVALID_ARG;
-    if (capacity < chord_moe_align_capacity(T, k, E_local, block_m) || capacity % block_m != 0)
-        return CHORD_ERR_CAPACITY;
     DeviceInfo dev;
     if ((st = device_info(&dev)) != CHORD_OK)
         return st;
