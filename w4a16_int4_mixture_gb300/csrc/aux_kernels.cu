@@ -814,7 +814,8 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
                                           : make_int4(-1, 0, 0, 0);
                 }
             const int E = a.E_local;
-            for (int64_t c = tid / kGroup; c < cx.total; c += ngrp) {
+            for (int64_t cc = tid / kGroup; cc < cx.total; cc += ngrp) {
+                const int64_t c = cx.total - 1 - cc;  // (last to first, as below)
                 // expert of compacted row c: the last e with a segment and coff[e] <= c
                 int lo = 0, hi = E - 1;
                 while (lo < hi) {
@@ -837,7 +838,11 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
             }
             return;
         }
-        for (int64_t r = tid / kGroup; r < rows; r += ngrp) {
+        // (rows are copied last to first: the gate/up GEMM starts on the first
+        // experts' rows, which are then the ones most recently written and
+        // still in L2)
+        for (int64_t rr = tid / kGroup; rr < rows; rr += ngrp) {
+            const int64_t r = rows - 1 - rr;
             const int p = a.gx_ids[r];
             const bool valid = p >= 0 && p < a.gx_pairs;  // sentinel rows become zeros
             if (gl == 0 && a.meta_out != nullptr)
