@@ -130,7 +130,11 @@ int64_t chord_moe_align_capacity(int64_t T, int k, int E_local, int block_m);
 int chord_select_block_m(int64_t T, int k, int E_global, int E_local, int H, int I);
 
 /* Writes a one-line description of the schedule the indexed path picks for a
- * shape (token tile, pipeline, combine form) into buf; returns its length. */
+ * shape (token tile, pipeline, combine form) into buf; returns its length.
+ * With a CUDA device current, the down GEMM's configuration is the one a call
+ * on that device launches (a one-stage K takes the token-stationary tile and
+ * a run of weight tiles per unit, chosen by the SM count); without one it is
+ * the token tile alone. */
 int chord_describe_schedule(int64_t T, int k, int E_global, int E_local, int H, int I, int flags,
                             char* buf, size_t buf_len);
 

@@ -751,12 +751,22 @@ int chord_describe_schedule(int64_t T, int k, int E_global, int E_local, int H, 
     const Schedule s = pick_schedule(tok_e, T, H, I, flags);
     static const char* names[] = {"decode-tile32", "decode-tile64", "decode-tile128",
                                   "prefill-tile192", "short-k-tile32", "short-k-tile64"};
+    // the down GEMM's weight tiles per unit depend on the SM count: with a
+    // device, the configuration and run a call on it would launch
+    int cfg_down = s.cfg_down;
+    int tpu = 0;
+    DeviceInfo dev;
+    if (H % 128 == 0 && device_info(&dev) == CHORD_OK)
+        tpu = pick_tpu(&cfg_down, I, H / 128, E_local, tok_e, dev.sms);
+    char run[32] = "";
+    if (tpu > 1)
+        snprintf(run, sizeof run, "x%d-tiles-per-unit", tpu);
     char tmp[256];
     const int n = snprintf(tmp, sizeof tmp,
-                           "tok_e=%.2f gate_up=%s(BK%d) down=%s(BK%d) combine=%s block_m=16 "
+                           "tok_e=%.2f gate_up=%s(BK%d) down=%s%s(BK%d) combine=%s block_m=16 "
                            "E_local=%d",
                            tok_e, names[s.cfg_gate_up], gemm_cfg_bk(s.cfg_gate_up),
-                           names[s.cfg_down], gemm_cfg_bk(s.cfg_down),
+                           names[cfg_down], run, gemm_cfg_bk(cfg_down),
                            s.reduce ? "fp32-reduce" : "ordered-pairs", E_local);
     if (buf && buf_len) {
         strncpy(buf, tmp, buf_len - 1);
