@@ -457,15 +457,13 @@ chord_status check_ws(void* ws, size_t bytes, size_t need)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int zero_blocks_for(int64_t count, int sms)
-{
-    if (count <= 0)
-        return 0;
-    int64_t b = (count / 4 + 1023) / 1024;
-    if (b > 2LL * sms)
-        b = 2LL * sms;
-    return static_cast<int>(b < 1 ? 1 : b);
-}
+// Worker blocks of the prep kernel.  Its 1024-thread blocks fit one per SM
+// and every loop in it strides over the grid, so block 0 (the chunk lists)
+// and 2 x SMs - 1 workers make two whole waves.  (Measured per call, CUDA
+// graph replays: against up to 2 x SMs workers, which left one block for a
+// third wave, TP8 T=2048 483.7 -> 473.1 us; one wave, SMs - 1 workers, gave
+// 471.1 us there but slowed the small calls, skewed decode 249.3 -> 250.5 us.)
+int prep_workers(int sms) { return 2 * sms - 1; }
 
 chord_status read_error_word(void* ws, cudaStream_t s, int* bits, bool clear)
 {
@@ -1022,9 +1020,7 @@ chord_status chord_w4a16_moe_indexed(const uint16_t* x, int64_t T, int H, int I,
     pa.gx_H = H;
     pa.err = err;
     set_pack_check(pa, packed, mx, w13_q, w2_q, E_local, H, I);
-    int work_blocks = zero_blocks_for(sc.reduce ? T * H : T * k, dev.sms);
-    if (work_blocks < dev.sms)
-        work_blocks = dev.sms;
+    const int work_blocks = prep_workers(dev.sms);
     if (launch_prep(pa, work_blocks, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     // (prepacked weights: the pack recorded its scales' range; the GEMMs report it)
@@ -1177,9 +1173,8 @@ chord_status chord_w4a16_moe_grouped(int mode, const uint16_t* a, int64_t M, int
     }
     pa.err = err;
     set_pack_check(pa, packed, mx, w13_q, w2_q, E_local, H, I);
-    int work_blocks = zero_blocks_for(with_tokens ? T * H : 0, dev.sms);
-    if ((with_tokens || compact) && work_blocks < dev.sms)
-        work_blocks = dev.sms;  // the row records and the compacted rows come from the worker blocks
+    // (the row records and the compacted rows come from the worker blocks)
+    const int work_blocks = (with_tokens || compact) ? prep_workers(dev.sms) : 0;
     if (launch_prep(pa, work_blocks, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     // (prepacked weights: the pack recorded its scales' range; the GEMMs report it)
