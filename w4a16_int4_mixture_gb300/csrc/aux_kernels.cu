@@ -1046,6 +1046,7 @@ __global__ void finalize_kernel(const float* __restrict__ acc, uint16_t* __restr
 // sum_j w_j * y_j over those slots in that order, so the result is
 // bit-identical run to run.  A token with no local slot gets zeros.
 constexpr int kCombineThreads = 128;
+constexpr int kCombineGroups = 4;  // 8-column groups per thread in flight
 
 __global__ void __launch_bounds__(kCombineThreads) combine_pairs_kernel(CombineArgs a)
 {
@@ -1071,27 +1072,55 @@ __global__ void __launch_bounds__(kCombineThreads) combine_pairs_kernel(CombineA
         }
         __syncthreads();
         const int n = s_n;
-        for (int c = threadIdx.x; c < H8; c += blockDim.x) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // kCombineGroups column groups per thread at a time, each slot's loads
+        // for all of them issued together (a token has about one local slot at
+        // EP8 prefill: one group's two loads per thread kept too few bytes in
+        // flight); the sum per column is still over the slots in ascending order
+        for (int c0 = threadIdx.x; c0 < H8; c0 += kCombineGroups * blockDim.x) {
+            float acc[kCombineGroups][8];
+#pragma unroll
+            for (int u = 0; u < kCombineGroups; ++u)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[u][e] = 0.f;
             for (int i = 0; i < n; ++i) {
-                const float4* y = reinterpret_cast<const float4*>(a.y_pairs + s_pair[i] * a.H) + 2 * c;
-                const float4 y0 = y[0], y1 = y[1];
+                const float4* y = reinterpret_cast<const float4*>(a.y_pairs + s_pair[i] * a.H);
                 const float w = s_w[i];
-                acc[0] += w * y0.x;
-                acc[1] += w * y0.y;
-                acc[2] += w * y0.z;
-                acc[3] += w * y0.w;
-                acc[4] += w * y1.x;
-                acc[5] += w * y1.y;
-                acc[6] += w * y1.z;
-                acc[7] += w * y1.w;
+                float4 y0[kCombineGroups], y1[kCombineGroups];
+#pragma unroll
+                for (int u = 0; u < kCombineGroups; ++u) {
+                    const int c = c0 + u * blockDim.x;
+                    if (c < H8) {
+                        y0[u] = y[2 * c];
+                        y1[u] = y[2 * c + 1];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kCombineGroups; ++u) {
+                    if (c0 + u * blockDim.x < H8) {
+                        acc[u][0] += w * y0[u].x;
+                        acc[u][1] += w * y0[u].y;
+                        acc[u][2] += w * y0[u].z;
+                        acc[u][3] += w * y0[u].w;
+                        acc[u][4] += w * y1[u].x;
+                        acc[u][5] += w * y1[u].y;
+                        acc[u][6] += w * y1[u].z;
+                        acc[u][7] += w * y1[u].w;
+                    }
+                }
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            reinterpret_cast<uint4*>(a.out + t * a.H)[c] = o;
+#pragma unroll
+            for (int u = 0; u < kCombineGroups; ++u) {
+                const int c = c0 + u * blockDim.x;
+                if (c < H8) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                    reinterpret_cast<uint4*>(a.out + t * a.H)[c] = o;
+                }
+            }
         }
         __syncthreads();
     }
