@@ -254,6 +254,7 @@ def device_inputs(inp, torch, dev, weights=True):
 
 L2_BYTES = 129 * 10**6          # GB300 L2
 L2_FLUSH_BYTES = 256 * 2**20    # written between replays when a step could stay in L2
+SPREAD_REPLAYS = 50             # single replays behind each median / p10 / p90 (after the timed region)
 
 
 def needs_l2_flush(step_bytes: int) -> bool:
@@ -467,6 +468,7 @@ def config_record(chord, torch, dev, stream, step, graph, work, steps, warmup, l
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     with Clocks(dev_index, uuid) as clk:
         ms = time_graph(graph, stream, steps, warmup, flush)
+    replay_us = replay_spread(graph, stream, max(steps, SPREAD_REPLAYS), flush)
     stage = stage_times(chord, step, stream, max(3, min(steps, 10)))
     roof, layer = roofline(work, stage, ms, is_decode(work), label)
     rec = {"value": round(ms * 1e3, 2), "unit": UNIT, "ms_per_step": round(ms, 5),
@@ -474,6 +476,7 @@ def config_record(chord, torch, dev, stream, step, graph, work, steps, warmup, l
            "timing": ("CUDA events over K CUDA-graph replays" if flush is None else
                       "CUDA events around each of K CUDA-graph replays, L2 flushed between them "
                       "outside the events"),
+           "replay_us": replay_us,
            "routed_pairs": work["pairs"], "touched_experts": work["touched"],
            "roofline": roof, "layer": layer,
            "stages_ms": {"prepare": round(stage[0], 5), "gate_up": round(stage[1], 5),
@@ -692,7 +695,7 @@ def run_ours(args, rank, world, dev_index):
     with Clocks(dev_index, uuid) as clk:
         local_ms = time_graph(graph, stream, args.steps, args.warmup, flush, barrier)
     ms = max_over_ranks(local_ms, world, dev)
-    replay_us = replay_spread(graph, stream, args.steps, flush)
+    replay_us = replay_spread(graph, stream, max(args.steps, SPREAD_REPLAYS), flush)
     stage = stage_times(chord, step, stream, args.steps)
 
     # end to end through the public API with host buffers: every step copies
