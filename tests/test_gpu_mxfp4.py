@@ -136,6 +136,10 @@ def _mx_verify(chord, inp, tokens=None, label=""):
     ("prefill-tile", (700, 2, 3, 3, 256, 256, 82)),
     ("split-k", (3, 8, 16, 16, 2048, 256, 83)),
     ("decode64", (64, 4, 8, 8, 512, 512, 84)),
+    # K = I = 256 is one stage: the 64-token token-stationary down tile
+    ("one-stage-down64", (64, 4, 8, 8, 512, 256, 88)),
+    # about 60 rows per expert: the 128-token tile
+    ("decode128", (120, 4, 8, 8, 512, 512, 89)),
 ])
 def test_mxfp4_indexed_small(chord, name, args):
     T, k, Eg, El, H, I, seed = args
@@ -167,6 +171,16 @@ def test_mxfp4_ep8_decode(chord):
     inp = synth.make_inputs(s, weight_format="mxfp4")
     tokens = np.random.default_rng(8).choice(s.T, 48, replace=False)
     _mx_verify(chord, inp, tokens, label="mxfp4 EP8 decode T=512 (48 sampled tokens)")
+
+
+def test_mxfp4_tp8_t128(chord):
+    """The TP8 shapes (384 experts, H = 7168, I = 256) with MXFP4 weights at
+    T = 128: the one-stage down GEMM runs token-stationary units of several
+    weight tiles each; sampled tokens."""
+    s = synth.workload("tp8", T=128)
+    inp = synth.make_inputs(s, weight_format="mxfp4")
+    tokens = np.random.default_rng(9).choice(s.T, 32, replace=False)
+    _mx_verify(chord, inp, tokens, label="mxfp4 TP8 T=128 (32 sampled tokens)")
 
 
 def test_mxfp4_packs_are_not_int4_packs(chord):
