@@ -24,7 +24,9 @@ namespace chord {
 constexpr int kPsDecode = 1024;
 constexpr int kPsWide = 1792;
 constexpr int kPsPrefill = 1792;
-template <bool G> using CfgD32 = GemmCfg<256, 6, 4, 3, 32, G ? 3 : 2, G, 32, G ? kPsDecode / 256 : 0>;
+// (three token stages, as many as A stages, so that the two rings share
+// their barriers: see FUSED_RINGS)
+template <bool G> using CfgD32 = GemmCfg<256, 6, 3, 3, 32, G ? 3 : 2, G, 32, G ? kPsDecode / 256 : 0>;
 template <bool G> using CfgD64 = GemmCfg<256, 6, 3, 3, 64, 2, G, 64, G ? kPsWide / 256 : 0>;
 // down GEMMs with a one-stage K (token-stationary units): a unit is one
 // chunk and a run of weight tiles sharing its token tile, each tile in the

@@ -87,6 +87,14 @@ struct GemmCfg {
     // the stage's scales as a TMA box (16-byte rows) when BK = 256; cp.async
     // (8-byte rows) when BK = 128
     static constexpr bool SCALES_TMA = BK == 256;
+    // One tile per unit and as many token stages as A stages: stage g uses A
+    // slot and token slot g % AS, so the two rings share their barriers.  The
+    // token tile's TMA completes on the A stage's full barrier (the four
+    // dequant arrivals plus the token producer's expect_tx arrival) and the
+    // A stage's empty barrier frees the token slot too: the MMA warp, the
+    // critical role of the decode tiles (measured), waits and commits once
+    // per stage instead of twice.
+    static constexpr bool FUSED_RINGS = !TS && ACCW == MAXN && AS == BS;
     static constexpr int B_STAGE = B_KBLK * B_REGION;
     static constexpr int HS_BYTES = GATE_UP ? MAXN * 128 : 0;  // 64 channels of bf16 per row
     static constexpr int META_BYTES = 0;  // (column records live in registers)
@@ -347,7 +355,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(codes_empty(s), 4);      // the 4 warps of one dequant group
         }
         for (int s = 0; s < C::AS; ++s) {
-            mbar_init(a_full(s), 4);
+            // the 4 dequant warps (+ the token tile's expect_tx arrival when fused)
+            mbar_init(a_full(s), C::FUSED_RINGS ? 5 : 4);
             mbar_init(a_empty(s), 1);          // tcgen05.commit
         }
         for (int s = 0; s < C::BS; ++s) {
@@ -551,23 +560,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             next2 = chunk_of_item(v + 2 * gridDim.x);
             for (int ks = it.k0; ks < it.k1; ++ks, ++g) {
                 const int s = g % C::BS;
-                if (!wait_side(b_empty(s), ((g / C::BS) & 1) ^ 1)) {
+                const uint32_t fbar = C::FUSED_RINGS ? a_full(s) : b_full(s);
+                if (!wait_side(C::FUSED_RINGS ? a_empty(s) : b_empty(s), ((g / C::BS) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
                     const uint32_t dst = sbase + C::OFF_B + s * C::B_STAGE;
                     if constexpr (C::B_3D) {
-                        mbar_arrive_expect_tx(b_full(s), C::B_STAGE);
-                        tma_load_3d(dst, &b_map, 0, row0, ks * (C::BK / 64), b_full(s), pol);
+                        mbar_arrive_expect_tx(fbar, C::B_STAGE);
+                        tma_load_3d(dst, &b_map, 0, row0, ks * (C::BK / 64), fbar, pol);
                     } else {
-                        mbar_arrive_expect_tx(b_full(s), C::B_KBLK * nbox * C::B_BOX_ROWS * 128);
+                        mbar_arrive_expect_tx(fbar, C::B_KBLK * nbox * C::B_BOX_ROWS * 128);
 #pragma unroll
                         for (int kb = 0; kb < C::B_KBLK; ++kb)
                             for (int ib = 0; ib < nbox; ++ib)
                                 tma_load_2d(dst + kb * C::B_REGION + ib * (C::B_BOX_ROWS * 128), &b_map,
-                                            ks * C::BK + kb * 64, row0 + ib * C::B_BOX_ROWS, b_full(s),
-                                            pol);
+                                            ks * C::BK + kb * 64, row0 + ib * C::B_BOX_ROWS, fbar, pol);
                     }
                 }
                 __syncwarp();
@@ -640,7 +649,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if constexpr (C::TPU_MAX == 1) {
                     const int sa = ga % C::AS;
                     const bool got = mbar_wait(a_full(sa), (ga / C::AS) & 1, abort_flag, err) &&
-                                     mbar_wait(b_full(sb), (gb / C::BS) & 1, abort_flag, err);
+                                     (C::FUSED_RINGS || mbar_wait(b_full(sb), (gb / C::BS) & 1, abort_flag, err));
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
@@ -672,7 +681,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         mma_commit_elect(a_empty(sa));
                     }
                 }
-                if (ok)
+                if (ok && !C::FUSED_RINGS)
                     mma_commit_elect(b_empty(sb));
             }
             if (!ok)
@@ -1158,7 +1167,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int depth = warp == 0 ? C::KS : C::BS;
             if (lane == 0)
                 for (int gg = issued_stages > depth ? issued_stages - depth : 0; gg < issued_stages; ++gg)
-                    mbar_drain(warp == 0 ? codes_full(gg % C::KS) : b_full(gg % C::BS),
+                    mbar_drain(warp == 0 ? codes_full(gg % C::KS)
+                                         : (C::FUSED_RINGS ? a_full(gg % C::AS) : b_full(gg % C::BS)),
                                (gg / depth) & 1);
             asm volatile("cp.async.wait_all;" ::: "memory");
             __syncwarp();
