@@ -1004,19 +1004,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (!epi_sync())
                     break;
                 const int64_t col0 = static_cast<int64_t>(nt0) * 64;
-                for (int idx = et; idx < ntok * 8; idx += 128) {
-                    const int c = idx >> 3;
-                    const int part = idx & 7;
-                    uint4 val = *reinterpret_cast<const uint4*>(hs + c * 64 + part * 8);
-                    if (args.h_zero_unpaired) {
-                        // (an unpaired row's token row was never written: its h is
-                        // whatever the MMA made of it)
+                // 16 rows per pass of the 128 threads (8 x 16 bytes per row).  An
+                // unpaired row's token row was never written, so its h is whatever
+                // the MMA made of it: it is stored as zeros.  Every pair record of
+                // the thread's rows is loaded before the first store, so the pass
+                // waits for one global load, not one per row.
+                constexpr int kPasses = C::MAXN / 16;
+                bool keep[kPasses];
+#pragma unroll
+                for (int ps = 0; ps < kPasses; ++ps) {
+                    const int c = (et >> 3) + 16 * ps;
+                    keep[ps] = true;
+                    if (args.h_zero_unpaired && c < ntok) {
                         const int p = args.pair_of_row[ch.row0 + c];
-                        if (p < 0 || p >= args.num_pairs)
-                            val = make_uint4(0u, 0u, 0u, 0u);
+                        keep[ps] = p >= 0 && p < args.num_pairs;
                     }
-                    *reinterpret_cast<uint4*>(args.h_out + static_cast<int64_t>(ch.row0 + c) * args.ld_h +
-                                              col0 + part * 8) = val;
+                }
+                const int part = et & 7;
+#pragma unroll
+                for (int ps = 0; ps < kPasses; ++ps) {
+                    const int c = (et >> 3) + 16 * ps;
+                    if (c < ntok) {
+                        uint4 val = *reinterpret_cast<const uint4*>(hs + c * 64 + part * 8);
+                        if (!keep[ps])
+                            val = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(args.h_out + static_cast<int64_t>(ch.row0 + c) * args.ld_h +
+                                                  col0 + part * 8) = val;
+                    }
                 }
                 if (args.pair_row != nullptr && nt0 == 0) {
                     for (int c = et; c < ntok; c += 128) {
