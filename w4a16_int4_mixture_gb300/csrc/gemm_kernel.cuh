@@ -10,9 +10,9 @@
 // optimisation / H200 and Blackwell indexed decode": dequantised weights take
 // the MMA-M operand), used here for every token count.
 //
-// Roles (16 warps; 20 for the down GEMM with token tiles <= 64 and for the
-// gate/up GEMM with three A stages):
-//   warp 0      code producer: packed INT4 codes of each K stage into a ring, one
+// Roles (16 warps; 20 with three dequant warps per quadrant or a second
+// epilogue group):
+//   warp 0      code producer: packed 4-bit codes of each K stage into a ring, one
 //               TMA box (gate and up halves as one 4-D box), L2 evict-first,
 //               and the group-32 scales (a TMA box, or cp.async for BK 128);
 //               for prepacked weights one or two plain bulk copies of the
@@ -20,22 +20,26 @@
 //   warp 1      token producer: the chunk's activation rows, contiguous in the
 //               B tensor map, as 128B-swizzled K-major TMA tiles (one 3-D box
 //               per stage for token tiles of up to 64 rows; the rows past the
-//               chunk only feed discarded columns).
+//               chunk only feed discarded columns).  With as many token stages
+//               as A stages the two rings share their barriers (FUSED_RINGS).
 //   warp 2      MMA issuer (the whole warp walks the schedule; elect.sync picks
 //               the issuing lane) and TMEM owner.
 //   warp 3      idle.
 //   warps 4-7   epilogue: TMEM -> registers; gate_up: SiLU(gate)*up -> bf16 h;
 //               down: per-pair fp32 store, fp32 reductions into token rows,
 //               or bf16 row store.
-//   warps 16-19 (down GEMM with token tiles <= 64 only) a second epilogue
-//               group taking every other unit.
-//   warps 8-15  dequant (8-19 for the gate/up GEMM with three A stages), two
-//               (three) warps per TMEM lane quadrant taking K stages in
+//   warps 8-15  dequant, two warps per TMEM lane quadrant (three, warps 8-19,
+//               in the configurations with three A stages and one epilogue
+//               group: the decode tiles of both GEMMs), taking K stages in
 //               order from a shared counter: codes + scales from shared memory
 //               -> w = bf16((q - 8) * s), one rounding of the exact product as
 //               in the page's order (exact q - 8, then the scale multiply),
-//               held as w * 2^-40 (undone on the fp32 accumulators) ->
-//               tcgen05.st into the A-operand stage in TMEM.
+//               held as w * 2^-40 (undone on the fp32 accumulators); MXFP4
+//               codes: w = bf16(e2m1(q) * 2^(e - 127)) by an exact placement
+//               and one multiply (see dequant_word_mx) -> tcgen05.st into the
+//               A-operand stage in TMEM.
+//   warps 16-19 (token-stationary down configurations) a second epilogue group
+//               taking every other tile.
 // Every wait is bounded (2 s); on expiry the CTA records CHORD_DEVERR_TIMEOUT,
 // every role leaves its loop, in-flight tensor-core work is drained and TMEM
 // is freed.
