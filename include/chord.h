@@ -258,14 +258,17 @@ chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global,
  *   (0 <= t < I/64) has rows 64t .. 64t+63 (gate) then I+64t .. I+64t+63 (up).
  * kind CHORD_PACK_DOWN: w_q [E, N, K/8], w_s [E, N, K/32]; tile t has rows
  *   128t .. 128t+127.
- * Sizes: K % 256 == 0 and N % 128 == 0 (else CHORD_ERR_UNSUPPORTED_SHAPE).
+ * Sizes: K % 128 == 0 and N % 128 == 0 (else CHORD_ERR_UNSUPPORTED_SHAPE).  A
+ * tile has KB = ceil(K / 256) blocks; when K % 256 == 128 the second half of
+ * its last block (codes and scales) is zero, and the GEMMs, which then run
+ * 128-deep K stages, never read it.
  *
  * Format (version 1), little-endian:
  *   bytes [0, 256): header of 64 uint32: [0] magic 0x4B504843 ("CHPK"),
  *     [1] version 1, [2] kind, [3] E, [4] N, [5] K, [6] block bytes 18432,
  *     [7] flags (bit 0: some scale outside the range of the header comment),
  *     [8] weight format (0 INT4; 1 MXFP4, chord_mxfp4_prepack), the rest 0.
- *   then blocks of 18432 bytes, block b = (e * (N/128) + t) * (K/256) + j for
+ *   then blocks of 18432 bytes, block b = (e * (N/128) + t) * KB + j for
  *   expert e, tile t and K block j (codes 256j .. 256j+255):
  *     [0, 16384) codes: half h (codes 256j + 128h ..) at 8192 h; in it, tile
  *       row r at 64 r; the row's four 16-byte pieces (32 codes each, one scale
@@ -273,8 +276,8 @@ chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global,
  *       position c ^ ((r >> 1) & 3);
  *     [16384, 18432) scales: tile row r at 16 r, its 8 bf16 scales of groups
  *       8j .. 8j+7.
- * Total bytes: chord_w4a16_prepack_size() = 256 + E * (N/128) * (K/256) *
- * 18432 (the same as codes + scales, plus the header).
+ * Total bytes: chord_w4a16_prepack_size() = 256 + E * (N/128) * KB * 18432
+ * (the same as codes + scales, plus the header, when K % 256 == 0).
  *
  *   w_q, w_s   device, as above (read only)
  *   packed     device, >= packed_bytes, 16-byte aligned; written entirely.

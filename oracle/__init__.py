@@ -256,7 +256,7 @@ def prepack(kind, w_q, w_s):
     sc = _c(w_s, np.uint16)
     E, N, K8 = q.shape
     K = K8 * 8
-    out = np.empty(256 + E * (N // 128) * (K // 256) * 18432, dtype=np.uint8)
+    out = np.empty(256 + E * (N // 128) * ((K + 255) // 256) * 18432, dtype=np.uint8)
     if _load().oracle_prepack(int(kind), _p(q), _p(sc), E, N, K, _p(out)) != 0:
         raise ValueError("oracle_prepack: bad kind or sizes")
     return out

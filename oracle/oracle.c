@@ -384,9 +384,11 @@ static int pack_scale_ok(uint16_t s)
 int oracle_prepack(int kind, const int32_t* w_q, const uint16_t* w_s, int64_t E, int64_t N,
                    int64_t K, uint8_t* out)
 {
-    if ((kind != 1 && kind != 2) || E < 1 || N % 128 != 0 || K % 256 != 0 || N < 128 || K < 256)
+    if ((kind != 1 && kind != 2) || E < 1 || N % 128 != 0 || K % 128 != 0 || N < 128 || K < 128)
         return -1;
-    const int64_t tiles = N / 128, kbs = K / 256;
+    /* a tile has ceil(K / 256) blocks; when K % 256 == 128 the second half of
+       the last one (codes and scales) stays zero */
+    const int64_t tiles = N / 128, kbs = (K + 255) / 256;
     uint32_t hdr[64];
     memset(hdr, 0, sizeof hdr);
     hdr[0] = 0x4B504843u;
@@ -397,12 +399,15 @@ int oracle_prepack(int kind, const int32_t* w_q, const uint16_t* w_s, int64_t E,
     hdr[5] = (uint32_t)K;
     hdr[6] = 18432;
     uint8_t* blk = out + 256;
+    memset(blk, 0, (size_t)(E * tiles * kbs) * 18432);
     for (int64_t e = 0; e < E; ++e)
         for (int64_t t = 0; t < tiles; ++t)
-            for (int64_t j = 0; j < kbs; ++j, blk += 18432)
+            for (int64_t j = 0; j < kbs; ++j, blk += 18432) {
+                /* halves of this block inside K: 2, or 1 for the tail block */
+                const int64_t halves = (256 * j + 256 <= K) ? 2 : 1;
                 for (int64_t r = 0; r < 128; ++r) {
                     const int64_t row = e * N + pack_tile_row(kind, N, t, r);
-                    for (int64_t h = 0; h < 2; ++h)
+                    for (int64_t h = 0; h < halves; ++h)
                         for (int64_t c = 0; c < 4; ++c) {
                             const int64_t pos =
                                 g_mutation == MUT_PACK_NO_SWIZZLE ? c : (c ^ ((r >> 1) & 3));
@@ -410,11 +415,12 @@ int oracle_prepack(int kind, const int32_t* w_q, const uint16_t* w_s, int64_t E,
                                    w_q + row * (K / 8) + 32 * j + 16 * h + 4 * c, 16);
                         }
                     const uint16_t* sc = w_s + row * (K / 32) + 8 * j;
-                    memcpy(blk + 16384 + 16 * r, sc, 16);
-                    for (int g = 0; g < 8; ++g)
+                    memcpy(blk + 16384 + 16 * r, sc, (size_t)(8 * halves));
+                    for (int g = 0; g < 4 * halves; ++g)
                         if (!pack_scale_ok(sc[g]))
                             hdr[7] |= 1u;
                 }
+            }
     memcpy(out, hdr, sizeof hdr);
     return 0;
 }

@@ -611,8 +611,9 @@ def _pack_positions(kind, E, N, K):
         t, r = nn // 64, nn % 64 + np.where(up, 64, 0)
     else:
         t, r = n // 128, n % 128
+    KB = (K + 255) // 256  # blocks of a tile (a 128 tail is half a block)
     j, h, c, m = k // 256, (k % 256) // 128, (k % 128) // 32, k % 32
-    block = 256 + ((e * (N // 128) + t) * (K // 256) + j) * 18432
+    block = 256 + ((e * (N // 128) + t) * KB + j) * 18432
     byte = block + h * 8192 + r * 64 + (c ^ ((r >> 1) & 3)) * 16 + (m // 8) * 4 + (m % 8) // 2
     high = (m % 2) == 1
     gs = np.arange(K // 32)
@@ -623,7 +624,7 @@ def _pack_positions(kind, E, N, K):
         tg, rg = nng // 64, nng % 64 + np.where(upg, 64, 0)
     else:
         tg, rg = ng // 128, ng % 128
-    sblock = 256 + ((eg * (N // 128) + tg) * (K // 256) + gg // 8) * 18432
+    sblock = 256 + ((eg * (N // 128) + tg) * KB + gg // 8) * 18432
     sbyte = sblock + 16384 + rg * 16 + (gg % 8) * 2
     return byte, high, sbyte
 
@@ -631,13 +632,16 @@ def _pack_positions(kind, E, N, K):
 def pin_prepack_positions(seed=61):
     """Every code and scale is where the packed format puts it, for both
     kinds, with random codes and scales: read back through the per-element
-    position map, the packed buffer gives the input codes and scales exactly."""
+    position map, the packed buffer gives the input codes and scales exactly.
+    With K % 256 == 128 (the last block half past K) every byte the map does
+    not reach, the tail halves included, is zero."""
     rng = np.random.default_rng(seed)
-    for kind, (E, N, K) in [(1, (2, 256, 512)), (2, (3, 128, 768)), (1, (1, 384, 256))]:
+    for kind, (E, N, K) in [(1, (2, 256, 512)), (2, (3, 128, 768)), (1, (1, 384, 256)),
+                            (2, (2, 256, 384)), (1, (1, 256, 128))]:
         w_q = rng.integers(0, 2**32, size=(E, N, K // 8), dtype=np.uint32).view(np.int32)
         w_s = rng.integers(0, 2**16, size=(E, N, K // 32), dtype=np.uint16)
         out = oracle.prepack(kind, w_q, w_s)
-        if out.size != 256 + E * (N // 128) * (K // 256) * 18432:
+        if out.size != 256 + E * (N // 128) * ((K + 255) // 256) * 18432:
             return False, f"size {out.size}"
         byte, high, sbyte = _pack_positions(kind, E, N, K)
         got = np.where(high, out[byte] >> 4, out[byte] & 0xF)
@@ -646,6 +650,13 @@ def pin_prepack_positions(seed=61):
         sg = out[sbyte].astype(np.uint16) | (out[sbyte + 1].astype(np.uint16) << 8)
         if not np.array_equal(sg, w_s):
             return False, f"scales misplaced (kind {kind}, {E}x{N}x{K})"
+        covered = np.zeros(out.size, bool)
+        covered[:256] = True
+        covered[byte.ravel()] = True
+        covered[sbyte.ravel()] = True
+        covered[sbyte.ravel() + 1] = True
+        if out[~covered].any():
+            return False, f"bytes outside the map are not zero (kind {kind}, {E}x{N}x{K})"
     return True, "ok"
 
 

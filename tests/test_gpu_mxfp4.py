@@ -56,7 +56,8 @@ def mx_small(T, k, Eg, El, H, I, seed, emap=True, center=121):
     return inp
 
 
-@pytest.mark.parametrize("kind,E,N,K", [(1, 2, 256, 512), (2, 3, 256, 256), (2, 1, 384, 2048)])
+@pytest.mark.parametrize("kind,E,N,K", [(1, 2, 256, 512), (2, 3, 256, 256), (2, 1, 384, 2048),
+                                        (2, 3, 256, 384)])
 def test_mxfp4_pack_matches_oracle(chord, kind, E, N, K):
     rng = np.random.default_rng(E * 100 + N + K + kind)
     w_q = rng.integers(0, 2**32, size=(E, N, K // 8), dtype=np.uint32).view(np.int32)

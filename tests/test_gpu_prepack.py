@@ -30,8 +30,9 @@ def _packed(chord, inp):
     return chord.prepack_weights(*w), w
 
 
+# (K = 384 and 128: K % 256 == 128, the last block's second half is zeros)
 @pytest.mark.parametrize("kind,E,N,K", [(1, 3, 256, 512), (2, 2, 384, 768), (1, 1, 128, 256),
-                                        (2, 5, 128, 2048)])
+                                        (2, 5, 128, 2048), (2, 3, 256, 384), (1, 2, 256, 128)])
 def test_prepack_matches_oracle(chord, kind, E, N, K):
     rng = np.random.default_rng(E * 1000 + N + K + kind)
     w_q = rng.integers(0, 2**32, size=(E, N, K // 8), dtype=np.uint32).view(np.int32)

@@ -141,13 +141,15 @@ def test_status_strings(lib):
 
 def test_prepack_size_and_host_checks(lib):
     """chord_w4a16_prepack_size is the header plus one 18432-byte block per
-    (expert, 128-row tile, 256-deep K block); bad arguments are rejected on
-    the host before any device work."""
+    (expert, 128-row tile, 256-deep K block, a 128 tail counting as a block);
+    bad arguments are rejected on the host before any device work."""
     lib.chord_w4a16_prepack_size.restype = ctypes.c_size_t
     assert lib.chord_w4a16_prepack_size(1, 48, 4096, 7168) == 256 + 48 * 32 * 28 * 18432
     assert lib.chord_w4a16_prepack_size(2, 48, 7168, 2048) == 256 + 48 * 56 * 8 * 18432
-    for bad in [(3, 1, 128, 256), (1, 0, 128, 256), (1, 1, 64, 256), (2, 1, 128, 128),
-                (2, 1, 200, 256)]:
+    assert lib.chord_w4a16_prepack_size(2, 3, 256, 384) == 256 + 3 * 2 * 2 * 18432
+    assert lib.chord_w4a16_prepack_size(1, 1, 128, 128) == 256 + 1 * 1 * 1 * 18432
+    for bad in [(3, 1, 128, 256), (1, 0, 128, 256), (1, 1, 64, 256), (2, 1, 128, 64),
+                (2, 1, 128, 320), (2, 1, 200, 256)]:
         assert lib.chord_w4a16_prepack_size(*bad) == 0
     n = lib.chord_w4a16_prepack_size(2, 1, 128, 256)
     assert lib.chord_w4a16_prepack(7, None, None, 1, 128, 256, None, n, None) == -1

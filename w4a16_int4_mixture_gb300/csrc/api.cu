@@ -679,7 +679,7 @@ chord_status prepack_common(int kind, const int32_t* w_q, const void* w_s, int f
 {
     if ((kind != CHORD_PACK_GATE_UP && kind != CHORD_PACK_DOWN) || E < 1 || N < 1 || K < 1)
         return CHORD_ERR_INVALID_ARG;
-    if (N % 128 != 0 || K % 256 != 0)
+    if (N % 128 != 0 || K % 128 != 0)
         return CHORD_ERR_UNSUPPORTED_SHAPE;
     if (!w_q || !w_s || !packed || !aligned16(w_q) || !aligned16(w_s) || !aligned16(packed))
         return CHORD_ERR_INVALID_ARG;
@@ -903,10 +903,10 @@ chord_status chord_moe_route_align(const float* logits, int64_t T, int E_global,
 
 size_t chord_w4a16_prepack_size(int kind, int E, int N, int K)
 {
-    if ((kind != CHORD_PACK_GATE_UP && kind != CHORD_PACK_DOWN) || E < 1 || N < 128 || K < 256 ||
-        N % 128 != 0 || K % 256 != 0)
+    if ((kind != CHORD_PACK_GATE_UP && kind != CHORD_PACK_DOWN) || E < 1 || N < 128 || K < 128 ||
+        N % 128 != 0 || K % 128 != 0)
         return 0;
-    return kPackHeaderBytes + static_cast<size_t>(E) * (N / 128) * (K / 256) * kPackBlockBytes;
+    return kPackHeaderBytes + static_cast<size_t>(E) * (N / 128) * pack_kblocks(K) * kPackBlockBytes;
 }
 
 

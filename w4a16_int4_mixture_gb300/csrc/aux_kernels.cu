@@ -922,7 +922,7 @@ __global__ void pack_header_kernel(PackArgs a)
 __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
 {
     const int tiles = a.N / 128;
-    const int kbs = a.K / 256;
+    const int kbs = pack_kblocks(a.K);  // the last block is half past K when K % 256 == 128
     const int64_t words_per_row = a.K / 8;
     const int64_t scales_per_row = a.K / 32;
     const int64_t total = static_cast<int64_t>(a.E) * tiles * kbs * 1152;
@@ -940,19 +940,24 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
         const int row = a.kind == CHORD_PACK_GATE_UP ? (r < 64 ? 64 * t + r : a.N / 2 + 64 * t + r - 64)
                                                      : 128 * t + r;
         const int64_t grow = e * a.N + row;
-        uint4 v;
+        // the second half of the last block lies past K when K % 256 == 128: zeros
+        const bool tail = kb == kbs - 1 && (a.K & 255) != 0;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (j < 1024) {
             const int h = j >> 9;
             const int c = (j & 3) ^ ((r >> 1) & 3);
-            v = *reinterpret_cast<const uint4*>(a.q + grow * words_per_row + kb * 32 + h * 16 + c * 4);
+            if (!(tail && h == 1))
+                v = *reinterpret_cast<const uint4*>(a.q + grow * words_per_row + kb * 32 + h * 16 + c * 4);
         } else if (a.fmt == static_cast<int>(kPackFmtMxfp4)) {
             // E8M0 byte e -> the bf16 value 2^(e - 127): exponent field e for
-            // 1 <= e <= 254, the subnormal 0x0040 for e = 0, NaN for e = 255
-            const uint2 b8 = *reinterpret_cast<const uint2*>(a.sc8 + grow * scales_per_row + kb * 8);
+            // 1 <= e <= 254, the subnormal 0x0040 for e = 0, NaN for e = 255.
+            // (4-byte reads: a row of K / 32 scale bytes is a multiple of 4.)
+            const uint32_t* src8 = reinterpret_cast<const uint32_t*>(a.sc8 + grow * scales_per_row + kb * 8);
+            const uint32_t b8[2] = {src8[0], tail ? 0u : src8[1]};
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const uint32_t src = q < 2 ? b8.x : b8.y;
+                const uint32_t src = b8[q >> 1];
                 uint32_t h[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -961,9 +966,13 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a)
                 }
                 o[q] = h[0] | (h[1] << 16);
             }
-            v = make_uint4(o[0], o[1], o[2], o[3]);
+            v = make_uint4(o[0], o[1], tail ? 0u : o[2], tail ? 0u : o[3]);
         } else {
-            v = *reinterpret_cast<const uint4*>(a.sc + grow * scales_per_row + kb * 8);
+            // (8-byte reads: a row of K / 32 bf16 scales is a multiple of 8 bytes)
+            const uint2* src = reinterpret_cast<const uint2*>(a.sc + grow * scales_per_row + kb * 8);
+            const uint2 lo = src[0];
+            const uint2 hi = tail ? make_uint2(0u, 0u) : src[1];
+            v = make_uint4(lo.x, lo.y, hi.x, hi.y);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q)

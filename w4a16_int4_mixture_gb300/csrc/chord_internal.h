@@ -72,6 +72,8 @@ constexpr int kPackHeaderBytes = 256;
 constexpr int kPackCodeBytes = 16384;          // one 256-deep K block of a 128-row tile
 constexpr int kPackBlockBytes = kPackCodeBytes + 2048;
 constexpr int kPackFormatWord = 8;             // header word: weight format of the pack
+// 256-deep K blocks of one pack tile (K % 128 == 0; a 128 tail is half a block)
+__host__ __device__ constexpr int pack_kblocks(int K) { return (K + 255) / 256; }
 constexpr uint32_t kPackFmtInt4 = 0;           // chord_w4a16_prepack
 constexpr uint32_t kPackFmtMxfp4 = 1;          // chord_mxfp4_prepack
 

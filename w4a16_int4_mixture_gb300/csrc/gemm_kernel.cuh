@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // prepacked: the stage's block (BK 256), or half h of it (BK 128)
                 const uint8_t* pblk = nullptr;
                 if constexpr (PK)
-                    pblk = args.pk + ((static_cast<int64_t>(e) * n_tiles + nt) * (args.K / 256) +
+                    pblk = args.pk + ((static_cast<int64_t>(e) * n_tiles + nt) * pack_kblocks(args.K) +
                                       ks / (256 / C::BK)) *
                                          kPackBlockBytes;
                 const int ph = C::BK == 256 ? 0 : (ks & 1);
