@@ -350,7 +350,7 @@ chord_status chord_mxfp4_prepack(int kind, const int32_t* w_q, const uint8_t* w_
  *   flags        CHORD_FLAG_* ; CHORD_FLAG_DETERMINISTIC gives run-to-run
  *                bit-identical outputs (slots summed in a fixed order); the
  *                default fp32 reductions are not bit-reproducible run to run
- * Limits (CHORD_ERR_UNSUPPORTED_SHAPE otherwise): H % 256 == 0, I % 128 == 0,
+ * Limits (CHORD_ERR_UNSUPPORTED_SHAPE otherwise): H % 128 == 0, I % 128 == 0,
  *   1 <= k <= 32, E_local >= 1, T*k < 2^31, block_m in [1, 256].
  * Work schedule of both GEMMs: one CTA per SM takes (chunk of rows, weight
  *   tile) units in turn.  When the last round of units would leave at least

@@ -1,8 +1,8 @@
 """Edges of the supported shapes on the GPU, each checked against the oracle
 and the fp64 anchor like the fixed cases: the largest top-k (32), more local
 experts than the align entry point and the masked layout's row compaction take
-(1024), a deep reduction (H = 4096) with a six-stage down GEMM (I = 1536), and
-an empty batch."""
+(1024), a deep reduction (H = 4096) with a six-stage down GEMM (I = 1536), a
+hidden size of 128 mod 256, and an empty batch."""
 
 import numpy as np
 import pytest
@@ -58,6 +58,22 @@ def test_deep_k(chord, form):
     if form == "packed":
         w = (chord.prepack_weights(*w), None, None, None)
     verify_indexed(inp, run_indexed_full(chord, inp, weights=w), label=f"deep K {form}")
+
+
+@pytest.mark.parametrize("form", ["plain", "packed", "grouped"])
+def test_hidden_size_128_mod_256(chord, form):
+    """H = 640 (K of the gate/up GEMM a multiple of 128, not of 256): the
+    gate/up GEMM runs the 128-deep stages; packs keep the last block's first
+    half."""
+    inp = small(48, 4, 8, 8, 640, 256, 514, emap=False)
+    w = weights_to(inp, DEV)
+    if form == "packed":
+        w = (chord.prepack_weights(*w), None, None, None)
+    if form == "grouped":
+        a3, mm, r2p = synth.grouped_masked_layout(inp)
+        masked_layer_check(chord, inp, a3, mm, r2p, w, "H=640 masked")
+        return
+    verify_indexed(inp, run_indexed_full(chord, inp, weights=w), label=f"H=640 {form}")
 
 
 def test_empty_batch(chord):

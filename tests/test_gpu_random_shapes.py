@@ -1,7 +1,7 @@
 """A seeded sweep of random supported shapes through the layer.
 
 The fixed cases elsewhere pick shapes for the schedule they exercise; this
-sweep draws shapes the way a caller might (hidden size a multiple of 256,
+sweep draws shapes the way a caller might (hidden size a multiple of 128,
 intermediate size a multiple of 128, top-k up to 8, any token count, local
 experts a subset of the global ones with or without an expert map, any
 padding granularity), weights plain INT4, prepacked INT4 or MXFP4, with or
@@ -30,7 +30,7 @@ def _draw(n=16, seed=2024):
     rng = np.random.default_rng(seed)
     cases = []
     for i in range(n):
-        H = int(rng.choice([256, 512, 768, 1024]))
+        H = int(rng.choice([256, 384, 512, 640, 768, 1024]))
         I = int(rng.choice([128, 256, 384, 512]))
         k = int(rng.choice([1, 2, 3, 4, 6, 8]))
         Eg = int(rng.integers(max(k, 2), 40))
@@ -71,7 +71,7 @@ def _draw_grouped(n=8, seed=2025):
     rng = np.random.default_rng(seed)
     cases = []
     for i in range(n):
-        H = int(rng.choice([256, 512, 768]))
+        H = int(rng.choice([256, 384, 512, 768]))
         I = int(rng.choice([128, 256, 384]))
         k = int(rng.choice([1, 2, 4, 8]))
         E = int(rng.integers(max(k, 2), 24))

@@ -86,7 +86,7 @@ placeholder_pointers = pytest.mark.skipif(
 def test_host_checks_reject_before_launch(lib):
     """Size, capacity and flag checks come before any pointer is looked at,
     so every call here passes NULL for every device pointer."""
-    # unsupported hidden size (not a multiple of 256)
+    # unsupported hidden size (not a multiple of 128)
     st = lib.chord_w4a16_moe_indexed(None, 4, 200, 128, 8, 8, 2, None, None, None, None, None,
                                      None, None, None, 1024, 16, None, 1 << 20, None, None, 0, None)
     assert st == -2

@@ -515,7 +515,8 @@ chord_status check_shape(int H, int I, int E_local, int k)
 {
     if (H <= 0 || I <= 0 || E_local <= 0 || k <= 0)
         return CHORD_ERR_INVALID_ARG;
-    if (H % 256 != 0 || I % 128 != 0 || k > 32)
+    // (a K of 128 mod 256, hidden or intermediate, runs the 128-deep stages)
+    if (H % 128 != 0 || I % 128 != 0 || k > 32)
         return CHORD_ERR_UNSUPPORTED_SHAPE;
     return CHORD_OK;
 }
