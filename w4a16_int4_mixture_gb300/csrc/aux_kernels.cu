@@ -481,6 +481,22 @@ struct CompactIdx {
     int* coff;  // [E_local] first compacted row
     int total;  // compacted rows
 };
+// 16-byte global load / store under an L2 cache policy (createpolicy)
+__device__ __forceinline__ uint4 ld16_hint(const uint4* p, uint64_t policy)
+{
+    uint4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+__device__ __forceinline__ void st16_hint(uint4* p, uint4 v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
+
 __device__ CompactIdx indexed_compaction(const PrepArgs& a)
 {
     __shared__ int s_seg[1024];
@@ -786,6 +802,13 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
         const int ntp = a.num_tokens_padded[0];
         const int64_t rows = (ntp >= 0 && ntp <= a.capacity) ? ntp : 0;
         const int n16 = a.gx_H / 8;
+        // Each token row is copied once per local slot (up to k times), far
+        // apart in the walk: the source rows are read with an L2 evict-last
+        // policy and the gathered rows written evict-first, so that the copies
+        // stream through L2 without pushing x out of it (measured at TP8
+        // T=2048, k = 8: without the policies 22 % of the copy's L2 reads hit).
+        const uint64_t keep = policy_evict_last();
+        const uint64_t pass = policy_evict_first();
         auto copy_row = [&](int p, int64_t drow) {
             const uint4* src = reinterpret_cast<const uint4*>(a.gx_src + static_cast<int64_t>(p / a.gx_topk) * a.gx_H);
             uint4* dst = reinterpret_cast<uint4*>(a.gx_out + drow * a.gx_H);
@@ -794,13 +817,13 @@ __global__ void __launch_bounds__(1024) prep_kernel(PrepArgs a)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int c = c0 + j * kGroup;
-                    v[j] = c < n16 ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                    v[j] = c < n16 ? ld16_hint(src + c, keep) : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int c = c0 + j * kGroup;
                     if (c < n16)
-                        dst[c] = v[j];
+                        st16_hint(dst + c, v[j], pass);
                 }
             }
         };
