@@ -104,3 +104,19 @@ def test_align_invalid_ids_are_reported(chord):
     assert bits & 2, "out-of-range ids must set the routing error bit"
     rsi, rei, rntp = oracle.moe_align(ids, 4, None, 4, 4)
     assert np.array_equal(si.cpu().numpy(), rsi) and int(ntp.item()) == rntp
+
+
+@pytest.mark.parametrize("T,E,spread", [(512, 512, "uniform"), (512, 384, "eight-experts"),
+                                        (513, 384, "uniform"), (385, 100, "eight-experts")])
+def test_align_one_cta_limit(chord, T, E, spread):
+    """Both sides of the one-CTA form's limit (4096 pairs): 512 tokens x 8
+    fill its four rounds per warp; with every pair on eight experts a warp's
+    count of one expert reaches 16 in a round and an expert's prefix over the
+    warps 512; 513 tokens take the three kernels."""
+    rng = np.random.default_rng(T + E)
+    if spread == "uniform":
+        ids = np.stack([rng.permutation(E)[:8] for _ in range(T)]).astype(np.int32)
+    else:
+        ids = np.stack([rng.permutation(8) for _ in range(T)]).astype(np.int32)
+    for bm in (1, 16, 64):
+        _compare(chord, ids, E, None, E, bm)

@@ -4,8 +4,8 @@ host owns every buffer).  Called through the C ABI and compared, bit for bit,
 with the oracle's align and with chord_moe_align, the entry point that takes a
 workspace: the outputs are integers, so they must match exactly.
 
-The draws cover both forms of the align: small routings (up to 4096 pairs and
-512 local experts) run in one CTA that keeps its histogram in shared memory;
+The draws cover both forms of the align: small routings (up to 16384 pairs and
+512 local experts) run in one CTA that keeps its counts in shared memory;
 larger ones run the histogram / scan / scatter kernels, whose per-tile
 histogram lives in the library's fixed scratch array.  The calls are issued
 back to back on one stream with different routings and read back only at the
@@ -28,9 +28,11 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-# (workload, T, seed): one-CTA form, then the three-kernel form at three sizes
-DRAWS = [("ep8-decode", None, 11), ("tp8", 128, 12), ("ep8-decode", 1024, 13),
-         ("ep8-prefill", None, 14), ("tp8", 2048, 15), ("ep8-decode", 1024, 16)]
+# (workload, T, seed): the one-CTA form (up to its limit, 512 x 8 pairs), then
+# the three-kernel form at four sizes (just past the limit first)
+DRAWS = [("ep8-decode", None, 11), ("tp8", 128, 12), ("tp8", 513, 17),
+         ("ep8-decode", 1024, 13), ("ep8-prefill", None, 14), ("tp8", 2048, 15),
+         ("ep8-decode", 1024, 16)]
 
 
 def test_noalloc_align_matches_oracle_and_workspace_align():

@@ -186,88 +186,127 @@ __global__ void __launch_bounds__(kAlignTile) align_scatter_kernel(AlignArgs a)
     }
 }
 
-// The whole align in one CTA for small routing batches (the three kernels above
-// cost three launches and a single-CTA scan in between): histogram in shared
-// memory (each pair's local expert kept there too), padded offsets, then the
-// same stable scatter as align_scatter_kernel in rounds of kSmallThreads pairs,
-// each pair ranked by warp match + per-warp counts + the counts of earlier
-// rounds.  Same output, bit for bit.
+// The whole align in one CTA for routing batches of up to 4096 pairs (the
+// three kernels above cost three launches and a single-CTA scan in between).
+// The sentinel goes over the whole capacity first (coalesced; the pairs
+// overwrite their rows after the barriers).  Warp w takes a contiguous range
+// of pairs and ranks them in rounds of 32 on its own: warp match for the
+// pairs of one expert inside a round, plus a per-warp running count of each
+// expert in shared memory.  One block barrier, then each expert's counts are
+// scanned over the warps (so warp w's pairs of expert e come after those of
+// warps 0 .. w-1), the padded segments over the experts, and every pair lands
+// at segment base + warp prefix + rank.  Same output as the three kernels,
+// bit for bit.  (With more pairs one CTA's scattered row writes cost more
+// than the three kernels: at 16384 pairs over 384 experts, 31 against 12 us.)
 constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kSmallMaxPairs = 4096;
 constexpr int kSmallMaxExperts = 512;
 
-// The one-CTA align (called by every thread of a 1024-thread block).
+// The one-CTA align (called by every thread of a 1024-thread block), for at
+// most R rounds of 32 pairs per warp (R * kSmallThreads pairs).
+template <int R>
 __device__ void align_small_run(const AlignArgs& a)
 {
-    __shared__ int cnt[kSmallMaxExperts];   // pass 1 counts, then pairs placed by earlier rounds
+    // pairs of each expert in each warp's range (a running count while the
+    // warp ranks its pairs), then the pairs of that expert in earlier warps;
+    // both are at most kSmallMaxPairs
+    __shared__ short wcnt[kSmallWarps][kSmallMaxExperts];
     __shared__ int base[kSmallMaxExperts];  // first padded row of each expert
-    __shared__ short wcnt[kSmallThreads / 32][kSmallMaxExperts];  // per warp of a round (<= 32)
-    __shared__ short lexp[kSmallMaxPairs];  // local expert of each pair (-1: not local)
     const int E = a.E_local;
-    constexpr int W = kSmallThreads / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int npairs = static_cast<int>(a.num_pairs);
     const int sentinel = npairs;
     const int bm = a.block_m;
+    const int64_t cap = a.capacity;
     if (threadIdx.x == 0)
         *a.err = 0;
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        cnt[e] = 0;
-    for (int64_t i = threadIdx.x; i < a.capacity; i += blockDim.x)
+    for (int i = threadIdx.x; i < kSmallWarps * kSmallMaxExperts / 2; i += blockDim.x)
+        reinterpret_cast<int*>(&wcnt[0][0])[i] = 0;
+    // pairs per warp: a multiple of 32, at most 32 R
+    const int per_warp = (npairs + kSmallThreads - 1) / kSmallThreads * 32;
+    const int rounds = per_warp / 32;
+    const int p0 = warp * per_warp + lane;
+    // per round: the pair's id, then its local expert (-1: none), then the
+    // expert and the pair's rank among this warp's pairs of it (l << 16 | rank;
+    // both below 2^9), or -1.  The loads go out before the barrier; a bad id
+    // is reported after it, once the error word has been cleared.
+    int rec[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        rec[r] = (r < rounds && p0 + 32 * r < npairs) ? a.topk_ids[p0 + 32 * r] : -1;
+    for (int64_t i = threadIdx.x; i < cap; i += blockDim.x)
         a.sorted_ids[i] = sentinel;
-    __syncthreads();
-    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-        const int l = local_expert_of(a.topk_ids[p], a.E_global, a.expert_map, E, a.err);
-        lexp[p] = static_cast<short>(l);
-        if (l >= 0)
-            atomicAdd(&cnt[l], 1);
+    bool bad = false;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const bool have = r < rounds && p0 + 32 * r < npairs;
+        bad |= have && (rec[r] < 0 || rec[r] >= a.E_global);
+        rec[r] = have ? local_expert_of(rec[r], a.E_global, a.expert_map, E, nullptr) : -1;
     }
     __syncthreads();
+    if (bad)
+        raise_error(a.err, CHORD_DEVERR_ROUTING);
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (r < rounds) {
+            const int l = rec[r];
+            const unsigned peers = __match_any_sync(0xffffffffu, l);
+            const int before = l >= 0 ? wcnt[warp][l] : 0;
+            __syncwarp();
+            if (l >= 0) {
+                rec[r] = (l << 16) | (before + __popc(peers & below));
+                if ((peers & below) == 0)
+                    wcnt[warp][l] = static_cast<short>(before + __popc(peers));
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // per expert: the warp counts become the counts of earlier warps (the
+    // loads eight at a time ahead of the stores)
     const int e = threadIdx.x;
-    const int padded = e < E ? (cnt[e] + bm - 1) / bm * bm : 0;
+    int total = 0;
+    if (e < E) {
+#pragma unroll
+        for (int h = 0; h < kSmallWarps; h += 8) {
+            int c[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                c[w] = wcnt[h + w][e];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                wcnt[h + w][e] = static_cast<short>(total);
+                total += c[w];
+            }
+        }
+    }
+    const int padded = e < E ? (total + bm - 1) / bm * bm : 0;
     int ntp;
     const int off = block_exclusive_scan(padded, &ntp);
     if (e < E) {
         base[e] = off;
-        cnt[e] = 0;
-        if (off + padded <= a.capacity)
+        if (off + padded <= cap)
             for (int b = off / bm; b < (off + padded) / bm; ++b)
                 a.expert_ids[b] = e;
     }
-    if (ntp > a.capacity && threadIdx.x == 0)
+    if (ntp > cap && threadIdx.x == 0)
         raise_error(a.err, CHORD_DEVERR_CAPACITY);
-    const int64_t nblocks = a.capacity / bm;
+    const int64_t nblocks = cap / bm;
     for (int64_t b = ntp / bm + threadIdx.x; b < nblocks; b += blockDim.x)
         a.expert_ids[b] = -1;
     if (threadIdx.x == 0)
-        a.num_tokens_padded[0] = ntp <= a.capacity ? ntp : 0;
-    for (int r0 = 0; r0 < npairs; r0 += blockDim.x) {
-        for (int i = threadIdx.x; i < W * kSmallMaxExperts / 2; i += blockDim.x)
-            reinterpret_cast<int*>(&wcnt[0][0])[i] = 0;
-        __syncthreads();
-        const int p = r0 + threadIdx.x;
-        const int l = p < npairs ? lexp[p] : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, l);
-        const unsigned lower = peers & ((1u << lane) - 1u);
-        if (l >= 0 && lower == 0)
-            wcnt[warp][l] = static_cast<short>(__popc(peers));
-        __syncthreads();
-        if (l >= 0) {
-            int rank = cnt[l] + __popc(lower);
-            for (int w = 0; w < warp; ++w)
-                rank += wcnt[w][l];
-            const int64_t pos = static_cast<int64_t>(base[l]) + rank;
-            if (pos < a.capacity)
-                a.sorted_ids[pos] = p;
+        a.num_tokens_padded[0] = ntp <= cap ? ntp : 0;
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (r < rounds && rec[r] >= 0) {
+            const int l = rec[r] >> 16;
+            const int64_t pos = static_cast<int64_t>(base[l]) + wcnt[warp][l] + (rec[r] & 0xffff);
+            if (pos < cap)
+                a.sorted_ids[pos] = p0 + 32 * r;
         }
-        __syncthreads();
-        for (int x = threadIdx.x; x < E; x += blockDim.x) {
-            int add = 0;
-            for (int w = 0; w < W; ++w)
-                add += wcnt[w][x];
-            cnt[x] += add;
-        }
-        __syncthreads();
     }
 }
 
@@ -275,7 +314,7 @@ __global__ void __launch_bounds__(kSmallThreads) align_small_kernel(AlignArgs a)
 {
     pdl_launch_dependents();
     pdl_wait();
-    align_small_run(a);
+    align_small_run<kSmallMaxPairs / kSmallThreads>(a);
 }
 
 // ---------------------------------------------------------------------------
@@ -360,8 +399,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs r)
         route_token_warp<NI>(r, t, lane);
 }
 
-// Router and align in one CTA (up to 64 tokens, 4096 pairs and 512 local
-// experts): the 32 warps route the tokens into topk_ids / topk_weights, then
+// Router and align in one CTA (up to 64 tokens and 512 local experts): the 32 warps route the tokens into topk_ids / topk_weights, then
 // the block aligns them.
 constexpr int kRouteFusedMaxT = 64;
 
@@ -374,13 +412,14 @@ __global__ void __launch_bounds__(kSmallThreads) route_align_small_kernel(RouteA
     for (int64_t t = warp; t < r.T; t += kSmallThreads / 32)
         route_token_warp<NI>(r, t, lane);
     __syncthreads();  // (the block's writes of topk_ids are visible to it)
-    align_small_run(a);
+    align_small_run<kRouteFusedMaxT * 32 / kSmallThreads>(a);
 }
 
 template <int NI>
 cudaError_t launch_route_align_ni(const RouteArgs& r, const AlignArgs& a, cudaStream_t s)
 {
-    if (r.T <= kRouteFusedMaxT && a.num_pairs <= kSmallMaxPairs && a.E_local <= kSmallMaxExperts)
+    // (k <= 32: at most kRouteFusedMaxT * 32 pairs, the rounds the fused kernel takes)
+    if (r.T <= kRouteFusedMaxT && a.num_pairs <= kRouteFusedMaxT * 32 && a.E_local <= kSmallMaxExperts)
         return launch_pdl(route_align_small_kernel<NI>, 1, kSmallThreads, 0, s, r, a);
     if (r.T > 0) {
         int64_t blocks = (r.T + 7) / 8;  // 8 warps per block, a token each
