@@ -1209,10 +1209,119 @@ cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int sms,
     return launch_pdl(finalize_kernel, static_cast<int>(blocks), 256, 0, s, acc, out, n);
 }
 
+// The same combine for fewer tokens: a block takes one token's slots over
+// kCombineThreads x G column groups (several blocks per token), and each
+// thread issues the loads of G groups x S slots together before it sums them
+// in ascending slot order (the same operations, in the same order, as
+// combine_pairs_kernel).  With one block per token, a token's eight slots cost
+// eight dependent round trips per column group: 12 us at one token.
+template <int G, int S>
+__global__ void __launch_bounds__(kCombineThreads) combine_pairs_split_kernel(CombineArgs a, int splits)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ int64_t s_pair[32];
+    __shared__ float s_w[32];
+    __shared__ int s_n;
+    const int H8 = a.H / 8;
+    const int64_t items = a.T * splits;
+    for (int64_t b = blockIdx.x; b < items; b += gridDim.x) {
+        const int64_t t = b / splits;
+        const int c0 = static_cast<int>(b % splits) * kCombineThreads * G + threadIdx.x;
+        if (threadIdx.x < 32) {
+            const int j = threadIdx.x;
+            const int64_t p = t * a.k + j;
+            const bool valid = j < a.k && a.pair_row[p] >= 0;
+            const uint32_t m = __ballot_sync(0xffffffffu, valid);
+            if (valid) {
+                const int idx = __popc(m & ((1u << j) - 1u));
+                s_pair[idx] = p;
+                s_w[idx] = a.topk_weights[p];
+            }
+            if (j == 0)
+                s_n = __popc(m);
+        }
+        __syncthreads();
+        const int n = s_n;
+        float acc[G][8];
+#pragma unroll
+        for (int u = 0; u < G; ++u)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[u][e] = 0.f;
+        for (int i0 = 0; i0 < n; i0 += S) {
+            float4 y0[G][S], y1[G][S];
+#pragma unroll
+            for (int v = 0; v < S; ++v) {
+                if (i0 + v < n) {
+                    const float4* y = reinterpret_cast<const float4*>(a.y_pairs + s_pair[i0 + v] * a.H);
+#pragma unroll
+                    for (int u = 0; u < G; ++u) {
+                        const int c = c0 + u * kCombineThreads;
+                        if (c < H8) {
+                            y0[u][v] = y[2 * c];
+                            y1[u][v] = y[2 * c + 1];
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int v = 0; v < S; ++v) {
+                if (i0 + v < n) {
+                    const float w = s_w[i0 + v];
+#pragma unroll
+                    for (int u = 0; u < G; ++u) {
+                        if (c0 + u * kCombineThreads < H8) {
+                            acc[u][0] += w * y0[u][v].x;
+                            acc[u][1] += w * y0[u][v].y;
+                            acc[u][2] += w * y0[u][v].z;
+                            acc[u][3] += w * y0[u][v].w;
+                            acc[u][4] += w * y1[u][v].x;
+                            acc[u][5] += w * y1[u][v].y;
+                            acc[u][6] += w * y1[u][v].z;
+                            acc[u][7] += w * y1[u][v].w;
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+            const int c = c0 + u * kCombineThreads;
+            if (c < H8) {
+                uint4 o;
+                o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                reinterpret_cast<uint4*>(a.out + t * a.H)[c] = o;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int G, int S>
+static cudaError_t launch_combine_split(const CombineArgs& a, cudaStream_t s)
+{
+    const int splits = (a.H / 8 + kCombineThreads * G - 1) / (kCombineThreads * G);
+    const int64_t items = a.T * splits;
+    const int64_t blocks = items < 65535 ? items : 65535;
+    return launch_pdl(combine_pairs_split_kernel<G, S>, static_cast<unsigned>(blocks), kCombineThreads, 0, s,
+                      a, splits);
+}
+
 cudaError_t launch_combine_pairs(const CombineArgs& a, cudaStream_t s)
 {
     if (a.T <= 0)
         return cudaSuccess;
+    // one group per thread and eight slots in flight for a few tokens (many
+    // slots each at TP8); four groups and two slots up to 2048 tokens; one
+    // block per token beyond
+    if (a.T <= 256)
+        return launch_combine_split<1, 8>(a, s);
+    if (a.T <= 2048)
+        return launch_combine_split<4, 2>(a, s);
     const int64_t blocks = a.T < 65535 ? a.T : 65535;
     return launch_pdl(combine_pairs_kernel, static_cast<unsigned>(blocks), kCombineThreads, 0, s, a);
 }
