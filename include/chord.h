@@ -226,7 +226,7 @@ chord_status chord_moe_align_noalloc(const int32_t* topk_ids, int64_t T, int k, 
  *                         chosen when renormalize != 0 (fp32; exp and the sums
  *                         in fp32, within a few ulp of the fp64 value);
  * then sorted_ids / expert_ids / num_tokens_padded exactly as chord_moe_align
- * on those ids.  Up to 64 tokens (4096 pairs, 512 local experts) both steps
+ * on those ids.  Up to 64 tokens (and 512 local experts) both steps
  * run in one CTA (one launch), else as a router kernel and the align kernels.
  *
  *   logits       device float [T, E_global], finite

@@ -155,7 +155,7 @@ struct CombineArgs {
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
 // Router, then align of its ids (a.topk_ids == r.ids): one CTA for both up to
-// 4096 pairs and 512 local experts, else a router kernel and launch_align.
+// 64 tokens and 512 local experts, else a router kernel and launch_align.
 cudaError_t launch_route_align(const RouteArgs& r, const AlignArgs& a, cudaStream_t s);
 
 // chord_w4a16_prepack: header, then every 16-byte piece of every block.
