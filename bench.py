@@ -56,8 +56,9 @@ def parse():
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
-                    help="time only the headline configuration (default: also every other "
-                         "configuration, under the `configs` key)")
+                    help="time only the headline configuration, and its align only as part of "
+                         "the step (default: also every other configuration, under the "
+                         "`configs` key, and each indexed configuration's align alone)")
     return ap.parse_args()
 
 
@@ -392,6 +393,48 @@ def stage_times(chord, step, stream, calls):
     return [v / max(n, 1) for v in stage_ms]
 
 
+ALIGN_REPS = 20
+
+
+def align_time_ms(align_call, stream, steps=20):
+    """Per-call ms of the align alone: a CUDA graph of ALIGN_REPS back-to-back
+    calls (after three eager ones), replayed `steps` times; the median replay
+    over ALIGN_REPS.  (The layer's own stages come from the library's stage
+    events; the align is a separate call, so it is timed this way.)"""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            align_call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(ALIGN_REPS):
+                align_call()
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            ev[2 * i].record(stream)
+            g.replay()
+            ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    return float(np.median([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)])) / ALIGN_REPS
+
+
+STAGES_HOW = ("align: a CUDA graph of 20 back-to-back align calls, replayed, per call; prepare, "
+              "gate_up, down, combine: the library's per-stage CUDA events over eager layer calls")
+
+
+def stages_record(stage, align_ms=None):
+    rec = {} if align_ms is None else {"align": round(align_ms, 5)}
+    rec.update({"prepare": round(stage[0], 5), "gate_up": round(stage[1], 5),
+                "down": round(stage[2], 5), "combine": round(stage[3], 5)})
+    return rec
+
+
 def roofline(work, stage, layer_ms, decode, label):
     """The dominant kernel's roofline (the gate/up GEMM: HBM-bound for decode
     shapes, tensor-bound for prefill) and the layer's achieved fractions."""
@@ -448,6 +491,15 @@ class IndexedCase:
                                                          s.I, self.bm, self.cap, flags),
                                 dtype=torch.uint8, device=dev)
 
+    def align_fn(self, d, T):
+        chord, s = self.chord, self.s
+        ids = d["ids"][:T]
+
+        def call():
+            chord.moe_align(ids, s.E_global, s.E_local, self.bm, expert_map=d["emap"],
+                            capacity=self.cap, workspace=self.ws_a, out=(self.si, self.ei, self.ntp))
+        return call
+
     def step_fn(self, d, w, T):
         chord, s = self.chord, self.s
         x, ids, tw, out = d["x"][:T], d["ids"][:T], d["tw"][:T], self.out[:T]
@@ -461,7 +513,7 @@ class IndexedCase:
 
 
 def config_record(chord, torch, dev, stream, step, graph, work, steps, warmup, label, extra,
-                  dev_index, uuid):
+                  dev_index, uuid, align_call=None):
     """Timing record of one extra configuration (same rules as the headline)."""
     flush = None
     if needs_l2_flush(work["layer"]["bytes"]):
@@ -470,6 +522,7 @@ def config_record(chord, torch, dev, stream, step, graph, work, steps, warmup, l
         ms = time_graph(graph, stream, steps, warmup, flush)
     replay_us = replay_spread(graph, stream, max(steps, SPREAD_REPLAYS), flush)
     stage = stage_times(chord, step, stream, max(3, min(steps, 10)))
+    align_ms = align_time_ms(align_call, stream) if align_call is not None else None
     roof, layer = roofline(work, stage, ms, is_decode(work), label)
     rec = {"value": round(ms * 1e3, 2), "unit": UNIT, "ms_per_step": round(ms, 5),
            "steps": steps, "warmup": warmup,
@@ -479,8 +532,7 @@ def config_record(chord, torch, dev, stream, step, graph, work, steps, warmup, l
            "replay_us": replay_us,
            "routed_pairs": work["pairs"], "touched_experts": work["touched"],
            "roofline": roof, "layer": layer,
-           "stages_ms": {"prepare": round(stage[0], 5), "gate_up": round(stage[1], 5),
-                         "down": round(stage[2], 5), "combine": round(stage[3], 5)},
+           "stages_ms": stages_record(stage, align_ms), "stages_how": STAGES_HOW,
            "clocks": clk.summary()}
     rec.update(extra)
     return rec
@@ -512,7 +564,7 @@ def run_configs(args, chord, torch, dev, stream, ep8_inp, ep8_dev, dev_index, uu
         if cap_T:
             extra["buffers"] = f"routing buffers and workspaces sized for {cap_T} tokens"
         return config_record(chord, torch, dev, stream, step, graph, work, steps, warmup, label,
-                             extra, dev_index, uuid)
+                             extra, dev_index, uuid, align_call=case.align_fn(d, T))
 
     # tiny: K = 128 of its down GEMM is below the prepack's 256-deep blocks
     s = synth.workload("tiny")
@@ -715,6 +767,9 @@ def run_ours(args, rank, world, dev_index):
     ms = max_over_ranks(local_ms, world, dev)
     replay_us = replay_spread(graph, stream, max(args.steps, SPREAD_REPLAYS), flush)
     stage = stage_times(chord, step, stream, args.steps)
+    # (the align-only graph adds ~460 align launches: left out of the short
+    # single-configuration runs that the ncu launch lists capture)
+    align_ms = None if args.no_configs else align_time_ms(case.align_fn(d, s.T), stream)
 
     # end to end through the public API with host buffers: every step copies
     # its inputs in from pinned host memory and its output back; the copies
@@ -752,8 +807,7 @@ def run_ours(args, rank, world, dev_index):
                             "N replicas complete per step"},
         "layer": layer,
         "replay_us": replay_us,
-        "stages_ms": {"prepare": round(stage[0], 5), "gate_up": round(stage[1], 5),
-                      "down": round(stage[2], 5), "combine": round(stage[3], 5)},
+        "stages_ms": stages_record(stage, align_ms), "stages_how": STAGES_HOW,
         "roofline": roof,
         "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
