@@ -548,18 +548,21 @@ struct LayerIO {
 // unit is short, and its fixed costs (waits, commits, the token tile) are
 // shared by a run of tiles of one chunk in a token-stationary configuration,
 // which loads the chunk's token tile once per run.  The run is the longest
-// (of 14, 8, 7, 4, 2 tiles, dividing the tile count) that still deals every
-// SM six units or more (the units are dealt with a stride of the grid, so
-// fewer, longer units leave more of the last round idle; measured against
-// twelve: TP8 down 36.9 -> 34.7 us at 16 tokens, 181.8 -> 178.8 us at 2048).  Returns the tiles
-// per unit and sets *cfg to the configuration that runs them.
+// (of 7, 4, 2 tiles, dividing the tile count) that still deals every SM six
+// units or more (the units are dealt with a stride of the grid, so fewer,
+// longer units leave more of the last round idle).  Measured on the TP8 down
+// GEMM (H = 7168: 56 tiles): runs of 7 against 14 took 179.9 -> 176.0 us at
+// 2048 tokens and 88.1 -> 86.7 us at 128; runs of 8 took 182.1 and 87.7 us;
+// a rule of twelve units per SM instead of six took 16 tokens from 34.7 to
+// 36.9 us.  Returns the tiles per unit and sets *cfg to the configuration
+// that runs them.
 int pick_tpu(int* cfg, int K, int n_tiles, int E_local, double tok_e, int sms)
 {
     const int s_cfg = *cfg == kCfgD32 ? kCfgS32 : *cfg == kCfgD64 ? kCfgS64 : -1;
     if (s_cfg < 0 || K != gemm_cfg_bk(s_cfg))
         return 1;
     const double chunks = E_local * (1.0 - std::exp(-(tok_e > 0 ? tok_e : 0.0)));
-    static const int runs[] = {14, 8, 7, 4, 2};
+    static const int runs[] = {7, 4, 2};
     for (int r : runs)
         if (r <= gemm_cfg_tpu_max_down(s_cfg) && n_tiles % r == 0 &&
             chunks * n_tiles / r >= 6.0 * sms) {
