@@ -552,7 +552,8 @@ struct LayerIO {
 // units or more (the units are dealt with a stride of the grid, so fewer,
 // longer units leave more of the last round idle).  Measured on the TP8 down
 // GEMM (H = 7168: 56 tiles): runs of 7 against 14 took 179.9 -> 176.0 us at
-// 2048 tokens and 88.1 -> 86.7 us at 128; runs of 8 took 182.1 and 87.7 us;
+// 2048 tokens and 88.1 -> 86.7 us at 128; runs of 8 took 182.1 and 87.7 us,
+// runs of 4 182.3 and 90.2 us;
 // a rule of twelve units per SM instead of six took 16 tokens from 34.7 to
 // 36.9 us.  Returns the tiles per unit and sets *cfg to the configuration
 // that runs them.
