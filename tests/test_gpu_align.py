@@ -118,5 +118,5 @@ def test_align_one_cta_limit(chord, T, E, spread):
         ids = np.stack([rng.permutation(E)[:8] for _ in range(T)]).astype(np.int32)
     else:
         ids = np.stack([rng.permutation(8) for _ in range(T)]).astype(np.int32)
-    for bm in (1, 16, 64):
+    for bm in (1, 16, 64, 256):
         _compare(chord, ids, E, None, E, bm)

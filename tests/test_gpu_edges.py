@@ -1,5 +1,6 @@
 """Edges of the supported shapes on the GPU, each checked against the oracle
-and the fp64 anchor like the fixed cases: the largest top-k (32), more local
+and the fp64 anchor like the fixed cases: the largest top-k (32, also through
+the ordered combine), more local
 experts than the align entry point and the masked layout's row compaction take
 (1024), a deep reduction (H = 4096) with a six-stage down GEMM (I = 1536), a
 hidden size of 128 mod 256, and an empty batch."""
@@ -21,6 +22,22 @@ pytestmark = pytest.mark.gpu
 def test_large_top_k(chord, k):
     inp = small(24, k, 64, 40, 256, 128, 500 + k)
     verify_indexed(inp, run_indexed_full(chord, inp), label=f"top-k {k}")
+
+
+@pytest.mark.parametrize("T", [24, 300, 2100])
+def test_large_top_k_ordered_combine(chord, T):
+    """Top-k 32 through the ordered combine (CHORD_FLAG_DETERMINISTIC): a
+    token's up to 32 local slots are loaded in batches (eight slots at a time
+    up to 256 tokens, two up to 2048, one beyond) and summed in ascending slot
+    order, so the three block shapes of the combine each see tokens with more
+    slots than one batch; two calls give the same bits."""
+    inp = small(T, 32, 64, 40, 256, 128, 520 + T)
+    run = run_indexed_full(chord, inp, flags=2)
+    tokens = None if T <= 300 else np.sort(np.random.default_rng(T).choice(T, 64, replace=False))
+    verify_indexed(inp, run, tokens, label=f"top-k 32 ordered T={T}")
+    again = run_indexed_full(chord, inp, flags=2)
+    assert np.array_equal(run.out.view(np.uint16), again.out.view(np.uint16)), \
+        "the ordered combine must be bit-reproducible"
 
 
 def test_more_local_experts_than_staged(chord):
